@@ -1,0 +1,613 @@
+"""fp64 CPU oracle for FLAMIA: causal flash attention with microscaled FP8 operands.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it.  It
+shares no code with the CUDA library (no kernels, headers, tables or helpers);
+the only module both sides use is the seeded input generator
+``flamia_workloads``, which holds none of the method's arithmetic.
+
+Sources (web pages about the paper "FLAMIA: FLAsh MIcroscaling Attention for
+Fast and Causally Safe Training on Blackwell", arXiv 2611.03344):
+  [EN] "FLAMIA technical review" (Zhongzhu Zhou, 2026-11-08), sections 1-11,
+       Algorithm 1 ("Microscaled forward and recomputed backward") and
+       Algorithm 2 ("Document-local work list and launch").
+  [KO] Korean review of the same paper (jaehun.me), sections 1-5.
+  [FA] "Model development: efficient execution" (blog post on FlashAttention
+       and low-precision formats), sections "Attention without the score
+       matrix" and "Lower precision".
+
+Everything is float64 numpy except where the method fixes a narrower format
+(E4M3 / E2M1 / UE8M0 codes, bf16 outputs, fp16 dQ partials); those are
+emulated exactly.  Where the pages are silent or garbled, the reading taken
+is named in the docstring (C-1 ... C-14, listed with reasons in the design
+notes).
+
+Parity status: the codecs, exponent rules, cost model, work list, the
+unquantized attention path and the prefix-isolation properties are pinned by
+tests against the pages and mathematics.  The quantized attention as a whole
+has no external anchor beyond its parts (the pages print no quantized output
+values) -- its end-to-end values are "parity unpinned" beyond those parts.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Iterable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+__all__ = [
+    "E4M3_MAX", "FP16_MAX", "e4m3_decode", "e4m3_round", "e4m3_encode", "e2m1_round", "e2m1_encode",
+    "e2m1_decode", "bf16_round", "fp16_round", "ue8m0_decode",
+    "roundup_exponent", "floor_exponent", "quantize_tokenblock", "dequantize_tokenblock",
+    "quantize_nvfp4", "dequantize_nvfp4",
+    "Options", "attention_forward", "attention_backward", "run_training_call",
+    "dense_attention", "dense_attention_grads", "visible_pairs", "work_list",
+    "bwd_key_tile_list", "dq_boost", "doc_ranges",
+]
+
+E4M3_MAX = 448.0          # largest finite E4M3 magnitude ([FA] "Lower precision", format table)
+E4M3_EMAX = 8             # binade of the largest code: 448 = 1.75 * 2**8
+FP16_MAX = 65504.0        # [FA] "Lower precision", format table
+BF16_MAX = float(np.ldexp(2.0 - 2.0 ** -7, 127))
+
+
+# --------------------------------------------------------------------------
+# Codecs.  [EN] section 2 "Codes, scales, and hardware layout"; [FA] "Lower
+# precision".  Reading C-1: OCP E4M3 "fn" (bias 7, max 448, NaN = S.1111.111,
+# no infinities, subnormals m * 2**-9), round to nearest with ties to even,
+# saturating to +-448.
+# --------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 byte -> value (fp64)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    ef = (c >> 3) & 0xF
+    mf = c & 0x7
+    mag = np.where(ef == 0, mf * 2.0 ** -9, (1.0 + mf / 8.0) * np.ldexp(1.0, ef - 7))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Nearest E4M3 value to x (ties to even), saturated to +-448; sign of zero kept."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, k = np.frexp(a)                      # a = f * 2**k with f in [0.5, 1)
+    binade = np.maximum(k - 1, -6)          # below 2**-6 the grid is the subnormal one
+    step = np.ldexp(1.0, binade - 3)        # 3 mantissa bits
+    with np.errstate(invalid="ignore"):
+        r = np.round(a / step) * step       # numpy rounds halves to even
+    r = np.where(np.isnan(a), np.nan, np.minimum(r, E4M3_MAX))
+    return np.copysign(r, x)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Value -> E4M3 byte after :func:`e4m3_round`."""
+    v = e4m3_round(x)
+    a = np.abs(v)
+    neg = np.signbit(v)
+    nan = np.isnan(a)
+    a = np.where(nan, 0.0, a)
+    _, k = np.frexp(a)
+    binade = k - 1
+    normal = a >= 2.0 ** -6
+    ef = np.where(normal, binade + 7, 0)
+    mant = np.where(normal, (a / np.ldexp(1.0, np.where(normal, binade, 0)) - 1.0) * 8.0,
+                    a / 2.0 ** -9)
+    code = (ef.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    code = np.where(nan, 0x7F, code)
+    code = code | np.where(neg, 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def ue8m0_decode(b) -> np.ndarray:
+    """UE8M0 scale byte -> 2**(b-127) (0xFF is NaN)."""
+    b = np.asarray(b, dtype=np.int64)
+    return np.where(b == 0xFF, np.nan, np.ldexp(1.0, b - 127))
+
+
+_E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_round(x) -> np.ndarray:
+    """Nearest E2M1 value (ties to the even code), saturated to +-6 ([EN] section 2:
+    NVFP4 = E2M1 codes with an E4M3 scale per 16 elements)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    r = np.minimum(np.round(a / step) * step, 6.0)
+    return np.copysign(r, x)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Value -> 4-bit E2M1 code (bit 3 = sign), one code per uint8."""
+    v = e2m1_round(x)
+    idx = np.searchsorted(_E2M1_VALUES, np.abs(v))
+    return (idx | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
+
+
+def e2m1_decode(c) -> np.ndarray:
+    c = np.asarray(c, dtype=np.int64)
+    return np.where(c & 8, -1.0, 1.0) * _E2M1_VALUES[c & 7]
+
+
+def _round_to_bits(x, mant_bits: int, min_binade: int, max_finite: float) -> np.ndarray:
+    """Round fp64 to a binary float with ``mant_bits`` stored mantissa bits (nearest even)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, k = np.frexp(a)
+    binade = np.maximum(k - 1, min_binade)
+    step = np.ldexp(1.0, binade - mant_bits)
+    with np.errstate(invalid="ignore", over="ignore"):
+        r = np.round(a / step) * step
+    r = np.where(r > max_finite, np.inf, r)
+    r = np.where(np.isnan(a), np.nan, r)
+    return np.copysign(r, x)
+
+
+def bf16_round(x) -> np.ndarray:
+    """fp64 -> nearest bf16 value (ties to even); overflow -> inf."""
+    return _round_to_bits(x, 7, -126, BF16_MAX)
+
+
+def fp16_round(x) -> np.ndarray:
+    """fp64 -> nearest IEEE half value (ties to even); overflow -> inf."""
+    return _round_to_bits(x, 10, -14, FP16_MAX)
+
+
+# --------------------------------------------------------------------------
+# Exponent rules.  [EN] section 4 "Why doubling the scale often preserves
+# E4M3 values" (clipping as the second failure; the conservative scale) and
+# [KO] section 3.2 (rounding the exponent up keeps the scaled maximum <= 448).
+# --------------------------------------------------------------------------
+
+def roundup_exponent(amax) -> np.ndarray:
+    """Reading C-2: the smallest integer e with amax <= 448 * 2**e.
+
+    A zero block takes e = 0 (the pages allow "a conventional finite scale");
+    e is clamped to the UE8M0 range [-127, 127]."""
+    amax = np.asarray(amax, dtype=np.float64)
+    pos = amax > 0
+    safe = np.where(pos, amax, 448.0)
+    e = np.ceil(np.log2(safe / E4M3_MAX)).astype(np.int64)
+    # log2 is not exact: settle the inequality with exact power-of-two products.
+    for _ in range(2):
+        e = np.where(safe > np.ldexp(E4M3_MAX, e), e + 1, e)
+        e = np.where(safe <= np.ldexp(E4M3_MAX, e - 1), e - 1, e)
+    e = np.where(pos, e, 0)
+    return np.clip(e, -127, 127)
+
+
+def floor_exponent(amax) -> np.ndarray:
+    """Negative control only: the floor rule e = floor(log2 amax) - emax with
+    emax = 8 for E4M3 ([KO] section 2; [EN] section 4 "A floor rule based only
+    on the largest code exponent").  It lets amax * 2**-e exceed 448."""
+    amax = np.asarray(amax, dtype=np.float64)
+    _, k = np.frexp(np.where(amax > 0, amax, 1.0))
+    e = (k - 1) - E4M3_EMAX
+    return np.clip(np.where(amax > 0, e, 0), -127, 127)
+
+
+# --------------------------------------------------------------------------
+# Packed documents.  [EN] section 6 "Preserve the logical row before
+# optimizing the physical tile": token blocks are local to each document; the
+# scale metadata is dense (one entry per token).
+# --------------------------------------------------------------------------
+
+def doc_ranges(cu) -> List[Tuple[int, int]]:
+    cu = [int(c) for c in cu]
+    return [(cu[n], cu[n + 1]) for n in range(len(cu) - 1)]
+
+
+def _doc_blocks(cu, block: int):
+    for s, t in doc_ranges(cu):
+        for b0 in range(s, t, block):
+            yield b0, min(b0 + block, t)
+
+
+def quantize_tokenblock(x, cu, block: int = 32, rule: str = "roundup"):
+    """Token-block MXFP8 quantizer ([EN] section 3 "Why one shared exponent can
+    serve two reductions"; [KO] section 3.1; Algorithm 1 step 03).
+
+    x: [T, H, d] values (bf16 values held in fp64).  For each document, each
+    head and each document-local block of ``block`` consecutive tokens (32 by
+    default; 1 for the strict per-token option of [EN] section 4): amax over the
+    block x head dim, e by the round-up rule, codes = E4M3(x * 2**-e) and one
+    UE8M0 byte (e + 127) stored for every token of the block.
+
+    Tokens outside every document keep code 0 and byte 127.
+    Returns (codes uint8 [T,H,d], scale bytes uint8 [T,H])."""
+    x = np.asarray(x, dtype=np.float64)
+    T, H, d = x.shape
+    codes = np.zeros((T, H, d), dtype=np.uint8)
+    sbytes = np.full((T, H), 127, dtype=np.uint8)
+    exp_rule = roundup_exponent if rule == "roundup" else floor_exponent
+    for b0, b1 in _doc_blocks(cu, block):
+        xb = x[b0:b1]
+        amax = np.abs(xb).max(axis=(0, 2))
+        e = exp_rule(amax)
+        codes[b0:b1] = e4m3_encode(xb * np.ldexp(1.0, -e)[None, :, None])
+        sbytes[b0:b1] = (e + 127).astype(np.uint8)[None, :]
+    return codes, sbytes
+
+
+def dequantize_tokenblock(codes, sbytes) -> np.ndarray:
+    """X^ = s_X * c_X with s_X = 2**(byte - 127) per token and head."""
+    return e4m3_decode(codes) * ue8m0_decode(sbytes)[:, :, None]
+
+
+def quantize_nvfp4(x):
+    """NVFP4 score operand ([EN] section 2; [KO] section 3.1), reading C-7: no
+    tensor scale; per (token, head, 16 head-dim elements) the scale is
+    E4M3(amax / 6) computed with an fp32 division and raised to 2**-9 when it
+    would round to zero for a non-zero group; codes are E2M1(fp32(x) / s) with
+    an IEEE fp32 division.  Returns (codes uint8 [T,H,d] one per byte,
+    scale bytes uint8 [T,H,d/16] as E4M3 codes)."""
+    x = np.asarray(x, dtype=np.float64)
+    T, H, d = x.shape
+    g = x.reshape(T, H, d // 16, 16)
+    amax = np.abs(g).max(axis=-1).astype(np.float32)
+    s = e4m3_round((amax / np.float32(6.0)).astype(np.float64))
+    s = np.where((amax > 0) & (s == 0), 2.0 ** -9, s)
+    s32 = s.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s32[..., None] > 0, g.astype(np.float32) / s32[..., None], np.float32(0))
+    codes = e2m1_encode(q.astype(np.float64)).reshape(T, H, d)
+    return codes, e4m3_encode(s)
+
+
+def dequantize_nvfp4(codes, scodes) -> np.ndarray:
+    T, H, d = codes.shape
+    v = e2m1_decode(codes).reshape(T, H, d // 16, 16) * e4m3_decode(scodes)[..., None]
+    return v.reshape(T, H, d)
+
+
+# --------------------------------------------------------------------------
+# Cost model and work list.  [EN] section 6 "Cost-based scheduling and tail
+# behavior" and Algorithm 2.
+# --------------------------------------------------------------------------
+
+def visible_pairs(lengths) -> int:
+    """Visible (query, key) pairs of causal packed documents: sum n(n+1)/2."""
+    return int(sum(int(n) * (int(n) + 1) // 2 for n in lengths))
+
+
+def work_list(cu, tile: int = 128, item_tiles: int = 2, num_ctas: Optional[int] = None):
+    """Algorithm 2 of [EN] (steps 03-06) with reading C-11: items of up to
+    ``item_tiles`` query tiles (256 queries) of one document; cost = number of
+    visible key tiles summed over the item's query tiles (causal); sort by
+    decreasing cost (ties keep document order, then query order); alternate the
+    assignment direction over persistent CTAs on every pass.
+
+    Returns a list of dicts in sorted order with keys doc, tile0, ntiles, cost
+    and (when num_ctas is given) cta."""
+    items = []
+    for n, (s, t) in enumerate(doc_ranges(cu)):
+        ntile = -(-(t - s) // tile)
+        for t0 in range(0, ntile, item_tiles):
+            nt = min(item_tiles, ntile - t0)
+            cost = sum(tt + 1 for tt in range(t0, t0 + nt))
+            items.append(dict(doc=n, tile0=t0, ntiles=nt, cost=cost))
+    order = sorted(range(len(items)), key=lambda i: (-items[i]["cost"], i))
+    out = [items[i] for i in order]
+    if num_ctas:
+        for r, it in enumerate(out):
+            p, pos = divmod(r, num_ctas)
+            it["cta"] = pos if p % 2 == 0 else num_ctas - 1 - pos
+    return out
+
+
+def bwd_key_tile_list(cu, tile: int = 128):
+    """Backward work ([EN] Algorithm 2 step 12): one item per document-local key
+    tile, cost = number of query tiles that see it, sorted by decreasing cost
+    (ties keep document order then key order)."""
+    items = []
+    for n, (s, t) in enumerate(doc_ranges(cu)):
+        ntile = -(-(t - s) // tile)
+        for u in range(ntile):
+            items.append(dict(doc=n, ktile=u, cost=ntile - u))
+    order = sorted(range(len(items)), key=lambda i: (-items[i]["cost"], i))
+    return [items[i] for i in order]
+
+
+# --------------------------------------------------------------------------
+# Attention.  [EN] section 2 (definitions, centred softmax gradient, online
+# recurrence), section 5 (Algorithm 1; range budget for probabilities) and
+# [KO] section 1.2 (S = QK^T/sqrt(d), P = softmax(S), O = PV and the five
+# backward products).
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Options:
+    quantized: bool = True         # False: every codec is the identity
+    block: int = 32                # operand token-block length (1 = strict per-token)
+    rule: str = "roundup"          # operand exponent rule ("floor" = negative control)
+    p_boost_log2: int = 8          # beta = 2**8 for the forward P operand (reading C-4)
+    p_lag_log2: int = 0            # tau: how far the retained max may lag (reading C-4)
+    bwd_p_boost_log2: int = 8      # backward P operand boost (reading C-6)
+    tile: int = 128                # query and key tile (reading C-11)
+    dq_headroom_log2: int = 14     # dQ boost target 2**14 (reading C-10)
+
+
+def _masked_scores(Qt, Ku, qpos, kpos, scale):
+    S = scale * (Qt @ Ku.T)
+    S = np.where(kpos[None, :] > qpos[:, None], -np.inf, S)
+    return S
+
+
+def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] = None,
+                      opts: Options = Options(), heads: Optional[Iterable[int]] = None,
+                      q_tiles: Optional[Dict[int, Iterable[int]]] = None):
+    """Forward of Algorithm 1 (steps 04-08) for causal packed documents.
+
+    Qh [T,hq,d], Kh/Vh [T,hkv,d]: reconstructed operands X^ = s*c (or plain
+    values when unquantized).  For every document, query head h (kv head
+    h // (hq/hkv)) and 128-row document-local query tile, visit the visible
+    128-key tiles in increasing order:
+
+      S   = scale * Q^ K^T, keys after the query masked to -inf
+      m'  = max(m, rowmax S)      (retained max may lag by tau, reading C-4)
+      p   = exp(S - m'),  l = l * exp(m - m') + sum(p)     (unrounded, C-5)
+      P^  = E4M3(beta * p) / beta                          (section 5)
+      acc = acc * exp(m - m') + P^ V^
+
+    and finish with O = bf16(acc / l), LSE = m + ln l ([EN] section 2 "Why
+    flash tiling recomputes scores").  Rows outside every document keep O = 0
+    and LSE = +inf ([EN] section 6).  Returns (O [T,hq,d], LSE [hq,T])."""
+    Qh = np.asarray(Qh, np.float64); Kh = np.asarray(Kh, np.float64); Vh = np.asarray(Vh, np.float64)
+    T, _, d = Qh.shape
+    g = hq // hkv
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    tile = opts.tile
+    beta = 2.0 ** opts.p_boost_log2
+    tau_nat = opts.p_lag_log2 * math.log(2.0)
+    O = np.zeros((T, hq, d))
+    LSE = np.full((hq, T), np.inf)
+    heads = range(hq) if heads is None else heads
+    for n, (s0, s1) in enumerate(doc_ranges(cu)):
+        ntile = -(-(s1 - s0) // tile)
+        tiles = range(ntile) if q_tiles is None else q_tiles.get(n, ())
+        for h in heads:
+            hk = h // g
+            for t in tiles:
+                r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
+                qpos = np.arange(r0, r1)
+                Qt = Qh[r0:r1, h]
+                m = np.full(r1 - r0, -np.inf)
+                l = np.zeros(r1 - r0)
+                acc = np.zeros((r1 - r0, d))
+                for u in range(t + 1):
+                    c0, c1 = s0 + u * tile, min(s0 + (u + 1) * tile, s1)
+                    S = _masked_scores(Qt, Kh[c0:c1, hk], qpos, np.arange(c0, c1), scale)
+                    rowmax = S.max(axis=1)
+                    m_new = np.where(rowmax > m + tau_nat, np.maximum(m, rowmax), m)
+                    alpha = np.where(np.isfinite(m), np.exp(m - m_new), 0.0)
+                    p = np.exp(S - m_new[:, None])
+                    l = l * alpha + p.sum(axis=1)
+                    Pq = e4m3_round(beta * p) / beta if opts.quantized else p
+                    acc = acc * alpha[:, None] + Pq @ Vh[c0:c1, hk]
+                    m = m_new
+                out = acc / l[:, None]
+                O[r0:r1, h] = bf16_round(out) if opts.quantized else out
+                LSE[h, r0:r1] = m + np.log(l)
+    return O, LSE
+
+
+def dq_boost(dOh_doc, Vh_doc, Kh_doc, headroom_log2: int = 14) -> float:
+    """Default dQ accumulator boost for one (document, query head), reading
+    C-10 of [EN] section 4 "Forward locality and backward locality differ":
+    M = 2 * max_i ||dO^_i|| * max_j ||V^_j|| * max_{j,d} |K^_jd| bounds every
+    partial |sum_j dS_ij K_jd|; c = 2**floor(log2(2**14 / M)); c = 1 if M = 0."""
+    M = 2.0 * np.sqrt((dOh_doc ** 2).sum(-1)).max(initial=0.0) \
+        * np.sqrt((Vh_doc ** 2).sum(-1)).max(initial=0.0) * np.abs(Kh_doc).max(initial=0.0)
+    if not (M > 0) or not np.isfinite(M):
+        return 1.0
+    e = math.floor(math.log2(2.0 ** headroom_log2 / M))
+    while 2.0 ** e * M > 2.0 ** headroom_log2:
+        e -= 1
+    while 2.0 ** (e + 1) * M <= 2.0 ** headroom_log2:
+        e += 1
+    e = max(-100, min(100, e))
+    return 2.0 ** e
+
+
+def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
+                       scale: Optional[float] = None, opts: Options = Options(),
+                       kv_heads: Optional[Iterable[int]] = None,
+                       k_tiles: Optional[Dict[int, Iterable[int]]] = None,
+                       q_tiles: Optional[Dict[int, Iterable[int]]] = None,
+                       diagnostics: bool = False):
+    """Backward of Algorithm 1 (steps 09-16).
+
+    dOh: the reconstructed incoming gradient dO^ (encoded once, step 09);
+    D_i = dO^_i . O_i with the saved bf16 O ([KO] section 3.3).  For every
+    document, kv head, document-local 128-key tile u (increasing) and every
+    query tile t >= u of each query head sharing the kv head:
+
+      S   = scale * Q^ K^T (same tiles and masks as the forward)
+      P   = exp(S - LSE)                                  (step 12)
+      dP  = dO^ V^T,  dS = P o (dP - D)                   (steps 13-14)
+      dS^ = per document-local 32x32 block: E4M3(dS * 2**-e) * 2**e with
+            e the round-up exponent of the block amax     (reading C-9)
+      dV += (E4M3(2**8 P) / 2**8)^T dO^                  (reading C-6)
+      dK += dS^^T Q^
+      h   = fp16(c * dS^ K^),  accQ = fp16(accQ + h)      (step 15)
+
+    then dK = bf16(scale * dK), dV = bf16(dV), dQ = bf16(scale * accQ / c)
+    (step 16).  Unquantized: every codec is the identity and accQ is exact.
+
+    k_tiles / q_tiles restrict which dK/dV key tiles and dQ query tiles are
+    produced (others stay zero); kv_heads restricts heads.
+    Returns dict with dq, dk, dv (and diagnostics when asked)."""
+    Qh = np.asarray(Qh, np.float64); Kh = np.asarray(Kh, np.float64)
+    Vh = np.asarray(Vh, np.float64); dOh = np.asarray(dOh, np.float64)
+    O = np.asarray(O, np.float64); LSE = np.asarray(LSE, np.float64)
+    T, _, d = Qh.shape
+    g = hq // hkv
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    tile = opts.tile
+    q = opts.quantized
+    beta_b = 2.0 ** opts.bwd_p_boost_log2
+    D = (dOh * O).sum(-1)                                   # [T, hq]
+    dQ = np.zeros((T, hq, d)); dK = np.zeros((T, hkv, d)); dV = np.zeros((T, hkv, d))
+    diag = dict(rowsum_ds=np.zeros((hq, T)), rowmax_ds=np.zeros((hq, T)),
+                rowsum_p=np.zeros((hq, T)), rowsum_pdp=np.zeros((hq, T)),
+                ds_nonzero=0, dsq_zero=0) if diagnostics else None
+    kv_heads = range(hkv) if kv_heads is None else kv_heads
+    for n, (s0, s1) in enumerate(doc_ranges(cu)):
+        ntile = -(-(s1 - s0) // tile)
+        ksel = set(range(ntile)) if k_tiles is None else set(k_tiles.get(n, ()))
+        qsel = set(range(ntile)) if q_tiles is None else set(q_tiles.get(n, ()))
+        for hk in kv_heads:
+            for h in range(hk * g, (hk + 1) * g):
+                c = dq_boost(dOh[s0:s1, h], Vh[s0:s1, hk], Kh[s0:s1, hk], opts.dq_headroom_log2) if q else 1.0
+                accQ = {t: np.zeros((min(tile, s1 - s0 - t * tile), d)) for t in qsel}
+                for u in range(ntile):
+                    c0, c1 = s0 + u * tile, min(s0 + (u + 1) * tile, s1)
+                    kpos = np.arange(c0, c1)
+                    for t in range(u, ntile):
+                        if u not in ksel and t not in qsel and not diagnostics:
+                            continue
+                        r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
+                        qpos = np.arange(r0, r1)
+                        S = _masked_scores(Qh[r0:r1, h], Kh[c0:c1, hk], qpos, kpos, scale)
+                        P = np.exp(S - LSE[h, r0:r1][:, None])
+                        dP = dOh[r0:r1, h] @ Vh[c0:c1, hk].T
+                        dS = P * (dP - D[r0:r1, h][:, None])
+                        if q:
+                            dSq = _quantize_ds_blocks(dS, r0 - s0, c0 - s0)
+                            Pq = e4m3_round(beta_b * P) / beta_b
+                        else:
+                            dSq, Pq = dS, P
+                        if u in ksel:
+                            dV[c0:c1, hk] += Pq.T @ dOh[r0:r1, h]
+                            dK[c0:c1, hk] += dSq.T @ Qh[r0:r1, h]
+                        if t in qsel:
+                            part = dSq @ Kh[c0:c1, hk]
+                            if q:
+                                accQ[t] = fp16_round(accQ[t] + fp16_round(c * part))
+                            else:
+                                accQ[t] = accQ[t] + part
+                        if diagnostics:
+                            diag["rowsum_ds"][h, r0:r1] += dS.sum(1)
+                            diag["rowmax_ds"][h, r0:r1] = np.maximum(diag["rowmax_ds"][h, r0:r1],
+                                                                     np.abs(dS).max(1))
+                            diag["rowsum_p"][h, r0:r1] += P.sum(1)
+                            diag["rowsum_pdp"][h, r0:r1] += (P * dP).sum(1)
+                            if q:
+                                nz = dS != 0
+                                diag["ds_nonzero"] += int(nz.sum())
+                                diag["dsq_zero"] += int((nz & (dSq == 0)).sum())
+                for t in qsel:
+                    r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
+                    dQ[r0:r1, h] = scale * accQ[t] / c
+    out = dict(dq=bf16_round(dQ) if q else dQ,
+               dk=bf16_round(scale * dK) if q else scale * dK,
+               dv=bf16_round(dV) if q else dV)
+    if diagnostics:
+        out["diag"] = diag
+    return out
+
+
+def _quantize_ds_blocks(dS, qoff: int, koff: int, block: int = 32):
+    """Reading C-9: one round-up exponent per document-local 32x32 block of dS
+    ([EN] section 3, "the analogous region is a 32 by 32 square"; section 5
+    "The paper's 32 by 32 maxima"; [KO] section 3.3).  qoff/koff are the
+    document-local offsets of the tile's first row/column (multiples of 32)."""
+    R, C = dS.shape
+    assert qoff % block == 0 and koff % block == 0
+    Rp, Cp = -(-R // block) * block, -(-C // block) * block
+    pad = np.zeros((Rp, Cp))
+    pad[:R, :C] = dS
+    blocks = pad.reshape(Rp // block, block, Cp // block, block)
+    e = roundup_exponent(np.abs(blocks).max(axis=(1, 3)))          # [Rb, Cb]
+    sc = np.ldexp(1.0, e)[:, None, :, None]
+    q = e4m3_round(blocks / sc) * sc
+    return q.reshape(Rp, Cp)[:R, :C]
+
+
+# --------------------------------------------------------------------------
+# Brute-force references (textbook definitions, no tiling).  [KO] section
+# 1.2; [EN] section 2 "The contraction moves between forward and backward".
+# --------------------------------------------------------------------------
+
+def dense_attention(Q, K, V, cu, hq: int, hkv: int, scale: Optional[float] = None):
+    """Masked softmax attention per document and head, whole score matrix at once.
+    Returns (O [T,hq,d], LSE [hq,T])."""
+    Q = np.asarray(Q, np.float64); K = np.asarray(K, np.float64); V = np.asarray(V, np.float64)
+    T, _, d = Q.shape
+    g = hq // hkv
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    O = np.zeros((T, hq, d)); LSE = np.full((hq, T), np.inf)
+    for s0, s1 in doc_ranges(cu):
+        pos = np.arange(s0, s1)
+        for h in range(hq):
+            S = _masked_scores(Q[s0:s1, h], K[s0:s1, h // g], pos, pos, scale)
+            mx = S.max(1, keepdims=True)
+            E = np.exp(S - mx)
+            Z = E.sum(1, keepdims=True)
+            O[s0:s1, h] = (E / Z) @ V[s0:s1, h // g]
+            LSE[h, s0:s1] = (mx + np.log(Z))[:, 0]
+    return O, LSE
+
+
+def dense_attention_grads(Q, K, V, dO, cu, hq: int, hkv: int, scale: Optional[float] = None):
+    """Textbook gradients: dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij,
+    dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q (GQA: summed over the
+    query heads of a kv head).  Returns dict dq, dk, dv, ds_rowsum [hq,T]."""
+    Q = np.asarray(Q, np.float64); K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64); dO = np.asarray(dO, np.float64)
+    T, _, d = Q.shape
+    g = hq // hkv
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dQ = np.zeros_like(Q); dK = np.zeros_like(K); dV = np.zeros_like(V)
+    rows = np.zeros((hq, T))
+    for s0, s1 in doc_ranges(cu):
+        pos = np.arange(s0, s1)
+        for h in range(hq):
+            hk = h // g
+            S = _masked_scores(Q[s0:s1, h], K[s0:s1, hk], pos, pos, scale)
+            P = np.exp(S - S.max(1, keepdims=True))
+            P /= P.sum(1, keepdims=True)
+            dP = dO[s0:s1, h] @ V[s0:s1, hk].T
+            Dv = (P * dP).sum(1, keepdims=True)
+            dS = P * (dP - Dv)
+            rows[h, s0:s1] = dS.sum(1)
+            dV[s0:s1, hk] += P.T @ dO[s0:s1, h]
+            dQ[s0:s1, h] = scale * dS @ K[s0:s1, hk]
+            dK[s0:s1, hk] += scale * dS.T @ Q[s0:s1, h]
+    return dict(dq=dQ, dk=dK, dv=dV, ds_rowsum=rows)
+
+
+# --------------------------------------------------------------------------
+# The training call: quantize Q, K, V; forward; encode dO; backward.
+# --------------------------------------------------------------------------
+
+def run_training_call(q, k, v, do, cu, hq: int, hkv: int, scale: Optional[float] = None,
+                      opts: Options = Options(), **sel):
+    """Quantize (Algorithm 1 steps 02-03), forward (04-08), encode dO (09) and
+    backward (10-16).  Inputs are bf16 values as fp64 arrays.  ``sel`` may hold
+    heads / q_tiles for the forward and kv_heads / k_tiles / bwd_q_tiles for the
+    backward (sampled parity at large sizes).  Returns a dict with the codes,
+    scale bytes, O, LSE, dq, dk, dv."""
+    out = {}
+    if opts.quantized:
+        for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
+            c, sb = quantize_tokenblock(x, cu, opts.block, opts.rule)
+            out[name + "_codes"], out[name + "_scales"] = c, sb
+            out[name + "_hat"] = dequantize_tokenblock(c, sb)
+    else:
+        for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
+            out[name + "_hat"] = np.asarray(x, np.float64)
+    O, LSE = attention_forward(out["q_hat"], out["k_hat"], out["v_hat"], cu, hq, hkv, scale, opts,
+                               heads=sel.get("heads"), q_tiles=sel.get("q_tiles"))
+    out["o"], out["lse"] = O, LSE
+    if do is not None:
+        g = attention_backward(out["q_hat"], out["k_hat"], out["v_hat"], O, LSE, out["do_hat"], cu,
+                               hq, hkv, scale, opts, kv_heads=sel.get("kv_heads"),
+                               k_tiles=sel.get("k_tiles"), q_tiles=sel.get("bwd_q_tiles"),
+                               diagnostics=sel.get("diagnostics", False))
+        out.update(g)
+    return out

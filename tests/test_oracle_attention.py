@@ -1,0 +1,283 @@
+"""Pins for the oracle's attention, cost model and work list (CPU only)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+from golden_io import rows
+from metrics import cosine, norm_max_err
+
+
+def _inputs(lengths, hq, hkv, d, seed=0, scale=1.0, bf16=True):
+    rng = np.random.default_rng(seed)
+    T = int(sum(lengths))
+    mk = lambda h: rng.standard_normal((T, h, d)) * scale
+    q, k, v, do = mk(hq), mk(hkv), mk(hkv), mk(hq)
+    if bf16:
+        q, k, v, do = (O.bf16_round(x) for x in (q, k, v, do))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(int)
+    return q, k, v, do, cu
+
+
+# ------------------------------------------------------------ cost model
+
+def _parse_lengths(spec):
+    out = []
+    for part in spec.split("+"):
+        n, L = part.split("x")
+        out += [int(L)] * int(n)
+    return out
+
+
+def test_visible_pairs_from_pages():
+    for spec, pairs in rows("pair_counts.txt"):
+        L = _parse_lengths(spec)
+        assert sum(L) == 65536
+        assert O.visible_pairs(L) == int(pairs)
+
+
+def test_visible_pairs_brute_force():
+    for L in ([1], [5, 3], [17, 1, 2, 40]):
+        cu = np.concatenate([[0], np.cumsum(L)])
+        brute = sum(1 for s, t in O.doc_ranges(cu) for i in range(s, t) for j in range(s, t) if j <= i)
+        assert O.visible_pairs(L) == brute
+
+
+# ------------------------------------------------------------ unquantized attention
+
+UNQ = O.Options(quantized=False)
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d", [([300, 77, 129, 1], 2, 1, 16), ([256], 2, 2, 8), ([130, 5], 4, 2, 8)])
+def test_tiled_forward_equals_dense_bruteforce(lengths, hq, hkv, d):
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d)
+    O1, L1 = O.attention_forward(q, k, v, cu, hq, hkv, opts=UNQ)
+    O2, L2 = O.dense_attention(q, k, v, cu, hq, hkv)
+    assert np.max(np.abs(O1 - O2)) <= 1e-12 * np.max(np.abs(O2))
+    assert np.max(np.abs(L1 - L2)) <= 1e-12 * np.max(np.abs(L2))
+
+
+def test_online_softmax_is_block_partition_invariant():
+    """[FA] "Attention without the score matrix": blocks of 32 keys agree with ordinary attention."""
+    q, k, v, do, cu = _inputs([200, 64], 2, 2, 8, seed=1)
+    ref, _ = O.dense_attention(q, k, v, cu, 2, 2)
+    for tile in (32, 64, 128):
+        o, _ = O.attention_forward(q, k, v, cu, 2, 2, opts=O.Options(quantized=False, tile=tile))
+        assert np.max(np.abs(o - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_dense_gradients_match_finite_differences():
+    """Autograd-free central differences of L = sum(dO * O) on tiny shapes."""
+    lengths, hq, hkv, d = [7, 5], 2, 1, 4
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=2, bf16=False)
+    g = O.dense_attention_grads(q, k, v, do, cu, hq, hkv)
+    loss = lambda q_, k_, v_: float((O.dense_attention(q_, k_, v_, cu, hq, hkv)[0] * do).sum())
+    eps = 1e-6
+    for name, x, gx in (("q", q, g["dq"]), ("k", k, g["dk"]), ("v", v, g["dv"])):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp = x.copy(); xp[idx] += eps
+            xm = x.copy(); xm[idx] -= eps
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp; lp = loss(args["q"], args["k"], args["v"])
+            args[name] = xm; lm = loss(args["q"], args["k"], args["v"])
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.max(np.abs(num - gx)) <= 1e-6 * max(1.0, np.max(np.abs(gx))), name
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d", [([300, 77, 129, 1], 2, 1, 16), ([140, 33], 4, 2, 8)])
+def test_tiled_backward_equals_dense_gradients(lengths, hq, hkv, d):
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=3)
+    o, lse = O.attention_forward(q, k, v, cu, hq, hkv, opts=UNQ)
+    gt = O.attention_backward(q, k, v, o, lse, do, cu, hq, hkv, opts=UNQ)
+    gd = O.dense_attention_grads(q, k, v, do, cu, hq, hkv)
+    for n in ("dq", "dk", "dv"):
+        assert np.max(np.abs(gt[n] - gd[n])) <= 1e-11 * np.max(np.abs(gd[n])), n
+
+
+def test_centered_softmax_gradient_row_invariant():
+    """[EN] section 2: sum_j dS_ij = 0 with matched P and normalisation."""
+    q, k, v, do, cu = _inputs([250, 40], 2, 2, 16, seed=4)
+    o, lse = O.attention_forward(q, k, v, cu, 2, 2, opts=UNQ)
+    g = O.attention_backward(q, k, v, o, lse, do, cu, 2, 2, opts=UNQ, diagnostics=True)
+    rs, rm = g["diag"]["rowsum_ds"], g["diag"]["rowmax_ds"]
+    assert np.max(np.abs(rs) / np.maximum(rm, 1e-300)) < 1e-12
+    assert np.max(np.abs(O.dense_attention_grads(q, k, v, do, cu, 2, 2)["ds_rowsum"])) < 1e-12
+
+
+# ------------------------------------------------------------ quantized path properties
+
+def test_quantized_path_tracks_unquantized_attention():
+    """The pages report cosines near 0.999 (output) and 0.998 (gradients) for MXFP8
+    against an FP32 reference ([EN] section 8); a dropped term, transposed operand or
+    wrong sign in the quantized oracle would fall far below these loose bounds."""
+    lengths, hq, hkv, d = [300, 200], 4, 2, 64
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=5)
+    out = O.run_training_call(q, k, v, do, cu, hq, hkv)
+    ref_o, _ = O.dense_attention(q, k, v, cu, hq, hkv)
+    ref_g = O.dense_attention_grads(q, k, v, do, cu, hq, hkv)
+    assert cosine(out["o"], ref_o) > 0.997
+    for n in ("dq", "dk", "dv"):
+        assert cosine(out[n], ref_g[n]) > 0.99, n
+        assert norm_max_err(out[n], ref_g[n]) < 0.15, n
+
+
+def test_forward_p_quantization_bound():
+    """With tau = 0 every boosted weight is <= 2**8 and never clips ([EN] section 5)."""
+    q, k, v, do, cu = _inputs([130], 1, 1, 16, seed=6, scale=3.0)
+    o0, _ = O.attention_forward(q, k, v, cu, 1, 1, opts=O.Options(p_boost_log2=8))
+    # the same call with beta = 2**8 and an unclipped codec differs only by rounding
+    o1, _ = O.attention_forward(q, k, v, cu, 1, 1, opts=O.Options(quantized=False))
+    assert cosine(o0, o1) > 0.999
+
+
+def test_lagging_max_with_tempting_boost_clips():
+    """[EN] section 5: tau = 2, beta = 2**8 lets a weight of 4 clip to 448/256 = 1.75."""
+    d = 2
+    # one query; key tile 0 holds a score of 0, key tile 1 a score of ln(4) (= 2 in log2 units)
+    T = 129
+    q = np.zeros((T, 1, d)); k = np.zeros((T, 1, d)); v = np.zeros((T, 1, d))
+    q[128, 0, 0] = 1.0
+    k[128, 0, 0] = math.log(4.0)                 # scale = 1 below
+    v[128, 0, 1] = 1.0
+    cu = [0, T]
+    opts = O.Options(p_lag_log2=2, p_boost_log2=8, quantized=True)
+    o, lse = O.attention_forward(q, k, v, cu, 1, 1, scale=1.0, opts=opts)
+    # row 128: 128 keys with weight 1 (tile 0, retained max 0), one key with weight 4 -> 1.75
+    assert o[128, 0, 1] == O.bf16_round(1.75 / (128 + 4.0))
+    o_ok, _ = O.attention_forward(q, k, v, cu, 1, 1, scale=1.0, opts=O.Options())
+    assert abs(o_ok[128, 0, 1] - 4.0 / 132.0) < 4.0 / 132.0 / 64
+
+
+# ------------------------------------------------------------ prefix isolation
+
+def _train(q, k, v, do, cu, hq, hkv, **kw):
+    return O.run_training_call(q, k, v, do, cu, hq, hkv, opts=O.Options(**kw))
+
+
+def test_suffix_perturbation_leaves_earlier_blocks_bit_identical():
+    """[EN] section 10 / [KO] section 4.5: changing tokens in a later 32-token block
+    leaves O and LSE of queries in earlier blocks bit-identical (default path)."""
+    lengths, hq, hkv, d = [260], 2, 1, 32
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=8)
+    base = _train(q, k, v, do, cu, hq, hkv)
+    bp = 5                                     # perturb block 5 = tokens 160..191
+    for name in ("q", "k", "v"):
+        x = {"q": q, "k": k, "v": v}
+        y = x[name].copy()
+        y[bp * 32 + 3, 0, 1] *= 16.0               # push the block amax over exponent thresholds
+        x[name] = y
+        pert = _train(x["q"], x["k"], x["v"], do, cu, hq, hkv)
+        lim = bp * 32
+        assert np.array_equal(pert["o"][:lim], base["o"][:lim]), name
+        assert np.array_equal(pert["lse"][:, :lim], base["lse"][:, :lim]), name
+        assert not np.array_equal(pert["o"], base["o"]) or name == "q"
+
+
+def test_within_block_perturbation_is_detected():
+    """Positive control: a later token inside the same 32-token block moves the
+    block exponent and changes an earlier row's output (the residual in-block leak
+    the pages describe for the default token-block scales)."""
+    lengths, hq, hkv, d = [64], 1, 1, 16
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=9)
+    base = _train(q, k, v, do, cu, hq, hkv)
+    v2 = v.copy(); v2[40, 0, 0] *= 2.0 ** 12        # same block as rows 32..63
+    pert = _train(q, k, v2, do, cu, hq, hkv)
+    assert np.array_equal(pert["o"][:32], base["o"][:32])
+    assert not np.array_equal(pert["o"][32:40], base["o"][32:40])
+
+
+def test_floor_rule_leaks_through_clamp_roundup_does_not():
+    """The clamp mechanism of [KO] section 2: with the floor rule, a masked later
+    token in the same block that lifts the amax across 448*2^k un-clips an
+    earlier value; round-up keeps the reconstruction (normal codes)."""
+    T, d = 32, 4
+    v = np.ones((T, 1, d)) * 1.0
+    v[3, 0, 0] = 460.0
+    v2 = v.copy(); v2[20, 0, 1] = 900.0
+    cu = [0, T]
+    f1 = O.dequantize_tokenblock(*O.quantize_tokenblock(v, cu, rule="floor"))
+    f2 = O.dequantize_tokenblock(*O.quantize_tokenblock(v2, cu, rule="floor"))
+    assert f1[3, 0, 0] == 448.0 and f2[3, 0, 0] == 448.0        # clamp, then RNE of 230
+    v[3, 0, 0] = 480.0; v2[3, 0, 0] = 480.0
+    f1 = O.dequantize_tokenblock(*O.quantize_tokenblock(v, cu, rule="floor"))
+    f2 = O.dequantize_tokenblock(*O.quantize_tokenblock(v2, cu, rule="floor"))
+    assert f1[3, 0, 0] == 448.0 and f2[3, 0, 0] == 480.0        # the leak
+    r1 = O.dequantize_tokenblock(*O.quantize_tokenblock(v, cu))
+    r2 = O.dequantize_tokenblock(*O.quantize_tokenblock(v2, cu))
+    assert r1[3, 0, 0] == r2[3, 0, 0] == 480.0
+
+
+def test_documents_are_isolated_and_offset_invariant():
+    """Negative control ([EN] section 10): another document's inputs and a
+    document's physical offset do not change its outputs or gradients."""
+    hq, hkv, d = 2, 1, 16
+    q, k, v, do, cu = _inputs([150, 90], hq, hkv, d, seed=10)
+    base = _train(q, k, v, do, cu, hq, hkv)
+    s = slice(150, 240)
+    q2 = q.copy(); q2[:150] *= 8; k2 = k.copy(); k2[:150] *= 0.25
+    pert = _train(q2, k2, v, do, cu, hq, hkv)
+    for n in ("o", "dq", "dk", "dv"):
+        assert np.array_equal(pert[n][s], base[n][s]), n
+    for shift in (1, 37, 127):
+        rng = np.random.default_rng(shift)
+        pre = lambda h: O.bf16_round(rng.standard_normal((shift, h, d)))
+        qs = np.concatenate([pre(hq), q[s]]); ks = np.concatenate([pre(hkv), k[s]])
+        vs = np.concatenate([pre(hkv), v[s]]); dos = np.concatenate([pre(hq), do[s]])
+        out = _train(qs, ks, vs, dos, [0, shift, shift + 90], hq, hkv)
+        for n in ("o", "dq", "dk", "dv"):
+            assert np.array_equal(out[n][shift:], base[n][s]), (n, shift)
+
+
+def test_dq_boost_definition():
+    rng = np.random.default_rng(12)
+    for _ in range(50):
+        a = rng.standard_normal((20, 8)) * np.exp2(rng.integers(-20, 20))
+        b = rng.standard_normal((20, 8)); c = rng.standard_normal((20, 8))
+        M = 2 * np.linalg.norm(a, axis=1).max() * np.linalg.norm(b, axis=1).max() * np.abs(c).max()
+        boost = O.dq_boost(a, b, c)
+        e = math.log2(boost)
+        assert e == int(e)
+        assert boost * M <= 2 ** 14 < 2 * boost * M
+    assert O.dq_boost(np.zeros((3, 4)), np.ones((3, 4)), np.ones((3, 4))) == 1.0
+
+
+def test_dq_boost_keeps_fp16_partials_in_range():
+    q, k, v, do, cu = _inputs([256], 1, 1, 32, seed=13, scale=20.0)
+    out = O.run_training_call(q, k, v, do, cu, 1, 1)
+    assert np.all(np.isfinite(out["dq"]))
+
+
+# ------------------------------------------------------------ work list
+
+def test_work_list_order_and_alternation():
+    cu = [0, 1000, 1200, 1201, 5000]
+    items = O.work_list(cu, num_ctas=3)
+    costs = [it["cost"] for it in items]
+    assert costs == sorted(costs, reverse=True)
+    # every (doc, query tile) covered exactly once, items <= 256 queries
+    seen = set()
+    for it in items:
+        assert 1 <= it["ntiles"] <= 2
+        for t in range(it["tile0"], it["tile0"] + it["ntiles"]):
+            assert (it["doc"], t) not in seen
+            seen.add((it["doc"], t))
+    want = {(n, t) for n, (s, e) in enumerate(O.doc_ranges(cu)) for t in range(-(-(e - s) // 128))}
+    assert seen == want
+    # cost = visible 128-key tiles summed over the item's query tiles
+    for it in items:
+        assert it["cost"] == sum(t + 1 for t in range(it["tile0"], it["tile0"] + it["ntiles"]))
+    # boustrophedon: 0 1 2 | 2 1 0 | 0 1 2 ...
+    assert [it["cta"] for it in items[:9]] == [0, 1, 2, 2, 1, 0, 0, 1, 2]
+    # ties keep document order
+    first_doc = [it["doc"] for it in items if it["cost"] == items[-1]["cost"]]
+    assert first_doc == sorted(first_doc)
+
+
+def test_bwd_key_tile_list():
+    cu = [0, 300, 301, 700]        # 3, 1 and 4 key tiles
+    items = O.bwd_key_tile_list(cu)
+    got = [(i["doc"], i["ktile"], i["cost"]) for i in items]
+    assert got == [(2, 0, 4), (0, 0, 3), (2, 1, 3), (0, 1, 2), (2, 2, 2),
+                   (0, 2, 1), (1, 0, 1), (2, 3, 1)]
