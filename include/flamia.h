@@ -1,0 +1,189 @@
+/*
+ * flamia.h -- C ABI of the GB300 (sm_103a) FLAMIA attention library.
+ *
+ * Causal flash attention forward + backward for training with microscaled FP8
+ * operands, following "FLAMIA: FLAsh MIcroscaling Attention for Fast and
+ * Causally Safe Training on Blackwell" (arXiv 2611.03344) as described by the
+ * FLAMIA technical review (English, sections 2-7, Algorithms 1 and 2) and the
+ * Korean review (jaehun.me, section 3).
+ *
+ * Conventions for every entry point
+ *  - All tensor arguments are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or retains them, and keeps no global state beyond
+ *    a cached driver entry point.  Every call is asynchronous on `stream`
+ *    (a cudaStream_t passed as void*; NULL = legacy default stream) and never
+ *    synchronises the host, so calls can be captured in a CUDA graph.
+ *  - Packed variable-length batches: `cu_seqlens` (device, int32, num_seqs+1
+ *    entries, cu[0] = 0, non-decreasing, cu[num_seqs] <= total_tokens).
+ *    Document n holds tokens [cu[n], cu[n+1]).  Tokens at or after
+ *    cu[num_seqs] belong to no document: their codes are 0, scale bytes 127,
+ *    outputs and gradients 0 and LSE +inf.  (FLAMIA review section 6,
+ *    "Preserve the logical row before optimizing the physical tile".)
+ *  - Activations are row-major [total_tokens, heads, head_dim], head_dim
+ *    contiguous; bf16 in, bf16 out.  head_dim must be 64 or 128.
+ *  - GQA: hq query heads share hkv key/value heads, hq % hkv == 0; query head
+ *    h reads kv head h / (hq / hkv).
+ *  - Return value: FLAMIA_OK (0) or a negative FLAMIA_ERR_* code; on error
+ *    nothing is launched.  Errors found on the device (malformed cu_seqlens,
+ *    a bounded wait that timed out) set bits in the plan's status word, read
+ *    back with flamia_get_device_status().
+ */
+#ifndef FLAMIA_H_
+#define FLAMIA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ----------------------------------------------------------- status codes */
+#define FLAMIA_OK 0
+#define FLAMIA_ERR_INVALID_ARG (-1)   /* null pointer, negative size, bad count */
+#define FLAMIA_ERR_UNSUPPORTED (-2)   /* head_dim not 64/128, hq % hkv != 0, causal == 0, too many tokens */
+#define FLAMIA_ERR_MISALIGNED (-3)    /* a tensor pointer is not 16-byte aligned */
+#define FLAMIA_ERR_WORKSPACE (-4)     /* workspace / plan buffer too small */
+#define FLAMIA_ERR_CUDA (-5)          /* a CUDA launch or driver call failed */
+
+/* device status bits (plan status word) */
+#define FLAMIA_DEV_BAD_CU_SEQLENS 1   /* cu[0] != 0, decreasing, or cu[N] > total_tokens */
+#define FLAMIA_DEV_TIMEOUT 2          /* a bounded mbarrier wait expired; outputs invalid */
+#define FLAMIA_DEV_CAPACITY 4         /* more work items than the plan was sized for */
+
+/* ----------------------------------------------------------- options */
+typedef struct flamia_options {
+  /* Boost beta = 2^p_boost_log2 applied to forward probabilities before E4M3
+     rounding, with the retained row maximum exact (tau = 0), so beta * 2^tau
+     = 256 <= 448 (FLAMIA review section 5, "A range budget for probability
+     quantization").  Only 8 is supported. */
+  int p_boost_log2;
+  /* Boost of the backward probability operand of dV = P^T dO (same section;
+     the value is stripped on the page, read as 2^8).  Only 8 is supported. */
+  int bwd_p_boost_log2;
+  /* dQ FP16 partial boost target: c = 2^floor(log2(2^headroom / M)) per
+     (document, query head) (FLAMIA review section 4, "Forward locality and
+     backward locality differ").  Default 14. */
+  int dq_headroom_log2;
+  /* Reserved for the strict options and the mixed NVFP4 score path; must be 0. */
+  int strict_per_token;
+  int strict_row_ds;
+  int strict_causal_dq;
+  int mixed_nvfp4;
+  int deterministic;
+} flamia_options;
+
+/* Fill *opt with the defaults above (p_boost_log2 = 8, bwd_p_boost_log2 = 8,
+   dq_headroom_log2 = 14, everything else 0). */
+void flamia_default_options(flamia_options* opt);
+
+/* ----------------------------------------------------------- quantized tensor view */
+typedef struct flamia_qtensor {
+  const void* codes;    /* uint8 E4M3 codes [T, H, head_dim] */
+  const void* scales;   /* uint8 UE8M0 scale bytes [T, H]; value 2^(byte-127),
+                           replicated over the tokens of each document-local
+                           32-token block (dense per-token metadata) */
+  const float* stats;   /* float2 [T, H]: (||x^_t||_2, max_d |x^_td|) of the
+                           reconstructed row, or NULL (required for k and v in
+                           flamia_bwd: the dQ boost reads them) */
+} flamia_qtensor;
+
+/* ----------------------------------------------------------- plan (work list)
+ * Algorithm 2 of the FLAMIA review ("Document-local work list and launch"),
+ * built on the GPU once per microbatch without a host synchronisation:
+ *   - per-document prefix counts of 32-token blocks and 128-token tiles;
+ *   - forward items: up to 2 query tiles (256 queries) of one document, cost =
+ *     visible 128-key tiles summed over the item's query tiles, sorted by
+ *     decreasing cost (ties keep document order, then query order);
+ *   - backward items: one per document-local 128-key tile, cost = number of
+ *     query tiles that see it, sorted the same way.
+ * Layout of the plan buffer (int32 words, all offsets in words):
+ *   [0]  status bits (FLAMIA_DEV_*)         [1]  num_seqs
+ *   [2]  total_tokens                         [3]  valid tokens = cu[num_seqs]
+ *   [4]  number of 32-token blocks            [5]  number of 128-token tiles
+ *   [6]  number of forward items              [7]  number of backward items
+ *   [8]  capacity (items)                     [16 ...] blk_prefix[num_seqs+1]
+ *   then tile_prefix[num_seqs+1], then (16-byte aligned) forward items as
+ *   int4 {doc, first query tile, query tile count, cost} x capacity, then
+ *   backward items as int4 {doc, key tile, cost, 0} x capacity.
+ * Ownership: caller-allocated device memory of flamia_plan_bytes() bytes,
+ * 16-byte aligned; it must stay valid until every call using it completed. */
+size_t flamia_plan_bytes(int64_t total_tokens, int num_seqs);
+int flamia_plan_build(const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, void* plan,
+                      size_t plan_bytes, void* stream);
+
+/* ----------------------------------------------------------- quantizer (a1)
+ * Token-block MXFP8 quantizer (FLAMIA review section 3, "Why one shared
+ * exponent can serve two reductions"; section 4 for the exponent rule; Korean
+ * review sections 3.1-3.2; Algorithm 1 step 03).  For each document, head and
+ * document-local block of 32 consecutive tokens (per_token != 0: of 1 token,
+ * the strict option of review section 4):
+ *   amax = max |x| over the block x head_dim,
+ *   e    = smallest integer with amax <= 448 * 2^e (0 for an all-zero block),
+ *          clamped to [-127, 127],
+ *   code = E4M3(x * 2^-e), round to nearest even, saturating,
+ *   scale byte = e + 127, written for every token of the block.
+ * x: bf16 [T, heads, head_dim] (device).  codes: uint8 [T, heads, head_dim];
+ * scales: uint8 [T, heads]; stats: float2 [T, heads] (||x^_t||_2, max |x^_t|)
+ * or NULL.  `plan` must have been built from the same cu_seqlens.  Codes and
+ * scale bytes are bit-exact with the oracle.  Non-finite inputs are not
+ * supported (their codes are unspecified). */
+int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int heads, int head_dim,
+                               const int32_t* cu_seqlens, int num_seqs, const void* plan, int per_token,
+                               void* codes_e4m3, void* scales_ue8m0, float* stats, void* stream);
+
+/* ----------------------------------------------------------- forward (a4-a6)
+ * Algorithm 1 steps 04-08 of the FLAMIA review.  For each document, query
+ * head and document-local 128-query tile, over the visible document-local
+ * 128-key tiles in increasing order:
+ *   S   = (scale * s_Q(i) * s_K(j)) * sum_d c_Q[i,d] c_K[j,d]   (E4M3 MMA
+ *         without block scales; row/column factors applied afterwards --
+ *         review section 3, "Factoring the scales out of the score MMA"),
+ *         keys after the query masked,
+ *   m   = running row max (exact), p = exp(S - m), l = running sum of p,
+ *   P^  = E4M3(2^8 p), O += P^ V^ / 2^8 (MXFP8 block-scaled MMA, V's token-
+ *         block scale per 32 keys),
+ * then O = bf16(O / l) and LSE = m + ln l (natural log).
+ * q, k, v: quantized views (stats unused here).  out: bf16 [T, hq, head_dim];
+ * lse: float [hq, T].  causal must be 1.  softmax_scale <= 0 selects
+ * 1/sqrt(head_dim).  opt may be NULL (defaults). */
+int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v,
+               const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim,
+               int causal, float softmax_scale, const flamia_options* opt, const void* plan, void* out_bf16,
+               float* lse, void* stream);
+
+/* ----------------------------------------------------------- backward (a7-a12)
+ * Algorithm 1 steps 09-16 of the FLAMIA review:
+ *   dO^ = token-block E4M3 encoding of dO (encoded once), D_i = dO^_i . O_i
+ *   (saved bf16 O; Korean review section 3.3), dQ boost c per (document,
+ *   query head) = 2^floor(log2(2^14 / M)) with M = 2 max||dO^_i|| max||V^_j||
+ *   max|K^_jd|; then per document-local key tile and every query tile that
+ *   sees it: S recomputed exactly as the forward, P = exp(S - LSE),
+ *   dP = dO^ V^T, dS = P o (dP - D), dS^ = E4M3 with one round-up exponent per
+ *   document-local 32x32 block, dV += (E4M3(2^8 P)/2^8)^T dO^,
+ *   dK += dS^^T Q^, dQ partial = fp16(c * dS^ K^) reduce-added into an fp16
+ *   accumulator; finally dQ = bf16(scale * acc / c), dK = bf16(scale * dK),
+ *   dV = bf16(dV).
+ * k and v need stats (from flamia_quantize_tokenblock).  out/lse: the
+ * forward's outputs; dout: bf16 [T, hq, head_dim].  dq: bf16 [T, hq, head_dim];
+ * dk, dv: bf16 [T, hkv, head_dim].  workspace: device scratch of at least
+ * flamia_bwd_workspace_bytes() bytes, 256-byte aligned, owned by the caller
+ * (holds the dO codes, scales and stats, D, the boosts and the fp16 dQ
+ * accumulator; contents on return are unspecified). */
+size_t flamia_bwd_workspace_bytes(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim);
+int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v, const void* out_bf16,
+               const float* lse, const void* dout_bf16, const int32_t* cu_seqlens, int num_seqs,
+               int64_t total_tokens, int hq, int hkv, int head_dim, int causal, float softmax_scale,
+               const flamia_options* opt, const void* plan, void* dq_bf16, void* dk_bf16, void* dv_bf16,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------- status */
+/* Copy the plan's device status word into *status_out (synchronises `stream`). */
+int flamia_get_device_status(const void* plan, int* status_out, void* stream);
+/* Static string for a FLAMIA_OK / FLAMIA_ERR_* code. */
+const char* flamia_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLAMIA_H_ */

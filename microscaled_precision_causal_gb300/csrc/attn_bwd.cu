@@ -1,0 +1,563 @@
+// FLAMIA backward attention (steps a8-a12 of the hot path) plus the dQ boost
+// and dQ finalisation kernels.
+//
+// FLAMIA technical review, Algorithm 1 steps 10-16 (and section 7, "Softmax
+// and TMEM resources": token scales are applied by the compute warps after the
+// feature-axis MMAs, so dP needs no TMEM scale operands):
+//   S^T  = K Q^T            (unscaled E4M3 MMA, factors s_K(j) s_Q(i) scale after)
+//   P    = 2^(x - LSE*log2 e)      (exactly the forward's tiles and masks)
+//   dP^T = V dO^T           (unscaled E4M3 MMA, factors s_V(j) s_dO(i) after)
+//   dS   = P o (dP - D)
+//   dS^  = E4M3 with one round-up exponent per document-local 32x32 block
+//          (section 3: the 32x32 square serves both contraction axes)
+//   dV  += E4M3(2^8 P)^T dO^ / 2^8     (MXF8, dO's scale per 32 queries)
+//   dK  += dS^^T Q^                    (MXF8, dS block and Q scales per 32 queries)
+//   dQp  = dS^ K^                      (MXF8, same dS codes read transposed)
+//   dQacc += fp16(c * dQp)             (section 4, boosted FP16 partials)
+//
+// One CTA per (document-local 128-key tile, kv head); it visits every query
+// head of the kv head's group and every query tile at or after the key tile.
+// Roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
+// allocator, warps 4-7 compute (thread = key row for S/dP, = query row for dQ).
+// TMEM: S^T / dQ partial [0,128), dP^T [128,256) whose first 24 columns carry
+// the block-scale words of the three MXF8 MMAs once dP^T has been read, dV
+// [256, 256+D), dK [384, 384+D).
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace flamia {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kQStages = 2;
+
+struct BwdParams {
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  const uint8_t* do_scales;
+  const float* lse;        // [hq, T]
+  const float* dvec;       // [hq, T]
+  const float* boost;      // [N, hq]
+  const int32_t* cu;
+  const int* plan;
+  int N, T, hq, hkv;
+  float scale_log2;        // softmax scale * log2(e)
+  float scale;
+  __half* dq_acc;          // [T, hq, D]
+  __nv_bfloat16* dk;       // [T, hkv, D]
+  __nv_bfloat16* dv;
+};
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kTileBytes = kTile * D;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;                  // [kQStages]
+  static constexpr int kDO = kQ + kQStages * kTileBytes;      // [kQStages]
+  static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query]
+  static constexpr int kDS = kPt + kTile * kTile;             // dS^ codes, [key][query]
+  static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
+  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // lse2, D, chunk scales
+  static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents
+  static constexpr int kBar = kE + 64;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void red_add_f16x8(__half* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qd_full = bars + 1;              // [kQStages]
+  uint64_t* qd_empty = bars + 1 + kQStages;  // [kQStages]
+  uint64_t* s_full = bars + 1 + 2 * kQStages;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* dq_full = s_full + 2;
+  uint64_t* dq_empty = s_full + 3;
+  uint64_t* acc_full = s_full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 5);
+  int* status = const_cast<int*>(p.plan) + kPlanStatus;
+
+  const int n_items = p.plan[kPlanBwdItems];
+  const int item_idx = blockIdx.x / p.hkv;
+  const int hk = blockIdx.x % p.hkv;
+  if (item_idx >= n_items) return;
+  const PlanView pv = plan_view(p.plan, p.T, p.N);
+  const int4 item = pv.bwd_items[item_idx];
+  const int doc = item.x, u = item.y;
+  const int doc_start = p.cu[doc];
+  const int doc_len = p.cu[doc + 1] - doc_start;
+  const int nt = (doc_len + kTile - 1) / kTile;
+  const int g = p.hq / p.hkv;
+  const int qtiles = nt - u;
+  const int nsteps = g * qtiles;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&qd_full[i], 1);
+      mbar_init(&qd_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(acc_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  constexpr uint32_t kS = 0, kP = 128, kDV = 256, kDK = 384;
+  constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
+  constexpr uint32_t kAtom = 8 * D;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes);
+      tma_load_3d(smem + L::kK, &tm_k, kv_full, 0, hk, doc_start + u * kTile);
+      tma_load_3d(smem + L::kV, &tm_v, kv_full, 0, hk, doc_start + u * kTile);
+      for (int k = 0; k < nsteps; ++k) {
+        const int st = k % kQStages;
+        if (k >= kQStages && !mbar_wait(&qd_empty[st], ((k / kQStages) - 1) & 1, status)) break;
+        const int h = hk * g + k / qtiles, t = u + k % qtiles;
+        mbar_arrive_expect_tx(&qd_full[st], 2 * L::kTileBytes);
+        tma_load_3d(smem + L::kQ + st * L::kTileBytes, &tm_q, &qd_full[st], 0, h, doc_start + t * kTile);
+        tma_load_3d(smem + L::kDO + st * L::kTileBytes, &tm_do, &qd_full[st], 0, h, doc_start + t * kTile);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sk = smem_u32(smem + L::kK), sv = smem_u32(smem + L::kV), sq = smem_u32(smem + L::kQ),
+                     sdo = smem_u32(smem + L::kDO), spt = smem_u32(smem + L::kPt), sds = smem_u32(smem + L::kDS);
+      auto issue_sp = [&](int st, bool do_s, bool do_p) {
+        const uint32_t qa = sq + st * L::kTileBytes, da = sdo + st * L::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < D / 32; ++s) {
+          if (do_p)
+            mma_f8(tbase + kP, smem_desc(sv + 32 * s, 16, kAtom, kLayout), smem_desc(da + 32 * s, 16, kAtom, kLayout),
+                   idesc_f8(128, 128, 0, 0), s > 0);
+          if (do_s)
+            mma_f8(tbase + kS, smem_desc(sk + 32 * s, 16, kAtom, kLayout), smem_desc(qa + 32 * s, 16, kAtom, kLayout),
+                   idesc_f8(128, 128, 0, 0), s > 0);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, status) && mbar_wait(&qd_full[0], 0, status);
+      if (ok) {
+        tc_fence_after();
+        issue_sp(0, true, true);
+        mma_commit(s_full);
+      }
+      for (int k = 0; k < nsteps && ok; ++k) {
+        const int st = k % kQStages;
+        ok = mbar_wait(p_full, k & 1, status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qa = sq + st * L::kTileBytes, da = sdo + st * L::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
+          mma_mxf8(tbase + kDV, smem_desc(spt + 32 * s, 16, 1024, kSwizzle128B),
+                   smem_desc(da + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
+                   tbase + kP + 0, tbase + kP + 4, (k > 0 || s > 0));
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          // dK += dS^^T Q
+          mma_mxf8(tbase + kDK, smem_desc(sds + 32 * s, 16, 1024, kSwizzle128B),
+                   smem_desc(qa + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
+                   tbase + kP + 8, tbase + kP + 12, (k > 0 || s > 0));
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          // dQp = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major)
+          mma_mxf8(tbase + kS, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
+                   smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
+                   tbase + kP + 16, tbase + kP + 20, s > 0);
+        }
+        mma_commit(dq_full);
+        mma_commit(&qd_empty[st]);
+        if (k + 1 < nsteps) {
+          const int st1 = (k + 1) % kQStages;
+          ok = mbar_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sp(st1, false, true);
+          ok = mbar_wait(dq_empty, k & 1, status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sp(st1, true, false);
+          mma_commit(s_full);
+        }
+      }
+      mma_commit(acc_full);
+      if (!ok) mbar_wait(acc_full, 0, status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute
+    const int quarter = warp & 3;
+    const int j = quarter * 32 + lane;                 // key row (TMEM lane) during S/dP
+    const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+    const bool key_valid = u * kTile + j < doc_len;
+    const int64_t ktok = (int64_t)doc_start + u * kTile + j;
+    const float sk_row = key_valid ? ue8m0_to_f32(p.k_scales[ktok * p.hkv + hk]) : 1.0f;
+    const float sv_row = key_valid ? ue8m0_to_f32(p.v_scales[ktok * p.hkv + hk]) : 1.0f;
+    uint32_t ksf = 0;   // K block scales per 32-key group (dQ MMA, B operand)
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+      const int kl = u * kTile + gg * 32;
+      const uint32_t b = kl < doc_len ? p.k_scales[((int64_t)doc_start + kl) * p.hkv + hk] : 127u;
+      ksf |= b << (8 * gg);
+    }
+    float* rowbuf = reinterpret_cast<float*>(smem + L::kRow);
+    uint32_t* Esm = reinterpret_cast<uint32_t*>(smem + L::kE);
+    uint8_t* sPt = smem + L::kPt;
+    uint8_t* sDS = smem + L::kDS;
+    bool ok = true;
+    for (int k = 0; k < nsteps; ++k) {
+      const int hh = k / qtiles, t = u + k % qtiles;
+      const int h = hk * g + hh;
+      const bool diag = (t == u);
+      // per-query data of this step (thread index = query row)
+      float* rb = rowbuf + (k & 1) * (L::kRowBuf / 4);
+      {
+        const int ql = t * kTile + j;
+        const bool qv = ql < doc_len;
+        const int64_t qtok = (int64_t)doc_start + ql;
+        rb[j] = qv ? p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : INFINITY;
+        rb[128 + j] = qv ? p.dvec[(int64_t)h * p.T + qtok] : 0.f;
+        if ((j & 31) == 0) {
+          uint8_t* cs = reinterpret_cast<uint8_t*>(rb + 256);
+          cs[j >> 5] = qv ? p.q_scales[qtok * p.hq + h] : 127;
+          cs[4 + (j >> 5)] = qv ? p.do_scales[qtok * p.hq + h] : 127;
+        }
+      }
+      ok = named_bar_and(1, 128, ok);
+      if (!ok) break;
+      const uint8_t* cs = reinterpret_cast<const uint8_t*>(rb + 256);
+      ok = named_bar_and(1, 128, mbar_wait(s_full, k & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t vs[32], vp[32];
+        tmem_ld32(lane_base + kS + 32 * c, vs);
+        tmem_ld32(lane_base + kP + 32 * c, vp);
+        tmem_ld_wait();
+        const float fS = p.scale_log2 * sk_row * ue8m0_to_f32(cs[c]);
+        const float fP = sv_row * ue8m0_to_f32(cs[4 + c]);
+        float ds[32];
+        uint32_t pk[8];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float pp[2];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int il = 32 * c + i + q;            // query row within the tile
+            const bool vis = !diag || il >= j;
+            const float pr = vis ? fast_exp2(fmaf(__uint_as_float(vs[i + q]), fS, -rb[il])) : 0.f;
+            const float dpv = __uint_as_float(vp[i + q]) * fP;
+            ds[i + q] = pr * (dpv - rb[128 + il]);
+            amax = fmaxf(amax, fabsf(ds[i + q]));
+            pp[q] = pr * 256.0f;
+          }
+          const uint32_t c2 = e4m3x2(pp[0], pp[1]);
+          if ((i & 2) == 0) pk[i >> 2] = c2; else pk[i >> 2] |= c2 << 16;
+        }
+        *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+        const int e = roundup_exp(amax);
+        const float sc = exp2i(-e);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          pk[i >> 2] = (uint32_t)e4m3x2(ds[i] * sc, ds[i + 1] * sc) | ((uint32_t)e4m3x2(ds[i + 2] * sc, ds[i + 3] * sc) << 16);
+        }
+        *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        if (lane == 0) reinterpret_cast<uint8_t*>(Esm)[quarter * 4 + c] = (uint8_t)(e + 127);
+      }
+      named_bar_sync(1, 128);
+      {
+        const uint8_t* E = reinterpret_cast<const uint8_t*>(Esm);   // E[key block][query chunk]
+        const uint32_t dosf = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
+        const uint32_t qsf = (uint32_t)cs[0] | (uint32_t)cs[1] << 8 | (uint32_t)cs[2] << 16 | (uint32_t)cs[3] << 24;
+        uint32_t dk_a[4], dq_a[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          // dK: A row = key in block cc, byte = query chunk; dQ: A row = query in chunk cc, byte = key block
+          dk_a[cc] = (uint32_t)E[cc * 4 + 0] | (uint32_t)E[cc * 4 + 1] << 8 | (uint32_t)E[cc * 4 + 2] << 16 |
+                     (uint32_t)E[cc * 4 + 3] << 24;
+          dq_a[cc] = (uint32_t)E[0 * 4 + cc] | (uint32_t)E[1 * 4 + cc] << 8 | (uint32_t)E[2 * 4 + cc] << 16 |
+                     (uint32_t)E[3 * 4 + cc] << 24;
+        }
+        tmem_st4(lane_base + kP + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_st4(lane_base + kP + 4, dosf, dosf, dosf, dosf);
+        tmem_st4(lane_base + kP + 8, dk_a[0], dk_a[1], dk_a[2], dk_a[3]);
+        tmem_st4(lane_base + kP + 12, qsf, qsf, qsf, qsf);
+        tmem_st4(lane_base + kP + 16, dq_a[0], dq_a[1], dq_a[2], dq_a[3]);
+        tmem_st4(lane_base + kP + 20, ksf, ksf, ksf, ksf);
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      // dQ partial of this step: thread index = query row
+      ok = named_bar_and(1, 128, mbar_wait(dq_full, k & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const int ql = t * kTile + j;
+        const bool qv = ql < doc_len;
+        const float cb = qv ? p.boost[(int64_t)doc * p.hq + h] : 0.f;
+        __half* dst = p.dq_acc + (((int64_t)doc_start + ql) * p.hq + h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + kS + 32 * c, v);
+          tmem_ld_wait();
+          if (qv) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint32_t hw[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                __half2 h2 = __floats2half2_rn(__uint_as_float(v[i + 2 * q]) * cb, __uint_as_float(v[i + 2 * q + 1]) * cb);
+                hw[q] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              red_add_f16x8(dst + 32 * c + i, hw[0], hw[1], hw[2], hw[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+    }
+    if (ok) ok = named_bar_and(1, 128, mbar_wait(acc_full, 0, status));
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? kDV : kDK;
+        const float mul = which == 0 ? (1.0f / 256.0f) : p.scale;
+        __nv_bfloat16* orow = (which == 0 ? p.dv : p.dk) + (ktok * p.hkv + hk) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + col + 32 * c, v);
+          tmem_ld_wait();
+          if (key_valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]) * mul, __uint_as_float(v[2 * q + 1]) * mul);
+              pk[q] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// dQ boost per (document, query head): c = 2^floor(log2(2^headroom / M)),
+// M = 2 max_i ||dO^_i|| max_j ||V^_j|| max_jd |K^_jd| over the document
+// (FLAMIA review section 4, "Forward locality and backward locality differ").
+__global__ void boost_kernel(const int32_t* cu, const int* plan, const float2* st_do, const float2* st_k,
+                             const float2* st_v, int hq, int hkv, int headroom, float* boost) {
+  const int doc = blockIdx.x, h = blockIdx.y;
+  const int hk = h / (hq / hkv);
+  if (plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS) return;
+  const int s0 = cu[doc], s1 = cu[doc + 1];
+  float a = 0.f, b = 0.f, c = 0.f;
+  for (int t = s0 + threadIdx.x; t < s1; t += blockDim.x) {
+    a = fmaxf(a, st_do[(int64_t)t * hq + h].x);
+    b = fmaxf(b, st_v[(int64_t)t * hkv + hk].x);
+    c = fmaxf(c, st_k[(int64_t)t * hkv + hk].y);
+  }
+  __shared__ float red[3][32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red[0][w] = a;
+    red[1][w] = b;
+    red[2][w] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) {
+      a = fmaxf(a, red[0][i]);
+      b = fmaxf(b, red[1][i]);
+      c = fmaxf(c, red[2][i]);
+    }
+    const double M = 2.0 * (double)a * (double)b * (double)c;
+    double cb = 1.0;
+    if (M > 0.0 && M < 1e300) {
+      const double target = ldexp(1.0, headroom);
+      int e = (int)floor(log2(target / M));
+      while (ldexp(M, e) > target) --e;
+      while (ldexp(M, e + 1) <= target) ++e;
+      e = e < -100 ? -100 : (e > 100 ? 100 : e);
+      cb = ldexp(1.0, e);
+    }
+    boost[(int64_t)doc * hq + h] = (float)cb;
+  }
+}
+
+// dQ = bf16(scale * acc / c) per row; rows outside every document and the dK /
+// dV rows outside every document are zeroed.
+template <int D>
+__global__ void dq_finalize_kernel(const __half* acc, const int32_t* cu, const int* plan, const float* boost, int N,
+                                   int T, int hq, int hkv, float scale, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                                   __nv_bfloat16* dv) {
+  const int valid = plan[kPlanValid];
+  const bool bad = plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS;
+  constexpr int kVec = 8;
+  const int64_t nvec = (int64_t)T * hq * (D / kVec);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t rowh = i / (D / kVec);
+    const int64_t row = rowh / hq;
+    const int h = (int)(rowh % hq);
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (!bad && row < valid) {
+      int lo = 0, hi = N;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= row) lo = mid; else hi = mid;
+      }
+      const float mul = scale / boost[(int64_t)lo * hq + h];
+      const uint4 in = reinterpret_cast<const uint4*>(acc)[i];
+      const __half2* hv = reinterpret_cast<const __half2*>(&in);
+      uint32_t* ov = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(hv[q]);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * mul, f.y * mul);
+        ov[q] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+    }
+    reinterpret_cast<uint4*>(dq)[i] = out;
+  }
+  // dK / dV rows outside every document
+  const int64_t tail = (int64_t)(T - (bad ? 0 : valid)) * hkv * (D / kVec);
+  const int64_t base = (int64_t)(bad ? 0 : valid) * hkv * (D / kVec);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < tail; i += (int64_t)gridDim.x * blockDim.x) {
+    reinterpret_cast<uint4*>(dk)[base + i] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(dv)[base + i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
+                         const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
+                         const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
+                         const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
+      !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
+      !make_tmap_u8_3d(&tv, vc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
+      !make_tmap_u8_3d(&tdo, doc_codes, D, hq, T, D, (uint64_t)hq * D, D, kTile))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.q_scales = static_cast<const uint8_t*>(qs);
+  p.k_scales = static_cast<const uint8_t*>(ks);
+  p.v_scales = static_cast<const uint8_t*>(vs);
+  p.do_scales = static_cast<const uint8_t*>(dos);
+  p.lse = lse;
+  p.dvec = dvec;
+  p.boost = boost;
+  p.cu = cu;
+  p.plan = static_cast<const int*>(plan);
+  p.N = N;
+  p.T = T;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.dq_acc = static_cast<__half*>(dq_acc);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  const int64_t max_items = (int64_t)T / kTile + N + 1;
+  const int64_t grid = max_items * hkv;
+  if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  constexpr int smem = BwdSmem<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_bwd_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dq_finalize_kernel<D><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
+                                                     hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float* st_do, const float* st_k,
+                         const float* st_v, int hq, int hkv, int headroom, float* boost, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  boost_kernel<<<dim3(N, hq), 256, 0, s>>>(cu, static_cast<const int*>(plan), reinterpret_cast<const float2*>(st_do),
+                                           reinterpret_cast<const float2*>(st_k), reinterpret_cast<const float2*>(st_v),
+                                           hq, hkv, headroom, boost);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
+                       const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
+                       const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
+                       const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream) {
+  if (D == 128)
+    return launch_bwd_d<128>(qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan,
+                             dq_acc, dq, dk, dv, stream);
+  if (D == 64)
+    return launch_bwd_d<64>(qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan,
+                            dq_acc, dq, dk, dv, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace flamia

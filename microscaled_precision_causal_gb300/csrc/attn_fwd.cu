@@ -1,0 +1,396 @@
+// FLAMIA forward attention (steps a4-a6 of the hot path): causal, packed
+// documents, MXFP8 token-block operands, tcgen05 MMAs with TMEM accumulators.
+//
+// FLAMIA technical review, Algorithm 1 steps 04-08:
+//   S   = (scale * s_Q(i) * s_K(j)) * sum_d c_Q[i,d] c_K[j,d]
+//         (section 3, "Factoring the scales out of the score MMA": an E4M3 MMA
+//         without block scales, the row/column factors applied afterwards),
+//   running row max (exact), p = 2^(x - m), l = sum p (unrounded),
+//   P^  = E4M3(2^8 p) (section 5, "A range budget for probability quantization"),
+//   O  += P^ V^ with V's token-block scale per 32 keys (MXF8 block-scaled MMA),
+//   O   = bf16(O / l), LSE = m + ln l.
+//
+// One CTA per (work item, query head): a work item is up to two document-local
+// 128-query tiles (Algorithm 2 step 03).  Roles (384 threads):
+//   warp 0      TMA producer: both Q tiles once, then K/V tiles through a ring
+//   warp 1      MMA issuer (one thread): S_w = Q_w K^T and O_w += P^_w V
+//   warp 2      TMEM allocator
+//   warps 4-7   softmax warpgroup 0 (query tile t0), thread = query row
+//   warps 8-11  softmax warpgroup 1 (query tile t0 + 1)
+// The two softmax warpgroups ping-pong: while one converts its score tile the
+// tensor core runs the other's PV and next QK^T.
+// TMEM columns: S_0 [0,128), O_0 [128,128+D), S_1 [256,384), O_1 [384,384+D).
+// The block-scale words of the PV MMA live in the last 8 columns of the
+// warpgroup's S region (written after S was read; the next S MMA is issued
+// after the PV MMA by the same thread, and tcgen05 MMAs run in issue order).
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace flamia {
+
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kThreads = 384;
+
+struct FwdParams {
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  const int32_t* cu;
+  const int* plan;
+  int N, T, hq, hkv;
+  float scale_log2;          // softmax scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTileBytes = kTile * D;          // one Q / K / V code tile
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kP = kV + kStages * kTileBytes;
+  static constexpr int kBar = kP + 2 * kTile * kTile;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;           // slack for 1024-byte alignment
+};
+
+__device__ __forceinline__ float scale_of(const uint8_t* s, int64_t tok, int H, int h, bool valid) {
+  return valid ? ue8m0_to_f32(s[tok * H + h]) : 1.0f;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;                 // [kStages]
+  uint64_t* kv_empty = bars + 1 + kStages;      // [kStages]
+  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2]
+  uint64_t* p_full = s_full + 2;                // [2]
+  uint64_t* o_full = p_full + 2;                // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 2);
+  int* status = const_cast<int*>(p.plan) + kPlanStatus;
+
+  const int n_items = p.plan[kPlanFwdItems];
+  const int item_idx = blockIdx.x / p.hq;
+  const int h = blockIdx.x % p.hq;
+  if (item_idx >= n_items) return;
+  const PlanView pv = plan_view(p.plan, p.T, p.N);
+  const int4 item = pv.fwd_items[item_idx];
+  const int doc = item.x, t0 = item.y, ntq = item.z;
+  const int doc_start = p.cu[doc];
+  const int doc_len = p.cu[doc + 1] - doc_start;
+  const int hk = h / (p.hq / p.hkv);
+  const int nk_w[2] = {t0 + 1, ntq > 1 ? t0 + 2 : 0};
+  const int nkv = ntq > 1 ? t0 + 2 : t0 + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&s_full[w], 1);
+      mbar_init(&p_full[w], 128);
+      mbar_init(&o_full[w], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  constexpr uint32_t kSCol[2] = {0, 256};
+  constexpr uint32_t kOCol[2] = {128, 384};
+  constexpr uint32_t kRowBytes = D;                 // K-major row of a Q/K/V tile
+  constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
+  constexpr uint32_t kAtom = 8 * D;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(q_full, ntq * L::kTileBytes);
+      for (int w = 0; w < ntq; ++w)
+        tma_load_3d(smem + L::kQ + w * L::kTileBytes, &tm_q, q_full, 0, h, doc_start + (t0 + w) * kTile);
+      for (int u = 0; u < nkv; ++u) {
+        const int st = u % kStages;
+        if (u >= kStages && !mbar_wait(&kv_empty[st], ((u / kStages) - 1) & 1, status)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTileBytes);
+        tma_load_3d(smem + L::kK + st * L::kTileBytes, &tm_k, &kv_full[st], 0, hk, doc_start + u * kTile);
+        tma_load_3d(smem + L::kV + st * L::kTileBytes, &tm_v, &kv_full[st], 0, hk, doc_start + u * kTile);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, status);
+      const uint32_t sq = smem_u32(smem + L::kQ), sk = smem_u32(smem + L::kK), sv = smem_u32(smem + L::kV),
+                     sp = smem_u32(smem + L::kP);
+      auto issue_s = [&](int w, int u) {
+        const int st = u % kStages;
+        const uint32_t qa = sq + w * L::kTileBytes, ka = sk + st * L::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < D / 32; ++s) {
+          mma_f8(tbase + kSCol[w], smem_desc(qa + 32 * s, 16, kAtom, kLayout),
+                 smem_desc(ka + 32 * s, 16, kAtom, kLayout), idesc_f8(128, 128, 0, 0), s > 0);
+        }
+      };
+      auto issue_pv = [&](int w, int u) {
+        const int st = u % kStages;
+        const uint32_t pa = sp + w * kTile * kTile, va = sv + st * L::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          mma_mxf8(tbase + kOCol[w], smem_desc(pa + 32 * s, 16, 1024, kSwizzle128B),
+                   smem_desc(va + s * 32 * kRowBytes, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
+                   tbase + kSCol[w] + 120, tbase + kSCol[w] + 124, (u > 0 || s > 0));
+        }
+      };
+      if (ok) ok = mbar_wait(&kv_full[0], 0, status);
+      if (ok) {
+        tc_fence_after();
+        for (int w = 0; w < ntq; ++w) {
+          issue_s(w, 0);
+          mma_commit(&s_full[w]);
+        }
+        for (int u = 0; u < nkv && ok; ++u) {
+          bool next_loaded = false;
+          for (int w = 0; w < ntq && ok; ++w) {
+            if (u >= nk_w[w]) continue;
+            ok = mbar_wait(&p_full[w], u & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(w, u);
+            if (u + 1 < nk_w[w]) {
+              if (!next_loaded) {
+                const int st = (u + 1) % kStages;
+                ok = mbar_wait(&kv_full[st], ((u + 1) / kStages) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                next_loaded = true;
+              }
+              issue_s(w, u + 1);
+              mma_commit(&s_full[w]);
+            } else {
+              mma_commit(&o_full[w]);
+            }
+          }
+          mma_commit(&kv_empty[u % kStages]);
+        }
+      }
+      if (!ok) {
+        // timed out: make sure nothing we issued is still running before TMEM is freed
+        mma_commit(&o_full[0]);
+        mbar_wait(&o_full[0], 0, status);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int w = (warp - 4) >> 2;        // warpgroup = query tile t0 + w
+    if (w < ntq) {
+      const int quarter = warp & 3;
+      const int r = quarter * 32 + lane;  // row within the tile (= TMEM lane)
+      const int t = t0 + w;
+      const int qrow_local = t * kTile + r;
+      const bool row_valid = qrow_local < doc_len;
+      const int64_t tok = (int64_t)doc_start + qrow_local;
+      const float fq = p.scale_log2 * scale_of(p.q_scales, tok, p.hq, h, row_valid);
+      const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t s_addr = lane_base + kSCol[w], o_addr = lane_base + kOCol[w];
+      uint8_t* sP = smem + L::kP + w * kTile * kTile;
+      float m = -INFINITY, lsum = 0.f;
+      bool ok = true;
+      const int nk = nk_w[w];
+      for (int u = 0; u < nk; ++u) {
+        // key-tile column factors and V block scales (one per 32-key group)
+        float fk[4];
+        uint32_t vsf = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int kl = u * kTile + g * 32;
+          const bool kv = kl < doc_len;
+          const int64_t ktok = (int64_t)doc_start + kl;
+          fk[g] = fq * scale_of(p.k_scales, ktok, p.hkv, hk, kv);
+          const uint32_t vb = kv ? p.v_scales[ktok * p.hkv + hk] : 127u;
+          vsf |= vb << (8 * g);
+        }
+        const bool diag = (u == t);
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], u & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        // pass 1: row max of x = S * log2(e) over visible keys
+        float mx = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t v[32];
+          tmem_ld32(s_addr + 32 * g, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = __uint_as_float(v[j]) * fk[g];
+            const bool vis = !diag || (g * 32 + j) <= r;
+            mx = vis ? fmaxf(mx, x) : mx;
+          }
+        }
+        const float m_new = fmaxf(m, mx);
+        const float alpha = fast_exp2(m - m_new);   // 0 on the first tile
+        // rescale the running O row when the max moved (warp-uniform decision)
+        if (u > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(o_addr + 32 * c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            tmem_st32(o_addr + 32 * c, v);
+          }
+          tmem_st_wait();
+        }
+        lsum *= alpha;
+        // pass 2: boosted weights 2^(x - m + 8), their E4M3 codes into the P tile
+        const float neg = 8.0f - m_new;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t v[32];
+          tmem_ld32(s_addr + 32 * g, v);
+          tmem_ld_wait();
+          uint32_t packed[8];
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float pw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const bool vis = !diag || (g * 32 + j + q) <= r;
+              pw[q] = vis ? fast_exp2(fmaf(__uint_as_float(v[j + q]), fk[g], neg)) : 0.f;
+              lsum += pw[q];
+            }
+            packed[j >> 2] = (uint32_t)e4m3x2(pw[0], pw[1]) | ((uint32_t)e4m3x2(pw[2], pw[3]) << 16);
+          }
+          *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g, 128)) =
+              make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g + 16, 128)) =
+              make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+        m = m_new;
+        // block-scale words of the PV MMA: P^ scale 1.0, V scale per 32-key group
+        tmem_st4(s_addr + 120, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_st4(s_addr + 124, vsf, vsf, vsf, vsf);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[w]);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[w], 0, status));
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.0f / lsum;
+        __nv_bfloat16* orow = p.out + (tok * p.hq + h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(o_addr + 32 * c, v);
+          tmem_ld_wait();
+          if (row_valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]) * inv,
+                                                        __uint_as_float(v[2 * j + 1]) * inv);
+              pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+        }
+        if (row_valid) p.lse[(int64_t)h * p.T + tok] = (m + __log2f(lsum) - 8.0f) * 0.69314718055994531f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// Rows outside every document: O = 0, LSE = +inf.
+template <int D>
+__global__ void fwd_tail_kernel(const int* plan, int T, int hq, __nv_bfloat16* out, float* lse) {
+  const int valid = plan[kPlanValid];
+  const int64_t n = (int64_t)(T - valid) * hq;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = valid + i / hq;
+    const int h = (int)(i % hq);
+    uint4* dst = reinterpret_cast<uint4*>(out + (row * hq + h) * D);
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) dst[j] = make_uint4(0, 0, 0, 0);
+    lse[(int64_t)h * T + row] = INFINITY;
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
+                         const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
+                         const void* plan, void* out, float* lse, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
+      !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
+      !make_tmap_u8_3d(&tv, vc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  p.q_scales = static_cast<const uint8_t*>(qs);
+  p.k_scales = static_cast<const uint8_t*>(ks);
+  p.v_scales = static_cast<const uint8_t*>(vs);
+  p.cu = cu;
+  p.plan = static_cast<const int*>(plan);
+  p.N = N;
+  p.T = T;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  const int64_t max_items = (int64_t)T / (kTile * kItemTiles) + N + 1;
+  const int64_t grid = max_items * hq;
+  if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  constexpr int smem = FwdSmem<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fwd_tail_kernel<D><<<152, 256, 0, stream>>>(static_cast<const int*>(plan), T, hq, static_cast<__nv_bfloat16*>(out),
+                                              lse);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
+                       const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
+                       const void* plan, void* out, float* lse, cudaStream_t stream) {
+  if (D == 128) return launch_fwd_d<128>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream);
+  if (D == 64) return launch_fwd_d<64>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace flamia

@@ -1,0 +1,122 @@
+// Shared definitions of the FLAMIA CUDA library: plan layout accessors and
+// small device helpers used by several kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/flamia.h"
+
+namespace flamia {
+
+constexpr int kTile = 128;        // query / key tile (document-local rows)
+constexpr int kBlock = 32;        // operand token block
+constexpr int kItemTiles = 2;     // forward work item: up to 2 query tiles (256 queries)
+
+// ---------------------------------------------------------------- plan layout
+// int32 words; see include/flamia.h for the documented layout.
+enum PlanWord : int {
+  kPlanStatus = 0,
+  kPlanNumSeqs = 1,
+  kPlanTotal = 2,
+  kPlanValid = 3,
+  kPlanBlocks = 4,
+  kPlanTiles = 5,
+  kPlanFwdItems = 6,
+  kPlanBwdItems = 7,
+  kPlanCapacity = 8,
+  kPlanHeaderWords = 16,
+};
+
+struct PlanView {
+  int* hdr;
+  const int* blk_prefix;    // [N+1] cumulative ceil(L/32)
+  const int* tile_prefix;   // [N+1] cumulative ceil(L/128)
+  const int* item_prefix;   // [N+1] cumulative ceil(L/256)
+  const int4* fwd_items;    // [cap] {doc, tile0, ntiles, cost}
+  const int4* bwd_items;    // [cap] {doc, ktile, cost, 0}
+  unsigned long long* sort_keys;  // [pow2(cap)]
+};
+
+__host__ __device__ inline int64_t plan_capacity(int64_t T, int N) { return T / kTile + N + 1; }
+__host__ __device__ inline int64_t pow2_ceil(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+__host__ __device__ inline int64_t plan_prefix_words(int N) { return ((int64_t)kPlanHeaderWords + 3 * (N + 1) + 3) & ~3LL; }
+__host__ __device__ inline size_t plan_bytes(int64_t T, int N) {
+  const int64_t cap = plan_capacity(T, N);
+  return (size_t)plan_prefix_words(N) * 4 + (size_t)cap * 32 + (size_t)pow2_ceil(cap) * 8 + 16;
+}
+__host__ __device__ inline PlanView plan_view(const void* plan, int64_t T, int N) {
+  PlanView v;
+  int* w = (int*)plan;
+  v.hdr = w;
+  v.blk_prefix = w + kPlanHeaderWords;
+  v.tile_prefix = v.blk_prefix + (N + 1);
+  v.item_prefix = v.tile_prefix + (N + 1);
+  const int64_t cap = plan_capacity(T, N);
+  int4* items = (int4*)(w + plan_prefix_words(N));
+  v.fwd_items = items;
+  v.bwd_items = items + cap;
+  v.sort_keys = (unsigned long long*)(items + 2 * cap);
+  return v;
+}
+
+// Document containing prefix-table index `idx`: largest n with prefix[n] <= idx.
+__device__ __forceinline__ int upper_doc(const int* prefix, int N, int idx) {
+  int lo = 0, hi = N;  // prefix[lo] <= idx < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= idx) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------- exponent rule
+// Smallest integer e with amax <= 448 * 2^e, for a finite non-negative fp32
+// amax; 0 for amax == 0; clamped to [-127, 127].  Integer arithmetic on the
+// fp32 encoding: amax = 1.f * 2^E, and 448 = 1.75 * 2^8, so e = E - 8 + [f > 0.75].
+__device__ __forceinline__ int roundup_exp(float amax) {
+  uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
+  if (b == 0) return 0;
+  int E;
+  uint32_t frac;
+  if ((b >> 23) == 0) {             // fp32 subnormal: b * 2^-149, leading one at bit 23 - lz
+    const int lz = __clz(b) - 8;
+    frac = (b << lz) & 0x7FFFFFu;
+    E = -126 - lz;
+  } else {
+    E = (int)(b >> 23) - 127;
+    frac = b & 0x7FFFFFu;
+  }
+  int e = E - 8 + (frac > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^e as fp32 for e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+// UE8M0 byte -> 2^(b - 127) as fp32 (b = 0 is the subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
+  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// 2^x with the MUFU ex2 instruction (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two fp32 -> two E4M3 bytes (round to nearest even, saturating); lo in bits 0-7.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+}  // namespace flamia

@@ -1,0 +1,203 @@
+// Work-list builder: Algorithm 2 of the FLAMIA technical review ("Document-
+// local work list and launch", steps 01-06), run on the GPU once per
+// microbatch with no host synchronisation (review section 6, "GPU list
+// construction avoids host synchronization").
+//
+// One CTA of 1024 threads:
+//   1. validate cu_seqlens (cu[0] = 0, non-decreasing, cu[N] <= T);
+//   2. per-document counts of 32-token blocks, 128-token tiles and 256-query
+//      items, exclusive prefix sums over documents;
+//   3. forward items (cost = visible key tiles summed over the item's query
+//      tiles) and backward key-tile items (cost = query tiles that see the
+//      key tile), each sorted by decreasing cost with ties in document, then
+//      tile order: a bitonic sort of 64-bit keys (cost descending, index).
+#include "common.cuh"
+
+namespace flamia {
+
+namespace {
+
+constexpr int kThreads = 1024;
+
+// Block-wide exclusive scan of one int per thread; returns the exclusive
+// prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  *total = warp_sums[31];
+  __syncthreads();
+  return before;
+}
+
+__device__ void bitonic_sort(unsigned long long* keys, int n) {  // n is a power of two
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = keys[i], b = keys[ixj];
+          const bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restrict__ cu, int N, int T,
+                                                        int* __restrict__ plan_words) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_bad;
+  __shared__ int s_carry[3];
+  PlanView pv = plan_view(plan_words, T, N);
+  int* blk_prefix = const_cast<int*>(pv.blk_prefix);
+  int* tile_prefix = const_cast<int*>(pv.tile_prefix);
+  int* item_prefix = const_cast<int*>(pv.item_prefix);
+  int4* fwd = const_cast<int4*>(pv.fwd_items);
+  int4* bwd = const_cast<int4*>(pv.bwd_items);
+  const int cap = (int)plan_capacity(T, N);
+
+  if (threadIdx.x == 0) {
+    s_bad = 0;
+    s_carry[0] = s_carry[1] = s_carry[2] = 0;
+  }
+  __syncthreads();
+  // 1. validation
+  for (int n = threadIdx.x; n < N; n += kThreads) {
+    const int a = cu[n], b = cu[n + 1];
+    if (b < a || (n == 0 && a != 0) || (n == N - 1 && b > T)) atomicOr(&s_bad, 1);
+  }
+  __syncthreads();
+  const int bad = s_bad;
+  // 2. prefix counts (chunks of kThreads documents)
+  for (int base = 0; base < N; base += kThreads) {
+    const int n = base + threadIdx.x;
+    int L = 0;
+    if (!bad && n < N) L = cu[n + 1] - cu[n];
+    const int nb = (L + kBlock - 1) / kBlock, nt = (L + kTile - 1) / kTile,
+              ni = (L + kTile * kItemTiles - 1) / (kTile * kItemTiles);
+    int tot;
+    const int pb = block_exclusive_scan(nb, warp_sums, &tot);
+    const int cb = s_carry[0];
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry[0] = cb + tot;
+    const int pt = block_exclusive_scan(nt, warp_sums, &tot);
+    const int ct = s_carry[1];
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry[1] = ct + tot;
+    const int pi = block_exclusive_scan(ni, warp_sums, &tot);
+    const int ci = s_carry[2];
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry[2] = ci + tot;
+    if (n < N) {
+      blk_prefix[n] = cb + pb;
+      tile_prefix[n] = ct + pt;
+      item_prefix[n] = ci + pi;
+    }
+    __syncthreads();
+  }
+  const int nblk = s_carry[0], ntile = s_carry[1], nitem = s_carry[2];
+  if (threadIdx.x == 0) {
+    blk_prefix[N] = nblk;
+    tile_prefix[N] = ntile;
+    item_prefix[N] = nitem;
+  }
+  __syncthreads();
+  const bool over = ntile > cap || nitem > cap;
+  if (threadIdx.x == 0) {
+    plan_words[kPlanStatus] = (bad ? FLAMIA_DEV_BAD_CU_SEQLENS : 0) | (over ? FLAMIA_DEV_CAPACITY : 0);
+    plan_words[kPlanNumSeqs] = N;
+    plan_words[kPlanTotal] = T;
+    plan_words[kPlanValid] = bad ? 0 : (N > 0 ? cu[N] : 0);
+    plan_words[kPlanBlocks] = bad ? 0 : nblk;
+    plan_words[kPlanTiles] = (bad || over) ? 0 : ntile;
+    plan_words[kPlanFwdItems] = (bad || over) ? 0 : nitem;
+    plan_words[kPlanBwdItems] = (bad || over) ? 0 : ntile;
+    plan_words[kPlanCapacity] = cap;
+  }
+  if (bad || over) return;
+  unsigned long long* keys = pv.sort_keys;
+  const unsigned long long kPad = ~0ull;
+  const unsigned kCostMax = 0x7FFFFFFFu;
+
+  // 3a. forward items
+  {
+    const int n2 = (int)pow2_ceil(nitem > 0 ? nitem : 1);
+    for (int i = threadIdx.x; i < n2; i += kThreads) {
+      unsigned long long key = kPad;
+      if (i < nitem) {
+        const int doc = upper_doc(item_prefix, N, i);
+        const int nt = tile_prefix[doc + 1] - tile_prefix[doc];
+        const int t0 = (i - item_prefix[doc]) * kItemTiles;
+        const int cnt = min(kItemTiles, nt - t0);
+        int cost = 0;
+        for (int t = t0; t < t0 + cnt; ++t) cost += t + 1;
+        key = ((unsigned long long)(kCostMax - (unsigned)cost) << 32) | (unsigned)i;
+      }
+      keys[i] = key;
+    }
+    __syncthreads();
+    bitonic_sort(keys, n2);
+    for (int r = threadIdx.x; r < nitem; r += kThreads) {
+      const int i = (int)(keys[r] & 0xFFFFFFFFull);
+      const int doc = upper_doc(item_prefix, N, i);
+      const int nt = tile_prefix[doc + 1] - tile_prefix[doc];
+      const int t0 = (i - item_prefix[doc]) * kItemTiles;
+      const int cnt = min(kItemTiles, nt - t0);
+      fwd[r] = make_int4(doc, t0, cnt, (int)(kCostMax - (unsigned)(keys[r] >> 32)));
+    }
+    __syncthreads();
+  }
+  // 3b. backward key-tile items
+  {
+    const int n2 = (int)pow2_ceil(ntile > 0 ? ntile : 1);
+    for (int i = threadIdx.x; i < n2; i += kThreads) {
+      unsigned long long key = kPad;
+      if (i < ntile) {
+        const int doc = upper_doc(tile_prefix, N, i);
+        const int nt = tile_prefix[doc + 1] - tile_prefix[doc];
+        const int cost = nt - (i - tile_prefix[doc]);
+        key = ((unsigned long long)(kCostMax - (unsigned)cost) << 32) | (unsigned)i;
+      }
+      keys[i] = key;
+    }
+    __syncthreads();
+    bitonic_sort(keys, n2);
+    for (int r = threadIdx.x; r < ntile; r += kThreads) {
+      const int i = (int)(keys[r] & 0xFFFFFFFFull);
+      const int doc = upper_doc(tile_prefix, N, i);
+      bwd[r] = make_int4(doc, i - tile_prefix[doc], (int)(kCostMax - (unsigned)(keys[r] >> 32)), 0);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* cu, int N, int T, void* plan, cudaStream_t s) {
+  plan_kernel<<<1, kThreads, 0, s>>>(cu, N, T, static_cast<int*>(plan));
+  return cudaGetLastError();
+}
+
+}  // namespace flamia

@@ -1,0 +1,201 @@
+// Token-block MXFP8 quantizer (step a1 of the hot path) and its fused
+// backward-prep variant (step a7).
+//
+// FLAMIA technical review section 3 ("Why one shared exponent can serve two
+// reductions"): one UE8M0 exponent per document-local block of <= 32
+// consecutive tokens x the whole head dimension; section 4: the exponent is
+// the smallest with amax <= 448 * 2^e (round-up rule, never clamps); section
+// 6: blocks are local to each document and the scale metadata is dense (one
+// byte per token).  The per-token variant is the strict option of section 4.
+//
+// Bandwidth-bound: one warp per (block, head); each lane moves 16 bytes per
+// load (coalesced 128-bit accesses along head_dim); amax is a warp-shuffle
+// max; codes come from the saturating round-to-nearest-even cvt to E4M3.
+//
+// The backward-prep variant (review Algorithm 1 step 09) encodes dO once and,
+// in the same pass, computes D_i = dO^_i . O_i from the saved bf16 O and
+// zeroes the fp16 dQ accumulator rows it owns.
+#include "common.cuh"
+
+namespace flamia {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+template <int D, bool PER_TOKEN, bool STATS, bool WITH_D>
+__global__ void __launch_bounds__(kWarps * 32)
+    quantize_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, const int32_t* __restrict__ cu, int N,
+                    const int* __restrict__ plan, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                    float2* __restrict__ stats, const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec,
+                    __half* __restrict__ dq_acc) {
+  constexpr int kLpr = D / 8;          // lanes per token row (16 bytes each)
+  constexpr int kRpi = 32 / kLpr;      // rows per iteration
+  constexpr int kIters = 32 / kRpi;    // 32 rows per warp
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int h = (int)(gw % H);
+  const int64_t unit = gw / H;
+  const PlanView pv = plan_view(plan, T, N);
+  const int valid = plan[kPlanValid];
+  const int nblk = plan[kPlanBlocks];
+
+  // rows [r0, r0 + nrows) of this warp; tail rows (no document) get zeros
+  int r0, nrows;
+  bool tail;
+  if (PER_TOKEN) {
+    r0 = (int)(unit * 32);
+    if (r0 >= T) return;
+    nrows = min(32, T - r0);
+    tail = false;  // per row below
+  } else {
+    if (unit < nblk) {
+      const int doc = upper_doc(pv.blk_prefix, N, (int)unit);
+      const int s0 = cu[doc], s1 = cu[doc + 1];
+      r0 = s0 + ((int)unit - pv.blk_prefix[doc]) * kBlock;
+      nrows = min(kBlock, s1 - r0);
+      tail = false;
+    } else {
+      r0 = valid + (int)(unit - nblk) * 32;
+      if (r0 >= T) return;
+      nrows = min(32, T - r0);
+      tail = true;
+    }
+  }
+  const int sub = lane / kLpr;            // row within an iteration
+  const int cb = (lane % kLpr) * 8;       // first of the 8 elements this lane owns
+
+  uint4 raw[kIters];
+  float amax_lane = 0.f;
+  float rowmax[kIters];
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int r = it * kRpi + sub;
+    raw[it] = make_uint4(0, 0, 0, 0);
+    const bool live = r < nrows && !tail && (!PER_TOKEN || r0 + r < valid);
+    if (live) raw[it] = __ldg(reinterpret_cast<const uint4*>(x + ((int64_t)(r0 + r) * H + h) * D + cb));
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[it]);
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(v[j]);
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+    rowmax[it] = m;
+    amax_lane = fmaxf(amax_lane, m);
+  }
+  int e_block = 0;
+  if (!PER_TOKEN) {
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) amax_lane = fmaxf(amax_lane, __shfl_xor_sync(0xffffffffu, amax_lane, o2));
+    e_block = roundup_exp(amax_lane);
+  }
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int r = it * kRpi + sub;
+    const bool inrange = r < nrows;
+    int e = e_block;
+    if (PER_TOKEN) {
+      float m = rowmax[it];
+#pragma unroll
+      for (int o2 = kLpr / 2; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
+      e = roundup_exp(m);
+    }
+    const float s = exp2i(-e);
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[it]);
+    uint32_t packed[2];
+    float ss = 0.f, mx = 0.f, dd = 0.f;
+    const float back = ue8m0_to_f32((uint32_t)(e + 127));
+    uint4 oraw = make_uint4(0, 0, 0, 0);
+    if (WITH_D && inrange && !tail) {
+      const int64_t row = r0 + r;
+      if (!PER_TOKEN || row < valid)
+        oraw = __ldg(reinterpret_cast<const uint4*>(o + (row * H + h) * D + cb));
+    }
+    const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oraw);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(v[j]);
+      const uint16_t c2 = e4m3x2(f.x * s, f.y * s);
+      if (j & 1) packed[j >> 1] |= (uint32_t)c2 << 16; else packed[j >> 1] = c2;
+      if (STATS || WITH_D) {
+        const float a = e4m3_to_f32((uint8_t)(c2 & 0xFF)) * back;
+        const float b = e4m3_to_f32((uint8_t)(c2 >> 8)) * back;
+        if (STATS) {
+          ss = fmaf(a, a, fmaf(b, b, ss));
+          mx = fmaxf(mx, fmaxf(fabsf(a), fabsf(b)));
+        }
+        if (WITH_D) {
+          const float2 of = __bfloat1622float2(ov[j]);
+          dd = fmaf(a, of.x, fmaf(b, of.y, dd));
+        }
+      }
+    }
+    if (inrange) {
+      const int64_t row = r0 + r;
+      *reinterpret_cast<uint2*>(codes + (row * H + h) * D + cb) = make_uint2(packed[0], packed[1]);
+      if (WITH_D) *reinterpret_cast<uint4*>(dq_acc + (row * H + h) * D + cb) = make_uint4(0, 0, 0, 0);
+    }
+    if (STATS || WITH_D) {
+#pragma unroll
+      for (int o2 = kLpr / 2; o2 > 0; o2 >>= 1) {
+        if (STATS) {
+          ss += __shfl_xor_sync(0xffffffffu, ss, o2);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+        }
+        if (WITH_D) dd += __shfl_xor_sync(0xffffffffu, dd, o2);
+      }
+    }
+    if (inrange && (lane % kLpr) == 0) {
+      const int64_t row = r0 + r;
+      if (STATS) stats[row * H + h] = make_float2(sqrtf(ss), mx);
+      if (WITH_D) dvec[(int64_t)h * T + row] = dd;
+      if (PER_TOKEN) scales[row * H + h] = (uint8_t)(e + 127);
+    }
+  }
+  if (!PER_TOKEN && lane < nrows) scales[(int64_t)(r0 + lane) * H + h] = (uint8_t)(tail ? 127 : e_block + 127);
+}
+
+template <int D, bool PT, bool ST, bool WD>
+cudaError_t launch_q(const void* x, int T, int H, const int32_t* cu, int N, const void* plan, void* codes,
+                     void* scales, float* stats, const void* o, float* dvec, void* dq_acc, cudaStream_t s) {
+  const int64_t units = PT ? (T + 31) / 32 : (int64_t)T / 32 + N + 1;
+  const int64_t warps = units * H;
+  const int64_t blocks = (warps + kWarps - 1) / kWarps;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  quantize_kernel<D, PT, ST, WD><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), T, H, cu, N, static_cast<const int*>(plan),
+      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), reinterpret_cast<float2*>(stats),
+      static_cast<const __nv_bfloat16*>(o), dvec, static_cast<__half*>(dq_acc));
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch(const void* x, int T, int H, const int32_t* cu, int N, const void* plan, int per_token,
+                     void* codes, void* scales, float* stats, const void* o, float* dvec, void* dq_acc,
+                     cudaStream_t s) {
+  const bool st = stats != nullptr, wd = o != nullptr;
+  if (wd) {
+    if (per_token) return launch_q<D, true, true, true>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+    return launch_q<D, false, true, true>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+  }
+  if (per_token) {
+    if (st) return launch_q<D, true, true, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+    return launch_q<D, true, false, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+  }
+  if (st) return launch_q<D, false, true, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+  return launch_q<D, false, false, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+}
+
+}  // namespace
+
+// o / dvec / dq_acc non-null selects the backward-prep variant (stats required).
+cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
+                            int per_token, void* codes, void* scales, float* stats, const void* o, float* dvec,
+                            void* dq_acc, cudaStream_t s) {
+  if (D == 128) return dispatch<128>(x, T, H, cu, N, plan, per_token, codes, scales, stats, o, dvec, dq_acc, s);
+  if (D == 64) return dispatch<64>(x, T, H, cu, N, plan, per_token, codes, scales, stats, o, dvec, dq_acc, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace flamia

@@ -1,0 +1,70 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function that
+include/flamia.h declares.  Host-side argument validation is exercised on the
+paths that return before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "flamia.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(flamia_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def flamia():
+    from microscaled_precision_causal_gb300 import build
+    build.build()
+    import microscaled_precision_causal_gb300 as F
+    return F
+
+
+def test_header_declares_the_three_named_entry_points():
+    names = _declared_functions()
+    for n in ("flamia_quantize_tokenblock", "flamia_fwd", "flamia_bwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(flamia):
+    L = flamia.lib()
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    assert set(flamia.EXPORTED) == set(_declared_functions())
+
+
+def test_host_validation_without_gpu(flamia):
+    L = flamia.lib()
+    F = flamia
+    assert L.flamia_status_string(0) == b"ok"
+    assert L.flamia_plan_bytes(-1, 1) == 0
+    assert L.flamia_plan_bytes(1024, 3) > 1024 // 128 * 32
+    assert L.flamia_bwd_workspace_bytes(1000, 2, 4, 2, 128) >= 1000 * 4 * 128 * 3
+    q = F.QTensor(16, 16, None)
+    o = F.default_options()
+    assert (o.p_boost_log2, o.bwd_p_boost_log2, o.dq_headroom_log2) == (8, 8, 14)
+    args = lambda **kw: dict(dict(hq=4, hkv=2, d=128, causal=1, opts=o, plan=256, out=256, lse=256), **kw)
+
+    def fwd(a):
+        return L.flamia_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), 256, 1, 100, a["hq"], a["hkv"], a["d"],
+                            a["causal"], 0.0, ctypes.byref(a["opts"]), a["plan"], a["out"], a["lse"], None)
+    assert fwd(args(d=96)) == -2                      # unsupported head dim
+    assert fwd(args(hq=3)) == -2                      # hq % hkv != 0
+    assert fwd(args(causal=0)) == -2                  # non-causal: not built
+    assert fwd(args(plan=0)) == -1                    # null plan
+    assert fwd(args(out=258)) == -3                   # misaligned output
+    bad = F.default_options(); bad.p_boost_log2 = 10
+    assert fwd(args(opts=bad)) == -2
+    qm = F.QTensor(17, 16, None)                      # misaligned codes
+    assert L.flamia_fwd(ctypes.byref(qm), ctypes.byref(q), ctypes.byref(q), 256, 1, 100, 4, 2, 128, 1, 0.0, None, 256,
+                        256, 256, None) == -3
+    assert L.flamia_quantize_tokenblock(256, 100, 2, 80, 256, 1, 256, 0, 256, 256, None, None) == -2
+    assert L.flamia_plan_build(256, 1, 100, 256, 8, None) == -4     # plan buffer too small
+    # backward needs k/v stats
+    assert L.flamia_bwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), 256, 256, 256, 256, 1, 100, 4, 2, 128, 1,
+                        0.0, None, 256, 256, 256, 256, 256, 1 << 30, None) == -1
