@@ -71,10 +71,17 @@ typedef struct flamia_options {
   int strict_causal_dq;
   int mixed_nvfp4;
   int deterministic;
+  /* Optional profiling hook (NULL = off): cudaEvent_t handles, two per internal
+     launch.  The call records timing_events[2i] just before and
+     timing_events[2i+1] just after its i-th launch, on its stream.
+     flamia_fwd: launch 0 = attention forward kernel.  flamia_bwd: 0 = dO
+     encoding with D (backward prep), 1 = dQ boosts, 2 = attention backward
+     kernel, 3 = dQ finalisation.  The events are caller-owned. */
+  void* const* timing_events;
 } flamia_options;
 
 /* Fill *opt with the defaults above (p_boost_log2 = 8, bwd_p_boost_log2 = 8,
-   dq_headroom_log2 = 14, everything else 0). */
+   dq_headroom_log2 = 14, everything else 0 / NULL). */
 void flamia_default_options(flamia_options* opt);
 
 /* ----------------------------------------------------------- quantized tensor view */

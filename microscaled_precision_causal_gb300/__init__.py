@@ -38,7 +38,7 @@ class FlamiaError(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "p_boost_log2", "bwd_p_boost_log2", "dq_headroom_log2", "strict_per_token", "strict_row_ds",
-        "strict_causal_dq", "mixed_nvfp4", "deterministic")]
+        "strict_causal_dq", "mixed_nvfp4", "deterministic")] + [("timing_events", ctypes.POINTER(ctypes.c_void_p))]
 
 
 class QTensor(ctypes.Structure):

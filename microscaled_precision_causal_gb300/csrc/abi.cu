@@ -14,13 +14,14 @@ cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* c
                             void* dq_acc, cudaStream_t s);
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* out, float* lse, cudaStream_t stream);
+                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev);
 cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float* st_do, const float* st_k,
                          const float* st_v, int hq, int hkv, int headroom, float* boost, cudaStream_t s);
 cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream);
+                       const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
+                       void* const* ev);
 }  // namespace flamia
 
 using namespace flamia;
@@ -63,6 +64,10 @@ int check_qt(const flamia_qtensor* t, bool need_stats) {
 }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA; }
+
+inline void record(void* const* ev, int i, cudaStream_t s) {
+  if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+}
 
 float resolve_scale(float s, int d) { return s > 0.f ? s : 1.0f / std::sqrt((float)d); }
 
@@ -138,7 +143,7 @@ int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (total_tokens == 0) return FLAMIA_OK;
   return cuda_status(launch_fwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, cu_seqlens,
                                 num_seqs, (int)total_tokens, hq, hkv, resolve_scale(softmax_scale, head_dim), plan,
-                                out_bf16, lse, (cudaStream_t)stream));
+                                out_bf16, lse, (cudaStream_t)stream, opt ? opt->timing_events : nullptr));
 }
 
 size_t flamia_bwd_workspace_bytes(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim) {
@@ -177,14 +182,19 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   float* dvec = reinterpret_cast<float*>(ws + w.dvec);
   float* boost = reinterpret_cast<float*>(ws + w.boost);
   void* dq_acc = ws + w.dq_acc;
+  void* const* ev = opt ? opt->timing_events : nullptr;
+  record(ev, 0, s);
   cudaError_t e = launch_quantize(dout_bf16, T, hq, head_dim, cu_seqlens, num_seqs, plan, 0, do_codes, do_scales,
                                   do_stats, out_bf16, dvec, dq_acc, s);
+  record(ev, 1, s);
+  record(ev, 2, s);
   if (e == cudaSuccess)
     e = launch_boost(cu_seqlens, num_seqs, plan, do_stats, k->stats, v->stats, hq, hkv, headroom, boost, s);
+  record(ev, 3, s);
   if (e == cudaSuccess)
     e = launch_bwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, do_codes, do_scales, lse,
                    dvec, boost, cu_seqlens, num_seqs, T, hq, hkv, resolve_scale(softmax_scale, head_dim), plan, dq_acc,
-                   dq_bf16, dk_bf16, dv_bf16, s);
+                   dq_bf16, dk_bf16, dv_bf16, s, ev ? ev + 4 : nullptr);
   return cuda_status(e);
 }
 

@@ -496,7 +496,8 @@ template <int D>
 cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                          const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                         const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream) {
+                         const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
+                         void* const* ev) {
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
@@ -528,12 +529,17 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   constexpr int smem = BwdSmem<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
   attn_bwd_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
+  if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
+  if (ev && ev[2]) cudaEventRecord(static_cast<cudaEvent_t>(ev[2]), stream);
   dq_finalize_kernel<D><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
                                                      hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (ev && ev[3]) cudaEventRecord(static_cast<cudaEvent_t>(ev[3]), stream);
+  return e;
 }
 
 }  // namespace
@@ -550,13 +556,14 @@ cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float
 cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream) {
+                       const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
+                       void* const* ev) {
   if (D == 128)
     return launch_bwd_d<128>(qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan,
-                             dq_acc, dq, dk, dv, stream);
+                             dq_acc, dq, dk, dv, stream, ev);
   if (D == 64)
     return launch_bwd_d<64>(qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan,
-                            dq_acc, dq, dk, dv, stream);
+                            dq_acc, dq, dk, dv, stream, ev);
   return cudaErrorInvalidValue;
 }
 

@@ -350,7 +350,7 @@ __global__ void fwd_tail_kernel(const int* plan, int T, int hq, __nv_bfloat16* o
 template <int D>
 cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                         const void* plan, void* out, float* lse, cudaStream_t stream) {
+                         const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev) {
   CUtensorMap tq, tk, tv;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
@@ -375,8 +375,10 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
   constexpr int smem = FwdSmem<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
   attn_fwd_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
+  if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
   fwd_tail_kernel<D><<<152, 256, 0, stream>>>(static_cast<const int*>(plan), T, hq, static_cast<__nv_bfloat16*>(out),
                                               lse);
@@ -387,9 +389,9 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
 
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* out, float* lse, cudaStream_t stream) {
-  if (D == 128) return launch_fwd_d<128>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream);
-  if (D == 64) return launch_fwd_d<64>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream);
+                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev) {
+  if (D == 128) return launch_fwd_d<128>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
+  if (D == 64) return launch_fwd_d<64>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
   return cudaErrorInvalidValue;
 }
 
