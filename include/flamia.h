@@ -10,7 +10,8 @@
  * Conventions for every entry point
  *  - All tensor arguments are DEVICE pointers owned by the caller; the library
  *    never allocates, frees or retains them, and keeps no global state beyond
- *    a cached driver entry point.  Every call is asynchronous on `stream`
+ *    a cached driver entry point (and, for flamia_bwd_static_scratch, its
+ *    static device scratch array and that array's per-device address).  Every call is asynchronous on `stream`
  *    (a cudaStream_t passed as void*; NULL = legacy default stream) and never
  *    synchronises the host, so calls can be captured in a CUDA graph.
  *  - Packed variable-length batches: `cu_seqlens` (device, int32, num_seqs+1
@@ -183,6 +184,28 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
                int64_t total_tokens, int hq, int hkv, int head_dim, int causal, float softmax_scale,
                const flamia_options* opt, const void* plan, void* dq_bf16, void* dk_bf16, void* dv_bf16,
                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------- backward without allocation
+ * No counterpart in the paper: a library convenience.
+ * flamia_bwd for callers that cannot allocate device memory (for example a
+ * plugin whose host framework hands it only input and output buffers, or a
+ * latency-critical loop that must avoid cudaMalloc's device-wide
+ * synchronisation).  Same arguments and results as flamia_bwd minus the
+ * workspace: the scratch is a file-scope device array of
+ * FLAMIA_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits.  Problems whose flamia_bwd_workspace_bytes() exceeds it
+ * are rejected with FLAMIA_ERR_WORKSPACE before anything is launched.  The
+ * first call on each device resolves the array's address (cudaGetSymbolAddress,
+ * with that device current) and caches it: make that first call before any
+ * stream capture.  The call allocates nothing.  All calls share the array:
+ * calls whose GPU work overlaps race and give wrong results; the fp16 dQ
+ * accumulator is cleared by every call. */
+#define FLAMIA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+int flamia_bwd_static_scratch(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v,
+                              const void* out_bf16, const float* lse, const void* dout_bf16,
+                              const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq, int hkv,
+                              int head_dim, int causal, float softmax_scale, const flamia_options* opt,
+                              const void* plan, void* dq_bf16, void* dk_bf16, void* dv_bf16, void* stream);
 
 /* ----------------------------------------------------------- status */
 /* Copy the plan's device status word into *status_out (synchronises `stream`). */

@@ -27,8 +27,9 @@ DEV_BAD_CU_SEQLENS, DEV_TIMEOUT, DEV_CAPACITY = 1, 2, 4
 EXPORTED = (
     "flamia_default_options", "flamia_plan_bytes", "flamia_plan_build", "flamia_quantize_tokenblock",
     "flamia_fwd", "flamia_bwd_workspace_bytes", "flamia_bwd", "flamia_get_device_status",
-    "flamia_status_string",
+    "flamia_status_string", "flamia_bwd_static_scratch",
 )
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class FlamiaError(RuntimeError):
@@ -69,6 +70,8 @@ def lib():
         "flamia_bwd_workspace_bytes": (sz, [i64, i32, i32, i32, i32]),
         "flamia_bwd": (i32, [qp, qp, qp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, f32, op, vp, vp, vp, vp, vp,
                              sz, vp]),
+        "flamia_bwd_static_scratch": (i32, [qp, qp, qp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, f32, op, vp,
+                                            vp, vp, vp, vp]),
         "flamia_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_int), vp]),
         "flamia_status_string": (ctypes.c_char_p, [i32]),
     }
@@ -151,6 +154,21 @@ def flamia_bwd(q: QTensor, k: QTensor, v: QTensor, out, lse, dout, cu_seqlens, n
                             ctypes.byref(opts) if opts else None, _ptr(plan), _ptr(dq), _ptr(dk), _ptr(dv),
                             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "flamia_bwd")
+
+
+def flamia_bwd_static_scratch(q: QTensor, k: QTensor, v: QTensor, out, lse, dout, cu_seqlens, num_seqs: int,
+                              total_tokens: int, hq: int, hkv: int, head_dim: int, plan, dq, dk, dv,
+                              softmax_scale: float = 0.0, opts: Optional[Options] = None, causal: int = 1,
+                              stream=None):
+    """flamia_bwd without a workspace argument, for callers that cannot allocate
+    device memory: the scratch is the library's static device array
+    (STATIC_SCRATCH_BYTES per GPU).  The first call on a device must come before
+    any stream capture; calls that overlap on the GPU race on the shared array."""
+    _check(lib().flamia_bwd_static_scratch(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), _ptr(out), _ptr(lse),
+                                           _ptr(dout), _ptr(cu_seqlens), num_seqs, total_tokens, hq, hkv, head_dim,
+                                           causal, softmax_scale, ctypes.byref(opts) if opts else None, _ptr(plan),
+                                           _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
+           "flamia_bwd_static_scratch")
 
 
 def flamia_get_device_status(plan, stream=None) -> int:
