@@ -17,11 +17,19 @@
 //
 // One CTA per (document-local 128-key tile, kv head); it visits every query
 // head of the kv head's group and every query tile at or after the key tile.
-// Roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
-// allocator, warps 4-7 compute (thread = key row for S/dP, = query row for dQ).
-// TMEM: S^T / dQ partial [0,128), dP^T [128,256) whose first 24 columns carry
-// the block-scale words of the three MXF8 MMAs once dP^T has been read, dV
-// [256, 256+D), dK [384, 384+D).
+// Roles (384 threads):
+//   warp 0      TMA producer (K, V once; Q and dO codes per step)
+//   warp 1      MMA issuer (one thread)
+//   warp 2      TMEM allocator
+//   warp 3      per-query row data of the next steps (LSE, D, chunk scales) into SMEM
+//   warps 4-7   compute warpgroup 0: query columns 0-63 of each step
+//   warps 8-11  compute warpgroup 1: query columns 64-127
+// Thread = key row while building P^ and dS^ codes, = query row while reading
+// the dQ partial.  TMEM: S^T [0,128) (its last 24 columns carry the block-scale
+// words of the three MXF8 MMAs once S^T has been read), dP^T / dQ partial
+// [128,256), dV [256, 256+D), dK [384, 384+D).  Per step the MMA thread issues
+// dV, dK, dQ(k), then S^T(k+1) straight away and dP^T(k+1) once the dQ partial
+// has been read, so the exponentials of step k+1 overlap the dP MMA.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -30,7 +38,8 @@ namespace flamia {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kCompute = 256;       // two compute warpgroups
 constexpr int kQStages = 2;
 
 struct BwdParams {
@@ -61,7 +70,7 @@ struct BwdSmem {
   static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query]
   static constexpr int kDS = kPt + kTile * kTile;             // dS^ codes, [key][query]
   static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
-  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // lse2, D, chunk scales
+  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // lse2[128], D[128], chunk scales[8]
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents
   static constexpr int kBar = kE + 64;
   static constexpr int kBytes = kBar + 256;
@@ -89,12 +98,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* qd_full = bars + 1;              // [kQStages]
   uint64_t* qd_empty = bars + 1 + kQStages;  // [kQStages]
-  uint64_t* s_full = bars + 1 + 2 * kQStages;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* dq_full = s_full + 2;
-  uint64_t* dq_empty = s_full + 3;
-  uint64_t* acc_full = s_full + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 5);
+  uint64_t* row_full = bars + 1 + 2 * kQStages;   // [2]
+  uint64_t* row_empty = row_full + 2;             // [2]
+  uint64_t* s_full = row_empty + 2;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* dq_full = s_full + 3;
+  uint64_t* dq_empty = s_full + 4;
+  uint64_t* acc_full = s_full + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 6);
   int* status = const_cast<int*>(p.plan) + kPlanStatus;
 
   const int n_items = p.plan[kPlanBwdItems];
@@ -118,10 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&row_full[i], 32);
+      mbar_init(&row_empty[i], kCompute);
+    }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, kCompute);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, kCompute);
     mbar_init(acc_full, 1);
     fence_mbar_init();
   }
@@ -134,8 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   constexpr uint32_t kS = 0, kP = 128, kDV = 256, kDK = 384;
+  constexpr uint32_t kSF = kS + 104;        // 24 block-scale words, valid once S^T was read
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
   constexpr uint32_t kAtom = 8 * D;
+  float* rowbuf = reinterpret_cast<float*>(smem + L::kRow);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -159,23 +178,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t sk = smem_u32(smem + L::kK), sv = smem_u32(smem + L::kV), sq = smem_u32(smem + L::kQ),
                      sdo = smem_u32(smem + L::kDO), spt = smem_u32(smem + L::kPt), sds = smem_u32(smem + L::kDS);
-      auto issue_sp = [&](int st, bool do_s, bool do_p) {
-        const uint32_t qa = sq + st * L::kTileBytes, da = sdo + st * L::kTileBytes;
+      auto issue_s = [&](int st) {
+        const uint32_t qa = sq + st * L::kTileBytes;
 #pragma unroll
-        for (int s = 0; s < D / 32; ++s) {
-          if (do_p)
-            mma_f8(tbase + kP, smem_desc(sv + 32 * s, 16, kAtom, kLayout), smem_desc(da + 32 * s, 16, kAtom, kLayout),
-                   idesc_f8(128, 128, 0, 0), s > 0);
-          if (do_s)
-            mma_f8(tbase + kS, smem_desc(sk + 32 * s, 16, kAtom, kLayout), smem_desc(qa + 32 * s, 16, kAtom, kLayout),
-                   idesc_f8(128, 128, 0, 0), s > 0);
-        }
+        for (int s = 0; s < D / 32; ++s)
+          mma_f8(tbase + kS, smem_desc(sk + 32 * s, 16, kAtom, kLayout), smem_desc(qa + 32 * s, 16, kAtom, kLayout),
+                 idesc_f8(128, 128, 0, 0), s > 0);
+      };
+      auto issue_dp = [&](int st) {
+        const uint32_t da = sdo + st * L::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < D / 32; ++s)
+          mma_f8(tbase + kP, smem_desc(sv + 32 * s, 16, kAtom, kLayout), smem_desc(da + 32 * s, 16, kAtom, kLayout),
+                 idesc_f8(128, 128, 0, 0), s > 0);
       };
       bool ok = mbar_wait(kv_full, 0, status) && mbar_wait(&qd_full[0], 0, status);
       if (ok) {
         tc_fence_after();
-        issue_sp(0, true, true);
+        issue_s(0);
         mma_commit(s_full);
+        issue_dp(0);
+        mma_commit(dp_full);
       }
       for (int k = 0; k < nsteps && ok; ++k) {
         const int st = k % kQStages;
@@ -188,21 +211,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
           mma_mxf8(tbase + kDV, smem_desc(spt + 32 * s, 16, 1024, kSwizzle128B),
                    smem_desc(da + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
-                   tbase + kP + 0, tbase + kP + 4, (k > 0 || s > 0));
+                   tbase + kSF + 0, tbase + kSF + 4, (k > 0 || s > 0));
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           // dK += dS^^T Q
           mma_mxf8(tbase + kDK, smem_desc(sds + 32 * s, 16, 1024, kSwizzle128B),
                    smem_desc(qa + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
-                   tbase + kP + 8, tbase + kP + 12, (k > 0 || s > 0));
+                   tbase + kSF + 8, tbase + kSF + 12, (k > 0 || s > 0));
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          // dQp = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major)
-          mma_mxf8(tbase + kS, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
+          // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major)
+          mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
                    smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
-                   tbase + kP + 16, tbase + kP + 20, s > 0);
+                   tbase + kSF + 16, tbase + kSF + 20, s > 0);
         }
         mma_commit(dq_full);
         mma_commit(&qd_empty[st]);
@@ -211,21 +234,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
           if (!ok) break;
           tc_fence_after();
-          issue_sp(st1, false, true);
+          issue_s(st1);
+          mma_commit(s_full);
           ok = mbar_wait(dq_empty, k & 1, status);
           if (!ok) break;
           tc_fence_after();
-          issue_sp(st1, true, false);
-          mma_commit(s_full);
+          issue_dp(st1);
+          mma_commit(dp_full);
         }
       }
       mma_commit(acc_full);
       if (!ok) mbar_wait(acc_full, 0, status);
     }
-  } else if (warp >= 4) {
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ per-query row data
+    for (int k = 0; k < nsteps; ++k) {
+      const int b = k & 1;
+      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&row_empty[b], ((k >> 1) - 1) & 1, status))) break;
+      const int h = hk * g + k / qtiles, t = u + k % qtiles;
+      float* rb = rowbuf + b * (L::kRowBuf / 4);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = q * 32 + lane;
+        const int ql = t * kTile + i;
+        const bool qv = ql < doc_len;
+        const int64_t qtok = (int64_t)doc_start + ql;
+        rb[i] = qv ? p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : INFINITY;
+        rb[128 + i] = qv ? p.dvec[(int64_t)h * p.T + qtok] : 0.f;
+      }
+      if (lane < 8) {
+        const int c = lane & 3;
+        const int ql = t * kTile + c * 32;
+        const bool qv = ql < doc_len;
+        const int64_t qtok = (int64_t)doc_start + ql;
+        const uint8_t* src = lane < 4 ? p.q_scales : p.do_scales;
+        reinterpret_cast<uint8_t*>(rb + 256)[lane] = qv ? src[qtok * p.hq + h] : (uint8_t)127;
+      }
+      mbar_arrive(&row_full[b]);
+    }
+  } else {
     // ------------------------------------------------------------ compute
+    const int wg = (warp - 4) >> 2;                    // query columns [64 wg, 64 wg + 64)
     const int quarter = warp & 3;
-    const int j = quarter * 32 + lane;                 // key row (TMEM lane) during S/dP
+    const int j = quarter * 32 + lane;                 // key row (TMEM lane) for S / dP; query row for dQ
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     const bool key_valid = u * kTile + j < doc_len;
     const int64_t ktok = (int64_t)doc_start + u * kTile + j;
@@ -238,8 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b = kl < doc_len ? p.k_scales[((int64_t)doc_start + kl) * p.hkv + hk] : 127u;
       ksf |= b << (8 * gg);
     }
-    float* rowbuf = reinterpret_cast<float*>(smem + L::kRow);
-    uint32_t* Esm = reinterpret_cast<uint32_t*>(smem + L::kE);
+    uint8_t* Esm = smem + L::kE;
     uint8_t* sPt = smem + L::kPt;
     uint8_t* sDS = smem + L::kDS;
     bool ok = true;
@@ -247,105 +297,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int hh = k / qtiles, t = u + k % qtiles;
       const int h = hk * g + hh;
       const bool diag = (t == u);
-      // per-query data of this step (thread index = query row)
-      float* rb = rowbuf + (k & 1) * (L::kRowBuf / 4);
-      {
-        const int ql = t * kTile + j;
-        const bool qv = ql < doc_len;
-        const int64_t qtok = (int64_t)doc_start + ql;
-        rb[j] = qv ? p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : INFINITY;
-        rb[128 + j] = qv ? p.dvec[(int64_t)h * p.T + qtok] : 0.f;
-        if ((j & 31) == 0) {
-          uint8_t* cs = reinterpret_cast<uint8_t*>(rb + 256);
-          cs[j >> 5] = qv ? p.q_scales[qtok * p.hq + h] : 127;
-          cs[4 + (j >> 5)] = qv ? p.do_scales[qtok * p.hq + h] : 127;
-        }
-      }
-      ok = named_bar_and(1, 128, ok);
-      if (!ok) break;
+      const int b = k & 1;
+      const float* rb = rowbuf + b * (L::kRowBuf / 4);
       const uint8_t* cs = reinterpret_cast<const uint8_t*>(rb + 256);
-      ok = named_bar_and(1, 128, mbar_wait(s_full, k & 1, status));
+      ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t vs[32], vp[32];
+      // P = 2^(x - LSE log2 e) for this warpgroup's two query chunks
+      float pr[2][32];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * wg + cc;
+        uint32_t vs[32];
         tmem_ld32(lane_base + kS + 32 * c, vs);
-        tmem_ld32(lane_base + kP + 32 * c, vp);
         tmem_ld_wait();
         const float fS = p.scale_log2 * sk_row * ue8m0_to_f32(cs[c]);
-        const float fP = sv_row * ue8m0_to_f32(cs[4 + c]);
-        float ds[32];
         uint32_t pk[8];
-        float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float pp[2];
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int il = 32 * c + i + q;            // query row within the tile
-            const bool vis = !diag || il >= j;
-            const float pr = vis ? fast_exp2(fmaf(__uint_as_float(vs[i + q]), fS, -rb[il])) : 0.f;
-            const float dpv = __uint_as_float(vp[i + q]) * fP;
-            ds[i + q] = pr * (dpv - rb[128 + il]);
-            amax = fmaxf(amax, fabsf(ds[i + q]));
-            pp[q] = pr * 256.0f;
-          }
-          const uint32_t c2 = e4m3x2(pp[0], pp[1]);
-          if ((i & 2) == 0) pk[i >> 2] = c2; else pk[i >> 2] |= c2 << 16;
+        for (int i = 0; i < 32; ++i) {
+          const int il = 32 * c + i;
+          const bool vis = !diag || il >= j;
+          pr[cc][i] = vis ? fast_exp2(fmaf(__uint_as_float(vs[i]), fS, -rb[il])) : 0.f;
         }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          pk[i >> 2] = (uint32_t)e4m3x2(pr[cc][i] * 256.f, pr[cc][i + 1] * 256.f) |
+                       ((uint32_t)e4m3x2(pr[cc][i + 2] * 256.f, pr[cc][i + 3] * 256.f) << 16);
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+      ok = named_bar_and(1, kCompute, mbar_wait(dp_full, k & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * wg + cc;
+        uint32_t vp[32];
+        tmem_ld32(lane_base + kP + 32 * c, vp);
+        tmem_ld_wait();
+        const float fP = sv_row * ue8m0_to_f32(cs[4 + c]);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float ds = pr[cc][i] * fmaf(__uint_as_float(vp[i]), fP, -rb[128 + 32 * c + i]);
+          pr[cc][i] = ds;
+          amax = fmaxf(amax, fabsf(ds));
+        }
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
         const int e = roundup_exp(amax);
         const float sc = exp2i(-e);
+        uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          pk[i >> 2] = (uint32_t)e4m3x2(ds[i] * sc, ds[i + 1] * sc) | ((uint32_t)e4m3x2(ds[i + 2] * sc, ds[i + 3] * sc) << 16);
-        }
+        for (int i = 0; i < 32; i += 4)
+          pk[i >> 2] = (uint32_t)e4m3x2(pr[cc][i] * sc, pr[cc][i + 1] * sc) |
+                       ((uint32_t)e4m3x2(pr[cc][i + 2] * sc, pr[cc][i + 3] * sc) << 16);
         *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        if (lane == 0) reinterpret_cast<uint8_t*>(Esm)[quarter * 4 + c] = (uint8_t)(e + 127);
+        if (lane == 0) Esm[quarter * 4 + c] = (uint8_t)(e + 127);
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kCompute);           // all block exponents written; S^T and dP^T fully read
       {
-        const uint8_t* E = reinterpret_cast<const uint8_t*>(Esm);   // E[key block][query chunk]
+        const uint8_t* E = Esm;               // E[key block][query chunk]
         const uint32_t dosf = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
         const uint32_t qsf = (uint32_t)cs[0] | (uint32_t)cs[1] << 8 | (uint32_t)cs[2] << 16 | (uint32_t)cs[3] << 24;
-        uint32_t dk_a[4], dq_a[4];
+        if (wg == 0) {
+          uint32_t dk_a[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          // dK: A row = key in block cc, byte = query chunk; dQ: A row = query in chunk cc, byte = key block
-          dk_a[cc] = (uint32_t)E[cc * 4 + 0] | (uint32_t)E[cc * 4 + 1] << 8 | (uint32_t)E[cc * 4 + 2] << 16 |
-                     (uint32_t)E[cc * 4 + 3] << 24;
-          dq_a[cc] = (uint32_t)E[0 * 4 + cc] | (uint32_t)E[1 * 4 + cc] << 8 | (uint32_t)E[2 * 4 + cc] << 16 |
-                     (uint32_t)E[3 * 4 + cc] << 24;
+          for (int cc = 0; cc < 4; ++cc)   // dK: A row = key in block cc, byte = query chunk
+            dk_a[cc] = (uint32_t)E[cc * 4 + 0] | (uint32_t)E[cc * 4 + 1] << 8 | (uint32_t)E[cc * 4 + 2] << 16 |
+                       (uint32_t)E[cc * 4 + 3] << 24;
+          tmem_st4(lane_base + kSF + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          tmem_st4(lane_base + kSF + 4, dosf, dosf, dosf, dosf);
+          tmem_st4(lane_base + kSF + 8, dk_a[0], dk_a[1], dk_a[2], dk_a[3]);
+          tmem_st4(lane_base + kSF + 12, qsf, qsf, qsf, qsf);
+        } else {
+          uint32_t dq_a[4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)   // dQ: A row = query in chunk cc, byte = key block
+            dq_a[cc] = (uint32_t)E[0 * 4 + cc] | (uint32_t)E[1 * 4 + cc] << 8 | (uint32_t)E[2 * 4 + cc] << 16 |
+                       (uint32_t)E[3 * 4 + cc] << 24;
+          tmem_st4(lane_base + kSF + 16, dq_a[0], dq_a[1], dq_a[2], dq_a[3]);
+          tmem_st4(lane_base + kSF + 20, ksf, ksf, ksf, ksf);
         }
-        tmem_st4(lane_base + kP + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        tmem_st4(lane_base + kP + 4, dosf, dosf, dosf, dosf);
-        tmem_st4(lane_base + kP + 8, dk_a[0], dk_a[1], dk_a[2], dk_a[3]);
-        tmem_st4(lane_base + kP + 12, qsf, qsf, qsf, qsf);
-        tmem_st4(lane_base + kP + 16, dq_a[0], dq_a[1], dq_a[2], dq_a[3]);
-        tmem_st4(lane_base + kP + 20, ksf, ksf, ksf, ksf);
         tmem_st_wait();
       }
       fence_proxy_async_smem();
       tc_fence_before();
+      mbar_arrive(&row_empty[b]);
       mbar_arrive(p_full);
-      // dQ partial of this step: thread index = query row
-      ok = named_bar_and(1, 128, mbar_wait(dq_full, k & 1, status));
+      // dQ partial of this step: thread index = query row, this warpgroup's half of the columns
+      ok = named_bar_and(1, kCompute, mbar_wait(dq_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
       {
         const int ql = t * kTile + j;
         const bool qv = ql < doc_len;
         const float cb = qv ? p.boost[(int64_t)doc * p.hq + h] : 0.f;
-        __half* dst = p.dq_acc + (((int64_t)doc_start + ql) * p.hq + h) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        __half* dst = p.dq_acc + (((int64_t)doc_start + ql) * p.hq + h) * D + wg * (D / 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
-          tmem_ld32(lane_base + kS + 32 * c, v);
+          tmem_ld32(lane_base + kP + wg * (D / 2) + 32 * c, v);
           tmem_ld_wait();
           if (qv) {
 #pragma unroll
@@ -364,16 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(dq_empty);
     }
-    if (ok) ok = named_bar_and(1, 128, mbar_wait(acc_full, 0, status));
+    if (ok) ok = named_bar_and(1, kCompute, mbar_wait(acc_full, 0, status));
     if (ok) {
       tc_fence_after();
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? kDV : kDK;
+        const uint32_t col = (which == 0 ? kDV : kDK) + wg * (D / 2);
         const float mul = which == 0 ? (1.0f / 256.0f) : p.scale;
-        __nv_bfloat16* orow = (which == 0 ? p.dv : p.dk) + (ktok * p.hkv + hk) * D;
+        __nv_bfloat16* orow = (which == 0 ? p.dv : p.dk) + (ktok * p.hkv + hk) * D + wg * (D / 2);
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
           tmem_ld32(lane_base + col + 32 * c, v);
           tmem_ld_wait();

@@ -234,18 +234,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], u & 1, status));
         if (!ok) break;
         tc_fence_after();
-        // pass 1: row max of x = S * log2(e) over visible keys
+        // pass 1: row max of x = S * log2(e) over visible keys.  The column factor
+        // is a positive power of two times a constant, so max(v * f) = f * max(v).
         float mx = -INFINITY;
+        if (!diag) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t v[32];
-          tmem_ld32(s_addr + 32 * g, v);
-          tmem_ld_wait();
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + 32 * g, v);
+            tmem_ld_wait();
+            float a[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = __uint_as_float(v[j]) * fk[g];
-            const bool vis = !diag || (g * 32 + j) <= r;
-            mx = vis ? fmaxf(mx, x) : mx;
+            for (int q = 0; q < 16; ++q) a[q] = fmaxf(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+            float b = fmax3(a[0], a[1], a[2]);
+            b = fmax3(b, a[3], a[4]);
+            b = fmax3(b, a[5], a[6]);
+            b = fmax3(b, a[7], a[8]);
+            b = fmax3(b, a[9], a[10]);
+            b = fmax3(b, a[11], a[12]);
+            b = fmax3(b, a[13], a[14]);
+            b = fmaxf(b, a[15]);
+            mx = fmaxf(mx, b * fk[g]);
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + 32 * g, v);
+            tmem_ld_wait();
+            float b = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) b = (g * 32 + j) <= r ? fmaxf(b, __uint_as_float(v[j])) : b;
+            mx = fmaxf(mx, b * fk[g]);
           }
         }
         const float m_new = fmaxf(m, mx);
@@ -266,28 +286,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         lsum *= alpha;
         // pass 2: boosted weights 2^(x - m + 8), their E4M3 codes into the P tile
         const float neg = 8.0f - m_new;
+        float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t v[32];
           tmem_ld32(s_addr + 32 * g, v);
           tmem_ld_wait();
           uint32_t packed[8];
+          const float2 f2 = make_float2(fk[g], fk[g]), n2 = make_float2(neg, neg);
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
-            float pw[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const bool vis = !diag || (g * 32 + j + q) <= r;
-              pw[q] = vis ? fast_exp2(fmaf(__uint_as_float(v[j + q]), fk[g], neg)) : 0.f;
-              lsum += pw[q];
+            float2 x0 = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), f2, n2);
+            float2 x1 = ffma2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), f2, n2);
+            float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+            float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+            if (diag) {
+              const int kc = g * 32 + j;
+              p0.x = kc <= r ? p0.x : 0.f;
+              p0.y = kc + 1 <= r ? p0.y : 0.f;
+              p1.x = kc + 2 <= r ? p1.x : 0.f;
+              p1.y = kc + 3 <= r ? p1.y : 0.f;
             }
-            packed[j >> 2] = (uint32_t)e4m3x2(pw[0], pw[1]) | ((uint32_t)e4m3x2(pw[2], pw[3]) << 16);
+            acc2 = fadd2(acc2, fadd2(p0, p1));
+            packed[j >> 2] = (uint32_t)e4m3x2(p0.x, p0.y) | ((uint32_t)e4m3x2(p1.x, p1.y) << 16);
           }
           *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g, 128)) =
               make_uint4(packed[0], packed[1], packed[2], packed[3]);
           *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g + 16, 128)) =
               make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
+        lsum += acc2.x + acc2.y;
         m = m_new;
         // block-scale words of the PV MMA: P^ scale 1.0, V scale per 32-key group
         tmem_st4(s_addr + 120, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);

@@ -66,8 +66,11 @@ __device__ void bitonic_sort(unsigned long long* keys, int n) {  // n is a power
   }
 }
 
+constexpr int kSmemKeys = 4096;   // sorts of up to this many keys run in shared memory
+
 __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restrict__ cu, int N, int T,
                                                         int* __restrict__ plan_words) {
+  __shared__ unsigned long long smem_keys[kSmemKeys];
   __shared__ int warp_sums[32];
   __shared__ int s_bad;
   __shared__ int s_carry[3];
@@ -138,13 +141,13 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     plan_words[kPlanCapacity] = cap;
   }
   if (bad || over) return;
-  unsigned long long* keys = pv.sort_keys;
   const unsigned long long kPad = ~0ull;
   const unsigned kCostMax = 0x7FFFFFFFu;
 
   // 3a. forward items
   {
     const int n2 = (int)pow2_ceil(nitem > 0 ? nitem : 1);
+    unsigned long long* keys = n2 <= kSmemKeys ? smem_keys : pv.sort_keys;
     for (int i = threadIdx.x; i < n2; i += kThreads) {
       unsigned long long key = kPad;
       if (i < nitem) {
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
   // 3b. backward key-tile items
   {
     const int n2 = (int)pow2_ceil(ntile > 0 ? ntile : 1);
+    unsigned long long* keys = n2 <= kSmemKeys ? smem_keys : pv.sort_keys;
     for (int i = threadIdx.x; i < n2; i += kThreads) {
       unsigned long long key = kPad;
       if (i < ntile) {

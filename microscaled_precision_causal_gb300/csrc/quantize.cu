@@ -24,7 +24,7 @@ namespace {
 constexpr int kWarps = 8;
 
 template <int D, bool PER_TOKEN, bool STATS, bool WITH_D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 4)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, const int32_t* __restrict__ cu, int N,
                     const int* __restrict__ plan, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                     float2* __restrict__ stats, const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec,
@@ -42,76 +42,72 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   // rows [r0, r0 + nrows) of this warp; tail rows (no document) get zeros
   int r0, nrows;
-  bool tail;
+  bool tail = false;
   if (PER_TOKEN) {
     r0 = (int)(unit * 32);
     if (r0 >= T) return;
     nrows = min(32, T - r0);
-    tail = false;  // per row below
+  } else if (unit < nblk) {
+    const int doc = upper_doc(pv.blk_prefix, N, (int)unit);
+    const int s0 = cu[doc], s1 = cu[doc + 1];
+    r0 = s0 + ((int)unit - pv.blk_prefix[doc]) * kBlock;
+    nrows = min(kBlock, s1 - r0);
   } else {
-    if (unit < nblk) {
-      const int doc = upper_doc(pv.blk_prefix, N, (int)unit);
-      const int s0 = cu[doc], s1 = cu[doc + 1];
-      r0 = s0 + ((int)unit - pv.blk_prefix[doc]) * kBlock;
-      nrows = min(kBlock, s1 - r0);
-      tail = false;
-    } else {
-      r0 = valid + (int)(unit - nblk) * 32;
-      if (r0 >= T) return;
-      nrows = min(32, T - r0);
-      tail = true;
-    }
+    r0 = valid + (int)(unit - nblk) * 32;
+    if (r0 >= T) return;
+    nrows = min(32, T - r0);
+    tail = true;
   }
   const int sub = lane / kLpr;            // row within an iteration
   const int cb = (lane % kLpr) * 8;       // first of the 8 elements this lane owns
-
-  uint4 raw[kIters];
-  float amax_lane = 0.f;
-  float rowmax[kIters];
-#pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int r = it * kRpi + sub;
-    raw[it] = make_uint4(0, 0, 0, 0);
-    const bool live = r < nrows && !tail && (!PER_TOKEN || r0 + r < valid);
-    if (live) raw[it] = __ldg(reinterpret_cast<const uint4*>(x + ((int64_t)(r0 + r) * H + h) * D + cb));
-    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[it]);
+  auto live = [&](int r) { return r < nrows && !tail && (!PER_TOKEN || r0 + r < valid); };
+  auto load8 = [&](const __nv_bfloat16* base, int r) {
+    return live(r) ? __ldg(reinterpret_cast<const uint4*>(base + ((int64_t)(r0 + r) * H + h) * D + cb))
+                   : make_uint4(0, 0, 0, 0);
+  };
+  auto absmax8 = [](const uint4& w) {
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&w);
     float m = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = __bfloat1622float2(v[j]);
-      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      m = fmax3(m, fabsf(f.x), fabsf(f.y));
     }
-    rowmax[it] = m;
-    amax_lane = fmaxf(amax_lane, m);
-  }
+    return m;
+  };
+
+  // pass 1 (token blocks): amax over the whole block; the data are re-read from
+  // L1/L2 in pass 2 instead of being held in registers.
   int e_block = 0;
   if (!PER_TOKEN) {
+    uint4 w[kIters];
 #pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) amax_lane = fmaxf(amax_lane, __shfl_xor_sync(0xffffffffu, amax_lane, o2));
-    e_block = roundup_exp(amax_lane);
+    for (int it = 0; it < kIters; ++it) w[it] = load8(x, it * kRpi + sub);
+    float a = 0.f;
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) a = fmaxf(a, absmax8(w[it]));
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o2));
+    e_block = roundup_exp(a);
   }
-#pragma unroll
+#pragma unroll 2
   for (int it = 0; it < kIters; ++it) {
     const int r = it * kRpi + sub;
     const bool inrange = r < nrows;
+    const uint4 raw = load8(x, r);
     int e = e_block;
     if (PER_TOKEN) {
-      float m = rowmax[it];
+      float m = absmax8(raw);
 #pragma unroll
       for (int o2 = kLpr / 2; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
       e = roundup_exp(m);
     }
     const float s = exp2i(-e);
-    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[it]);
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
     uint32_t packed[2];
     float ss = 0.f, mx = 0.f, dd = 0.f;
     const float back = ue8m0_to_f32((uint32_t)(e + 127));
-    uint4 oraw = make_uint4(0, 0, 0, 0);
-    if (WITH_D && inrange && !tail) {
-      const int64_t row = r0 + r;
-      if (!PER_TOKEN || row < valid)
-        oraw = __ldg(reinterpret_cast<const uint4*>(o + (row * H + h) * D + cb));
-    }
+    const uint4 oraw = WITH_D ? load8(o, r) : make_uint4(0, 0, 0, 0);
     const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oraw);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -123,7 +119,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         const float b = e4m3_to_f32((uint8_t)(c2 >> 8)) * back;
         if (STATS) {
           ss = fmaf(a, a, fmaf(b, b, ss));
-          mx = fmaxf(mx, fmaxf(fabsf(a), fabsf(b)));
+          mx = fmax3(mx, fabsf(a), fabsf(b));
         }
         if (WITH_D) {
           const float2 of = __bfloat1622float2(ov[j]);
