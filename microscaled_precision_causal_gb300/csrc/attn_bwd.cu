@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(&row_full[b]);
     }
-  } else {
-    // ------------------------------------------------------------ compute
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute (warps 4-11)
     const int wg = (warp - 4) >> 2;                    // query columns [64 wg, 64 wg + 64)
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;                 // key row (TMEM lane) for S / dP; query row for dQ
