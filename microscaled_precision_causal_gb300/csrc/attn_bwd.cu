@@ -13,7 +13,9 @@
 //   dV  += E4M3(2^8 P)^T dO^ / 2^8     (MXF8, dO's scale per 32 queries)
 //   dK  += dS^^T Q^                    (MXF8, dS block and Q scales per 32 queries)
 //   dQp  = dS^ K^                      (MXF8, same dS codes read transposed)
-//   dQacc += fp16(c * dQp)             (section 4, boosted FP16 partials)
+//   dQacc += fp16(c * dQp)             (section 4, boosted FP16 partials; staged in
+//                                       shared memory, reduce-added with coalesced
+//                                       16-byte red.global.add.f16x2)
 //
 // One CTA per (document-local 128-key tile, kv head); it visits every query
 // head of the kv head's group and every query tile at or after the key tile.
@@ -70,9 +72,11 @@ struct BwdSmem {
   static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query]
   static constexpr int kDS = kPt + kTile * kTile;             // dS^ codes, [key][query]
   static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
-  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // lse2[128], D[128], chunk scales[8]
+  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // -lse2[128], -D[128], chunk scales[8]
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents
-  static constexpr int kBar = kE + 64;
+  static constexpr int kStageBytes = kTile * D;               // one warpgroup's fp16 half of the dQ tile
+  static constexpr int kStage = (kE + 64 + 1023) & ~1023;     // [warpgroup]
+  static constexpr int kBar = kStage + 2 * kStageBytes;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -259,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ql = t * kTile + i;
         const bool qv = ql < doc_len;
         const int64_t qtok = (int64_t)doc_start + ql;
-        rb[i] = qv ? p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : INFINITY;
-        rb[128 + i] = qv ? p.dvec[(int64_t)h * p.T + qtok] : 0.f;
+        rb[i] = qv ? -p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : -INFINITY;
+        rb[128 + i] = qv ? -p.dvec[(int64_t)h * p.T + qtok] : 0.f;
       }
       if (lane < 8) {
         const int c = lane & 3;
@@ -312,17 +316,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_base + kS + 32 * c, vs);
         tmem_ld_wait();
         const float fS = p.scale_log2 * sk_row * ue8m0_to_f32(cs[c]);
+        const float2 fS2 = make_float2(fS, fS), b2 = make_float2(256.f, 256.f);
+        const float4* nl4 = reinterpret_cast<const float4*>(rb + 32 * c);   // -LSE * log2(e)
         uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int il = 32 * c + i;
-          const bool vis = !diag || il >= j;
-          pr[cc][i] = vis ? fast_exp2(fmaf(__uint_as_float(vs[i]), fS, -rb[il])) : 0.f;
+        for (int i = 0; i < 32; i += 4) {
+          const float4 nl = nl4[i >> 2];
+          float2 x0 = ffma2(make_float2(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1])), fS2, make_float2(nl.x, nl.y));
+          float2 x1 = ffma2(make_float2(__uint_as_float(vs[i + 2]), __uint_as_float(vs[i + 3])), fS2, make_float2(nl.z, nl.w));
+          float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+          float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+          if (diag) {
+            const int il = 32 * c + i;
+            p0.x = il >= j ? p0.x : 0.f;
+            p0.y = il + 1 >= j ? p0.y : 0.f;
+            p1.x = il + 2 >= j ? p1.x : 0.f;
+            p1.y = il + 3 >= j ? p1.y : 0.f;
+          }
+          pr[cc][i] = p0.x; pr[cc][i + 1] = p0.y; pr[cc][i + 2] = p1.x; pr[cc][i + 3] = p1.y;
+          const float2 q0 = fmul2(p0, b2), q1 = fmul2(p1, b2);
+          pk[i >> 2] = (uint32_t)e4m3x2(q0.x, q0.y) | ((uint32_t)e4m3x2(q1.x, q1.y) << 16);
         }
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          pk[i >> 2] = (uint32_t)e4m3x2(pr[cc][i] * 256.f, pr[cc][i + 1] * 256.f) |
-                       ((uint32_t)e4m3x2(pr[cc][i + 2] * 256.f, pr[cc][i + 3] * 256.f) << 16);
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
@@ -336,22 +350,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_base + kP + 32 * c, vp);
         tmem_ld_wait();
         const float fP = sv_row * ue8m0_to_f32(cs[4 + c]);
+        const float2 fP2 = make_float2(fP, fP);
+        const float4* nd4 = reinterpret_cast<const float4*>(rb + 128 + 32 * c);   // -D
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float ds = pr[cc][i] * fmaf(__uint_as_float(vp[i]), fP, -rb[128 + 32 * c + i]);
-          pr[cc][i] = ds;
-          amax = fmaxf(amax, fabsf(ds));
+        for (int i = 0; i < 32; i += 4) {
+          const float4 nd = nd4[i >> 2];
+          const float2 t0 = ffma2(make_float2(__uint_as_float(vp[i]), __uint_as_float(vp[i + 1])), fP2, make_float2(nd.x, nd.y));
+          const float2 t1 = ffma2(make_float2(__uint_as_float(vp[i + 2]), __uint_as_float(vp[i + 3])), fP2, make_float2(nd.z, nd.w));
+          const float2 d0 = fmul2(make_float2(pr[cc][i], pr[cc][i + 1]), t0);
+          const float2 d1 = fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), t1);
+          pr[cc][i] = d0.x; pr[cc][i + 1] = d0.y; pr[cc][i + 2] = d1.x; pr[cc][i + 3] = d1.y;
+          amax = fmax3(amax, fabsf(d0.x), fabsf(d0.y));
+          amax = fmax3(amax, fabsf(d1.x), fabsf(d1.y));
         }
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
         const int e = roundup_exp(amax);
         const float sc = exp2i(-e);
+        const float2 sc2 = make_float2(sc, sc);
         uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          pk[i >> 2] = (uint32_t)e4m3x2(pr[cc][i] * sc, pr[cc][i + 1] * sc) |
-                       ((uint32_t)e4m3x2(pr[cc][i + 2] * sc, pr[cc][i + 3] * sc) << 16);
+        for (int i = 0; i < 32; i += 4) {
+          const float2 q0 = fmul2(make_float2(pr[cc][i], pr[cc][i + 1]), sc2);
+          const float2 q1 = fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), sc2);
+          pk[i >> 2] = (uint32_t)e4m3x2(q0.x, q0.y) | ((uint32_t)e4m3x2(q1.x, q1.y) << 16);
+        }
         *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         if (lane == 0) Esm[quarter * 4 + c] = (uint8_t)(e + 127);
@@ -391,31 +415,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       {
+        // read this warpgroup's half of the dQ partial, release the TMEM columns,
+        // stage c * partial as fp16 in shared memory, then reduce-add it into the
+        // fp16 accumulator (rows outside the document are skipped).
         const int ql = t * kTile + j;
         const bool qv = ql < doc_len;
         const float cb = qv ? p.boost[(int64_t)doc * p.hq + h] : 0.f;
-        __half* dst = p.dq_acc + (((int64_t)doc_start + ql) * p.hq + h) * D + wg * (D / 2);
+        uint32_t v[D / 2];
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + kP + wg * (D / 2) + 32 * c, v);
-          tmem_ld_wait();
-          if (qv) {
+        for (int c = 0; c < D / 64; ++c) tmem_ld32(lane_base + kP + wg * (D / 2) + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        uint8_t* sb = smem + L::kStage + wg * L::kStageBytes;
+        const float2 cb2 = make_float2(cb, cb);
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint32_t hw[4];
+        for (int c16 = 0; c16 < D / 16; ++c16) {  // 16-byte chunks of this row's D/2 fp16 values
+          uint32_t hw[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                __half2 h2 = __floats2half2_rn(__uint_as_float(v[i + 2 * q]) * cb, __uint_as_float(v[i + 2 * q + 1]) * cb);
-                hw[q] = *reinterpret_cast<uint32_t*>(&h2);
-              }
-              red_add_f16x8(dst + 32 * c + i, hw[0], hw[1], hw[2], hw[3]);
-            }
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = fmul2(make_float2(__uint_as_float(v[8 * c16 + 2 * q]), __uint_as_float(v[8 * c16 + 2 * q + 1])), cb2);
+            __half2 h2 = __floats2half2_rn(f.x, f.y);
+            hw[q] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(sb + swz_offset(j, 16 * c16, D)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+        named_bar_sync(2 + wg, 128);
+        // coalesced reduce-add: a warp covers whole 16-byte-chunked rows (4 rows of
+        // 128 B for D = 128), so every red instruction touches complete lines
+        constexpr int kChunks = D / 16;                     // 16-byte chunks per staged row
+        const int tw = threadIdx.x & 127;
+#pragma unroll
+        for (int it = 0; it < kChunks; ++it) {
+          const int qc = it * 128 + tw;
+          const int row = qc / kChunks, ch = qc % kChunks;
+          const int qrl = t * kTile + row;
+          if (qrl < doc_len) {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(sb + swz_offset(row, 16 * ch, D));
+            __half* dst = p.dq_acc + (((int64_t)doc_start + qrl) * p.hq + h) * D + wg * (D / 2) + 8 * ch;
+            red_add_f16x8(dst, w4.x, w4.y, w4.z, w4.w);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(dq_empty);
     }
     if (ok) ok = named_bar_and(1, kCompute, mbar_wait(acc_full, 0, status));
     if (ok) {

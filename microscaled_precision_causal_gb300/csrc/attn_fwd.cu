@@ -238,24 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is a positive power of two times a constant, so max(v * f) = f * max(v).
         float mx = -INFINITY;
         if (!diag) {
+          // fused TMEM load + row max (all keys visible)
+          float cm[4];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            uint32_t v[32];
-            tmem_ld32(s_addr + 32 * g, v);
-            tmem_ld_wait();
-            float a[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) a[q] = fmaxf(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-            float b = fmax3(a[0], a[1], a[2]);
-            b = fmax3(b, a[3], a[4]);
-            b = fmax3(b, a[5], a[6]);
-            b = fmax3(b, a[7], a[8]);
-            b = fmax3(b, a[9], a[10]);
-            b = fmax3(b, a[11], a[12]);
-            b = fmax3(b, a[13], a[14]);
-            b = fmaxf(b, a[15]);
-            mx = fmaxf(mx, b * fk[g]);
+            uint32_t v[32];               // the values are not needed here, only their max
+            tmem_ld32_max(s_addr + 32 * g, v, cm[g]);
+            tmem_ld_wait();               // before the registers can be reused
           }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) mx = fmaxf(mx, cm[g] * fk[g]);
         } else {
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
