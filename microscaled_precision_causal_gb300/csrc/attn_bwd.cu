@@ -19,13 +19,14 @@
 //
 // One CTA per (document-local 128-key tile, kv head); it visits every query
 // head of the kv head's group and every query tile at or after the key tile.
-// Roles (384 threads):
+// Roles (640 threads at d = 128, 384 at d = 64):
 //   warp 0      TMA producer (K, V once; Q and dO codes per step)
 //   warp 1      MMA issuer (one thread)
 //   warp 2      TMEM allocator
 //   warp 3      per-query row data of the next steps (LSE, D, chunk scales) into SMEM
-//   warps 4-7   compute warpgroup 0: query columns 0-63 of each step
-//   warps 8-11  compute warpgroup 1: query columns 64-127
+//   warps 4..    compute warpgroups (four at d = 128, two at d = 64): each owns
+//               32 of the 128 query columns of a step and 32 of the head-dim
+//               columns of the dQ partial and the dK / dV accumulators
 // Thread = key row while building P^ and dS^ codes, = query row while reading
 // the dQ partial.  TMEM: S^T [0,128) (its last 24 columns carry the block-scale
 // words of the three MXF8 MMAs once S^T has been read), dP^T / dQ partial
@@ -40,9 +41,17 @@ namespace flamia {
 
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kCompute = 256;       // two compute warpgroups
 constexpr int kQStages = 2;
+// Compute warpgroups: each owns 32 of the 128 query columns of a step (as 4 / kWG
+// chunks of 32) and 32 of the head-dim columns of dQ / dK / dV.
+template <int D>
+struct BwdShape {
+  static constexpr int kWG = D == 128 ? 4 : 2;
+  static constexpr int kChunksPerWG = 4 / kWG;
+  static constexpr int kCols = D / kWG;                     // head-dim columns per warpgroup (32)
+  static constexpr int kCompute = 128 * kWG;
+  static constexpr int kThreads = 128 + kCompute;
+};
 
 struct BwdParams {
   const uint8_t* q_scales;
@@ -74,9 +83,9 @@ struct BwdSmem {
   static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
   static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // -lse2[128], -D[128], chunk scales[8]
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents
-  static constexpr int kStageBytes = kTile * D;               // one warpgroup's fp16 half of the dQ tile
+  static constexpr int kStageBytes = kTile * BwdShape<D>::kCols * 2;   // one warpgroup's fp16 slice of the dQ tile
   static constexpr int kStage = (kE + 64 + 1023) & ~1023;     // [warpgroup]
-  static constexpr int kBar = kStage + 2 * kStageBytes;
+  static constexpr int kBar = kStage + BwdShape<D>::kWG * kStageBytes;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -91,11 +100,13 @@ __device__ __forceinline__ void red_add_f16x8(__half* dst, uint32_t a, uint32_t 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams p) {
   using L = BwdSmem<D>;
+  constexpr int kWG = BwdShape<D>::kWG, kCPW = BwdShape<D>::kChunksPerWG, kCols = BwdShape<D>::kCols;
+  constexpr int kCompute = BwdShape<D>::kCompute;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -277,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&row_full[b]);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ compute (warps 4-11)
-    const int wg = (warp - 4) >> 2;                    // query columns [64 wg, 64 wg + 64)
+    // ------------------------------------------------------------ compute (warps 4 .. 4 + 4 kWG - 1)
+    const int wg = (warp - 4) >> 2;                    // query columns [32 kCPW wg, 32 kCPW (wg + 1))
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;                 // key row (TMEM lane) for S / dP; query row for dQ
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
@@ -296,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* Esm = smem + L::kE;
     uint8_t* sPt = smem + L::kPt;
     uint8_t* sDS = smem + L::kDS;
+    uint8_t* sb = smem + L::kStage + wg * L::kStageBytes;
     bool ok = true;
     for (int k = 0; k < nsteps; ++k) {
       const int hh = k / qtiles, t = u + k % qtiles;
@@ -307,11 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
-      // P = 2^(x - LSE log2 e) for this warpgroup's two query chunks
-      float pr[2][32];
+      // P = 2^(x - LSE log2 e) for this warpgroup's query chunks
+      float pr[kCPW][32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * wg + cc;
+      for (int cc = 0; cc < kCPW; ++cc) {
+        const int c = kCPW * wg + cc;
         uint32_t vs[32];
         tmem_ld32(lane_base + kS + 32 * c, vs);
         tmem_ld_wait();
@@ -344,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * wg + cc;
+      for (int cc = 0; cc < kCPW; ++cc) {
+        const int c = kCPW * wg + cc;
         uint32_t vp[32];
         tmem_ld32(lane_base + kP + 32 * c, vp);
         tmem_ld_wait();
@@ -382,27 +394,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar_sync(1, kCompute);           // all block exponents written; S^T and dP^T fully read
       {
+        // block-scale words of the three MXF8 MMAs, one operand pair per warpgroup
         const uint8_t* E = Esm;               // E[key block][query chunk]
-        const uint32_t dosf = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
-        const uint32_t qsf = (uint32_t)cs[0] | (uint32_t)cs[1] << 8 | (uint32_t)cs[2] << 16 | (uint32_t)cs[3] << 24;
-        if (wg == 0) {
-          uint32_t dk_a[4];
+        const int pair0 = wg, pair1 = wg + kWG;   // pairs 0 = dV, 1 = dK, 2 = dQ
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)   // dK: A row = key in block cc, byte = query chunk
-            dk_a[cc] = (uint32_t)E[cc * 4 + 0] | (uint32_t)E[cc * 4 + 1] << 8 | (uint32_t)E[cc * 4 + 2] << 16 |
-                       (uint32_t)E[cc * 4 + 3] << 24;
-          tmem_st4(lane_base + kSF + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          tmem_st4(lane_base + kSF + 4, dosf, dosf, dosf, dosf);
-          tmem_st4(lane_base + kSF + 8, dk_a[0], dk_a[1], dk_a[2], dk_a[3]);
-          tmem_st4(lane_base + kSF + 12, qsf, qsf, qsf, qsf);
-        } else {
-          uint32_t dq_a[4];
+        for (int pi = 0; pi < 2; ++pi) {
+          const int pair = pi == 0 ? pair0 : pair1;
+          if (pair > 2) continue;
+          uint32_t a[4], bw;
+          if (pair == 0) {          // dV: A = P^ (scale 1), B = dO per query chunk
+            a[0] = a[1] = a[2] = a[3] = 0x7F7F7F7Fu;
+            bw = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
+          } else if (pair == 1) {   // dK: A row = key in block cc, byte = query chunk; B = Q per query chunk
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)   // dQ: A row = query in chunk cc, byte = key block
-            dq_a[cc] = (uint32_t)E[0 * 4 + cc] | (uint32_t)E[1 * 4 + cc] << 8 | (uint32_t)E[2 * 4 + cc] << 16 |
-                       (uint32_t)E[3 * 4 + cc] << 24;
-          tmem_st4(lane_base + kSF + 16, dq_a[0], dq_a[1], dq_a[2], dq_a[3]);
-          tmem_st4(lane_base + kSF + 20, ksf, ksf, ksf, ksf);
+            for (int cc = 0; cc < 4; ++cc)
+              a[cc] = (uint32_t)E[cc * 4 + 0] | (uint32_t)E[cc * 4 + 1] << 8 | (uint32_t)E[cc * 4 + 2] << 16 |
+                      (uint32_t)E[cc * 4 + 3] << 24;
+            bw = (uint32_t)cs[0] | (uint32_t)cs[1] << 8 | (uint32_t)cs[2] << 16 | (uint32_t)cs[3] << 24;
+          } else {                  // dQ: A row = query in chunk cc, byte = key block; B = K per key block
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              a[cc] = (uint32_t)E[0 * 4 + cc] | (uint32_t)E[1 * 4 + cc] << 8 | (uint32_t)E[2 * 4 + cc] << 16 |
+                      (uint32_t)E[3 * 4 + cc] << 24;
+            bw = ksf;
+          }
+          tmem_st4(lane_base + kSF + 8 * pair, a[0], a[1], a[2], a[3]);
+          tmem_st4(lane_base + kSF + 8 * pair + 4, bw, bw, bw, bw);
         }
         tmem_st_wait();
       }
@@ -410,27 +427,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&row_empty[b]);
       mbar_arrive(p_full);
-      // dQ partial of this step: thread index = query row, this warpgroup's half of the columns
+      // dQ partial of this step: thread index = query row, this warpgroup's kCols columns
       ok = named_bar_and(1, kCompute, mbar_wait(dq_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
       {
-        // read this warpgroup's half of the dQ partial, release the TMEM columns,
+        // read this warpgroup's columns of the dQ partial, release the TMEM columns,
         // stage c * partial as fp16 in shared memory, then reduce-add it into the
         // fp16 accumulator (rows outside the document are skipped).
         const int ql = t * kTile + j;
         const bool qv = ql < doc_len;
         const float cb = qv ? p.boost[(int64_t)doc * p.hq + h] : 0.f;
-        uint32_t v[D / 2];
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tmem_ld32(lane_base + kP + wg * (D / 2) + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+        uint32_t v[32];
+        tmem_ld32(lane_base + kP + wg * kCols, v);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(dq_empty);
-        uint8_t* sb = smem + L::kStage + wg * L::kStageBytes;
         const float2 cb2 = make_float2(cb, cb);
+        constexpr int kRowBytes = kCols * 2;                // 64: one staged row of fp16
+        constexpr int kChunks = kRowBytes / 16;             // 16-byte chunks per staged row
 #pragma unroll
-        for (int c16 = 0; c16 < D / 16; ++c16) {  // 16-byte chunks of this row's D/2 fp16 values
+        for (int c16 = 0; c16 < kChunks; ++c16) {
           uint32_t hw[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -438,12 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __half2 h2 = __floats2half2_rn(f.x, f.y);
             hw[q] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(sb + swz_offset(j, 16 * c16, D)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(sb + swz_offset(j, 16 * c16, kRowBytes)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         }
         named_bar_sync(2 + wg, 128);
-        // coalesced reduce-add: a warp covers whole 16-byte-chunked rows (4 rows of
-        // 128 B for D = 128), so every red instruction touches complete lines
-        constexpr int kChunks = D / 16;                     // 16-byte chunks per staged row
+        // coalesced reduce-add: consecutive lanes cover consecutive 16-byte chunks of
+        // consecutive staged rows
         const int tw = threadIdx.x & 127;
 #pragma unroll
         for (int it = 0; it < kChunks; ++it) {
@@ -451,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = qc / kChunks, ch = qc % kChunks;
           const int qrl = t * kTile + row;
           if (qrl < doc_len) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(sb + swz_offset(row, 16 * ch, D));
-            __half* dst = p.dq_acc + (((int64_t)doc_start + qrl) * p.hq + h) * D + wg * (D / 2) + 8 * ch;
+            const uint4 w4 = *reinterpret_cast<const uint4*>(sb + swz_offset(row, 16 * ch, kRowBytes));
+            __half* dst = p.dq_acc + (((int64_t)doc_start + qrl) * p.hq + h) * D + wg * kCols + 8 * ch;
             red_add_f16x8(dst, w4.x, w4.y, w4.z, w4.w);
           }
         }
@@ -463,25 +479,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which == 0 ? kDV : kDK) + wg * (D / 2);
+        const uint32_t col = (which == 0 ? kDV : kDK) + wg * kCols;
         const float mul = which == 0 ? (1.0f / 256.0f) : p.scale;
-        __nv_bfloat16* orow = (which == 0 ? p.dv : p.dk) + (ktok * p.hkv + hk) * D + wg * (D / 2);
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + col + 32 * c, v);
-          tmem_ld_wait();
-          if (key_valid) {
-            uint32_t pk[16];
+        __nv_bfloat16* orow = (which == 0 ? p.dv : p.dk) + (ktok * p.hkv + hk) * D + wg * kCols;
+        uint32_t v[32];
+        tmem_ld32(lane_base + col, v);
+        tmem_ld_wait();
+        if (key_valid) {
+          uint32_t pk[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]) * mul, __uint_as_float(v[2 * q + 1]) * mul);
-              pk[q] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 16; ++q) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]) * mul, __uint_as_float(v[2 * q + 1]) * mul);
+            pk[q] = *reinterpret_cast<uint32_t*>(&b2);
           }
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
     }
@@ -624,7 +637,7 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
-  attn_bwd_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_kernel<D><<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
   if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
