@@ -81,7 +81,7 @@ struct BwdSmem {
   static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query]
   static constexpr int kDS = kPt + kTile * kTile;             // dS^ codes, [key][query]
   static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
-  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // -lse2[128], -D[128], chunk scales[8]
+  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // -lse2[128], -D[128], chunk scales[8], dQ boost
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents
   static constexpr int kStageBytes = kTile * BwdShape<D>::kCols * 2;   // one warpgroup's fp16 slice of the dQ tile
   static constexpr int kStage = (kE + 64 + 1023) & ~1023;     // [warpgroup]
@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         rb[i] = qv ? -p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : -INFINITY;
         rb[128 + i] = qv ? -p.dvec[(int64_t)h * p.T + qtok] : 0.f;
       }
+      if (lane == 8) rb[258] = p.boost[(int64_t)doc * p.hq + h];   // dQ boost of (document, query head)
       if (lane < 8) {
         const int c = lane & 3;
         const int ql = t * kTile + c * 32;
@@ -319,6 +320,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
+      const float boost_step = rb[258];    // read before the row buffer is released below
       // P = 2^(x - LSE log2 e) for this warpgroup's query chunks
       float pr[kCPW][32];
 #pragma unroll
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         // fp16 accumulator (rows outside the document are skipped).
         const int ql = t * kTile + j;
         const bool qv = ql < doc_len;
-        const float cb = qv ? p.boost[(int64_t)doc * p.hq + h] : 0.f;
+        const float cb = qv ? boost_step : 0.f;
         uint32_t v[32];
         tmem_ld32(lane_base + kP + wg * kCols, v);
         tmem_ld_wait();

@@ -217,19 +217,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, lsum = 0.f;
       bool ok = true;
       const int nk = nk_w[w];
-      for (int u = 0; u < nk; ++u) {
-        // key-tile column factors and V block scales (one per 32-key group)
-        float fk[4];
-        uint32_t vsf = 0;
+      // K / V block-scale bytes of one key tile (one per 32-key group), fetched a
+      // tile ahead so their global-load latency overlaps the current tile
+      auto fetch_scales = [&](int uu, uint32_t& kw, uint32_t& vw) {
+        kw = 0x7F7F7F7Fu;
+        vw = 0x7F7F7F7Fu;
+        if (uu >= nk) return;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const int kl = u * kTile + g * 32;
-          const bool kv = kl < doc_len;
-          const int64_t ktok = (int64_t)doc_start + kl;
-          fk[g] = fq * scale_of(p.k_scales, ktok, p.hkv, hk, kv);
-          const uint32_t vb = kv ? p.v_scales[ktok * p.hkv + hk] : 127u;
-          vsf |= vb << (8 * g);
+          const int kl = uu * kTile + g * 32;
+          if (kl < doc_len) {
+            const int64_t ktok = (int64_t)doc_start + kl;
+            kw = (kw & ~(0xFFu << (8 * g))) | ((uint32_t)p.k_scales[ktok * p.hkv + hk] << (8 * g));
+            vw = (vw & ~(0xFFu << (8 * g))) | ((uint32_t)p.v_scales[ktok * p.hkv + hk] << (8 * g));
+          }
         }
+      };
+      uint32_t kw_next, vw_next;
+      fetch_scales(0, kw_next, vw_next);
+      for (int u = 0; u < nk; ++u) {
+        const uint32_t kw = kw_next, vsf = vw_next;
+        fetch_scales(u + 1, kw_next, vw_next);
+        float fk[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) fk[g] = fq * ue8m0_to_f32((kw >> (8 * g)) & 0xFFu);
         const bool diag = (u == t);
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], u & 1, status));
         if (!ok) break;
