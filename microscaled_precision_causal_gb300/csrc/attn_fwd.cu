@@ -53,7 +53,9 @@ struct FwdSmem {
   static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kP = kV + kStages * kTileBytes;
-  static constexpr int kBar = kP + 2 * kTile * kTile;
+  static constexpr int kScaleTab = kP + 2 * kTile * kTile;      // per key tile: K word, V word
+  static constexpr int kMaxTabTiles = 4096;
+  static constexpr int kBar = kScaleTab + kMaxTabTiles * 8;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;           // slack for 1024-byte alignment
 };
@@ -109,6 +111,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
+  }
+  // K / V block-scale bytes of every key tile of the item (one byte per 32-key
+  // group, 127 past the document end), staged once so the softmax loop reads
+  // them from shared memory
+  uint32_t* scale_tab = reinterpret_cast<uint32_t*>(smem + L::kScaleTab);
+  const bool tab_ok = nkv <= L::kMaxTabTiles;
+  if (tab_ok) {
+    uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
+    for (int i = threadIdx.x; i < nkv * 4; i += kThreads) {
+      const int uu = i >> 2, gg = i & 3;
+      const int kl = uu * kTile + gg * 32;
+      const int64_t ktok = (int64_t)doc_start + kl;
+      const bool kv = kl < doc_len;
+      tb[uu * 8 + gg] = kv ? p.k_scales[ktok * p.hkv + hk] : (uint8_t)127;
+      tb[uu * 8 + 4 + gg] = kv ? p.v_scales[ktok * p.hkv + hk] : (uint8_t)127;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -217,12 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, lsum = 0.f;
       bool ok = true;
       const int nk = nk_w[w];
-      // K / V block-scale bytes of one key tile (one per 32-key group), fetched a
-      // tile ahead so their global-load latency overlaps the current tile
-      auto fetch_scales = [&](int uu, uint32_t& kw, uint32_t& vw) {
+      auto tile_scales = [&](int uu, uint32_t& kw, uint32_t& vw) {
+        if (tab_ok) {
+          const uint2 kv2 = *reinterpret_cast<const uint2*>(scale_tab + 2 * uu);
+          kw = kv2.x;
+          vw = kv2.y;
+          return;
+        }
         kw = 0x7F7F7F7Fu;
         vw = 0x7F7F7F7Fu;
-        if (uu >= nk) return;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int kl = uu * kTile + g * 32;
@@ -233,11 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      uint32_t kw_next, vw_next;
-      fetch_scales(0, kw_next, vw_next);
       for (int u = 0; u < nk; ++u) {
-        const uint32_t kw = kw_next, vsf = vw_next;
-        fetch_scales(u + 1, kw_next, vw_next);
+        uint32_t kw, vsf;
+        tile_scales(u, kw, vsf);
         float fk[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) fk[g] = fq * ue8m0_to_f32((kw >> (8 * g)) & 0xFFu);
