@@ -43,7 +43,7 @@ __all__ = [
     "quantize_nvfp4", "dequantize_nvfp4",
     "Options", "attention_forward", "attention_backward", "run_training_call",
     "dense_attention", "dense_attention_grads", "visible_pairs", "work_list",
-    "bwd_key_tile_list", "dq_boost", "doc_ranges",
+    "bwd_key_tile_list", "dq_boost", "causal_dq_boost", "doc_ranges",
 ]
 
 E4M3_MAX = 448.0          # largest finite E4M3 magnitude ([FA] "Lower precision", format table)
@@ -323,6 +323,8 @@ def bwd_key_tile_list(cu, tile: int = 128):
 class Options:
     quantized: bool = True         # False: every codec is the identity
     block: int = 32                # operand token-block length (1 = strict per-token)
+    strict: bool = False           # strict options: per-token scales folded into the companion
+                                   # operand, per-query-row dS exponents, causal dQ boost
     rule: str = "roundup"          # operand exponent rule ("floor" = negative control)
     p_boost_log2: int = 8          # beta = 2**8 for the forward P operand (reading C-4)
     p_lag_log2: int = 0            # tau: how far the retained max may lag (reading C-4)
@@ -339,7 +341,7 @@ def _masked_scores(Qt, Ku, qpos, kpos, scale):
 
 def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] = None,
                       opts: Options = Options(), heads: Optional[Iterable[int]] = None,
-                      q_tiles: Optional[Dict[int, Iterable[int]]] = None):
+                      q_tiles: Optional[Dict[int, Iterable[int]]] = None, v_scale=None):
     """Forward of Algorithm 1 (steps 04-08) for causal packed documents.
 
     Qh [T,hq,d], Kh/Vh [T,hkv,d]: reconstructed operands X^ = s*c (or plain
@@ -355,7 +357,14 @@ def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] 
 
     and finish with O = bf16(acc / l), LSE = m + ln l ([EN] section 2 "Why
     flash tiling recomputes scores").  Rows outside every document keep O = 0
-    and LSE = +inf ([EN] section 6).  Returns (O [T,hq,d], LSE [hq,T])."""
+    and LSE = +inf ([EN] section 6).
+
+    Strict options ([EN] section 4, "Folding a local scale into the companion
+    operand"; reading in the design notes): operands carry per-token scales
+    (v_scale [T, hkv] for V); the per-key V scale is folded into the
+    probability operand, P~_ij = beta p_ij s_V(j), which is E4M3-rounded with
+    one round-up exponent per (query row, document-local 32-key group), and
+    multiplies the V codes.  Returns (O [T,hq,d], LSE [hq,T])."""
     Qh = np.asarray(Qh, np.float64); Kh = np.asarray(Kh, np.float64); Vh = np.asarray(Vh, np.float64)
     T, _, d = Qh.shape
     g = hq // hkv
@@ -366,6 +375,7 @@ def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] 
     O = np.zeros((T, hq, d))
     LSE = np.full((hq, T), np.inf)
     heads = range(hq) if heads is None else heads
+    V_scale = np.asarray(v_scale, np.float64) if opts.strict else None   # [T, hkv] powers of two
     for n, (s0, s1) in enumerate(doc_ranges(cu)):
         ntile = -(-(s1 - s0) // tile)
         tiles = range(ntile) if q_tiles is None else q_tiles.get(n, ())
@@ -386,7 +396,15 @@ def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] 
                     alpha = np.where(np.isfinite(m), np.exp(m - m_new), 0.0)
                     p = np.exp(S - m_new[:, None])
                     l = l * alpha + p.sum(axis=1)
-                    Pq = e4m3_round(beta * p) / beta if opts.quantized else p
+                    if not opts.quantized:
+                        Pq = p
+                    elif opts.strict:
+                        # per-key V scale folded into P, quantized with one round-up exponent
+                        # per (query row, document-local 32-key group)
+                        sv = V_scale[c0:c1, hk]
+                        Pq = _fold_quantize(beta * p * sv[None, :], group_axis=1, offset=c0 - s0) / (beta * sv[None, :])
+                    else:
+                        Pq = e4m3_round(beta * p) / beta
                     acc = acc * alpha[:, None] + Pq @ Vh[c0:c1, hk]
                     m = m_new
                 out = acc / l[:, None]
@@ -418,7 +436,7 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                        kv_heads: Optional[Iterable[int]] = None,
                        k_tiles: Optional[Dict[int, Iterable[int]]] = None,
                        q_tiles: Optional[Dict[int, Iterable[int]]] = None,
-                       diagnostics: bool = False):
+                       diagnostics: bool = False, tok_scales: Optional[dict] = None):
     """Backward of Algorithm 1 (steps 09-16).
 
     dOh: the reconstructed incoming gradient dO^ (encoded once, step 09);
@@ -438,6 +456,14 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
     then dK = bf16(scale * dK), dV = bf16(dV), dQ = bf16(scale * accQ / c)
     (step 16).  Unquantized: every codec is the identity and accQ is exact.
 
+    Strict options (tok_scales = per-token powers of two of q, k, do): the
+    per-token scale of the contraction-axis operand is folded into its
+    companion, which is E4M3-rounded with one round-up exponent per (row of the
+    companion, document-local 32-token group): dV uses beta P s_dO(i) per (key,
+    32-query group); dK uses dS s_Q(i) per (key, 32-query group); dQ uses
+    dS s_K(j) per (query row, 32-key block) -- the per-query-row dS exponent
+    ("K fold").  The dQ boost is the causal per-row c_i (causal_dq_boost).
+
     k_tiles / q_tiles restrict which dK/dV key tiles and dQ query tiles are
     produced (others stay zero); kv_heads restricts heads.
     Returns dict with dq, dk, dv (and diagnostics when asked)."""
@@ -456,13 +482,20 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                 rowsum_p=np.zeros((hq, T)), rowsum_pdp=np.zeros((hq, T)),
                 ds_nonzero=0, dsq_zero=0) if diagnostics else None
     kv_heads = range(hkv) if kv_heads is None else kv_heads
+    if opts.strict:   # per-token scales s_X = 2**e of the strict per-token quantization
+        Q_scale, K_scale, dO_scale = (np.asarray(tok_scales[n], np.float64) for n in ("q", "k", "do"))
     for n, (s0, s1) in enumerate(doc_ranges(cu)):
         ntile = -(-(s1 - s0) // tile)
         ksel = set(range(ntile)) if k_tiles is None else set(k_tiles.get(n, ()))
         qsel = set(range(ntile)) if q_tiles is None else set(q_tiles.get(n, ()))
         for hk in kv_heads:
             for h in range(hk * g, (hk + 1) * g):
-                c = dq_boost(dOh[s0:s1, h], Vh[s0:s1, hk], Kh[s0:s1, hk], opts.dq_headroom_log2) if q else 1.0
+                if q and opts.strict:
+                    c = causal_dq_boost(dOh[s0:s1, h], Vh[s0:s1, hk], Kh[s0:s1, hk], opts.dq_headroom_log2)
+                elif q:
+                    c = dq_boost(dOh[s0:s1, h], Vh[s0:s1, hk], Kh[s0:s1, hk], opts.dq_headroom_log2)
+                else:
+                    c = 1.0
                 accQ = {t: np.zeros((min(tile, s1 - s0 - t * tile), d)) for t in qsel}
                 for u in range(ntile):
                     c0, c1 = s0 + u * tile, min(s0 + (u + 1) * tile, s1)
@@ -476,18 +509,31 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                         P = np.exp(S - LSE[h, r0:r1][:, None])
                         dP = dOh[r0:r1, h] @ Vh[c0:c1, hk].T
                         dS = P * (dP - D[r0:r1, h][:, None])
-                        if q:
+                        if q and opts.strict:
+                            # per-token scales folded into the companion operand of each
+                            # token-axis product; one round-up exponent per (row of the
+                            # result operand, document-local 32-token group)
+                            sdo, sq_ = dO_scale[r0:r1, h], Q_scale[r0:r1, h]
+                            sk_ = K_scale[c0:c1, hk]
+                            Pq = _fold_quantize(beta_b * P * sdo[:, None], group_axis=0, offset=r0 - s0) / \
+                                (beta_b * sdo[:, None])                       # dV: fold s_dO into P^T
+                            dSk = _fold_quantize(dS * sq_[:, None], group_axis=0, offset=r0 - s0) / sq_[:, None]
+                            dSq = _fold_quantize(dS * sk_[None, :], group_axis=1, offset=c0 - s0) / sk_[None, :]
+                        elif q:
                             dSq = _quantize_ds_blocks(dS, r0 - s0, c0 - s0)
+                            dSk = dSq
                             Pq = e4m3_round(beta_b * P) / beta_b
                         else:
-                            dSq, Pq = dS, P
+                            dSq = dSk = dS
+                            Pq = P
                         if u in ksel:
                             dV[c0:c1, hk] += Pq.T @ dOh[r0:r1, h]
-                            dK[c0:c1, hk] += dSq.T @ Qh[r0:r1, h]
+                            dK[c0:c1, hk] += dSk.T @ Qh[r0:r1, h]
                         if t in qsel:
                             part = dSq @ Kh[c0:c1, hk]
                             if q:
-                                accQ[t] = fp16_round(accQ[t] + fp16_round(c * part))
+                                ct = c[r0 - s0:r1 - s0, None] if np.ndim(c) else c
+                                accQ[t] = fp16_round(accQ[t] + fp16_round(ct * part))
                             else:
                                 accQ[t] = accQ[t] + part
                         if diagnostics:
@@ -502,12 +548,52 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                                 diag["dsq_zero"] += int((nz & (dSq == 0)).sum())
                 for t in qsel:
                     r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
-                    dQ[r0:r1, h] = scale * accQ[t] / c
+                    ct = c[r0 - s0:r1 - s0, None] if np.ndim(c) else c
+                    dQ[r0:r1, h] = scale * accQ[t] / ct
     out = dict(dq=bf16_round(dQ) if q else dQ,
                dk=bf16_round(scale * dK) if q else scale * dK,
                dv=bf16_round(dV) if q else dV)
     if diagnostics:
         out["diag"] = diag
+    return out
+
+
+def _fold_quantize(X, group_axis: int, offset: int, group: int = 32):
+    """E4M3 with one round-up exponent per (line, 32-element group along
+    group_axis); groups are document-local (offset = document-local index of
+    the first element along group_axis, a multiple of 32).  Zero groups take
+    exponent 0.  Returns the reconstructed values."""
+    assert offset % group == 0
+    Xm = np.moveaxis(np.asarray(X, np.float64), group_axis, -1)
+    n = Xm.shape[-1]
+    npad = -(-n // group) * group
+    pad = np.zeros(Xm.shape[:-1] + (npad,))
+    pad[..., :n] = Xm
+    g = pad.reshape(Xm.shape[:-1] + (npad // group, group))
+    e = roundup_exponent(np.abs(g).max(axis=-1))
+    sc = np.ldexp(1.0, e)[..., None]
+    out = (e4m3_round(g / sc) * sc).reshape(pad.shape)[..., :n]
+    return np.moveaxis(out, -1, group_axis)
+
+
+def causal_dq_boost(dOh_doc, Vh_doc, Kh_doc, headroom_log2: int = 14):
+    """Strict causal dQ boost ([EN] section 4, "the causal accumulator scale
+    combines ||dO_i|| with running maxima of key and value magnitudes"), reading
+    C-10: M_i = 2 ||dO^_i|| max_{j<=i} ||V^_j|| max_{j<=i,d} |K^_jd| and
+    c_i = 2**floor(log2(2**14 / M_i)) (1 where M_i = 0).  Returns c per row."""
+    a = np.sqrt((dOh_doc ** 2).sum(-1))
+    b = np.maximum.accumulate(np.sqrt((Vh_doc ** 2).sum(-1)))
+    k = np.maximum.accumulate(np.abs(Kh_doc).max(-1))
+    M = 2.0 * a * b * k
+    out = np.ones_like(M)
+    for i, m in enumerate(M):
+        if m > 0 and np.isfinite(m):
+            e = math.floor(math.log2(2.0 ** headroom_log2 / m))
+            while 2.0 ** e * m > 2.0 ** headroom_log2:
+                e -= 1
+            while 2.0 ** (e + 1) * m <= 2.0 ** headroom_log2:
+                e += 1
+            out[i] = 2.0 ** max(-100, min(100, e))
     return out
 
 
@@ -594,20 +680,25 @@ def run_training_call(q, k, v, do, cu, hq: int, hkv: int, scale: Optional[float]
     scale bytes, O, LSE, dq, dk, dv."""
     out = {}
     if opts.quantized:
+        blk = 1 if opts.strict else opts.block
         for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
-            c, sb = quantize_tokenblock(x, cu, opts.block, opts.rule)
+            if x is None:
+                continue
+            c, sb = quantize_tokenblock(x, cu, blk, opts.rule)
             out[name + "_codes"], out[name + "_scales"] = c, sb
             out[name + "_hat"] = dequantize_tokenblock(c, sb)
     else:
         for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
             out[name + "_hat"] = np.asarray(x, np.float64)
+    tok = {n: ue8m0_decode(out[n + "_scales"]) for n in ("q", "k", "v", "do") if n + "_scales" in out} \
+        if opts.quantized else {}
     O, LSE = attention_forward(out["q_hat"], out["k_hat"], out["v_hat"], cu, hq, hkv, scale, opts,
-                               heads=sel.get("heads"), q_tiles=sel.get("q_tiles"))
+                               heads=sel.get("heads"), q_tiles=sel.get("q_tiles"), v_scale=tok.get("v"))
     out["o"], out["lse"] = O, LSE
     if do is not None:
         g = attention_backward(out["q_hat"], out["k_hat"], out["v_hat"], O, LSE, out["do_hat"], cu,
                                hq, hkv, scale, opts, kv_heads=sel.get("kv_heads"),
                                k_tiles=sel.get("k_tiles"), q_tiles=sel.get("bwd_q_tiles"),
-                               diagnostics=sel.get("diagnostics", False))
+                               diagnostics=sel.get("diagnostics", False), tok_scales=tok)
         out.update(g)
     return out

@@ -281,3 +281,85 @@ def test_bwd_key_tile_list():
     got = [(i["doc"], i["ktile"], i["cost"]) for i in items]
     assert got == [(2, 0, 4), (0, 0, 3), (2, 1, 3), (0, 1, 2), (2, 2, 2),
                    (0, 2, 1), (1, 0, 1), (2, 3, 1)]
+
+
+# ------------------------------------------------------------ strict options
+
+def _strict(q, k, v, do, cu, hq, hkv):
+    return O.run_training_call(q, k, v, do, cu, hq, hkv, opts=O.Options(strict=True))
+
+
+def test_strict_options_make_earlier_rows_bit_identical():
+    """[EN] section 4 / [KO] section 4.5: with per-token operand scales, per-row
+    dS exponents and the causal dQ scale, perturbing any later token (with dO
+    fixed) leaves O, LSE and dQ of every earlier row bit-identical."""
+    lengths, hq, hkv, d = [290, 60], 2, 1, 32
+    rng = np.random.default_rng(20)
+    T = sum(lengths)
+    mk = lambda h: O.bf16_round(rng.standard_t(3, (T, h, d)))
+    q, k, v, do = mk(hq), mk(hkv), mk(hkv), mk(hq)
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    base = _strict(q, k, v, do, cu, hq, hkv)
+    for t in (1, 33, 150, 289):
+        for name in ("q", "k", "v"):
+            x = {"q": q, "k": k, "v": v}
+            y = x[name].copy()
+            y[t] *= 16.0                                   # crosses exponent thresholds
+            x[name] = y
+            pert = _strict(x["q"], x["k"], x["v"], do, cu, hq, hkv)
+            assert np.array_equal(pert["o"][:t], base["o"][:t]), (name, t)
+            assert np.array_equal(pert["lse"][:, :t], base["lse"][:, :t]), (name, t)
+            assert np.array_equal(pert["dq"][:t], base["dq"][:t]), (name, t)
+            if name != "q":   # positive control: the perturbed key/value reaches its own row
+                assert not np.array_equal(pert["o"][t], base["o"][t]), (name, t)
+
+
+def test_default_dq_boost_leaks_across_the_sequence():
+    """Negative counterpart: the default sequence-wide dQ boost lets a later
+    outlier change earlier dQ rows (the residual dependency the pages report)."""
+    lengths, hq, hkv, d = [200], 1, 1, 16
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=21)
+    base = O.run_training_call(q, k, v, do, cu, hq, hkv)
+    do2 = do.copy(); do2[190] *= 2.0 ** 20                 # lowers the sequence-wide boost by ~2^20
+    pert = O.run_training_call(q, k, v, do2, cu, hq, hkv)
+    # earlier rows' fp16 partials now round at a coarser relative step
+    assert not np.array_equal(pert["dq"][:128], base["dq"][:128])
+    strict_b = O.run_training_call(q, k, v, do, cu, hq, hkv, opts=O.Options(strict=True))
+    strict_p = O.run_training_call(q, k, v, do2, cu, hq, hkv, opts=O.Options(strict=True))
+    assert np.array_equal(strict_p["dq"][:190], strict_b["dq"][:190])
+
+
+def test_fold_quantize_roundup_groups():
+    rng = np.random.default_rng(22)
+    X = rng.standard_normal((40, 70)) * np.exp2(rng.integers(-10, 10, (40, 70)))
+    R = O.flamia_oracle._fold_quantize(X, group_axis=1, offset=0)
+    for g0 in range(0, 70, 32):
+        blk = X[:, g0:g0 + 32]
+        e = O.roundup_exponent(np.abs(blk).max(1))
+        want = O.e4m3_round(blk * np.exp2(-e)[:, None]) * np.exp2(e)[:, None]
+        assert np.array_equal(R[:, g0:g0 + 32], want)
+        scaled = np.abs(blk).max(1) * np.exp2(-e.astype(float))
+        assert np.all((scaled > 224) & (scaled <= 448))
+    R0 = O.flamia_oracle._fold_quantize(X.T, group_axis=0, offset=32)
+    assert np.array_equal(R0, R.T)
+
+
+def test_causal_dq_boost_is_prefix_local():
+    rng = np.random.default_rng(23)
+    a, b, c = rng.standard_normal((50, 8)), rng.standard_normal((50, 8)), rng.standard_normal((50, 8))
+    full = O.causal_dq_boost(a, b, c)
+    for i in (0, 7, 31, 49):
+        M = 2 * np.linalg.norm(a[i]) * np.linalg.norm(b[:i + 1], axis=1).max() * np.abs(c[:i + 1]).max()
+        assert full[i] * M <= 2 ** 14 < 2 * full[i] * M
+        assert O.causal_dq_boost(a[:i + 1], b[:i + 1], c[:i + 1])[i] == full[i]
+
+
+def test_strict_path_tracks_unquantized_attention():
+    lengths, hq, hkv, d = [300, 200], 4, 2, 64
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=24)
+    out = _strict(q, k, v, do, cu, hq, hkv)
+    ref_o, _ = O.dense_attention(q, k, v, cu, hq, hkv)
+    ref_g = O.dense_attention_grads(q, k, v, do, cu, hq, hkv)
+    assert cosine(out["o"], ref_o) > 0.997
+    for n in ("dq", "dk", "dv"):
+        assert cosine(out[n], ref_g[n]) > 0.99, n
