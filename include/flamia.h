@@ -66,7 +66,26 @@ typedef struct flamia_options {
      (document, query head) (FLAMIA review section 4, "Forward locality and
      backward locality differ").  Default 14. */
   int dq_headroom_log2;
-  /* Reserved for the strict options and the mixed NVFP4 score path; must be 0. */
+  /* Strict options (FLAMIA review section 4, "Strict options"; Korean review
+     section 4.5).  Set all three together, or none (a partial set returns
+     FLAMIA_ERR_UNSUPPORTED):
+       strict_per_token: Q, K, V and dO carry one UE8M0 scale per token (quantize
+         them with per_token = 1; flamia_bwd encodes dO per token itself).  Each
+         per-token scale of a contraction-axis operand is folded into the
+         companion operand (the probabilities for P V and dV, dS for dK and dQ),
+         which is E4M3-rounded with one round-up exponent per (row, document-
+         local 32-token group);
+       strict_row_ds: dQ uses one dS exponent per (query row, 32-key block);
+       strict_causal_dq: the dQ boost is per query row, from prefix maxima
+         (c_i = 2^floor(log2(2^headroom / M_i)), M_i = 2 ||dO^_i||
+         max_{j<=i} ||V^_j|| max_{j<=i,d} |K^_jd|).
+     With them, the dQ partials are summed in increasing key-tile order by one
+     CTA per query tile (no atomics): results are bitwise reproducible and a
+     later token never changes an earlier row's O, LSE or dQ.
+     Strict calls support documents of up to 16384 tokens (longer ones set
+     FLAMIA_DEV_CAPACITY and leave the outputs unspecified).
+     deterministic: accepted only with the strict set (which implies it).
+     mixed_nvfp4: the mixed NVFP4/FP8 score path is not built; must be 0. */
   int strict_per_token;
   int strict_row_ds;
   int strict_causal_dq;
@@ -77,7 +96,8 @@ typedef struct flamia_options {
      timing_events[2i+1] just after its i-th launch, on its stream.
      flamia_fwd: launch 0 = attention forward kernel.  flamia_bwd: 0 = dO
      encoding with D (backward prep), 1 = dQ boosts, 2 = attention backward
-     kernel, 3 = dQ finalisation.  The events are caller-owned. */
+     kernel, 3 = dQ finalisation (strict: the ordered dQ kernel and the zeroing
+     of rows outside every document).  The events are caller-owned. */
   void* const* timing_events;
 } flamia_options;
 

@@ -186,7 +186,8 @@ class FlamiaAttention:
     quantized Q/K/V views and the backward workspace (allocated once through
     torch, reused across calls: nothing is allocated per call)."""
 
-    def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, device="cuda"):
+    def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, device="cuda",
+                 strict: bool = False):
         import torch
         self.T, self.N, self.hq, self.hkv, self.d = total_tokens, num_seqs, hq, hkv, head_dim
         self.device = torch.device(device)
@@ -209,6 +210,10 @@ class FlamiaAttention:
         ws = flamia_bwd_workspace_bytes(total_tokens, num_seqs, hq, hkv, head_dim)
         self.workspace = torch.empty(ws, dtype=u8, device=dev)
         self.opts = default_options()
+        self.strict = bool(strict)
+        if self.strict:   # per-token operand scales, per-query-row dS exponents, causal dQ boost, deterministic dQ
+            for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq", "deterministic"):
+                setattr(self.opts, f, 1)
 
     def views(self):
         return (qtensor(self.q_codes, self.q_scales), qtensor(self.k_codes, self.k_scales, self.k_stats),
@@ -218,10 +223,11 @@ class FlamiaAttention:
         flamia_plan_build(cu_seqlens, self.N, self.T, self.plan, stream)
 
     def quantize(self, q, k, v, cu_seqlens, stream=None):
-        flamia_quantize_tokenblock(q, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, None, False, stream)
-        flamia_quantize_tokenblock(k, cu_seqlens, self.N, self.plan, self.k_codes, self.k_scales, self.k_stats, False,
+        pt = self.strict
+        flamia_quantize_tokenblock(q, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, None, pt, stream)
+        flamia_quantize_tokenblock(k, cu_seqlens, self.N, self.plan, self.k_codes, self.k_scales, self.k_stats, pt,
                                    stream)
-        flamia_quantize_tokenblock(v, cu_seqlens, self.N, self.plan, self.v_codes, self.v_scales, self.v_stats, False,
+        flamia_quantize_tokenblock(v, cu_seqlens, self.N, self.plan, self.v_codes, self.v_scales, self.v_stats, pt,
                                    stream)
 
     def forward(self, cu_seqlens, softmax_scale: float = 0.0, stream=None):

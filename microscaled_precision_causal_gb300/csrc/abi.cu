@@ -14,14 +14,15 @@ cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* c
                             void* dq_acc, cudaStream_t s);
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev);
+                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict);
 cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float* st_do, const float* st_k,
-                         const float* st_v, int hq, int hkv, int headroom, float* boost, cudaStream_t s);
+                         const float* st_v, int T, int hq, int hkv, int headroom, float* boost, bool causal,
+                         cudaStream_t s);
 cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
-                       void* const* ev);
+                       void* const* ev, bool strict);
 }  // namespace flamia
 
 using namespace flamia;
@@ -40,12 +41,18 @@ int check_common(int64_t T, int N, const void* cu, const void* plan) {
   return FLAMIA_OK;
 }
 
+// The strict options come as a set (per-token operand scales, per-query-row dS
+// exponents, causal dQ boost; the dQ reduction is then deterministic).
+bool is_strict(const flamia_options* o) { return o && o->strict_per_token; }
+
 int check_opts(const flamia_options* o) {
   if (!o) return FLAMIA_OK;
   if (o->p_boost_log2 != 8 || o->bwd_p_boost_log2 != 8) return FLAMIA_ERR_UNSUPPORTED;
   if (o->dq_headroom_log2 < 1 || o->dq_headroom_log2 > 15) return FLAMIA_ERR_UNSUPPORTED;
-  if (o->strict_per_token || o->strict_row_ds || o->strict_causal_dq || o->mixed_nvfp4 || o->deterministic)
-    return FLAMIA_ERR_UNSUPPORTED;
+  const int s = o->strict_per_token + o->strict_row_ds + o->strict_causal_dq;
+  if (s != 0 && s != 3) return FLAMIA_ERR_UNSUPPORTED;
+  if (o->deterministic && s == 0) return FLAMIA_ERR_UNSUPPORTED;
+  if (o->mixed_nvfp4) return FLAMIA_ERR_UNSUPPORTED;
   return FLAMIA_OK;
 }
 
@@ -81,7 +88,7 @@ BwdWorkspace bwd_layout(int64_t T, int N, int hq, int d) {
   w.do_scales = off; off = round256(off + (size_t)T * hq);
   w.do_stats = off; off = round256(off + (size_t)T * hq * 8);
   w.dvec = off; off = round256(off + (size_t)T * hq * 4);
-  w.boost = off; off = round256(off + (size_t)(N > 0 ? N : 1) * hq * 4);
+  w.boost = off; off = round256(off + ((size_t)(N > 0 ? N : 1) + (size_t)T) * hq * 4);   // per doc, or per row (strict)
   w.dq_acc = off; off = round256(off + (size_t)T * hq * d * 2);
   w.total = off;
   return w;
@@ -143,7 +150,8 @@ int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (total_tokens == 0) return FLAMIA_OK;
   return cuda_status(launch_fwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, cu_seqlens,
                                 num_seqs, (int)total_tokens, hq, hkv, resolve_scale(softmax_scale, head_dim), plan,
-                                out_bf16, lse, (cudaStream_t)stream, opt ? opt->timing_events : nullptr));
+                                out_bf16, lse, (cudaStream_t)stream, opt ? opt->timing_events : nullptr,
+                                is_strict(opt)));
 }
 
 size_t flamia_bwd_workspace_bytes(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim) {
@@ -184,17 +192,18 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   void* dq_acc = ws + w.dq_acc;
   void* const* ev = opt ? opt->timing_events : nullptr;
   record(ev, 0, s);
-  cudaError_t e = launch_quantize(dout_bf16, T, hq, head_dim, cu_seqlens, num_seqs, plan, 0, do_codes, do_scales,
-                                  do_stats, out_bf16, dvec, dq_acc, s);
+  const bool strict = is_strict(opt);
+  cudaError_t e = launch_quantize(dout_bf16, T, hq, head_dim, cu_seqlens, num_seqs, plan, strict ? 1 : 0, do_codes,
+                                  do_scales, do_stats, out_bf16, dvec, dq_acc, s);
   record(ev, 1, s);
   record(ev, 2, s);
   if (e == cudaSuccess)
-    e = launch_boost(cu_seqlens, num_seqs, plan, do_stats, k->stats, v->stats, hq, hkv, headroom, boost, s);
+    e = launch_boost(cu_seqlens, num_seqs, plan, do_stats, k->stats, v->stats, T, hq, hkv, headroom, boost, strict, s);
   record(ev, 3, s);
   if (e == cudaSuccess)
     e = launch_bwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, do_codes, do_scales, lse,
                    dvec, boost, cu_seqlens, num_seqs, T, hq, hkv, resolve_scale(softmax_scale, head_dim), plan, dq_acc,
-                   dq_bf16, dk_bf16, dv_bf16, s, ev ? ev + 4 : nullptr);
+                   dq_bf16, dk_bf16, dv_bf16, s, ev ? ev + 4 : nullptr, strict);
   return cuda_status(e);
 }
 

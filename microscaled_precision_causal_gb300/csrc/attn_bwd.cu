@@ -81,10 +81,12 @@ struct BwdSmem {
   static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query]
   static constexpr int kDS = kPt + kTile * kTile;             // dS^ codes, [key][query]
   static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
-  static constexpr int kRowBuf = 128 * 4 * 2 + 16;            // -lse2[128], -D[128], chunk scales[8], dQ boost
-  static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents
+  // per-query row data: -lse2[128], -D[128], chunk scale bytes[8] + dQ boost (4 words),
+  // then (strict) s_Q[128] and s_dO[128] as floats
+  static constexpr int kRowBuf = (128 * 2 + 4 + 128 * 2) * 4;
+  static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents (+ strict per-row exponents)
   static constexpr int kStageBytes = kTile * BwdShape<D>::kCols * 2;   // one warpgroup's fp16 slice of the dQ tile
-  static constexpr int kStage = (kE + 64 + 1023) & ~1023;     // [warpgroup]
+  static constexpr int kStage = (kE + 64 + 1024 + 1023) & ~1023;   // [warpgroup]
   static constexpr int kBar = kStage + BwdShape<D>::kWG * kStageBytes;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
@@ -99,7 +101,7 @@ __device__ __forceinline__ void red_add_f16x8(__half* dst, uint32_t a, uint32_t 
                : "memory");
 }
 
-template <int D>
+template <int D, bool STRICT>
 __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -235,14 +237,16 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
                    smem_desc(qa + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
                    tbase + kSF + 8, tbase + kSF + 12, (k > 0 || s > 0));
         }
+        if (!STRICT) {
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major)
-          mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
-                   smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
-                   tbase + kSF + 16, tbase + kSF + 20, s > 0);
+          for (int s = 0; s < 4; ++s) {
+            // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major)
+            mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
+                     smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
+                     tbase + kSF + 16, tbase + kSF + 20, s > 0);
+          }
+          mma_commit(dq_full);
         }
-        mma_commit(dq_full);
         mma_commit(&qd_empty[st]);
         if (k + 1 < nsteps) {
           const int st1 = (k + 1) % kQStages;
@@ -251,9 +255,11 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
           tc_fence_after();
           issue_s(st1);
           mma_commit(s_full);
-          ok = mbar_wait(dq_empty, k & 1, status);
-          if (!ok) break;
-          tc_fence_after();
+          if (!STRICT) {      // the dQ partial occupies the dP columns until it has been read
+            ok = mbar_wait(dq_empty, k & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+          }
           issue_dp(st1);
           mma_commit(dp_full);
         }
@@ -277,7 +283,18 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         rb[i] = qv ? -p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : -INFINITY;
         rb[128 + i] = qv ? -p.dvec[(int64_t)h * p.T + qtok] : 0.f;
       }
-      if (lane == 8) rb[258] = p.boost[(int64_t)doc * p.hq + h];   // dQ boost of (document, query head)
+      if (lane == 8 && !STRICT) rb[258] = p.boost[(int64_t)doc * p.hq + h];   // dQ boost of (document, query head)
+      if (STRICT) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = q * 32 + lane;
+          const int ql = t * kTile + i;
+          const bool qv = ql < doc_len;
+          const int64_t qtok = (int64_t)doc_start + ql;
+          rb[260 + i] = qv ? ue8m0_to_f32(p.q_scales[qtok * p.hq + h]) : 1.0f;
+          rb[388 + i] = qv ? ue8m0_to_f32(p.do_scales[qtok * p.hq + h]) : 1.0f;
+        }
+      }
       if (lane < 8) {
         const int c = lane & 3;
         const int ql = t * kTile + c * 32;
@@ -329,15 +346,23 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         uint32_t vs[32];
         tmem_ld32(lane_base + kS + 32 * c, vs);
         tmem_ld_wait();
-        const float fS = p.scale_log2 * sk_row * ue8m0_to_f32(cs[c]);
+        const float fS = p.scale_log2 * sk_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[c]));
         const float2 fS2 = make_float2(fS, fS), b2 = make_float2(256.f, 256.f);
         const float4* nl4 = reinterpret_cast<const float4*>(rb + 32 * c);   // -LSE * log2(e)
+        const float4* sq4 = reinterpret_cast<const float4*>(rb + 260 + 32 * c);   // strict: s_Q per query
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 nl = nl4[i >> 2];
-          float2 x0 = ffma2(make_float2(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1])), fS2, make_float2(nl.x, nl.y));
-          float2 x1 = ffma2(make_float2(__uint_as_float(vs[i + 2]), __uint_as_float(vs[i + 3])), fS2, make_float2(nl.z, nl.w));
+          float2 d0 = make_float2(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1]));
+          float2 d1 = make_float2(__uint_as_float(vs[i + 2]), __uint_as_float(vs[i + 3]));
+          if (STRICT) {
+            const float4 sq = sq4[i >> 2];
+            d0 = fmul2(d0, make_float2(sq.x, sq.y));
+            d1 = fmul2(d1, make_float2(sq.z, sq.w));
+          }
+          float2 x0 = ffma2(d0, fS2, make_float2(nl.x, nl.y));
+          float2 x1 = ffma2(d1, fS2, make_float2(nl.z, nl.w));
           float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
           float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
           if (diag) {
@@ -348,8 +373,31 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
             p1.y = il + 3 >= j ? p1.y : 0.f;
           }
           pr[cc][i] = p0.x; pr[cc][i + 1] = p0.y; pr[cc][i + 2] = p1.x; pr[cc][i + 3] = p1.y;
-          const float2 q0 = fmul2(p0, b2), q1 = fmul2(p1, b2);
-          pk[i >> 2] = (uint32_t)e4m3x2(q0.x, q0.y) | ((uint32_t)e4m3x2(q1.x, q1.y) << 16);
+          if (!STRICT) {
+            const float2 q0 = fmul2(p0, b2), q1 = fmul2(p1, b2);
+            pk[i >> 2] = (uint32_t)e4m3x2(q0.x, q0.y) | ((uint32_t)e4m3x2(q1.x, q1.y) << 16);
+          }
+        }
+        if (STRICT) {
+          // dV operand with dO's per-token scale folded in: 2^8 P s_dO(i), one round-up
+          // exponent per (key row, 32-query chunk)
+          const float4* sd4 = reinterpret_cast<const float4*>(rb + 388 + 32 * c);
+          float pf[32];
+          float gmax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 sd = sd4[i >> 2];
+            const float2 a0 = fmul2(fmul2(make_float2(pr[cc][i], pr[cc][i + 1]), make_float2(sd.x, sd.y)), b2);
+            const float2 a1 = fmul2(fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), make_float2(sd.z, sd.w)), b2);
+            pf[i] = a0.x; pf[i + 1] = a0.y; pf[i + 2] = a1.x; pf[i + 3] = a1.y;
+            gmax = fmax3(gmax, fmaxf(a0.x, a0.y), fmaxf(a1.x, a1.y));
+          }
+          const int ev = roundup_exp(gmax);
+          const float sc = exp2i(-ev);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            pk[i >> 2] = (uint32_t)e4m3x2(pf[i] * sc, pf[i + 1] * sc) | ((uint32_t)e4m3x2(pf[i + 2] * sc, pf[i + 3] * sc) << 16);
+          Esm[64 + j * 4 + c] = (uint8_t)(ev + 127);
         }
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -363,23 +411,39 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         uint32_t vp[32];
         tmem_ld32(lane_base + kP + 32 * c, vp);
         tmem_ld_wait();
-        const float fP = sv_row * ue8m0_to_f32(cs[4 + c]);
+        const float fP = sv_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[4 + c]));
         const float2 fP2 = make_float2(fP, fP);
         const float4* nd4 = reinterpret_cast<const float4*>(rb + 128 + 32 * c);   // -D
+        const float4* sd4 = reinterpret_cast<const float4*>(rb + 388 + 32 * c);   // strict: s_dO
+        const float4* sq4 = reinterpret_cast<const float4*>(rb + 260 + 32 * c);   // strict: s_Q
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 nd = nd4[i >> 2];
-          const float2 t0 = ffma2(make_float2(__uint_as_float(vp[i]), __uint_as_float(vp[i + 1])), fP2, make_float2(nd.x, nd.y));
-          const float2 t1 = ffma2(make_float2(__uint_as_float(vp[i + 2]), __uint_as_float(vp[i + 3])), fP2, make_float2(nd.z, nd.w));
-          const float2 d0 = fmul2(make_float2(pr[cc][i], pr[cc][i + 1]), t0);
-          const float2 d1 = fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), t1);
+          float2 v0 = make_float2(__uint_as_float(vp[i]), __uint_as_float(vp[i + 1]));
+          float2 v1 = make_float2(__uint_as_float(vp[i + 2]), __uint_as_float(vp[i + 3]));
+          if (STRICT) {
+            const float4 sd = sd4[i >> 2];
+            v0 = fmul2(v0, make_float2(sd.x, sd.y));
+            v1 = fmul2(v1, make_float2(sd.z, sd.w));
+          }
+          const float2 t0 = ffma2(v0, fP2, make_float2(nd.x, nd.y));
+          const float2 t1 = ffma2(v1, fP2, make_float2(nd.z, nd.w));
+          float2 d0 = fmul2(make_float2(pr[cc][i], pr[cc][i + 1]), t0);
+          float2 d1 = fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), t1);
+          if (STRICT) {     // dK operand: Q's per-token scale folded into dS
+            const float4 sq = sq4[i >> 2];
+            d0 = fmul2(d0, make_float2(sq.x, sq.y));
+            d1 = fmul2(d1, make_float2(sq.z, sq.w));
+          }
           pr[cc][i] = d0.x; pr[cc][i + 1] = d0.y; pr[cc][i + 2] = d1.x; pr[cc][i + 3] = d1.y;
           amax = fmax3(amax, fabsf(d0.x), fabsf(d0.y));
           amax = fmax3(amax, fabsf(d1.x), fabsf(d1.y));
         }
+        if (!STRICT) {      // 32 x 32 block: the warp's 32 key rows
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+          for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+        }
         const int e = roundup_exp(amax);
         const float sc = exp2i(-e);
         const float2 sc2 = make_float2(sc, sc);
@@ -392,9 +456,30 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         }
         *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        if (lane == 0) Esm[quarter * 4 + c] = (uint8_t)(e + 127);
+        if (STRICT) Esm[576 + j * 4 + c] = (uint8_t)(e + 127);
+        else if (lane == 0) Esm[quarter * 4 + c] = (uint8_t)(e + 127);
       }
       named_bar_sync(1, kCompute);           // all block exponents written; S^T and dP^T fully read
+      if (STRICT) {
+        // A-operand scales are per key row: row j's word sits in lane j, column
+        // (base + j / 32), i.e. this warp's quarter; B operands (dO, Q) are folded.
+        if (wg == 0 || wg == 1 % kWG) {
+          if (wg == 0) {
+            tmem_st1(lane_base + kSF + 0 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 64 + j * 4));
+            tmem_st4(lane_base + kSF + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          }
+          if (wg == 1 % kWG) {
+            tmem_st1(lane_base + kSF + 8 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 576 + j * 4));
+            tmem_st4(lane_base + kSF + 12, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&row_empty[b]);
+        mbar_arrive(p_full);
+        continue;                            // dQ comes from the deterministic dQ kernel
+      }
       {
         // block-scale words of the three MXF8 MMAs, one operand pair per warpgroup
         const uint8_t* E = Esm;               // E[key block][query chunk]
@@ -601,7 +686,380 @@ __global__ void dq_finalize_kernel(const __half* acc, const int32_t* cu, const i
   }
 }
 
+// Strict causal dQ boost ([EN] section 4, "the causal accumulator scale combines
+// ||dO_i|| with running maxima of key and value magnitudes"): per query row,
+// M_i = 2 ||dO^_i|| max_{j<=i} ||V^_j|| max_{j<=i,d} |K^_jd| over the document and
+// c_i = 2^floor(log2(2^headroom / M_i)) (1 where M_i = 0).  One CTA per
+// (document, query head), a chunked prefix-max scan over the document's tokens.
+__global__ void __launch_bounds__(256) causal_boost_kernel(const int32_t* cu, const int* plan, const float2* st_do,
+                                                           const float2* st_k, const float2* st_v, int T, int hq,
+                                                           int hkv, int headroom, float* cvec) {
+  const int doc = blockIdx.x, h = blockIdx.y;
+  const int hk = h / (hq / hkv);
+  if (plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS) return;
+  const int s0 = cu[doc], s1 = cu[doc + 1];
+  __shared__ float wv[8], wk[8];
+  __shared__ float carry[2];
+  if (threadIdx.x == 0) carry[0] = carry[1] = 0.f;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = s0; base < s1; base += 256) {
+    const int t = base + threadIdx.x;
+    const bool in = t < s1;
+    float v = in ? st_v[(int64_t)t * hkv + hk].x : 0.f;
+    float k = in ? st_k[(int64_t)t * hkv + hk].y : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float pv = __shfl_up_sync(0xffffffffu, v, o), pk = __shfl_up_sync(0xffffffffu, k, o);
+      if (lane >= o) { v = fmaxf(v, pv); k = fmaxf(k, pk); }
+    }
+    if (lane == 31) { wv[warp] = v; wk[warp] = k; }
+    __syncthreads();
+    float cv = carry[0], ck = carry[1];
+    for (int w = 0; w < warp; ++w) { cv = fmaxf(cv, wv[w]); ck = fmaxf(ck, wk[w]); }
+    v = fmaxf(v, cv);
+    k = fmaxf(k, ck);
+    if (in) {
+      const double M = 2.0 * (double)st_do[(int64_t)t * hq + h].x * (double)v * (double)k;
+      double cb = 1.0;
+      if (M > 0.0 && M < 1e300) {
+        const double target = ldexp(1.0, headroom);
+        int e = (int)floor(log2(target / M));
+        while (ldexp(M, e) > target) --e;
+        while (ldexp(M, e + 1) <= target) ++e;
+        e = e < -100 ? -100 : (e > 100 ? 100 : e);
+        cb = ldexp(1.0, e);
+      }
+      cvec[(int64_t)h * T + t] = (float)cb;
+    }
+    __syncthreads();
+    if (threadIdx.x == 255) { carry[0] = v; carry[1] = k; }
+    __syncthreads();
+  }
+}
+
+// Rows outside every document: dQ, dK and dV are zero.
 template <int D>
+__global__ void bwd_tail_kernel(const int* plan, int T, int hq, int hkv, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                                __nv_bfloat16* dv) {
+  const bool bad = plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS;
+  const int valid = bad ? 0 : plan[kPlanValid];
+  const int64_t nq = (int64_t)(T - valid) * hq * (D / 8), nk = (int64_t)(T - valid) * hkv * (D / 8);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nq + 2 * nk; i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < nq) reinterpret_cast<uint4*>(dq)[(int64_t)valid * hq * (D / 8) + i] = make_uint4(0, 0, 0, 0);
+    else if (i < nq + nk) reinterpret_cast<uint4*>(dk)[(int64_t)valid * hkv * (D / 8) + (i - nq)] = make_uint4(0, 0, 0, 0);
+    else reinterpret_cast<uint4*>(dv)[(int64_t)valid * hkv * (D / 8) + (i - nq - nk)] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Deterministic dQ (strict options): one CTA per (forward work item, query head)
+// processes the item's query tiles one after another; for each, the visible key
+// tiles in increasing order.  Thread = query row.  Per key tile: S = Q K^T and
+// dP = dO V^T (unscaled E4M3 MMAs), P = 2^(x - LSE log2 e), dS = P o (dP - D),
+// the K fold dS'' = dS s_K(j) quantized with one round-up exponent per (query
+// row, 32-key block) (the strict per-row dS exponent), dQ partial = dS'' K^ codes
+// (MXF8 MMA), then acc = fp16(acc + fp16(c_i * partial)) in registers in the
+// fixed key-tile order; finally dQ = bf16(scale * acc / c_i).
+// Roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
+// allocator, warp 3 per-key factors (s_K, s_V) into SMEM, warps 4-7 compute.
+// TMEM: S [0,128), dP [128,256) (its last 8 columns carry the dQ MMA's scale
+// words once dP was read), dQ partial [256, 256 + D).
+constexpr int kDqStages = 2;
+
+struct DqParams {
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  const uint8_t* do_scales;
+  const float* lse;
+  const float* dvec;
+  const float* cvec;       // [hq, T] causal boosts
+  const int32_t* cu;
+  const int* plan;
+  int N, T, hq, hkv;
+  float scale_log2, scale;
+  __nv_bfloat16* dq;
+};
+
+template <int D>
+struct DqSmem {
+  static constexpr int kTileBytes = kTile * D;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTileBytes;
+  static constexpr int kK = kDO + kTileBytes;                  // [kDqStages]
+  static constexpr int kV = kK + kDqStages * kTileBytes;       // [kDqStages]
+  static constexpr int kDS = kV + kDqStages * kTileBytes;      // dS'' codes, [query][key]
+  static constexpr int kKD = kDS + kTile * kTile;              // per-key factors [2 buffers][2][128] floats
+  static constexpr int kBar = kKD + 2 * 2 * 128 * 4;
+  static constexpr int kBytes = kBar + 256;
+  // at least 116 KB so that one CTA (holding all 512 TMEM columns) fits per SM
+  static constexpr int kAlloc = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    attn_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const DqParams p) {
+  using L = DqSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* qd_full = bars + 0;
+  uint64_t* qd_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;                 // [kDqStages]
+  uint64_t* kv_empty = bars + 2 + kDqStages;    // [kDqStages]
+  uint64_t* kd_full = bars + 2 + 2 * kDqStages; // [2]
+  uint64_t* kd_empty = kd_full + 2;             // [2]
+  uint64_t* s_full = kd_empty + 2;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* dq_full = s_full + 2;
+  uint64_t* dq_empty = s_full + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 4);
+  int* status = const_cast<int*>(p.plan) + kPlanStatus;
+
+  const int n_items = p.plan[kPlanFwdItems];
+  const int item_idx = blockIdx.x / p.hq;
+  const int h = blockIdx.x % p.hq;
+  if (item_idx >= n_items) return;
+  const PlanView pv = plan_view(p.plan, p.T, p.N);
+  const int4 item = pv.fwd_items[item_idx];
+  const int doc = item.x, t0 = item.y, ntq = item.z;
+  const int doc_start = p.cu[doc];
+  const int doc_len = p.cu[doc + 1] - doc_start;
+  const int hk = h / (p.hq / p.hkv);
+  // pairs (query tile w, key tile u), w-major, u = 0 .. t0 + w
+  const int npairs = ntq == 1 ? t0 + 1 : 2 * t0 + 3;
+  auto pair_of = [&](int k, int& w, int& u) {
+    if (k <= t0) { w = 0; u = k; } else { w = 1; u = k - (t0 + 1); }
+  };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(qd_full, 1);
+    mbar_init(qd_empty, 1);
+    for (int i = 0; i < kDqStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kd_full[i], 32);
+      mbar_init(&kd_empty[i], 128);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  constexpr uint32_t kS = 0, kP = 128, kDQ = 256;
+  constexpr uint32_t kSF = kP + 120;
+  constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
+  constexpr uint32_t kAtom = 8 * D;
+  float* kdbuf = reinterpret_cast<float*>(smem + L::kKD);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int k = 0; k < npairs && ok; ++k) {
+        int w, u;
+        pair_of(k, w, u);
+        if (u == 0) {     // a new query tile: Q and dO codes
+          if (w == 1) ok = mbar_wait(qd_empty, 0, status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(qd_full, 2 * L::kTileBytes);
+          tma_load_3d(smem + L::kQ, &tm_q, qd_full, 0, h, doc_start + (t0 + w) * kTile);
+          tma_load_3d(smem + L::kDO, &tm_do, qd_full, 0, h, doc_start + (t0 + w) * kTile);
+        }
+        const int st = k % kDqStages;
+        if (k >= kDqStages && !mbar_wait(&kv_empty[st], ((k / kDqStages) - 1) & 1, status)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTileBytes);
+        tma_load_3d(smem + L::kK + st * L::kTileBytes, &tm_k, &kv_full[st], 0, hk, doc_start + u * kTile);
+        tma_load_3d(smem + L::kV + st * L::kTileBytes, &tm_v, &kv_full[st], 0, hk, doc_start + u * kTile);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t sq = smem_u32(smem + L::kQ), sdo = smem_u32(smem + L::kDO), sk = smem_u32(smem + L::kK),
+                     sv = smem_u32(smem + L::kV), sds = smem_u32(smem + L::kDS);
+      bool ok = true;
+      for (int k = 0; k < npairs && ok; ++k) {
+        int w, u;
+        pair_of(k, w, u);
+        const int st = k % kDqStages;
+        if (u == 0) ok = mbar_wait(qd_full, w, status);
+        if (ok) ok = mbar_wait(&kv_full[st], (k / kDqStages) & 1, status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ka = sk + st * L::kTileBytes, va = sv + st * L::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < D / 32; ++s) {
+          mma_f8(tbase + kS, smem_desc(sq + 32 * s, 16, kAtom, kLayout), smem_desc(ka + 32 * s, 16, kAtom, kLayout),
+                 idesc_f8(128, 128, 0, 0), s > 0);
+          mma_f8(tbase + kP, smem_desc(sdo + 32 * s, 16, kAtom, kLayout), smem_desc(va + 32 * s, 16, kAtom, kLayout),
+                 idesc_f8(128, 128, 0, 0), s > 0);
+        }
+        mma_commit(s_full);
+        ok = mbar_wait(p_full, k & 1, status);
+        if (ok && k > 0) ok = mbar_wait(dq_empty, (k - 1) & 1, status);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          // dQ partial = dS'' K (A: queries x keys, K-major; B: K keys x d, MN-major)
+          mma_mxf8(tbase + kDQ, smem_desc(sds + 32 * s, 16, 1024, kSwizzle128B),
+                   smem_desc(ka + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
+                   tbase + kSF, tbase + kSF + 4, s > 0);
+        }
+        mma_commit(dq_full);
+        mma_commit(&kv_empty[st]);
+        if (u == t0 + w) mma_commit(qd_empty);     // last key tile of this query tile
+      }
+      if (!ok) {
+        mma_commit(dq_full);
+        mbar_wait(dq_full, 0, status);
+      }
+    }
+  } else if (warp == 3) {
+    // per-key factors s_K(j), s_V(j) of each key tile
+    for (int k = 0; k < npairs; ++k) {
+      int w, u;
+      pair_of(k, w, u);
+      const int b = k & 1;
+      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&kd_empty[b], ((k >> 1) - 1) & 1, status))) break;
+      float* kd = kdbuf + b * 256;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = q * 32 + lane;
+        const int kl = u * kTile + j;
+        const bool kv = kl < doc_len;
+        const int64_t ktok = (int64_t)doc_start + kl;
+        kd[j] = kv ? ue8m0_to_f32(p.k_scales[ktok * p.hkv + hk]) : 1.0f;
+        kd[128 + j] = kv ? ue8m0_to_f32(p.v_scales[ktok * p.hkv + hk]) : 1.0f;
+      }
+      mbar_arrive(&kd_full[b]);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int i = quarter * 32 + lane;               // query row within the tile (TMEM lane)
+    const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* sDS = smem + L::kDS;
+    bool ok = true;
+    __half2 acc[D / 2];
+    float nl = 0.f, nd = 0.f, fq = 0.f, sdo = 0.f, cb = 1.f;
+    bool qv = false;
+    int64_t qtok = 0;
+    for (int k = 0; k < npairs; ++k) {
+      int w, u;
+      pair_of(k, w, u);
+      const int t = t0 + w;
+      if (u == 0) {
+        const int ql = t * kTile + i;
+        qv = ql < doc_len;
+        qtok = (int64_t)doc_start + ql;
+        nl = qv ? -p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : -INFINITY;
+        nd = qv ? -p.dvec[(int64_t)h * p.T + qtok] : 0.f;
+        fq = qv ? p.scale_log2 * ue8m0_to_f32(p.q_scales[qtok * p.hq + h]) : 0.f;
+        sdo = qv ? ue8m0_to_f32(p.do_scales[qtok * p.hq + h]) : 0.f;
+        cb = qv ? p.cvec[(int64_t)h * p.T + qtok] : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 2; ++c) acc[c] = __floats2half2_rn(0.f, 0.f);
+      }
+      const bool diag = (u == t);
+      const int b = k & 1;
+      const float* kd = kdbuf + b * 256;
+      ok = named_bar_and(1, 128, mbar_wait(s_full, k & 1, status) && mbar_wait(&kd_full[b], (k >> 1) & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sfa = 0;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t vs[32], vp[32];
+        tmem_ld32(lane_base + kS + 32 * c, vs);
+        tmem_ld32(lane_base + kP + 32 * c, vp);
+        tmem_ld_wait();
+        float ds[32];
+        float amax = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * c + jj;
+          const float sk = kd[j];
+          const float x = __uint_as_float(vs[jj]) * (fq * sk) + nl;
+          const bool vis = !diag || j <= i;
+          const float pr = vis ? fast_exp2(x) : 0.f;
+          const float dp = __uint_as_float(vp[jj]) * (sdo * kd[128 + j]) + nd;
+          const float v = pr * dp * sk;                // K fold
+          ds[jj] = v;
+          amax = fmaxf(amax, fabsf(v));
+        }
+        const int e = roundup_exp(amax);
+        const float sc = exp2i(-e);
+        sfa |= (uint32_t)(e + 127) << (8 * c);
+        uint32_t pk[8];
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 4)
+          pk[jj >> 2] = (uint32_t)e4m3x2(ds[jj] * sc, ds[jj + 1] * sc) | ((uint32_t)e4m3x2(ds[jj + 2] * sc, ds[jj + 3] * sc) << 16);
+        *reinterpret_cast<uint4*>(sDS + swz_offset(i, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(sDS + swz_offset(i, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+      // A scale of row i: lane i, column (base + i / 32); B (K codes) carries no scale
+      tmem_st1(lane_base + kSF + quarter, sfa);
+      tmem_st4(lane_base + kSF + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&kd_empty[b]);
+      mbar_arrive(p_full);
+      ok = named_bar_and(1, 128, mbar_wait(dq_full, k & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + kDQ + 32 * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const __half2 hpart = __floats2half2_rn(__uint_as_float(v[2 * q]) * cb, __uint_as_float(v[2 * q + 1]) * cb);
+          acc[16 * c + q] = __hadd2(acc[16 * c + q], hpart);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      if (u == t && qv) {          // last key tile of this query tile: dQ = bf16(scale * acc / c_i)
+        const float mul = p.scale / cb;
+        __nv_bfloat16* orow = p.dq + (qtok * p.hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(acc[4 * c + q]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * mul, f.y * mul);
+            o[q] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          reinterpret_cast<uint4*>(orow)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool STRICT>
 cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                          const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
@@ -636,16 +1094,46 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   const int64_t grid = max_items * hkv;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
   constexpr int smem = BwdSmem<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_bwd_kernel<D, STRICT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
-  attn_bwd_kernel<D><<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_kernel<D, STRICT><<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
   if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
   if (ev && ev[2]) cudaEventRecord(static_cast<cudaEvent_t>(ev[2]), stream);
-  dq_finalize_kernel<D><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
-                                                     hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
+  if (!STRICT) {
+    dq_finalize_kernel<D><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
+                                                       hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
+  } else {
+    DqParams dp;
+    dp.q_scales = p.q_scales;
+    dp.k_scales = p.k_scales;
+    dp.v_scales = p.v_scales;
+    dp.do_scales = p.do_scales;
+    dp.lse = lse;
+    dp.dvec = dvec;
+    dp.cvec = boost;
+    dp.cu = cu;
+    dp.plan = p.plan;
+    dp.N = N;
+    dp.T = T;
+    dp.hq = hq;
+    dp.hkv = hkv;
+    dp.scale_log2 = p.scale_log2;
+    dp.scale = scale;
+    dp.dq = static_cast<__nv_bfloat16*>(dq);
+    constexpr int dsmem = DqSmem<D>::kAlloc;
+    e = cudaFuncSetAttribute(attn_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
+    if (e != cudaSuccess) return e;
+    const int64_t dgrid = ((int64_t)T / (kTile * kItemTiles) + N + 1) * hq;
+    if (dgrid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    attn_dq_kernel<D><<<(unsigned)dgrid, 256, dsmem, stream>>>(tq, tk, tv, tdo, dp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_tail_kernel<D><<<152, 256, 0, stream>>>(p.plan, T, hq, hkv, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
+  }
   e = cudaGetLastError();
   if (ev && ev[3]) cudaEventRecord(static_cast<cudaEvent_t>(ev[3]), stream);
   return e;
@@ -654,11 +1142,18 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
 }  // namespace
 
 cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float* st_do, const float* st_k,
-                         const float* st_v, int hq, int hkv, int headroom, float* boost, cudaStream_t s) {
+                         const float* st_v, int T, int hq, int hkv, int headroom, float* boost, bool causal,
+                         cudaStream_t s) {
   if (N == 0) return cudaSuccess;
-  boost_kernel<<<dim3(N, hq), 256, 0, s>>>(cu, static_cast<const int*>(plan), reinterpret_cast<const float2*>(st_do),
-                                           reinterpret_cast<const float2*>(st_k), reinterpret_cast<const float2*>(st_v),
-                                           hq, hkv, headroom, boost);
+  if (causal)
+    causal_boost_kernel<<<dim3(N, hq), 256, 0, s>>>(cu, static_cast<const int*>(plan),
+                                                    reinterpret_cast<const float2*>(st_do),
+                                                    reinterpret_cast<const float2*>(st_k),
+                                                    reinterpret_cast<const float2*>(st_v), T, hq, hkv, headroom, boost);
+  else
+    boost_kernel<<<dim3(N, hq), 256, 0, s>>>(cu, static_cast<const int*>(plan), reinterpret_cast<const float2*>(st_do),
+                                             reinterpret_cast<const float2*>(st_k),
+                                             reinterpret_cast<const float2*>(st_v), hq, hkv, headroom, boost);
   return cudaGetLastError();
 }
 
@@ -666,13 +1161,14 @@ cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, co
                        const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
-                       void* const* ev) {
-  if (D == 128)
-    return launch_bwd_d<128>(qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan,
-                             dq_acc, dq, dk, dv, stream, ev);
-  if (D == 64)
-    return launch_bwd_d<64>(qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan,
-                            dq_acc, dq, dk, dv, stream, ev);
+                       void* const* ev, bool strict) {
+#define FLAMIA_BWD_ARGS qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan, \
+                        dq_acc, dq, dk, dv, stream, ev
+  if (D == 128 && strict) return launch_bwd_d<128, true>(FLAMIA_BWD_ARGS);
+  if (D == 128) return launch_bwd_d<128, false>(FLAMIA_BWD_ARGS);
+  if (D == 64 && strict) return launch_bwd_d<64, true>(FLAMIA_BWD_ARGS);
+  if (D == 64) return launch_bwd_d<64, false>(FLAMIA_BWD_ARGS);
+#undef FLAMIA_BWD_ARGS
   return cudaErrorInvalidValue;
 }
 

@@ -54,8 +54,9 @@ struct FwdSmem {
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kP = kV + kStages * kTileBytes;
   static constexpr int kScaleTab = kP + 2 * kTile * kTile;      // per key tile: K word, V word
-  static constexpr int kMaxTabTiles = 4096;
-  static constexpr int kBar = kScaleTab + kMaxTabTiles * 8;
+  static constexpr int kMaxTabTiles = 4096;                      // (strict: 256 bytes per tile, 128 tiles)
+  static constexpr int kKeyF = kScaleTab + kMaxTabTiles * 8;     // strict: [wg][2 buffers][3][128] floats
+  static constexpr int kBar = kKeyF + 2 * 2 * 3 * 128 * 4;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;           // slack for 1024-byte alignment
 };
@@ -64,7 +65,7 @@ __device__ __forceinline__ float scale_of(const uint8_t* s, int64_t tok, int H, 
   return valid ? ue8m0_to_f32(s[tok * H + h]) : 1.0f;
 }
 
-template <int D>
+template <int D, bool STRICT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -116,8 +117,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // group, 127 past the document end), staged once so the softmax loop reads
   // them from shared memory
   uint32_t* scale_tab = reinterpret_cast<uint32_t*>(smem + L::kScaleTab);
-  const bool tab_ok = nkv <= L::kMaxTabTiles;
-  if (tab_ok) {
+  const bool tab_ok = STRICT ? nkv * 32 <= L::kMaxTabTiles : nkv <= L::kMaxTabTiles;
+  if (STRICT && tab_ok) {
+    // strict: per-token scale bytes of every key of the item, 128 K then 128 V per tile
+    uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
+    for (int i = threadIdx.x; i < nkv * kTile; i += kThreads) {
+      const int uu = i >> 7, j = i & 127;
+      const int kl = uu * kTile + j;
+      const int64_t ktok = (int64_t)doc_start + kl;
+      const bool kv = kl < doc_len;
+      tb[uu * 256 + j] = kv ? p.k_scales[ktok * p.hkv + hk] : (uint8_t)127;
+      tb[uu * 256 + 128 + j] = kv ? p.v_scales[ktok * p.hkv + hk] : (uint8_t)127;
+    }
+  } else if (STRICT && threadIdx.x == 0) {
+    atomicOr(status, FLAMIA_DEV_CAPACITY);         // document too long for the strict per-key table
+  }
+  if (!STRICT && tab_ok) {
     uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
     for (int i = threadIdx.x; i < nkv * 4; i += kThreads) {
       const int uu = i >> 2, gg = i & 3;
@@ -138,7 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
   constexpr uint32_t kAtom = 8 * D;
 
-  if (warp == 0) {
+  const bool run = !STRICT || tab_ok;
+  if (!run) {
+    // strict call on a document longer than the per-key table: nothing is computed
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -254,20 +272,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      float* keyf = reinterpret_cast<float*>(smem + L::kKeyF) + w * (2 * 3 * 128);   // strict only
       for (int u = 0; u < nk; ++u) {
-        uint32_t kw, vsf;
-        tile_scales(u, kw, vsf);
+        uint32_t kw = 0, vsf = 0x7F7F7F7Fu;
         float fk[4];
+        const float* kf = nullptr;     // strict: per-key s_K, V exponent, 2^-eV of this tile
+        if constexpr (STRICT) {
+          float* buf = keyf + (u & 1) * (3 * 128);
+          const uint8_t* tb = reinterpret_cast<const uint8_t*>(scale_tab) + u * 256;
+          const int kb = tb[r], vb = tb[128 + r];
+          buf[r] = ue8m0_to_f32((uint32_t)kb);
+          buf[128 + r] = (float)(vb - 127);
+          buf[256 + r] = ue8m0_to_f32((uint32_t)(254 - vb));
+          kf = buf;                      // published by the warpgroup barrier below
 #pragma unroll
-        for (int g = 0; g < 4; ++g) fk[g] = fq * ue8m0_to_f32((kw >> (8 * g)) & 0xFFu);
+          for (int g = 0; g < 4; ++g) fk[g] = fq;
+        } else {
+          tile_scales(u, kw, vsf);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) fk[g] = fq * ue8m0_to_f32((kw >> (8 * g)) & 0xFFu);
+        }
         const bool diag = (u == t);
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], u & 1, status));
+        if constexpr (STRICT) {
+          // warpgroup-wide: publishes the per-key factors and leaves together on a timeout
+          ok = named_bar_and(2 + w, 128, mbar_wait(&s_full[w], u & 1, status));
+        } else {
+          ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], u & 1, status));
+        }
         if (!ok) break;
         tc_fence_after();
         // pass 1: row max of x = S * log2(e) over visible keys.  The column factor
         // is a positive power of two times a constant, so max(v * f) = f * max(v).
         float mx = -INFINITY;
-        if (!diag) {
+        if (STRICT) {
+          // per-key column factors: x_j = dot_j * s_K(j) * fq
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + 32 * g, v);
+            tmem_ld_wait();
+            float b = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float x = __uint_as_float(v[j]) * kf[32 * g + j];
+              b = (!diag || (g * 32 + j) <= r) ? fmaxf(b, x) : b;
+            }
+            mx = fmaxf(mx, b * fq);
+          }
+        } else if (!diag) {
           // fused TMEM load + row max (all keys visible)
           float cm[4];
 #pragma unroll
@@ -306,8 +358,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
         }
         lsum *= alpha;
-        // pass 2: boosted weights 2^(x - m + 8), their E4M3 codes into the P tile
         const float neg = 8.0f - m_new;
+        if constexpr (STRICT) {
+          // pass 2 (strict): V's per-key scale folded into the boosted weight,
+          // pf_j = 2^(x_j - m + 8 + eV_j); one round-up exponent per 32-key group;
+          // the normaliser accumulates pf_j * 2^-eV_j (= the unfolded boosted weight)
+          uint32_t sfa = 0;
+          float lacc = 0.f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + 32 * g, v);
+            tmem_ld_wait();
+            float pf[32];
+            float gmax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int kc = g * 32 + j;
+              const float x = __uint_as_float(v[j]) * kf[kc] * fq;
+              float e = fast_exp2(x + neg + kf[128 + kc]);
+              e = (!diag || kc <= r) ? e : 0.f;
+              pf[j] = e;
+              lacc = fmaf(e, kf[256 + kc], lacc);
+              gmax = fmaxf(gmax, e);
+            }
+            const int eg = roundup_exp(gmax);
+            const float sc = exp2i(-eg);
+            sfa |= (uint32_t)(eg + 127) << (8 * g);
+            uint32_t packed[8];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              packed[j >> 2] = (uint32_t)e4m3x2(pf[j] * sc, pf[j + 1] * sc) |
+                               ((uint32_t)e4m3x2(pf[j + 2] * sc, pf[j + 3] * sc) << 16);
+            *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g, 128)) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g + 16, 128)) =
+                make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+          lsum += lacc;
+          // A scale of row r is read from lane r, column (base + r / 32): this warp's quarter
+          tmem_st1(s_addr + 120 + quarter, sfa);
+        } else {
+        // pass 2: boosted weights 2^(x - m + 8), their E4M3 codes into the P tile
         float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -338,9 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
         lsum += acc2.x + acc2.y;
+        }
         m = m_new;
-        // block-scale words of the PV MMA: P^ scale 1.0, V scale per 32-key group
-        tmem_st4(s_addr + 120, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        // block-scale words of the PV MMA: P^ scale 1.0 (strict: per-row group
+        // exponents, written above), V scale per 32-key group (strict: 1.0)
+        if (!STRICT) tmem_st4(s_addr + 120, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
         tmem_st4(s_addr + 124, vsf, vsf, vsf, vsf);
         tmem_st_wait();
         fence_proxy_async_smem();
@@ -397,7 +491,7 @@ __global__ void fwd_tail_kernel(const int* plan, int T, int hq, __nv_bfloat16* o
   }
 }
 
-template <int D>
+template <int D, bool STRICT>
 cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                          const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev) {
@@ -423,10 +517,11 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
   const int64_t grid = max_items * hq;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
   constexpr int smem = FwdSmem<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_fwd_kernel<D, STRICT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
-  attn_fwd_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, STRICT><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
@@ -439,9 +534,13 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
 
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev) {
-  if (D == 128) return launch_fwd_d<128>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
-  if (D == 64) return launch_fwd_d<64>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
+                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict) {
+  if (D == 128 && strict)
+    return launch_fwd_d<128, true>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
+  if (D == 128) return launch_fwd_d<128, false>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
+  if (D == 64 && strict)
+    return launch_fwd_d<64, true>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
+  if (D == 64) return launch_fwd_d<64, false>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
   return cudaErrorInvalidValue;
 }
 

@@ -21,14 +21,14 @@ def cu_tensor(lengths, device="cuda"):
     return torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=device)
 
 
-def run_gpu(inputs, lengths, hq, hkv, d, total_tokens=None, with_bwd=True, scale=0.0):
+def run_gpu(inputs, lengths, hq, hkv, d, total_tokens=None, with_bwd=True, scale=0.0, strict=False):
     """inputs: dict of bf16 bit arrays (uint16) q, k, v[, do] of shape [T, H, d]."""
     import torch
     import microscaled_precision_causal_gb300 as F
     T = inputs["q"].shape[0] if total_tokens is None else total_tokens
     N = len(lengths)
     cu = cu_tensor(lengths)
-    att = F.FlamiaAttention(T, N, hq, hkv, d)
+    att = F.FlamiaAttention(T, N, hq, hkv, d, strict=strict)
     q, k, v = (to_device_bf16(inputs[n]) for n in ("q", "k", "v"))
     att.plan_build(cu)
     att.quantize(q, k, v, cu)

@@ -1,0 +1,140 @@
+"""GPU parity of the strict options against the oracle (FLAMIA technical
+review section 4, "Strict options"; Korean review section 4.5).
+
+Strict = per-token operand scales (Q, K, V, dO), per-query-row dS exponents for
+dQ (the K fold), the causal per-row dQ boost and the fixed-order dQ reduction.
+Same bar as the default path: codes and scale bytes bit-exact, O/dQ/dK/dV
+within 1e-2 normalised max-abs error, LSE within 1e-3; and the property the
+options exist for: a later token never changes an earlier row's O, LSE or dQ,
+bit for bit.
+"""
+import numpy as np
+import pytest
+
+import flamia_workloads as W
+import oracle as O
+from gpu_harness import run_gpu, run_oracle
+from metrics import cosine, norm_max_err
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+STRICT = O.Options(strict=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from microscaled_precision_causal_gb300 import build
+    build.build()
+
+
+CASES = [
+    ("ragged_gqa_d128_t3", [300, 77, 129, 1], 2, 1, 128, 0, "student_t3"),
+    ("mha_tail_d64", [130, 5, 260], 2, 2, 64, 19, "normal"),
+    ("gqa4_two_docs_d128", [200, 517], 4, 1, 128, 0, "student_t3"),
+]
+
+
+@pytest.mark.parametrize("name,lengths,hq,hkv,d,extra,dist", CASES, ids=[c[0] for c in CASES])
+def test_strict_training_call_matches_oracle(name, lengths, hq, hkv, d, extra, dist):
+    T = sum(lengths) + extra
+    w = W.custom([T], hq, hkv, d, dist=dist, seed=31)
+    inp = W.make_inputs(w)
+    g = run_gpu(inp, lengths, hq, hkv, d, total_tokens=T, strict=True)
+    o = run_oracle(inp, lengths, hq, hkv, d, opts=STRICT)
+    assert g["status"] == 0
+    for n in ("q", "k", "v"):
+        assert np.array_equal(g[n + "_codes"], o[n + "_codes"]), n
+        assert np.array_equal(g[n + "_scales"], o[n + "_scales"]), n
+    assert np.array_equal(g["do_codes"], o["do_codes"]) and np.array_equal(g["do_scales"], o["do_scales"])
+    valid = sum(lengths)
+    assert np.max(np.abs(g["lse"][:, :valid] - o["lse"][:, :valid])) < 1e-3
+    msgs, worst = [], 0.0
+    for n in ("o", "dq", "dk", "dv"):
+        e = norm_max_err(g[n][:valid], o[n][:valid])
+        worst = max(worst, e)
+        msgs.append(f"{n}: err {e:.2e} cos {cosine(g[n][:valid], o[n][:valid]):.6f}")
+    assert worst <= TOL, "; ".join(msgs)
+    for n in ("o", "dq", "dk", "dv"):
+        assert np.all(g[n][valid:] == 0), n
+
+
+def test_strict_is_deterministic():
+    lengths, hq, hkv, d = [600, 300], 4, 2, 128
+    w = W.custom(lengths, hq, hkv, d, dist="student_t3", seed=32)
+    inp = W.make_inputs(w)
+    a = run_gpu(inp, lengths, hq, hkv, d, strict=True)
+    b = run_gpu(inp, lengths, hq, hkv, d, strict=True)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_strict_earlier_rows_are_bit_identical(d):
+    """Perturbing token t of Q, K or V (dO fixed) leaves O, LSE and dQ of every
+    row before t unchanged bit for bit; the perturbed token reaches row t."""
+    lengths, hq, hkv = [290, 60], 2, 1
+    w = W.custom(lengths, hq, hkv, d, dist="student_t3", seed=33)
+    inp = W.make_inputs(w)
+    base = run_gpu(inp, lengths, hq, hkv, d, strict=True)
+    for t in (1, 33, 150, 289):
+        for name in ("q", "k", "v"):
+            pert = {k_: v_.copy() for k_, v_ in inp.items()}
+            pert[name][t] = W.f32_to_bf16_bits(W.bf16_bits_to_f32(pert[name][t]) * 16.0)
+            c = run_gpu(pert, lengths, hq, hkv, d, strict=True)
+            assert np.array_equal(c["o"][:t], base["o"][:t]), (name, t)
+            assert np.array_equal(c["lse"][:, :t], base["lse"][:, :t]), (name, t)
+            assert np.array_equal(c["dq"][:t], base["dq"][:t]), (name, t)
+            # positive control: the perturbed token reaches its own row
+            assert any(not np.array_equal(c[n][t], base[n][t]) for n in ("o", "dq", "dk", "dv")), (name, t)
+
+
+def test_strict_dq_ignores_a_later_gradient_outlier():
+    """The causal dQ boost: a 2^20 outlier in dO at row 190 leaves dQ of rows
+    < 190 bit-identical (the default document-wide boost would not)."""
+    lengths, hq, hkv, d = [200], 2, 1, 64
+    w = W.custom(lengths, hq, hkv, d, seed=34)
+    inp = W.make_inputs(w)
+    base = run_gpu(inp, lengths, hq, hkv, d, strict=True)
+    pert = {k_: v_.copy() for k_, v_ in inp.items()}
+    pert["do"][190] = W.f32_to_bf16_bits(W.bf16_bits_to_f32(pert["do"][190]) * 2.0 ** 20)
+    c = run_gpu(pert, lengths, hq, hkv, d, strict=True)
+    assert np.array_equal(c["dq"][:190], base["dq"][:190])
+
+
+def test_strict_full_size_sampled_parity():
+    """4 x 8192 tokens, 16 heads, Student-t(3) inputs in the benchmark's launch
+    configuration; the oracle recomputes the last document's last head on
+    sampled tiles."""
+    w = W.WORKLOADS["strict_packed_4x8192_h16_t3"]
+    inp = W.make_inputs(w)
+    g = run_gpu(inp, list(w.lengths), w.hq, w.hkv, w.d, strict=True)
+    assert g["status"] == 0
+    lengths = list(w.lengths)
+    n = len(lengths) - 1
+    s0 = int(np.sum(lengths[:n])); L = lengths[n]; s1 = s0 + L
+    hk = w.hkv - 1
+    gsz = w.hq // w.hkv
+    heads = list(range(hk * gsz, (hk + 1) * gsz))
+    sub = {name: arr[s0:s1][:, heads if name in ("q", "do") else [hk]] for name, arr in inp.items()}
+    nt = -(-L // 128)
+    # the backward of a sampled tile needs the forward LSE of every query tile it
+    # meets: dQ tiles {1, nt-1} and key tiles {nt-2, nt-1} meet query tiles {1, nt-2, nt-1}
+    sel = dict(q_tiles={0: [0, 1, nt - 2, nt - 1]}, k_tiles={0: [nt - 2, nt - 1]}, bwd_q_tiles={0: [1, nt - 1]})
+    o = run_oracle(sub, [L], gsz, 1, w.d, opts=STRICT, **sel)
+    rows_o = np.r_[0:256, (nt - 2) * 128:L]
+    rows_q = np.r_[128:256, (nt - 1) * 128:L]
+    rows_k = np.r_[(nt - 2) * 128:L]
+    gl = {key: (g[key][s0:s1][:, heads] if key in ("o", "dq") else g[key][s0:s1][:, [hk]]) for key in
+          ("o", "dq", "dk", "dv")}
+    for key, rows in (("o", rows_o), ("dq", rows_q), ("dk", rows_k), ("dv", rows_k)):
+        e = norm_max_err(gl[key][rows], o[key][rows])
+        assert e <= TOL, f"{key}: {e:.3e} cos {cosine(gl[key][rows], o[key][rows]):.6f}"
+    lse_g = g["lse"][heads][:, s0:s1][:, rows_o]
+    assert np.max(np.abs(lse_g - o["lse"][:, rows_o])) < 1e-3
+    for nme in ("q", "k", "v"):
+        hsel = heads if nme == "q" else [hk]
+        assert np.array_equal(g[nme + "_codes"][s0:s1][:, hsel], o[nme + "_codes"]), nme
+        assert np.array_equal(g[nme + "_scales"][s0:s1][:, hsel], o[nme + "_scales"]), nme
