@@ -171,7 +171,8 @@ def roundup_exponent(amax) -> np.ndarray:
     amax = np.asarray(amax, dtype=np.float64)
     pos = amax > 0
     safe = np.where(pos, amax, 448.0)
-    e = np.ceil(np.log2(safe / E4M3_MAX)).astype(np.int64)
+    # log2 of each factor separately: amax / 448 can underflow for tiny (subnormal) amax
+    e = np.clip(np.ceil(np.log2(safe) - np.log2(E4M3_MAX)), -128, 128).astype(np.int64)
     # log2 is not exact: settle the inequality with exact power-of-two products.
     for _ in range(2):
         e = np.where(safe > np.ldexp(E4M3_MAX, e), e + 1, e)
@@ -331,6 +332,7 @@ class Options:
     bwd_p_boost_log2: int = 8      # backward P operand boost (reading C-6)
     tile: int = 128                # query and key tile (reading C-11)
     dq_headroom_log2: int = 14     # dQ boost target 2**14 (reading C-10)
+    mixed: bool = False            # mixed route: NVFP4 score operands, diagonal per-key V (C-7, C-8)
 
 
 def _masked_scores(Qt, Ku, qpos, kpos, scale):
@@ -341,7 +343,8 @@ def _masked_scores(Qt, Ku, qpos, kpos, scale):
 
 def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] = None,
                       opts: Options = Options(), heads: Optional[Iterable[int]] = None,
-                      q_tiles: Optional[Dict[int, Iterable[int]]] = None, v_scale=None):
+                      q_tiles: Optional[Dict[int, Iterable[int]]] = None, v_scale=None,
+                      score_ops=None, v_diag=None):
     """Forward of Algorithm 1 (steps 04-08) for causal packed documents.
 
     Qh [T,hq,d], Kh/Vh [T,hkv,d]: reconstructed operands X^ = s*c (or plain
@@ -364,8 +367,18 @@ def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] 
     (v_scale [T, hkv] for V); the per-key V scale is folded into the
     probability operand, P~_ij = beta p_ij s_V(j), which is E4M3-rounded with
     one round-up exponent per (query row, document-local 32-key group), and
-    multiplies the V codes.  Returns (O [T,hq,d], LSE [hq,T])."""
+    multiplies the V codes.
+
+    Mixed route ([EN] section 2, "the mixed route quantizes Q and K again in
+    E4M3 for the gradient products"; [KO] section 3.1; readings C-7, C-8):
+    score_ops = (Q~, K~), the reconstructed NVFP4 copies, replace Q^ and K^ in
+    S.  On the diagonal key tile (the key tile with the query tile's document-
+    local index) V is taken per key: v_diag = (V per-token reconstructed
+    [T,hkv,d], s_V [T,hkv]); the per-key scale is folded into the probability
+    operand exactly as in the strict route.  Other tiles are unchanged.
+    Returns (O [T,hq,d], LSE [hq,T])."""
     Qh = np.asarray(Qh, np.float64); Kh = np.asarray(Kh, np.float64); Vh = np.asarray(Vh, np.float64)
+    Qs, Ks = (Qh, Kh) if score_ops is None else (np.asarray(x, np.float64) for x in score_ops)
     T, _, d = Qh.shape
     g = hq // hkv
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -384,28 +397,33 @@ def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] 
             for t in tiles:
                 r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
                 qpos = np.arange(r0, r1)
-                Qt = Qh[r0:r1, h]
+                Qt = Qs[r0:r1, h]
                 m = np.full(r1 - r0, -np.inf)
                 l = np.zeros(r1 - r0)
                 acc = np.zeros((r1 - r0, d))
                 for u in range(t + 1):
                     c0, c1 = s0 + u * tile, min(s0 + (u + 1) * tile, s1)
-                    S = _masked_scores(Qt, Kh[c0:c1, hk], qpos, np.arange(c0, c1), scale)
+                    S = _masked_scores(Qt, Ks[c0:c1, hk], qpos, np.arange(c0, c1), scale)
                     rowmax = S.max(axis=1)
                     m_new = np.where(rowmax > m + tau_nat, np.maximum(m, rowmax), m)
                     alpha = np.where(np.isfinite(m), np.exp(m - m_new), 0.0)
                     p = np.exp(S - m_new[:, None])
                     l = l * alpha + p.sum(axis=1)
+                    Vt = Vh[c0:c1, hk]
                     if not opts.quantized:
                         Pq = p
-                    elif opts.strict:
+                    elif opts.strict or (opts.mixed and u == t):
                         # per-key V scale folded into P, quantized with one round-up exponent
                         # per (query row, document-local 32-key group)
-                        sv = V_scale[c0:c1, hk]
+                        if opts.strict:
+                            sv = V_scale[c0:c1, hk]
+                        else:
+                            Vt = np.asarray(v_diag[0], np.float64)[c0:c1, hk]
+                            sv = np.asarray(v_diag[1], np.float64)[c0:c1, hk]
                         Pq = _fold_quantize(beta * p * sv[None, :], group_axis=1, offset=c0 - s0) / (beta * sv[None, :])
                     else:
                         Pq = e4m3_round(beta * p) / beta
-                    acc = acc * alpha[:, None] + Pq @ Vh[c0:c1, hk]
+                    acc = acc * alpha[:, None] + Pq @ Vt
                     m = m_new
                 out = acc / l[:, None]
                 O[r0:r1, h] = bf16_round(out) if opts.quantized else out
@@ -436,7 +454,7 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                        kv_heads: Optional[Iterable[int]] = None,
                        k_tiles: Optional[Dict[int, Iterable[int]]] = None,
                        q_tiles: Optional[Dict[int, Iterable[int]]] = None,
-                       diagnostics: bool = False, tok_scales: Optional[dict] = None):
+                       diagnostics: bool = False, tok_scales: Optional[dict] = None, score_ops=None):
     """Backward of Algorithm 1 (steps 09-16).
 
     dOh: the reconstructed incoming gradient dO^ (encoded once, step 09);
@@ -464,12 +482,17 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
     dS s_K(j) per (query row, 32-key block) -- the per-query-row dS exponent
     ("K fold").  The dQ boost is the causal per-row c_i (causal_dq_boost).
 
+    Mixed route: score_ops = (Q~, K~) (NVFP4 copies) replace Q^ and K^ in the
+    recomputed S only -- the same scores as the forward; every gradient product
+    uses the E4M3 copies as in the default route.
+
     k_tiles / q_tiles restrict which dK/dV key tiles and dQ query tiles are
     produced (others stay zero); kv_heads restricts heads.
     Returns dict with dq, dk, dv (and diagnostics when asked)."""
     Qh = np.asarray(Qh, np.float64); Kh = np.asarray(Kh, np.float64)
     Vh = np.asarray(Vh, np.float64); dOh = np.asarray(dOh, np.float64)
     O = np.asarray(O, np.float64); LSE = np.asarray(LSE, np.float64)
+    Qs, Ks = (Qh, Kh) if score_ops is None else (np.asarray(x, np.float64) for x in score_ops)
     T, _, d = Qh.shape
     g = hq // hkv
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -505,7 +528,7 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                             continue
                         r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
                         qpos = np.arange(r0, r1)
-                        S = _masked_scores(Qh[r0:r1, h], Kh[c0:c1, hk], qpos, kpos, scale)
+                        S = _masked_scores(Qs[r0:r1, h], Ks[c0:c1, hk], qpos, kpos, scale)
                         P = np.exp(S - LSE[h, r0:r1][:, None])
                         dP = dOh[r0:r1, h] @ Vh[c0:c1, hk].T
                         dS = P * (dP - D[r0:r1, h][:, None])
@@ -679,6 +702,8 @@ def run_training_call(q, k, v, do, cu, hq: int, hkv: int, scale: Optional[float]
     backward (sampled parity at large sizes).  Returns a dict with the codes,
     scale bytes, O, LSE, dq, dk, dv."""
     out = {}
+    if opts.strict and opts.mixed:
+        raise ValueError("the strict options and the mixed route are separate configurations")
     if opts.quantized:
         blk = 1 if opts.strict else opts.block
         for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
@@ -692,13 +717,29 @@ def run_training_call(q, k, v, do, cu, hq: int, hkv: int, scale: Optional[float]
             out[name + "_hat"] = np.asarray(x, np.float64)
     tok = {n: ue8m0_decode(out[n + "_scales"]) for n in ("q", "k", "v", "do") if n + "_scales" in out} \
         if opts.quantized else {}
+    score_ops = v_diag = None
+    if opts.mixed:
+        if opts.quantized:
+            for name, x in (("q", q), ("k", k)):
+                c, sc = quantize_nvfp4(x)
+                out[name + "_nvfp4_codes"], out[name + "_nvfp4_scales"] = c, sc
+                out[name + "_nvfp4_hat"] = dequantize_nvfp4(c, sc)
+            c, sb = quantize_tokenblock(v, cu, 1, opts.rule)          # per-key V for diagonal tiles
+            out["v_tok_codes"], out["v_tok_scales"] = c, sb
+            out["v_tok_hat"] = dequantize_tokenblock(c, sb)
+            score_ops = (out["q_nvfp4_hat"], out["k_nvfp4_hat"])
+            v_diag = (out["v_tok_hat"], ue8m0_decode(sb))
+        else:
+            v_diag = (out["v_hat"], np.ones(np.asarray(v).shape[:2]))
     O, LSE = attention_forward(out["q_hat"], out["k_hat"], out["v_hat"], cu, hq, hkv, scale, opts,
-                               heads=sel.get("heads"), q_tiles=sel.get("q_tiles"), v_scale=tok.get("v"))
+                               heads=sel.get("heads"), q_tiles=sel.get("q_tiles"), v_scale=tok.get("v"),
+                               score_ops=score_ops, v_diag=v_diag)
     out["o"], out["lse"] = O, LSE
     if do is not None:
         g = attention_backward(out["q_hat"], out["k_hat"], out["v_hat"], O, LSE, out["do_hat"], cu,
                                hq, hkv, scale, opts, kv_heads=sel.get("kv_heads"),
                                k_tiles=sel.get("k_tiles"), q_tiles=sel.get("bwd_q_tiles"),
-                               diagnostics=sel.get("diagnostics", False), tok_scales=tok)
+                               diagnostics=sel.get("diagnostics", False), tok_scales=tok,
+                               score_ops=score_ops)
         out.update(g)
     return out

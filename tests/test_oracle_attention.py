@@ -363,3 +363,95 @@ def test_strict_path_tracks_unquantized_attention():
     assert cosine(out["o"], ref_o) > 0.997
     for n in ("dq", "dk", "dv"):
         assert cosine(out[n], ref_g[n]) > 0.99, n
+
+
+# ------------------------------------------------------------ mixed NVFP4 / FP8 route
+
+def _mixed(q, k, v, do, cu, hq, hkv):
+    return O.run_training_call(q, k, v, do, cu, hq, hkv, opts=O.Options(mixed=True))
+
+
+def test_mixed_route_earlier_rows_are_bit_identical():
+    """[KO] section 3.2 (NVFP4 scales stay inside one token) and [EN] section 4
+    (the per-key V scale folded into P on diagonal tiles keeps masked keys at
+    zero): in the mixed route a change to ANY later token of Q, K or V leaves O
+    and LSE of every earlier row bit-identical -- not only rows of earlier
+    32-token blocks, as in the default route.  The factor 2^12 lifts a shared
+    exponent far enough that every other value of the group falls below the
+    E4M3 normal range, so any shared scale on the path would show."""
+    lengths, hq, hkv, d = [200, 70], 2, 1, 32
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=40)
+    base = _mixed(q, k, v, do, cu, hq, hkv)
+    for t in (5, 40, 130, 199):
+        for name in ("q", "k", "v"):
+            x = {"q": q, "k": k, "v": v}
+            y = x[name].copy()
+            y[t] *= 2.0 ** 12
+            x[name] = y
+            pert = _mixed(x["q"], x["k"], x["v"], do, cu, hq, hkv)
+            assert np.array_equal(pert["o"][:t], base["o"][:t]), (name, t)
+            assert np.array_equal(pert["lse"][:, :t], base["lse"][:, :t]), (name, t)
+            assert not np.array_equal(pert["o"][t:200], base["o"][t:200]), (name, t)   # positive control
+
+
+def test_default_route_leaks_within_the_diagonal_block_mixed_does_not():
+    """Negative control for the diagonal per-key V: the same V perturbation at
+    token 40 changes rows 32..39 in the default route (shared block exponent)
+    but not in the mixed route."""
+    lengths, hq, hkv, d = [64], 1, 1, 16
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=9)
+    v2 = v.copy(); v2[40, 0, 0] *= 2.0 ** 12
+    d0, d1 = _train(q, k, v, do, cu, hq, hkv), _train(q, k, v2, do, cu, hq, hkv)
+    m0, m1 = _mixed(q, k, v, do, cu, hq, hkv), _mixed(q, k, v2, do, cu, hq, hkv)
+    assert not np.array_equal(d0["o"][32:40], d1["o"][32:40])
+    assert np.array_equal(m0["o"][:40], m1["o"][:40])
+
+
+def test_mixed_route_scores_come_from_the_nvfp4_copies():
+    """With Q and K on the E2M1 grid (every 16-group holding a 6, so the NVFP4
+    scale is exactly 1 and the token-block E4M3 codes are exact too) the mixed
+    and default routes see the same scores; with Q and K off that grid the
+    NVFP4 rounding (coarser than E4M3) changes them."""
+    rng = np.random.default_rng(41)
+    T, hq, hkv, d = 96, 1, 1, 32
+    grid = np.array([-6, -4, -3, -2, -1.5, -1, -0.5, 0, 0.5, 1, 1.5, 2, 3, 4, 6], float)
+    mk = lambda: rng.choice(grid, size=(T, 1, d))
+    q, k = mk(), mk()
+    q[:, :, ::16] = 6.0; k[:, :, ::16] = 6.0
+    v = O.bf16_round(rng.standard_normal((T, 1, d)))
+    do = O.bf16_round(rng.standard_normal((T, 1, d)))
+    cu = np.array([0, T])
+    m = _mixed(q, k, v, do, cu, hq, hkv)
+    assert np.array_equal(m["q_nvfp4_hat"], q) and np.array_equal(m["k_nvfp4_hat"], k)
+    assert np.array_equal(m["q_hat"], q) and np.array_equal(m["k_hat"], k)
+    # same scores: the routes differ only through the diagonal per-key V, so the
+    # gradients of the first query tile's fully visible part agree closely
+    dflt = _train(q, k, v, do, cu, hq, hkv)
+    assert np.array_equal(m["lse"], dflt["lse"])
+    qn = O.bf16_round(rng.standard_normal((T, 1, d)))
+    m2 = _mixed(qn, k, v, do, cu, hq, hkv)
+    d2 = _train(qn, k, v, do, cu, hq, hkv)
+    assert not np.array_equal(m2["lse"], d2["lse"])
+
+
+def test_mixed_route_tracks_unquantized_attention():
+    """[EN] section 8 reports cosine 0.9920 (output) and 0.9906 (gradients) for the
+    mixed route against an FP32 reference on 4x4096 causal inputs; small N(0,1)
+    inputs land in the same range, below the MXFP8 route."""
+    lengths, hq, hkv, d = [300, 212], 4, 2, 64
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=42)
+    out = _mixed(q, k, v, do, cu, hq, hkv)
+    ref_o, _ = O.dense_attention(q, k, v, cu, hq, hkv)
+    ref_g = O.dense_attention_grads(q, k, v, do, cu, hq, hkv)
+    dflt = _train(q, k, v, do, cu, hq, hkv)
+    co = cosine(out["o"], ref_o)
+    assert 0.988 < co < 0.996 and co < cosine(dflt["o"], ref_o)
+    for n in ("dq", "dk", "dv"):
+        cg = cosine(out[n], ref_g[n])
+        assert 0.986 < cg < 0.996 and cg < cosine(dflt[n], ref_g[n]), n
+
+
+def test_mixed_and_strict_are_separate():
+    q, k, v, do, cu = _inputs([40], 1, 1, 16, seed=43)
+    with pytest.raises(ValueError):
+        O.run_training_call(q, k, v, do, cu, 1, 1, opts=O.Options(mixed=True, strict=True))
