@@ -85,7 +85,10 @@ typedef struct flamia_options {
      Strict calls support documents of up to 16384 tokens (longer ones set
      FLAMIA_DEV_CAPACITY and leave the outputs unspecified).
      deterministic: accepted only with the strict set (which implies it).
-     mixed_nvfp4: the mixed NVFP4/FP8 score path is not built; must be 0. */
+     mixed_nvfp4: the mixed NVFP4/FP8 route (head_dim 128 only; not with the
+     strict options): scores and their backward recomputation from NVFP4 Q and
+     K (opt->mixed), diagonal key tiles of the forward with per-key V scales
+     folded into P. */
   int strict_per_token;
   int strict_row_ds;
   int strict_causal_dq;
@@ -99,7 +102,28 @@ typedef struct flamia_options {
      kernel, 3 = dQ finalisation (strict: the ordered dQ kernel and the zeroing
      of rows outside every document).  The events are caller-owned. */
   void* const* timing_events;
+  /* Mixed route operands (required when mixed_nvfp4 = 1, else ignored). */
+  const struct flamia_mixed_operands* mixed;
 } flamia_options;
+
+/* Operands of the mixed NVFP4/FP8 route (FLAMIA review section 2, "The mixed
+   route quantizes Q and K again in E4M3 for the gradient products"; Korean
+   review section 3.1: only the Q and K used by the scores and their
+   recomputation are stored as NVFP4).  All device pointers, 16-byte aligned.
+   The E4M3 token-block q, k, v views of flamia_fwd / flamia_bwd stay in use
+   for every other product. */
+typedef struct flamia_mixed_operands {
+  const void* q_codes_e2m1;   /* uint8 [T, hq, head_dim/2]: two E2M1 codes per byte,
+                                 element 2k in the low nibble (flamia_quantize_nvfp4) */
+  const void* q_scales_e4m3;  /* uint8 [T, hq, head_dim/16]: E4M3 scale per 16 elements */
+  const void* k_codes_e2m1;   /* uint8 [T, hkv, head_dim/2] */
+  const void* k_scales_e4m3;  /* uint8 [T, hkv, head_dim/16] */
+  const void* v_tok_codes;    /* uint8 E4M3 [T, hkv, head_dim]: V quantized per token
+                                 (flamia_quantize_tokenblock with per_token = 1); the
+                                 forward reads it on diagonal key tiles only (reading
+                                 C-8: per-key V scales folded into P there) */
+  const void* v_tok_scales;   /* uint8 UE8M0 [T, hkv] */
+} flamia_mixed_operands;
 
 /* Fill *opt with the defaults above (p_boost_log2 = 8, bwd_p_boost_log2 = 8,
    dq_headroom_log2 = 14, everything else 0 / NULL). */
@@ -159,6 +183,23 @@ int flamia_plan_build(const int32_t* cu_seqlens, int num_seqs, int64_t total_tok
 int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int heads, int head_dim,
                                const int32_t* cu_seqlens, int num_seqs, const void* plan, int per_token,
                                void* codes_e4m3, void* scales_ue8m0, float* stats, void* stream);
+
+/* ----------------------------------------------------------- NVFP4 quantizer (a2)
+ * Score operands of the mixed route (FLAMIA review section 2: E2M1 codes and
+ * an E4M3 scale per 16 elements; Korean review section 3.2: the scale groups
+ * stay inside one token, so no document or block structure is involved).
+ * Per (token, head, 16 consecutive head-dim elements), reading C-7 (no
+ * tensor-level scale):
+ *   s    = E4M3(amax / 6), IEEE fp32 division, round to nearest even,
+ *          saturating; a non-zero group whose s rounds to 0 gets 2^-9;
+ *   code = E2M1(x / s), IEEE fp32 division, round to nearest even,
+ *          saturating to +-6 (0 for an all-zero group).
+ * x: bf16 [T, heads, head_dim] (device).  codes_e2m1: uint8 [T, heads,
+ * head_dim/2], element 2k in the low nibble of byte k; scales_e4m3: uint8
+ * [T, heads, head_dim/16].  Bit-exact with the oracle.  head_dim 64 or 128;
+ * x and codes 16-byte aligned. */
+int flamia_quantize_nvfp4(const void* x_bf16, int64_t total_tokens, int heads, int head_dim, void* codes_e2m1,
+                          void* scales_e4m3, void* stream);
 
 /* ----------------------------------------------------------- forward (a4-a6)
  * Algorithm 1 steps 04-08 of the FLAMIA review.  For each document, query

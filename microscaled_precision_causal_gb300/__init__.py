@@ -27,7 +27,7 @@ DEV_BAD_CU_SEQLENS, DEV_TIMEOUT, DEV_CAPACITY = 1, 2, 4
 EXPORTED = (
     "flamia_default_options", "flamia_plan_bytes", "flamia_plan_build", "flamia_quantize_tokenblock",
     "flamia_fwd", "flamia_bwd_workspace_bytes", "flamia_bwd", "flamia_get_device_status",
-    "flamia_status_string", "flamia_bwd_static_scratch",
+    "flamia_status_string", "flamia_bwd_static_scratch", "flamia_quantize_nvfp4",
 )
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -39,11 +39,17 @@ class FlamiaError(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "p_boost_log2", "bwd_p_boost_log2", "dq_headroom_log2", "strict_per_token", "strict_row_ds",
-        "strict_causal_dq", "mixed_nvfp4", "deterministic")] + [("timing_events", ctypes.POINTER(ctypes.c_void_p))]
+        "strict_causal_dq", "mixed_nvfp4", "deterministic")] + [("timing_events", ctypes.POINTER(ctypes.c_void_p)),
+                                                                 ("mixed", ctypes.c_void_p)]
 
 
 class QTensor(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("stats", ctypes.c_void_p)]
+
+
+class MixedOperands(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q_codes_e2m1", "q_scales_e4m3", "k_codes_e2m1", "k_scales_e4m3",
+                                               "v_tok_codes", "v_tok_scales")]
 
 
 _lib = None
@@ -74,6 +80,7 @@ def lib():
                                             vp, vp, vp, vp]),
         "flamia_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_int), vp]),
         "flamia_status_string": (ctypes.c_char_p, [i32]),
+        "flamia_quantize_nvfp4": (i32, [vp, i64, i32, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -134,6 +141,12 @@ def flamia_quantize_tokenblock(x, cu_seqlens, num_seqs: int, plan, codes, scales
            "flamia_quantize_tokenblock")
 
 
+def flamia_quantize_nvfp4(x, codes, scales, stream=None):
+    T, H, d = x.shape
+    _check(lib().flamia_quantize_nvfp4(_ptr(x), T, H, d, _ptr(codes), _ptr(scales), _stream(stream)),
+           "flamia_quantize_nvfp4")
+
+
 def flamia_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens, num_seqs: int, total_tokens: int, hq: int, hkv: int,
                head_dim: int, plan, out, lse, softmax_scale: float = 0.0, opts: Optional[Options] = None,
                causal: int = 1, stream=None):
@@ -187,7 +200,7 @@ class FlamiaAttention:
     torch, reused across calls: nothing is allocated per call)."""
 
     def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, device="cuda",
-                 strict: bool = False):
+                 strict: bool = False, mixed: bool = False):
         import torch
         self.T, self.N, self.hq, self.hkv, self.d = total_tokens, num_seqs, hq, hkv, head_dim
         self.device = torch.device(device)
@@ -214,6 +227,19 @@ class FlamiaAttention:
         if self.strict:   # per-token operand scales, per-query-row dS exponents, causal dQ boost, deterministic dQ
             for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq", "deterministic"):
                 setattr(self.opts, f, 1)
+        self.mixed = bool(mixed)
+        if self.mixed:    # NVFP4 score operands, per-token V copy for the diagonal key tiles
+            T = total_tokens
+            self.q4_codes = torch.empty(T, hq, head_dim // 2, dtype=u8, device=dev)
+            self.q4_scales = torch.empty(T, hq, head_dim // 16, dtype=u8, device=dev)
+            self.k4_codes = torch.empty(T, hkv, head_dim // 2, dtype=u8, device=dev)
+            self.k4_scales = torch.empty(T, hkv, head_dim // 16, dtype=u8, device=dev)
+            self.vt_codes = torch.empty(T, hkv, head_dim, dtype=u8, device=dev)
+            self.vt_scales = torch.empty(T, hkv, dtype=u8, device=dev)
+            self._mixed_ops = MixedOperands(_ptr(self.q4_codes), _ptr(self.q4_scales), _ptr(self.k4_codes),
+                                            _ptr(self.k4_scales), _ptr(self.vt_codes), _ptr(self.vt_scales))
+            self.opts.mixed_nvfp4 = 1
+            self.opts.mixed = ctypes.cast(ctypes.pointer(self._mixed_ops), ctypes.c_void_p)
 
     def views(self):
         return (qtensor(self.q_codes, self.q_scales), qtensor(self.k_codes, self.k_scales, self.k_stats),
@@ -229,6 +255,11 @@ class FlamiaAttention:
                                    stream)
         flamia_quantize_tokenblock(v, cu_seqlens, self.N, self.plan, self.v_codes, self.v_scales, self.v_stats, pt,
                                    stream)
+        if self.mixed:
+            flamia_quantize_nvfp4(q, self.q4_codes, self.q4_scales, stream)
+            flamia_quantize_nvfp4(k, self.k4_codes, self.k4_scales, stream)
+            flamia_quantize_tokenblock(v, cu_seqlens, self.N, self.plan, self.vt_codes, self.vt_scales, None, True,
+                                       stream)
 
     def forward(self, cu_seqlens, softmax_scale: float = 0.0, stream=None):
         q, k, v = self.views()

@@ -18,7 +18,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libflamia.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["plan.cu", "quantize.cu", "attn_fwd.cu", "attn_bwd.cu", "abi.cu", "static_scratch.cu"]
+SOURCES = ["plan.cu", "quantize.cu", "attn_fwd.cu", "attn_fwd_coop.cu", "attn_bwd.cu", "abi.cu",
+           "static_scratch.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "tmap.h"]
 
 NVCC_FLAGS = [

@@ -15,6 +15,12 @@ cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* c
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict);
+cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, void* scales, cudaStream_t s);
+cudaError_t launch_fwd_coop(int D, int mixed, const void* qc, const void* qs, const void* kc, const void* ks,
+                            const void* vc, const void* vs, const void* q4c, const void* q4s, const void* k4c,
+                            const void* k4s, const void* vtc, const void* vts, const int32_t* cu, int N, int T, int hq,
+                            int hkv, float scale, const void* plan, void* out, float* lse, cudaStream_t stream);
+cudaError_t launch_fwd_tail(int D, const void* plan, int T, int hq, void* out, float* lse, cudaStream_t stream);
 cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float* st_do, const float* st_k,
                          const float* st_v, int T, int hq, int hkv, int headroom, float* boost, bool causal,
                          cudaStream_t s);
@@ -52,9 +58,20 @@ int check_opts(const flamia_options* o) {
   const int s = o->strict_per_token + o->strict_row_ds + o->strict_causal_dq;
   if (s != 0 && s != 3) return FLAMIA_ERR_UNSUPPORTED;
   if (o->deterministic && s == 0) return FLAMIA_ERR_UNSUPPORTED;
-  if (o->mixed_nvfp4) return FLAMIA_ERR_UNSUPPORTED;
+  if (o->mixed_nvfp4) {
+    if (s != 0) return FLAMIA_ERR_UNSUPPORTED;        // the strict options and the mixed route are separate
+    const flamia_mixed_operands* m = o->mixed;
+    if (!m || !m->q_codes_e2m1 || !m->q_scales_e4m3 || !m->k_codes_e2m1 || !m->k_scales_e4m3 || !m->v_tok_codes ||
+        !m->v_tok_scales)
+      return FLAMIA_ERR_INVALID_ARG;
+    if (!aligned16(m->q_codes_e2m1) || !aligned16(m->k_codes_e2m1) || !aligned16(m->v_tok_codes) ||
+        (reinterpret_cast<uintptr_t>(m->q_scales_e4m3) & 7u) || (reinterpret_cast<uintptr_t>(m->k_scales_e4m3) & 7u))
+      return FLAMIA_ERR_MISALIGNED;
+  }
   return FLAMIA_OK;
 }
+
+bool is_mixed(const flamia_options* o) { return o && o->mixed_nvfp4; }
 
 int check_heads(int hq, int hkv, int d) {
   if (hq <= 0 || hkv <= 0) return FLAMIA_ERR_INVALID_ARG;
@@ -134,6 +151,17 @@ int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int hea
                                      (cudaStream_t)stream));
 }
 
+int flamia_quantize_nvfp4(const void* x_bf16, int64_t total_tokens, int heads, int head_dim, void* codes_e2m1,
+                          void* scales_e4m3, void* stream) {
+  if (total_tokens < 0 || heads <= 0) return FLAMIA_ERR_INVALID_ARG;
+  if (!x_bf16 || !codes_e2m1 || !scales_e4m3) return FLAMIA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return FLAMIA_ERR_UNSUPPORTED;
+  if (!aligned16(x_bf16) || !aligned16(codes_e2m1)) return FLAMIA_ERR_MISALIGNED;
+  if (total_tokens == 0) return FLAMIA_OK;
+  return cuda_status(launch_quantize_nvfp4(x_bf16, total_tokens * heads * head_dim, codes_e2m1, scales_e4m3,
+                                           (cudaStream_t)stream));
+}
+
 int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v, const int32_t* cu_seqlens,
                int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim, int causal, float softmax_scale,
                const flamia_options* opt, const void* plan, void* out_bf16, float* lse, void* stream) {
@@ -147,11 +175,24 @@ int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (causal != 1) return FLAMIA_ERR_UNSUPPORTED;
   if (!out_bf16 || !lse) return FLAMIA_ERR_INVALID_ARG;
   if (!aligned16(out_bf16) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FLAMIA_ERR_MISALIGNED;
+  if (is_mixed(opt) && head_dim != 128) return FLAMIA_ERR_UNSUPPORTED;
   if (total_tokens == 0) return FLAMIA_OK;
+  const float scale = resolve_scale(softmax_scale, head_dim);
+  if (is_mixed(opt)) {
+    const flamia_mixed_operands* m = opt->mixed;
+    cudaStream_t s = (cudaStream_t)stream;
+    record(opt->timing_events, 0, s);
+    cudaError_t e = launch_fwd_coop(head_dim, 1, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales,
+                                    m->q_codes_e2m1, m->q_scales_e4m3, m->k_codes_e2m1, m->k_scales_e4m3,
+                                    m->v_tok_codes, m->v_tok_scales, cu_seqlens, num_seqs, (int)total_tokens, hq, hkv,
+                                    scale, plan, out_bf16, lse, s);
+    record(opt->timing_events, 1, s);
+    if (e == cudaSuccess) e = launch_fwd_tail(head_dim, plan, (int)total_tokens, hq, out_bf16, lse, s);
+    return cuda_status(e);
+  }
   return cuda_status(launch_fwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, cu_seqlens,
-                                num_seqs, (int)total_tokens, hq, hkv, resolve_scale(softmax_scale, head_dim), plan,
-                                out_bf16, lse, (cudaStream_t)stream, opt ? opt->timing_events : nullptr,
-                                is_strict(opt)));
+                                num_seqs, (int)total_tokens, hq, hkv, scale, plan, out_bf16, lse, (cudaStream_t)stream,
+                                opt ? opt->timing_events : nullptr, is_strict(opt)));
 }
 
 size_t flamia_bwd_workspace_bytes(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim) {
@@ -177,6 +218,7 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (!aligned16(out_bf16) || !aligned16(dout_bf16) || !aligned16(dq_bf16) || !aligned16(dk_bf16) ||
       !aligned16(dv_bf16) || (reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FLAMIA_ERR_MISALIGNED;
+  if (is_mixed(opt)) return FLAMIA_ERR_UNSUPPORTED;
   const BwdWorkspace w = bwd_layout(total_tokens, num_seqs, hq, head_dim);
   if (workspace_bytes < w.total) return FLAMIA_ERR_WORKSPACE;
   if (total_tokens == 0) return FLAMIA_OK;

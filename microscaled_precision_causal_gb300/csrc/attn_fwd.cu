@@ -532,6 +532,18 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
 
 }  // namespace
 
+cudaError_t launch_fwd_tail(int D, const void* plan, int T, int hq, void* out, float* lse, cudaStream_t stream) {
+  if (D == 128)
+    fwd_tail_kernel<128><<<152, 256, 0, stream>>>(static_cast<const int*>(plan), T, hq,
+                                                  static_cast<__nv_bfloat16*>(out), lse);
+  else if (D == 64)
+    fwd_tail_kernel<64><<<152, 256, 0, stream>>>(static_cast<const int*>(plan), T, hq,
+                                                 static_cast<__nv_bfloat16*>(out), lse);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict) {

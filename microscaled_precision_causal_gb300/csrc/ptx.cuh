@@ -138,6 +138,18 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// NVFP4 block-scaled MMA: E2M1 operands packed two per byte (K-major only), one
+// E4M3 scale per 16 elements, four scale bytes per row and instruction (K = 64).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // Arrive (once) on bar when every tcgen05 op issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -225,6 +237,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_mn_major, 
          (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
          (static_cast<uint32_t>(sfa_id & 3) << 29);
+}
+
+// Instruction descriptor, kind::mxf4nvf4: A, B = E2M1 (K-major), UE4M3 scales,
+// F32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10)                      // A, B = E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)     // scale format bit 23 = 0: UE4M3
+         | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Byte offset of byte `col_byte` of row `row` in a tile of `row_bytes`-long

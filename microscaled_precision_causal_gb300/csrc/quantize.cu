@@ -15,6 +15,8 @@
 // The backward-prep variant (review Algorithm 1 step 09) encodes dO once and,
 // in the same pass, computes D_i = dO^_i . O_i from the saved bf16 O and
 // zeroes the fp16 dQ accumulator rows it owns.
+#include <cuda_fp4.h>
+
 #include "common.cuh"
 
 namespace flamia {
@@ -183,7 +185,61 @@ cudaError_t dispatch(const void* x, int T, int H, const int32_t* cu, int N, cons
   return launch_q<D, false, false, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
 }
 
+// NVFP4 score operand (step a2, the mixed route; FLAMIA technical review section
+// 2, "NVFP4 uses E2M1 codes, a local E4M3 scale for each 16-element group";
+// Korean review section 3.2: the scales stay inside one token).  Reading C-7:
+// no tensor-level scale; s = E4M3(amax / 6) (IEEE fp32 division, round to
+// nearest even, saturating), raised to the smallest subnormal 2^-9 when a
+// non-zero group would get a zero scale; code = E2M1(x / s) (IEEE fp32
+// division, round to nearest even, saturating to +-6).
+// One thread per 16-element group: 32 contiguous bytes in, 8 bytes of packed
+// codes (element 2k in the low nibble of byte k) and one scale byte out.
+__global__ void __launch_bounds__(256) nvfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t groups,
+                                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
+       gi += (int64_t)gridDim.x * blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + gi * 16);
+    uint4 w[2] = {__ldg(src), __ldg(src + 1)};
+    float f[16];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 v = __bfloat1622float2(b[k]);
+        f[8 * j + 2 * k] = v.x;
+        f[8 * j + 2 * k + 1] = v.y;
+        amax = fmax3(amax, fabsf(v.x), fabsf(v.y));
+      }
+    }
+    uint8_t sc = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f), __NV_SATFINITE, __NV_E4M3);
+    if (amax > 0.f && sc == 0) sc = 0x01;   // 2^-9
+    const float s = e4m3_to_f32(sc);
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float q0 = s > 0.f ? __fdiv_rn(f[2 * k], s) : 0.f;
+      const float q1 = s > 0.f ? __fdiv_rn(f[2 * k + 1], s) : 0.f;
+      const uint32_t b = (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(q0, q1), __NV_E2M1, cudaRoundNearest);
+      packed[k >> 2] |= (b & 0xFFu) << (8 * (k & 3));
+    }
+    *reinterpret_cast<uint2*>(codes + gi * 8) = make_uint2(packed[0], packed[1]);
+    scales[gi] = sc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, void* scales, cudaStream_t s) {
+  const int64_t groups = elems / 16;
+  if (groups == 0) return cudaSuccess;
+  int64_t blocks = (groups + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  nvfp4_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), groups,
+                                                static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales));
+  return cudaGetLastError();
+}
 
 // o / dvec / dq_acc non-null selects the backward-prep variant (stats required).
 cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,

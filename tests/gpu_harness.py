@@ -21,14 +21,14 @@ def cu_tensor(lengths, device="cuda"):
     return torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=device)
 
 
-def run_gpu(inputs, lengths, hq, hkv, d, total_tokens=None, with_bwd=True, scale=0.0, strict=False):
+def run_gpu(inputs, lengths, hq, hkv, d, total_tokens=None, with_bwd=True, scale=0.0, strict=False, mixed=False):
     """inputs: dict of bf16 bit arrays (uint16) q, k, v[, do] of shape [T, H, d]."""
     import torch
     import microscaled_precision_causal_gb300 as F
     T = inputs["q"].shape[0] if total_tokens is None else total_tokens
     N = len(lengths)
     cu = cu_tensor(lengths)
-    att = F.FlamiaAttention(T, N, hq, hkv, d, strict=strict)
+    att = F.FlamiaAttention(T, N, hq, hkv, d, strict=strict, mixed=mixed)
     q, k, v = (to_device_bf16(inputs[n]) for n in ("q", "k", "v"))
     att.plan_build(cu)
     att.quantize(q, k, v, cu)
@@ -43,6 +43,9 @@ def run_gpu(inputs, lengths, hq, hkv, d, total_tokens=None, with_bwd=True, scale
     out.update(q_codes=att.q_codes, q_scales=att.q_scales, k_codes=att.k_codes, k_scales=att.k_scales,
                v_codes=att.v_codes, v_scales=att.v_scales, k_stats=att.k_stats, v_stats=att.v_stats,
                o=att.out, lse=att.lse, plan=att.plan)
+    if mixed:
+        out.update(q4_codes=att.q4_codes, q4_scales=att.q4_scales, k4_codes=att.k4_codes, k4_scales=att.k4_scales,
+                   vt_codes=att.vt_codes, vt_scales=att.vt_scales)
     res = {}
     for key, val in out.items():
         if val.dtype == torch.bfloat16:

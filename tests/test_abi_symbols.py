@@ -73,8 +73,8 @@ def test_host_validation_without_gpu(flamia):
 def test_strict_options_come_as_a_set(flamia):
     """The strict options are accepted together (per-token scales, per-row dS
     exponents, causal dQ boost; deterministic may be added); a partial set, a
-    deterministic flag without them, or the mixed NVFP4 score path is refused
-    before any CUDA call."""
+    deterministic flag without them, the mixed route without its operands or
+    together with the strict options is refused before any CUDA call."""
     L, F = flamia.lib(), flamia
     q = F.QTensor(16, 16, None)
 
@@ -82,7 +82,8 @@ def test_strict_options_come_as_a_set(flamia):
         return L.flamia_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), 256, 1, 100, 4, 2, 128, 1, 0.0,
                             ctypes.byref(o), 256, 258, 256, None)   # misaligned output: reached only if opts pass
     for flags, want in ((("strict_per_token",), -2), (("strict_per_token", "strict_row_ds"), -2),
-                        (("strict_causal_dq",), -2), (("deterministic",), -2), (("mixed_nvfp4",), -2),
+                        (("strict_causal_dq",), -2), (("deterministic",), -2), (("mixed_nvfp4",), -1),
+                        (("mixed_nvfp4", "strict_per_token", "strict_row_ds", "strict_causal_dq"), -2),
                         (("strict_per_token", "strict_row_ds", "strict_causal_dq"), -3),
                         (("strict_per_token", "strict_row_ds", "strict_causal_dq", "deterministic"), -3)):
         o = F.default_options()

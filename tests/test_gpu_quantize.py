@@ -114,3 +114,29 @@ def test_quantizer_outlier_heavy_input(F):
         oc, osb = O.quantize_tokenblock(bf16_values(bits), [0, 500, 800])
         assert np.array_equal(scales.cpu().numpy(), osb)
         assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+def _unpack_e2m1(packed):
+    lo, hi = packed & 0x0F, packed >> 4
+    return np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+
+
+@pytest.mark.parametrize("dist,d", [("normal", 128), ("normal_outliers", 128), ("student_t3", 64)])
+def test_nvfp4_quantizer_bit_exact(F, dist, d):
+    """NVFP4 score operands (reading C-7): E2M1 codes and E4M3 group scales equal
+    the oracle's, bit for bit; element 2k sits in the low nibble of byte k."""
+    import torch
+    T, H = 777, 3
+    w = W.custom([T], H, H, d, dist=dist, seed=5)
+    bits = W.make_inputs(w, tensors=("q",))["q"]
+    x = bf16_values(bits)
+    x[3, 0, :16] = 0.0                                   # an all-zero group
+    x[4, 1, 16:32] = x[4, 1, 16:32] * 2.0 ** -40         # scales below the E4M3 range: raised to 2^-9
+    bits = W.f32_to_bf16_bits(x.astype(np.float32))
+    codes = torch.zeros(T, H, d // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(T, H, d // 16, dtype=torch.uint8, device="cuda")
+    F.flamia_quantize_nvfp4(to_device_bf16(bits), codes, scales)
+    torch.cuda.synchronize()
+    oc, osc = O.quantize_nvfp4(bf16_values(bits))
+    assert np.array_equal(scales.cpu().numpy(), osc)
+    assert np.array_equal(_unpack_e2m1(codes.cpu().numpy()), oc)
