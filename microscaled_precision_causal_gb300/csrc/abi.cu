@@ -28,7 +28,8 @@ cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, co
                        const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
-                       void* const* ev, bool strict);
+                       void* const* ev, bool strict, const void* q4c, const void* q4s, const void* k4c,
+                       const void* k4s);
 }  // namespace flamia
 
 using namespace flamia;
@@ -218,7 +219,7 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (!aligned16(out_bf16) || !aligned16(dout_bf16) || !aligned16(dq_bf16) || !aligned16(dk_bf16) ||
       !aligned16(dv_bf16) || (reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FLAMIA_ERR_MISALIGNED;
-  if (is_mixed(opt)) return FLAMIA_ERR_UNSUPPORTED;
+  if (is_mixed(opt) && head_dim != 128) return FLAMIA_ERR_UNSUPPORTED;
   const BwdWorkspace w = bwd_layout(total_tokens, num_seqs, hq, head_dim);
   if (workspace_bytes < w.total) return FLAMIA_ERR_WORKSPACE;
   if (total_tokens == 0) return FLAMIA_OK;
@@ -245,7 +246,11 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (e == cudaSuccess)
     e = launch_bwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, do_codes, do_scales, lse,
                    dvec, boost, cu_seqlens, num_seqs, T, hq, hkv, resolve_scale(softmax_scale, head_dim), plan, dq_acc,
-                   dq_bf16, dk_bf16, dv_bf16, s, ev ? ev + 4 : nullptr, strict);
+                   dq_bf16, dk_bf16, dv_bf16, s, ev ? ev + 4 : nullptr, strict,
+                   is_mixed(opt) ? opt->mixed->q_codes_e2m1 : nullptr,
+                   is_mixed(opt) ? opt->mixed->q_scales_e4m3 : nullptr,
+                   is_mixed(opt) ? opt->mixed->k_codes_e2m1 : nullptr,
+                   is_mixed(opt) ? opt->mixed->k_scales_e4m3 : nullptr);
   return cuda_status(e);
 }
 

@@ -66,12 +66,14 @@ struct BwdParams {
   int N, T, hq, hkv;
   float scale_log2;        // softmax scale * log2(e)
   float scale;
+  const uint8_t* q4_scales;   // mixed route: E4M3 scale codes [T, hq, D/16] of the NVFP4 score operands
+  const uint8_t* k4_scales;   // [T, hkv, D/16]
   __half* dq_acc;          // [T, hq, D]
   __nv_bfloat16* dk;       // [T, hkv, D]
   __nv_bfloat16* dv;
 };
 
-template <int D>
+template <int D, bool MIXED>
 struct BwdSmem {
   static constexpr int kTileBytes = kTile * D;
   static constexpr int kK = 0;
@@ -87,7 +89,10 @@ struct BwdSmem {
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents (+ strict per-row exponents)
   static constexpr int kStageBytes = kTile * BwdShape<D>::kCols * 2;   // one warpgroup's fp16 slice of the dQ tile
   static constexpr int kStage = (kE + 64 + 1024 + 1023) & ~1023;   // [warpgroup]
-  static constexpr int kBar = kStage + BwdShape<D>::kWG * kStageBytes;
+  static constexpr int kScoreBytes = kTile * D / 2;           // mixed route: one E2M1 score-operand tile
+  static constexpr int kK4 = kStage + BwdShape<D>::kWG * kStageBytes;
+  static constexpr int kQ4 = kK4 + (MIXED ? kScoreBytes : 0);          // [kQStages]
+  static constexpr int kBar = kQ4 + (MIXED ? kQStages * kScoreBytes : 0);
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -101,12 +106,15 @@ __device__ __forceinline__ void red_add_f16x8(__half* dst, uint32_t a, uint32_t 
                : "memory");
 }
 
-template <int D, bool STRICT>
+template <int D, bool STRICT, bool MIXED>
 __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_q4, const __grid_constant__ CUtensorMap tm_k4,
                     const BwdParams p) {
-  using L = BwdSmem<D>;
+  static_assert(!(STRICT && MIXED), "the strict options and the mixed route are separate");
+  static_assert(!MIXED || D == 128, "the mixed route is built for head_dim 128");
+  using L = BwdSmem<D, MIXED>;
   constexpr int kWG = BwdShape<D>::kWG, kCPW = BwdShape<D>::kChunksPerWG, kCols = BwdShape<D>::kCols;
   constexpr int kCompute = BwdShape<D>::kCompute;
   extern __shared__ uint8_t smem_raw[];
@@ -123,7 +131,8 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   uint64_t* dq_full = s_full + 3;
   uint64_t* dq_empty = s_full + 4;
   uint64_t* acc_full = s_full + 5;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 6);
+  uint64_t* sf_ready = s_full + 6;            // mixed: score scale words of step 0 written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
   int* status = const_cast<int*>(p.plan) + kPlanStatus;
 
   const int n_items = p.plan[kPlanBwdItems];
@@ -157,6 +166,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, kCompute);
     mbar_init(acc_full, 1);
+    mbar_init(sf_ready, 128);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -178,16 +188,19 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes);
+      mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
       tma_load_3d(smem + L::kK, &tm_k, kv_full, 0, hk, doc_start + u * kTile);
       tma_load_3d(smem + L::kV, &tm_v, kv_full, 0, hk, doc_start + u * kTile);
+      if (MIXED) tma_load_3d(smem + L::kK4, &tm_k4, kv_full, 0, hk, doc_start + u * kTile);
       for (int k = 0; k < nsteps; ++k) {
         const int st = k % kQStages;
         if (k >= kQStages && !mbar_wait(&qd_empty[st], ((k / kQStages) - 1) & 1, status)) break;
         const int h = hk * g + k / qtiles, t = u + k % qtiles;
-        mbar_arrive_expect_tx(&qd_full[st], 2 * L::kTileBytes);
+        mbar_arrive_expect_tx(&qd_full[st], 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
         tma_load_3d(smem + L::kQ + st * L::kTileBytes, &tm_q, &qd_full[st], 0, h, doc_start + t * kTile);
         tma_load_3d(smem + L::kDO + st * L::kTileBytes, &tm_do, &qd_full[st], 0, h, doc_start + t * kTile);
+        if (MIXED)
+          tma_load_3d(smem + L::kQ4 + st * L::kScoreBytes, &tm_q4, &qd_full[st], 0, h, doc_start + t * kTile);
       }
     }
   } else if (warp == 1) {
@@ -196,11 +209,22 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       const uint32_t sk = smem_u32(smem + L::kK), sv = smem_u32(smem + L::kV), sq = smem_u32(smem + L::kQ),
                      sdo = smem_u32(smem + L::kDO), spt = smem_u32(smem + L::kPt), sds = smem_u32(smem + L::kDS);
       auto issue_s = [&](int st) {
-        const uint32_t qa = sq + st * L::kTileBytes;
+        if constexpr (MIXED) {
+          // S^T = K~ Q~^T from the NVFP4 copies (64 E2M1 elements per instruction); the
+          // scale words sit in the first 16 dP columns, free once the dQ partial was read
+          const uint32_t k4 = smem_u32(smem + L::kK4), q4 = smem_u32(smem + L::kQ4) + st * L::kScoreBytes;
 #pragma unroll
-        for (int s = 0; s < D / 32; ++s)
-          mma_f8(tbase + kS, smem_desc(sk + 32 * s, 16, kAtom, kLayout), smem_desc(qa + 32 * s, 16, kAtom, kLayout),
-                 idesc_f8(128, 128, 0, 0), s > 0);
+          for (int s = 0; s < 2; ++s)
+            mma_nvf4(tbase + kS, smem_desc(k4 + 32 * s, 16, 8 * 64, kSwizzle64B),
+                     smem_desc(q4 + 32 * s, 16, 8 * 64, kSwizzle64B), idesc_nvf4(128, 128), tbase + kP + 4 * s,
+                     tbase + kP + 8 + 4 * s, s > 0);
+        } else {
+          const uint32_t qa = sq + st * L::kTileBytes;
+#pragma unroll
+          for (int s = 0; s < D / 32; ++s)
+            mma_f8(tbase + kS, smem_desc(sk + 32 * s, 16, kAtom, kLayout), smem_desc(qa + 32 * s, 16, kAtom, kLayout),
+                   idesc_f8(128, 128, 0, 0), s > 0);
+        }
       };
       auto issue_dp = [&](int st) {
         const uint32_t da = sdo + st * L::kTileBytes;
@@ -210,6 +234,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
                  idesc_f8(128, 128, 0, 0), s > 0);
       };
       bool ok = mbar_wait(kv_full, 0, status) && mbar_wait(&qd_full[0], 0, status);
+      if (ok && MIXED) ok = mbar_wait(sf_ready, 0, status);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -251,11 +276,12 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         if (k + 1 < nsteps) {
           const int st1 = (k + 1) % kQStages;
           ok = mbar_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
+          if (ok && MIXED) ok = mbar_wait(dq_empty, k & 1, status);   // score scale words of step k + 1 written
           if (!ok) break;
           tc_fence_after();
           issue_s(st1);
           mma_commit(s_full);
-          if (!STRICT) {      // the dQ partial occupies the dP columns until it has been read
+          if (!STRICT && !MIXED) {      // the dQ partial occupies the dP columns until it has been read
             ok = mbar_wait(dq_empty, k & 1, status);
             if (!ok) break;
             tc_fence_after();
@@ -327,6 +353,36 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     uint8_t* sDS = smem + L::kDS;
     uint8_t* sb = smem + L::kStage + wg * L::kStageBytes;
     bool ok = true;
+    // mixed route: scale words of the score MMA, written by warpgroup 0 into the first
+    // 16 dP columns before every score MMA, replicated over the four lane quarters
+    // (lane 32q + l, column c holds row 32c + l): K~ rows (A, fixed) and the Q~ rows of
+    // the step's query tile (B); per row and instruction one word of four E4M3 scales
+    uint2 k4w[4] = {}, q4w[4] = {};
+    auto load_sf_rows = [&](const uint8_t* base, int64_t tok0, int H, int hh_, uint2 (&w4)[4]) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t tok = tok0 + 32 * c + lane;
+        w4[c] = tok < p.T ? *reinterpret_cast<const uint2*>(base + (tok * H + hh_) * (D / 16)) : make_uint2(0u, 0u);
+      }
+    };
+    auto step_qsf = [&](int kk) {
+      load_sf_rows(p.q4_scales, (int64_t)doc_start + (u + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles, q4w);
+    };
+    auto store_score_sf = [&]() {
+      tmem_st4(lane_base + kP + 0, k4w[0].x, k4w[1].x, k4w[2].x, k4w[3].x);
+      tmem_st4(lane_base + kP + 4, k4w[0].y, k4w[1].y, k4w[2].y, k4w[3].y);
+      tmem_st4(lane_base + kP + 8, q4w[0].x, q4w[1].x, q4w[2].x, q4w[3].x);
+      tmem_st4(lane_base + kP + 12, q4w[0].y, q4w[1].y, q4w[2].y, q4w[3].y);
+    };
+    if (MIXED && wg == 0) {
+      load_sf_rows(p.k4_scales, (int64_t)doc_start + u * kTile, p.hkv, hk, k4w);
+      step_qsf(0);
+      store_score_sf();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(sf_ready);
+      if (nsteps > 1) step_qsf(1);
+    }
     for (int k = 0; k < nsteps; ++k) {
       const int hh = k / qtiles, t = u + k % qtiles;
       const int h = hk * g + hh;
@@ -346,7 +402,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         uint32_t vs[32];
         tmem_ld32(lane_base + kS + 32 * c, vs);
         tmem_ld_wait();
-        const float fS = p.scale_log2 * sk_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[c]));
+        const float fS = MIXED ? p.scale_log2 : p.scale_log2 * sk_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[c]));
         const float2 fS2 = make_float2(fS, fS), b2 = make_float2(256.f, 256.f);
         const float4* nl4 = reinterpret_cast<const float4*>(rb + 32 * c);   // -LSE * log2(e)
         const float4* sq4 = reinterpret_cast<const float4*>(rb + 260 + 32 * c);   // strict: s_Q per query
@@ -528,8 +584,13 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         uint32_t v[32];
         tmem_ld32(lane_base + kP + wg * kCols, v);
         tmem_ld_wait();
+        if (MIXED && wg == 0 && k + 1 < nsteps) {
+          store_score_sf();                   // q4w holds the rows of step k + 1
+          tmem_st_wait();
+        }
         tc_fence_before();
         mbar_arrive(dq_empty);
+        if (MIXED && wg == 0 && k + 2 < nsteps) step_qsf(k + 2);
         const float2 cb2 = make_float2(cb, cb);
         constexpr int kRowBytes = kCols * 2;                // 64: one staged row of fp16
         constexpr int kChunks = kRowBytes / 16;             // 16-byte chunks per staged row
@@ -1059,18 +1120,26 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int D, bool STRICT>
+template <int D, bool STRICT, bool MIXED>
 cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                          const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                          const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
-                         void* const* ev) {
-  CUtensorMap tq, tk, tv, tdo;
+                         void* const* ev, const void* q4c, const void* q4s, const void* k4c, const void* k4s) {
+  CUtensorMap tq, tk, tv, tdo, tq4, tk4;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
       !make_tmap_u8_3d(&tv, vc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
       !make_tmap_u8_3d(&tdo, doc_codes, D, hq, T, D, (uint64_t)hq * D, D, kTile))
     return cudaErrorInvalidValue;
+  if (MIXED) {
+    if (!make_tmap_u8_3d(&tq4, q4c, D / 2, hq, T, D / 2, (uint64_t)hq * D / 2, D / 2, kTile) ||
+        !make_tmap_u8_3d(&tk4, k4c, D / 2, hkv, T, D / 2, (uint64_t)hkv * D / 2, D / 2, kTile))
+      return cudaErrorInvalidValue;
+  } else {
+    tq4 = tq;
+    tk4 = tk;
+  }
   BwdParams p;
   p.q_scales = static_cast<const uint8_t*>(qs);
   p.k_scales = static_cast<const uint8_t*>(ks);
@@ -1087,18 +1156,21 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   p.hkv = hkv;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
+  p.q4_scales = static_cast<const uint8_t*>(q4s);
+  p.k4_scales = static_cast<const uint8_t*>(k4s);
   p.dq_acc = static_cast<__half*>(dq_acc);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   const int64_t max_items = (int64_t)T / kTile + N + 1;
   const int64_t grid = max_items * hkv;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  constexpr int smem = BwdSmem<D>::kAlloc;
+  constexpr int smem = BwdSmem<D, MIXED>::kAlloc;
   cudaError_t e =
-      cudaFuncSetAttribute(attn_bwd_kernel<D, STRICT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(attn_bwd_kernel<D, STRICT, MIXED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
-  attn_bwd_kernel<D, STRICT><<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_kernel<D, STRICT, MIXED>
+      <<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
   e = cudaGetLastError();
   if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
@@ -1161,13 +1233,17 @@ cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, co
                        const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
-                       void* const* ev, bool strict) {
+                       void* const* ev, bool strict, const void* q4c, const void* q4s, const void* k4c,
+                       const void* k4s) {
 #define FLAMIA_BWD_ARGS qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan, \
-                        dq_acc, dq, dk, dv, stream, ev
-  if (D == 128 && strict) return launch_bwd_d<128, true>(FLAMIA_BWD_ARGS);
-  if (D == 128) return launch_bwd_d<128, false>(FLAMIA_BWD_ARGS);
-  if (D == 64 && strict) return launch_bwd_d<64, true>(FLAMIA_BWD_ARGS);
-  if (D == 64) return launch_bwd_d<64, false>(FLAMIA_BWD_ARGS);
+                        dq_acc, dq, dk, dv, stream, ev, q4c, q4s, k4c, k4s
+  const bool mixed = q4c != nullptr;
+  if (D == 128 && mixed) return launch_bwd_d<128, false, true>(FLAMIA_BWD_ARGS);
+  if (mixed) return cudaErrorInvalidValue;
+  if (D == 128 && strict) return launch_bwd_d<128, true, false>(FLAMIA_BWD_ARGS);
+  if (D == 128) return launch_bwd_d<128, false, false>(FLAMIA_BWD_ARGS);
+  if (D == 64 && strict) return launch_bwd_d<64, true, false>(FLAMIA_BWD_ARGS);
+  if (D == 64) return launch_bwd_d<64, false, false>(FLAMIA_BWD_ARGS);
 #undef FLAMIA_BWD_ARGS
   return cudaErrorInvalidValue;
 }
