@@ -34,7 +34,10 @@ import flamia_workloads as W  # noqa: E402
 
 METRIC = "causal packed MXFP8 attn fwd+bwd TFLOPS and % of GB300 dense FP8 peak"
 DEFAULT_WORKLOAD = "packed_16k_h16_d128"
-LAUNCHES_PER_STEP = 10   # plan, 3 quantize, fwd, fwd tail, dO prep, boost, bwd, dQ finalise
+# kernels launched per step: plan, 3 quantize, fwd, fwd tail, dO prep, dQ boost, bwd, dQ finalise;
+# strict: the ordered dQ kernel and the zeroing of rows outside every document replace the
+# finalise; mixed: 3 more quantize launches (NVFP4 Q and K, per-token V)
+LAUNCHES_PER_STEP = {"default": 10, "strict": 11, "mixed": 13}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -45,6 +48,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--mode", default="default", choices=["default", "strict", "mixed"],
+                    help="strict options or the mixed NVFP4/FP8 route (head_dim 128)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -120,7 +125,12 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle sample
 
-def oracle_sample(w, budget_s, max_tokens=None):
+def oracle_opts(mode):
+    import oracle as O
+    return O.Options(strict=mode == "strict", mixed=mode == "mixed")
+
+
+def oracle_sample(w, budget_s, max_tokens=None, mode="default"):
     """Time the oracle (as it stands) on a bounded sample of the workload: the
     first S tokens of the longest document for G kv-head groups, S doubled from
     256 (up to the document length), then G doubled (up to hkv), until about
@@ -135,7 +145,7 @@ def oracle_sample(w, budget_s, max_tokens=None):
         S = min(S, L)
         sub = {n: v[:S, :(G * g if n in ("q", "do") else G)] for n, v in vals.items()}
         t0 = time.perf_counter()
-        O.run_training_call(sub["q"], sub["k"], sub["v"], sub["do"], [0, S], G * g, G)
+        O.run_training_call(sub["q"], sub["k"], sub["v"], sub["do"], [0, S], G * g, G, opts=oracle_opts(mode))
         dt = time.perf_counter() - t0
         spent += dt
         flops = 14.0 * w.d * G * g * S * (S + 1) / 2
@@ -171,13 +181,14 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = W.WORKLOADS[args.workload]
-    probe = oracle_sample(w, budget_s=6.0)
+    probe = oracle_sample(w, budget_s=6.0, mode=args.mode)
     S, Hs = probe["tokens"], probe["heads"]
     import oracle as O
     g = w.hq // w.hkv
     inp = W.make_inputs(W.custom([S], Hs, Hs // g, w.d, dist=w.dist, seed=w.seed))
     vals = {n: W.bf16_bits_to_f32(b).astype(np.float64) for n, b in inp.items()}
-    step = lambda: O.run_training_call(vals["q"], vals["k"], vals["v"], vals["do"], [0, S], Hs, Hs // g)
+    step = lambda: O.run_training_call(vals["q"], vals["k"], vals["v"], vals["do"], [0, S], Hs, Hs // g,
+                                       opts=oracle_opts(args.mode))
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -191,7 +202,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample_tokens": S, "sample_heads": Hs, "head_dim": w.d},
+        "config": {"workload": w.name, "mode": args.mode, "sample_tokens": S, "sample_heads": Hs, "head_dim": w.d},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -235,7 +246,8 @@ def run_ours(args, rank, world, local_rank):
     x = {n: t.to(dev) for n, t in host.items()}
     cu_host = torch.tensor(w.cu_seqlens, dtype=torch.int32).pin_memory()
     cu = cu_host.to(dev)
-    att = F.FlamiaAttention(T, N, hq, hkv, d, device=dev)
+    att = F.FlamiaAttention(T, N, hq, hkv, d, device=dev, strict=args.mode == "strict",
+                            mixed=args.mode == "mixed")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -246,11 +258,13 @@ def run_ours(args, rank, world, local_rank):
         for e in evs:
             e.record(stream)          # creates the underlying cudaEvent_t
         arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
-        o = F.default_options()
+        o = F.Options()
+        ctypes.pointer(o)[0] = att.opts          # the mode's flags and operands
         o.timing_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
         return evs, arr, o
 
-    o_plain = F.default_options()
+    o_plain = F.Options()
+    ctypes.pointer(o_plain)[0] = att.opts
 
     def step(o_fwd=None, o_bwd=None):
         att.plan_build(cu)
@@ -299,6 +313,7 @@ def run_ours(args, rank, world, local_rank):
     kf = [f[0][0].elapsed_time(f[0][1]) for f, _ in per_step]
     kb = [b[0][4].elapsed_time(b[0][5]) for _, b in per_step]
     kbp = [b[0][0].elapsed_time(b[0][1]) for _, b in per_step]
+    kfin = [b[0][6].elapsed_time(b[0][7]) for _, b in per_step]
     total_ms = float(sum(ms))
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -352,22 +367,23 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": w.name, "total_tokens": T, "num_docs": N, "hq": hq, "hkv": hkv, "head_dim": d,
+        "config": {"workload": w.name, "mode": args.mode, "total_tokens": T, "num_docs": N, "hq": hq, "hkv": hkv, "head_dim": d,
                    "visible_pairs": pairs, "flops_per_step": flops_step,
                    "l2": "flushed between timed steps (256 MiB write); step inputs 256 MiB > L2",
                    "frac_of_fp8_peak": value / world / fp8_peak,
                    "fp8_peak_tflops": fp8_peak, "peak_source": pk["src"] + " (2 x bf16 burst)"},
-        "phases_ms": {"fwd_kernel": kf_ms, "bwd_kernel": kb_ms, "bwd_prep": float(np.mean(kbp))},
+        "phases_ms": {"fwd_kernel": kf_ms, "bwd_kernel": kb_ms, "bwd_prep": float(np.mean(kbp)),
+                      "bwd_finalise": float(np.mean(kfin))},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp8_peak, "traffic": traffic,
                      "per_unit": "FLOPs per launch = %s * head_dim * hq * visible pairs" % ("10" if "bwd" in dom else "4")},
         "e2e": {"value": world * flops_step / (e2e_mean * 1e-3) / 1e12, "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP[args.mode] * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
-        s = oracle_sample(w, args.cpu_seconds)
+        s = oracle_sample(w, args.cpu_seconds, mode=args.mode)
         res["cpu_baseline"] = {
             "value": s["tflops"], "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle",
             "sample": (f"oracle fwd+bwd (fp64 numpy) on the first {s['tokens']} tokens of the longest document, "

@@ -107,7 +107,7 @@ BwdWorkspace bwd_layout(int64_t T, int N, int hq, int d) {
   w.do_stats = off; off = round256(off + (size_t)T * hq * 8);
   w.dvec = off; off = round256(off + (size_t)T * hq * 4);
   w.boost = off; off = round256(off + ((size_t)(N > 0 ? N : 1) + (size_t)T) * hq * 4);   // per doc, or per row (strict)
-  w.dq_acc = off; off = round256(off + (size_t)T * hq * d * 2);
+  w.dq_acc = off; off = round256(off + dq_acc_bytes(T, N, hq, d));   // fp16 chunks per (document tile, head, slice)
   w.total = off;
   return w;
 }
@@ -237,7 +237,7 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   record(ev, 0, s);
   const bool strict = is_strict(opt);
   cudaError_t e = launch_quantize(dout_bf16, T, hq, head_dim, cu_seqlens, num_seqs, plan, strict ? 1 : 0, do_codes,
-                                  do_scales, do_stats, out_bf16, dvec, dq_acc, s);
+                                  do_scales, do_stats, out_bf16, dvec, strict ? nullptr : dq_acc, s);
   record(ev, 1, s);
   record(ev, 2, s);
   if (e == cudaSuccess)

@@ -68,7 +68,7 @@ struct BwdParams {
   float scale;
   const uint8_t* q4_scales;   // mixed route: E4M3 scale codes [T, hq, D/16] of the NVFP4 score operands
   const uint8_t* k4_scales;   // [T, hkv, D/16]
-  __half* dq_acc;          // [T, hq, D]
+  __half* dq_acc;          // fp16 accumulator chunks (dq_chunk_elems layout)
   __nv_bfloat16* dk;       // [T, hkv, D]
   __nv_bfloat16* dv;
 };
@@ -88,9 +88,9 @@ struct BwdSmem {
   static constexpr int kRowBuf = (128 * 2 + 4 + 128 * 2) * 4;
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents (+ strict per-row exponents)
   static constexpr int kStageBytes = kTile * BwdShape<D>::kCols * 2;   // one warpgroup's fp16 slice of the dQ tile
-  static constexpr int kStage = (kE + 64 + 1024 + 1023) & ~1023;   // [warpgroup]
+  static constexpr int kStage = (kE + 64 + 1024 + 1023) & ~1023;   // [warpgroup][2 buffers]
   static constexpr int kScoreBytes = kTile * D / 2;           // mixed route: one E2M1 score-operand tile
-  static constexpr int kK4 = kStage + BwdShape<D>::kWG * kStageBytes;
+  static constexpr int kK4 = kStage + 2 * BwdShape<D>::kWG * kStageBytes;
   static constexpr int kQ4 = kK4 + (MIXED ? kScoreBytes : 0);          // [kQStages]
   static constexpr int kBar = kQ4 + (MIXED ? kQStages * kScoreBytes : 0);
   static constexpr int kBytes = kBar + 256;
@@ -99,11 +99,6 @@ struct BwdSmem {
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ void red_add_f16x8(__half* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("red.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
 }
 
 template <int D, bool STRICT, bool MIXED>
@@ -248,6 +243,17 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t qa = sq + st * L::kTileBytes, da = sdo + st * L::kTileBytes;
+        if (!STRICT) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major);
+            // first, so that its readout overlaps the dV and dK products
+            mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
+                     smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
+                     tbase + kSF + 16, tbase + kSF + 20, s > 0);
+          }
+          mma_commit(dq_full);
+        }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
@@ -261,16 +267,6 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
           mma_mxf8(tbase + kDK, smem_desc(sds + 32 * s, 16, 1024, kSwizzle128B),
                    smem_desc(qa + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
                    tbase + kSF + 8, tbase + kSF + 12, (k > 0 || s > 0));
-        }
-        if (!STRICT) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major)
-            mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
-                     smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
-                     tbase + kSF + 16, tbase + kSF + 20, s > 0);
-          }
-          mma_commit(dq_full);
         }
         mma_commit(&qd_empty[st]);
         if (k + 1 < nsteps) {
@@ -351,7 +347,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     uint8_t* Esm = smem + L::kE;
     uint8_t* sPt = smem + L::kPt;
     uint8_t* sDS = smem + L::kDS;
-    uint8_t* sb = smem + L::kStage + wg * L::kStageBytes;
+    uint8_t* sb = smem + L::kStage + wg * 2 * L::kStageBytes;   // this warpgroup's two staging buffers
     bool ok = true;
     // mixed route: scale words of the score MMA, written by warpgroup 0 into the first
     // 16 dP columns before every score MMA, replicated over the four lane quarters
@@ -593,7 +589,8 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         if (MIXED && wg == 0 && k + 2 < nsteps) step_qsf(k + 2);
         const float2 cb2 = make_float2(cb, cb);
         constexpr int kRowBytes = kCols * 2;                // 64: one staged row of fp16
-        constexpr int kChunks = kRowBytes / 16;             // 16-byte chunks per staged row
+        constexpr int kChunks = kRowBytes / 16;             // 16-byte units per staged row
+        uint8_t* sbk = sb + (k & 1) * L::kStageBytes;       // double-buffered staging
 #pragma unroll
         for (int c16 = 0; c16 < kChunks; ++c16) {
           uint32_t hw[4];
@@ -603,25 +600,22 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
             __half2 h2 = __floats2half2_rn(f.x, f.y);
             hw[q] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(sb + swz_offset(j, 16 * c16, kRowBytes)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(sbk + dq_chunk_byte(j, 16 * c16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         }
+        fence_proxy_async_smem();
         named_bar_sync(2 + wg, 128);
-        // coalesced reduce-add: consecutive lanes cover consecutive 16-byte chunks of
-        // consecutive staged rows
-        const int tw = threadIdx.x & 127;
-#pragma unroll
-        for (int it = 0; it < kChunks; ++it) {
-          const int qc = it * 128 + tw;
-          const int row = qc / kChunks, ch = qc % kChunks;
-          const int qrl = t * kTile + row;
-          if (qrl < doc_len) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(sb + swz_offset(row, 16 * ch, kRowBytes));
-            __half* dst = p.dq_acc + (((int64_t)doc_start + qrl) * p.hq + h) * D + wg * kCols + 8 * ch;
-            red_add_f16x8(dst, w4.x, w4.y, w4.z, w4.w);
-          }
+        if ((threadIdx.x & 127) == 0) {
+          // one bulk fp16 reduce-add of the whole staged slice into the tile's accumulator
+          // chunk (rows past the document end were staged as zeros); the wait leaves at
+          // most this copy reading shared memory, so the other buffer is free next step
+          __half* dst = p.dq_acc + dq_chunk_elems(pv.tile_prefix[doc] + t, h, wg, p.hq, D);
+          bulk_reduce_add_f16(dst, smem_u32(sbk), L::kStageBytes);
+          bulk_commit();
+          bulk_wait_read<1>();
         }
       }
     }
+    if ((threadIdx.x & 127) == 0) bulk_wait_all();
     if (ok) ok = named_bar_and(1, kCompute, mbar_wait(acc_full, 0, status));
     if (ok) {
       tc_fence_after();
@@ -712,6 +706,7 @@ __global__ void dq_finalize_kernel(const __half* acc, const int32_t* cu, const i
                                    __nv_bfloat16* dv) {
   const int valid = plan[kPlanValid];
   const bool bad = plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS;
+  const int* tile_prefix = plan_view(plan, T, N).tile_prefix;
   constexpr int kVec = 8;
   const int64_t nvec = (int64_t)T * hq * (D / kVec);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
@@ -726,7 +721,11 @@ __global__ void dq_finalize_kernel(const __half* acc, const int32_t* cu, const i
         if (cu[mid] <= row) lo = mid; else hi = mid;
       }
       const float mul = scale / boost[(int64_t)lo * hq + h];
-      const uint4 in = reinterpret_cast<const uint4*>(acc)[i];
+      const int rl = (int)(row - cu[lo]);                         // document-local row
+      const int col = (int)(i % (D / kVec)) * kVec;
+      const __half* chunk = acc + dq_chunk_elems(tile_prefix[lo] + rl / kTile, h, col / 32, hq, D);
+      const uint4 in = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(chunk) +
+                                                       dq_chunk_byte(rl % kTile, (col % 32) * 2));
       const __half2* hv = reinterpret_cast<const __half2*>(&in);
       uint32_t* ov = reinterpret_cast<uint32_t*>(&out);
 #pragma unroll

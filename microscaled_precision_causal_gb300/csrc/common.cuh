@@ -40,6 +40,23 @@ struct PlanView {
 };
 
 __host__ __device__ inline int64_t plan_capacity(int64_t T, int N) { return T / kTile + N + 1; }
+// fp16 dQ accumulator of the default backward (workspace-internal layout): one
+// contiguous 8 KB chunk per (document tile, query head, 32-column slice of the
+// head dim), tile = tile_prefix[doc] + document-local tile index.  A chunk holds
+// the tile's 128 rows of 32 fp16 (64 bytes each) with the 16-byte units of every
+// row permuted by the 64-byte TMA/UMMA swizzle, the layout in which the backward
+// stages a slice in shared memory and reduces it with one bulk copy.
+__host__ __device__ inline size_t dq_chunk_elems(int64_t tile, int h, int slice, int hq, int D) {
+  return (((size_t)tile * hq + h) * (size_t)(D / 32) + slice) * (size_t)(kTile * 32);
+}
+// Byte offset of byte `col_byte` (0..63) of row `r` inside a chunk.
+__host__ __device__ inline uint32_t dq_chunk_byte(int r, int col_byte) {
+  const uint32_t lin = (uint32_t)r * 64u + (uint32_t)col_byte;
+  return lin ^ (((lin >> 7) & 3u) << 4);
+}
+__host__ __device__ inline size_t dq_acc_bytes(int64_t T, int N, int hq, int D) {
+  return (size_t)plan_capacity(T, N) * hq * D * kTile * 2;
+}
 __host__ __device__ inline int64_t pow2_ceil(int64_t x) {
   int64_t p = 1;
   while (p < x) p <<= 1;

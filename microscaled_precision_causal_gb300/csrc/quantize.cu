@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   // rows [r0, r0 + nrows) of this warp; tail rows (no document) get zeros
   int r0, nrows;
   bool tail = false;
+  int64_t dq_tile0 = 0;   // backward prep: accumulator tile of the block's document tile
+  int dq_row0 = 0;
   if (PER_TOKEN) {
     r0 = (int)(unit * 32);
     if (r0 >= T) return;
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     const int s0 = cu[doc], s1 = cu[doc + 1];
     r0 = s0 + ((int)unit - pv.blk_prefix[doc]) * kBlock;
     nrows = min(kBlock, s1 - r0);
+    dq_tile0 = pv.tile_prefix[doc] + (r0 - s0) / kTile;
+    dq_row0 = (r0 - s0) % kTile;
   } else {
     r0 = valid + (int)(unit - nblk) * 32;
     if (r0 >= T) return;
@@ -132,7 +136,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     if (inrange) {
       const int64_t row = r0 + r;
       *reinterpret_cast<uint2*>(codes + (row * H + h) * D + cb) = make_uint2(packed[0], packed[1]);
-      if (WITH_D) *reinterpret_cast<uint4*>(dq_acc + (row * H + h) * D + cb) = make_uint4(0, 0, 0, 0);
+      if (WITH_D && !PER_TOKEN && !tail && dq_acc)      // zero the row's slice of its accumulator chunk
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(dq_acc + dq_chunk_elems(dq_tile0, h, cb / 32, H, D)) +
+                                  dq_chunk_byte(dq_row0 + r, (cb % 32) * 2)) = make_uint4(0, 0, 0, 0);
     }
     if (STATS || WITH_D) {
 #pragma unroll
