@@ -11,7 +11,8 @@ namespace flamia {
 cudaError_t launch_plan(const int32_t* cu, int N, int T, void* plan, cudaStream_t s);
 cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
                             int per_token, void* codes, void* scales, float* stats, const void* o, float* dvec,
-                            void* dq_acc, cudaStream_t s);
+                            void* dq_acc, cudaStream_t s, const float* k_stats = nullptr,
+                            const float* v_stats = nullptr, int hkv = 1, float* maxima = nullptr);
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict);
@@ -23,7 +24,7 @@ cudaError_t launch_fwd_coop(int D, int mixed, const void* qc, const void* qs, co
 cudaError_t launch_fwd_tail(int D, const void* plan, int T, int hq, void* out, float* lse, cudaStream_t stream);
 cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float* st_do, const float* st_k,
                          const float* st_v, int T, int hq, int hkv, int headroom, float* boost, bool causal,
-                         cudaStream_t s);
+                         const float* maxima, cudaStream_t s);
 cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
@@ -97,7 +98,7 @@ inline void record(void* const* ev, int i, cudaStream_t s) {
 float resolve_scale(float s, int d) { return s > 0.f ? s : 1.0f / std::sqrt((float)d); }
 
 struct BwdWorkspace {
-  size_t do_codes, do_scales, do_stats, dvec, boost, dq_acc, total;
+  size_t do_codes, do_scales, do_stats, dvec, boost, maxima, dq_acc, total;
 };
 BwdWorkspace bwd_layout(int64_t T, int N, int hq, int d) {
   BwdWorkspace w;
@@ -107,6 +108,7 @@ BwdWorkspace bwd_layout(int64_t T, int N, int hq, int d) {
   w.do_stats = off; off = round256(off + (size_t)T * hq * 8);
   w.dvec = off; off = round256(off + (size_t)T * hq * 4);
   w.boost = off; off = round256(off + ((size_t)(N > 0 ? N : 1) + (size_t)T) * hq * 4);   // per doc, or per row (strict)
+  w.maxima = off; off = round256(off + (size_t)(N > 0 ? N : 1) * hq * 3 * 4);   // dQ boost inputs per (doc, head)
   w.dq_acc = off; off = round256(off + dq_acc_bytes(T, N, hq, d));   // fp16 chunks per (document tile, head, slice)
   w.total = off;
   return w;
@@ -232,16 +234,22 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   float* do_stats = reinterpret_cast<float*>(ws + w.do_stats);
   float* dvec = reinterpret_cast<float*>(ws + w.dvec);
   float* boost = reinterpret_cast<float*>(ws + w.boost);
+  float* maxima = reinterpret_cast<float*>(ws + w.maxima);
   void* dq_acc = ws + w.dq_acc;
   void* const* ev = opt ? opt->timing_events : nullptr;
   record(ev, 0, s);
   const bool strict = is_strict(opt);
-  cudaError_t e = launch_quantize(dout_bf16, T, hq, head_dim, cu_seqlens, num_seqs, plan, strict ? 1 : 0, do_codes,
-                                  do_scales, do_stats, out_bf16, dvec, strict ? nullptr : dq_acc, s);
+  cudaError_t e = cudaSuccess;
+  if (!strict) e = cudaMemsetAsync(maxima, 0, (size_t)num_seqs * hq * 3 * 4, s);
+  if (e == cudaSuccess)
+    e = launch_quantize(dout_bf16, T, hq, head_dim, cu_seqlens, num_seqs, plan, strict ? 1 : 0, do_codes, do_scales,
+                        do_stats, out_bf16, dvec, strict ? nullptr : dq_acc, s, k->stats, v->stats, hkv,
+                        strict ? nullptr : maxima);
   record(ev, 1, s);
   record(ev, 2, s);
   if (e == cudaSuccess)
-    e = launch_boost(cu_seqlens, num_seqs, plan, do_stats, k->stats, v->stats, T, hq, hkv, headroom, boost, strict, s);
+    e = launch_boost(cu_seqlens, num_seqs, plan, do_stats, k->stats, v->stats, T, hq, hkv, headroom, boost, strict,
+                     maxima, s);
   record(ev, 3, s);
   if (e == cudaSuccess)
     e = launch_bwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, do_codes, do_scales, lse,

@@ -649,84 +649,54 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   }
 }
 
-// dQ boost per (document, query head): c = 2^floor(log2(2^headroom / M)),
-// M = 2 max_i ||dO^_i|| max_j ||V^_j|| max_jd |K^_jd| over the document
-// (FLAMIA review section 4, "Forward locality and backward locality differ").
-__global__ void boost_kernel(const int32_t* cu, const int* plan, const float2* st_do, const float2* st_k,
-                             const float2* st_v, int hq, int hkv, int headroom, float* boost) {
-  const int doc = blockIdx.x, h = blockIdx.y;
-  const int hk = h / (hq / hkv);
-  if (plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS) return;
-  const int s0 = cu[doc], s1 = cu[doc + 1];
-  float a = 0.f, b = 0.f, c = 0.f;
-  for (int t = s0 + threadIdx.x; t < s1; t += blockDim.x) {
-    a = fmaxf(a, st_do[(int64_t)t * hq + h].x);
-    b = fmaxf(b, st_v[(int64_t)t * hkv + hk].x);
-    c = fmaxf(c, st_k[(int64_t)t * hkv + hk].y);
+// dQ boost of (document, query head) from the maxima the backward prep folded in
+// (review section 4, "Forward locality and backward locality differ"; reading
+// C-10): c = 2^floor(log2(2^headroom / M)), M = 2 max ||dO^_i|| max ||V^_j|| max |K^_jd|.
+__global__ void boost_from_max_kernel(const float* maxima, const int* plan, int N, int hq, int headroom,
+                                      float* boost) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N * hq || (plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS)) return;
+  const double M = 2.0 * (double)maxima[3 * i] * (double)maxima[3 * i + 1] * (double)maxima[3 * i + 2];
+  double cb = 1.0;
+  if (M > 0.0 && M < 1e300) {
+    const double target = ldexp(1.0, headroom);
+    int e = (int)floor(log2(target / M));
+    while (ldexp(M, e) > target) --e;
+    while (ldexp(M, e + 1) <= target) ++e;
+    e = e < -100 ? -100 : (e > 100 ? 100 : e);
+    cb = ldexp(1.0, e);
   }
-  __shared__ float red[3][32];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
-    c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
-  }
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) {
-    red[0][w] = a;
-    red[1][w] = b;
-    red[2][w] = c;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) {
-      a = fmaxf(a, red[0][i]);
-      b = fmaxf(b, red[1][i]);
-      c = fmaxf(c, red[2][i]);
-    }
-    const double M = 2.0 * (double)a * (double)b * (double)c;
-    double cb = 1.0;
-    if (M > 0.0 && M < 1e300) {
-      const double target = ldexp(1.0, headroom);
-      int e = (int)floor(log2(target / M));
-      while (ldexp(M, e) > target) --e;
-      while (ldexp(M, e + 1) <= target) ++e;
-      e = e < -100 ? -100 : (e > 100 ? 100 : e);
-      cb = ldexp(1.0, e);
-    }
-    boost[(int64_t)doc * hq + h] = (float)cb;
-  }
+  boost[i] = (float)cb;
 }
 
-// dQ = bf16(scale * acc / c) per row; rows outside every document and the dK /
-// dV rows outside every document are zeroed.
+// dQ = bf16(scale * acc / c), read from the accumulator chunks one (document
+// tile, query head) at a time; then the rows outside every document of dQ, dK
+// and dV are zeroed.
 template <int D>
-__global__ void dq_finalize_kernel(const __half* acc, const int32_t* cu, const int* plan, const float* boost, int N,
-                                   int T, int hq, int hkv, float scale, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                                   __nv_bfloat16* dv) {
-  const int valid = plan[kPlanValid];
+__global__ void __launch_bounds__(256) dq_finalize_kernel(const __half* acc, const int32_t* cu, const int* plan,
+                                                          const float* boost, int N, int T, int hq, int hkv,
+                                                          float scale, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                                                          __nv_bfloat16* dv) {
   const bool bad = plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS;
-  const int* tile_prefix = plan_view(plan, T, N).tile_prefix;
-  constexpr int kVec = 8;
-  const int64_t nvec = (int64_t)T * hq * (D / kVec);
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t rowh = i / (D / kVec);
-    const int64_t row = rowh / hq;
-    const int h = (int)(rowh % hq);
-    uint4 out = make_uint4(0, 0, 0, 0);
-    if (!bad && row < valid) {
-      int lo = 0, hi = N;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cu[mid] <= row) lo = mid; else hi = mid;
-      }
-      const float mul = scale / boost[(int64_t)lo * hq + h];
-      const int rl = (int)(row - cu[lo]);                         // document-local row
-      const int col = (int)(i % (D / kVec)) * kVec;
-      const __half* chunk = acc + dq_chunk_elems(tile_prefix[lo] + rl / kTile, h, col / 32, hq, D);
+  const int valid = bad ? 0 : plan[kPlanValid];
+  const int ntiles = bad ? 0 : plan[kPlanTiles];
+  const PlanView pv = plan_view(plan, T, N);
+  constexpr int kVec = 8, kVpr = D / kVec;             // 16-byte vectors per row
+  const int64_t units = (int64_t)ntiles * hq;
+  for (int64_t un = blockIdx.x; un < units; un += gridDim.x) {
+    const int tile = (int)(un / hq), h = (int)(un % hq);
+    const int doc = upper_doc(pv.tile_prefix, N, tile);
+    const int t = tile - pv.tile_prefix[doc];
+    const int s0 = cu[doc];
+    const int rows = min(kTile, cu[doc + 1] - s0 - t * kTile);
+    const float mul = scale / boost[(int64_t)doc * hq + h];
+    for (int i = threadIdx.x; i < rows * kVpr; i += blockDim.x) {
+      const int r = i / kVpr, col = (i % kVpr) * kVec;
+      const __half* chunk = acc + dq_chunk_elems(tile, h, col / 32, hq, D);
       const uint4 in = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(chunk) +
-                                                       dq_chunk_byte(rl % kTile, (col % 32) * 2));
+                                                       dq_chunk_byte(r, (col % 32) * 2));
       const __half2* hv = reinterpret_cast<const __half2*>(&in);
+      uint4 out;
       uint32_t* ov = reinterpret_cast<uint32_t*>(&out);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -734,15 +704,16 @@ __global__ void dq_finalize_kernel(const __half* acc, const int32_t* cu, const i
         __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * mul, f.y * mul);
         ov[q] = *reinterpret_cast<uint32_t*>(&b2);
       }
+      *reinterpret_cast<uint4*>(dq + (((int64_t)s0 + t * kTile + r) * hq + h) * D + col) = out;
     }
-    reinterpret_cast<uint4*>(dq)[i] = out;
   }
-  // dK / dV rows outside every document
-  const int64_t tail = (int64_t)(T - (bad ? 0 : valid)) * hkv * (D / kVec);
-  const int64_t base = (int64_t)(bad ? 0 : valid) * hkv * (D / kVec);
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < tail; i += (int64_t)gridDim.x * blockDim.x) {
-    reinterpret_cast<uint4*>(dk)[base + i] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(dv)[base + i] = make_uint4(0, 0, 0, 0);
+  // rows outside every document
+  const int64_t tq = (int64_t)(T - valid) * hq * kVpr, tk = (int64_t)(T - valid) * hkv * kVpr;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < tq + 2 * tk;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < tq) reinterpret_cast<uint4*>(dq)[(int64_t)valid * hq * kVpr + i] = make_uint4(0, 0, 0, 0);
+    else if (i < tq + tk) reinterpret_cast<uint4*>(dk)[(int64_t)valid * hkv * kVpr + (i - tq)] = make_uint4(0, 0, 0, 0);
+    else reinterpret_cast<uint4*>(dv)[(int64_t)valid * hkv * kVpr + (i - tq - tk)] = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -1214,7 +1185,7 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
 
 cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float* st_do, const float* st_k,
                          const float* st_v, int T, int hq, int hkv, int headroom, float* boost, bool causal,
-                         cudaStream_t s) {
+                         const float* maxima, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   if (causal)
     causal_boost_kernel<<<dim3(N, hq), 256, 0, s>>>(cu, static_cast<const int*>(plan),
@@ -1222,9 +1193,8 @@ cudaError_t launch_boost(const int32_t* cu, int N, const void* plan, const float
                                                     reinterpret_cast<const float2*>(st_k),
                                                     reinterpret_cast<const float2*>(st_v), T, hq, hkv, headroom, boost);
   else
-    boost_kernel<<<dim3(N, hq), 256, 0, s>>>(cu, static_cast<const int*>(plan), reinterpret_cast<const float2*>(st_do),
-                                             reinterpret_cast<const float2*>(st_k),
-                                             reinterpret_cast<const float2*>(st_v), hq, hkv, headroom, boost);
+    boost_from_max_kernel<<<(N * hq + 255) / 256, 256, 0, s>>>(maxima, static_cast<const int*>(plan), N, hq, headroom,
+                                                               boost);
   return cudaGetLastError();
 }
 

@@ -23,18 +23,28 @@ namespace flamia {
 
 namespace {
 
-constexpr int kWarps = 8;
+// Launch shape: the plain quantizer holds its block in registers between the two
+// passes (4 warps, 3 blocks per SM); the backward prep streams dO and O and keeps
+// more warps in flight instead, re-reading the block from L1/L2 in pass 2.
+template <bool WITH_D>
+struct QShape {
+  static constexpr int kWarps = WITH_D ? 8 : 4;
+  static constexpr int kMinBlocks = WITH_D ? 4 : 3;
+};
 
 template <int D, bool PER_TOKEN, bool STATS, bool WITH_D>
-__global__ void __launch_bounds__(kWarps * 32, 4)
+__global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::kMinBlocks)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, const int32_t* __restrict__ cu, int N,
                     const int* __restrict__ plan, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                     float2* __restrict__ stats, const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec,
-                    __half* __restrict__ dq_acc) {
+                    __half* __restrict__ dq_acc, const float2* __restrict__ k_stats,
+                    const float2* __restrict__ v_stats, int hkv, float* __restrict__ maxima) {
   constexpr int kLpr = D / 8;          // lanes per token row (16 bytes each)
   constexpr int kRpi = 32 / kLpr;      // rows per iteration
   constexpr int kIters = 32 / kRpi;    // 32 rows per warp
   const int lane = threadIdx.x & 31;
+  constexpr int kWarps = QShape<WITH_D>::kWarps;
+  constexpr bool kHold = !PER_TOKEN && !WITH_D;   // block held in registers for pass 2
   const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int h = (int)(gw % H);
   const int64_t unit = gw / H;
@@ -47,12 +57,13 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   bool tail = false;
   int64_t dq_tile0 = 0;   // backward prep: accumulator tile of the block's document tile
   int dq_row0 = 0;
+  int doc = -1;
   if (PER_TOKEN) {
     r0 = (int)(unit * 32);
     if (r0 >= T) return;
     nrows = min(32, T - r0);
   } else if (unit < nblk) {
-    const int doc = upper_doc(pv.blk_prefix, N, (int)unit);
+    doc = upper_doc(pv.blk_prefix, N, (int)unit);
     const int s0 = cu[doc], s1 = cu[doc + 1];
     r0 = s0 + ((int)unit - pv.blk_prefix[doc]) * kBlock;
     nrows = min(kBlock, s1 - r0);
@@ -82,25 +93,30 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     return m;
   };
 
-  // pass 1 (token blocks): amax over the whole block; the data are re-read from
-  // L1/L2 in pass 2 instead of being held in registers.
+  float mdo = 0.f;        // backward prep: max ||dO^_i|| over the block's rows
+  // pass 1 (token blocks): amax over the whole block; the block stays in
+  // registers for pass 2 (32 rows x 16 bytes per lane)
   int e_block = 0;
+  uint4 w[kHold ? kIters : 1];
   if (!PER_TOKEN) {
-    uint4 w[kIters];
+    uint4 w1[kHold ? 1 : kIters];
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) w[it] = load8(x, it * kRpi + sub);
+    for (int it = 0; it < kIters; ++it) {
+      if (kHold) w[kHold ? it : 0] = load8(x, it * kRpi + sub);
+      else w1[kHold ? 0 : it] = load8(x, it * kRpi + sub);
+    }
     float a = 0.f;
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) a = fmaxf(a, absmax8(w[it]));
+    for (int it = 0; it < kIters; ++it) a = fmaxf(a, absmax8(kHold ? w[kHold ? it : 0] : w1[kHold ? 0 : it]));
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o2));
     e_block = roundup_exp(a);
   }
-#pragma unroll 2
+#pragma unroll(kHold ? kIters : 2)
   for (int it = 0; it < kIters; ++it) {
     const int r = it * kRpi + sub;
     const bool inrange = r < nrows;
-    const uint4 raw = load8(x, r);
+    const uint4 raw = kHold ? w[kHold ? it : 0] : load8(x, r);
     int e = e_block;
     if (PER_TOKEN) {
       float m = absmax8(raw);
@@ -111,27 +127,35 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     const float s = exp2i(-e);
     const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
     uint32_t packed[2];
-    float ss = 0.f, mx = 0.f, dd = 0.f;
-    const float back = ue8m0_to_f32((uint32_t)(e + 127));
-    const uint4 oraw = WITH_D ? load8(o, r) : make_uint4(0, 0, 0, 0);
-    const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oraw);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = __bfloat1622float2(v[j]);
       const uint16_t c2 = e4m3x2(f.x * s, f.y * s);
       if (j & 1) packed[j >> 1] |= (uint32_t)c2 << 16; else packed[j >> 1] = c2;
-      if (STATS || WITH_D) {
-        const float a = e4m3_to_f32((uint8_t)(c2 & 0xFF)) * back;
-        const float b = e4m3_to_f32((uint8_t)(c2 >> 8)) * back;
-        if (STATS) {
-          ss = fmaf(a, a, fmaf(b, b, ss));
-          mx = fmax3(mx, fabsf(a), fabsf(b));
-        }
-        if (WITH_D) {
-          const float2 of = __bfloat1622float2(ov[j]);
-          dd = fmaf(a, of.x, fmaf(b, of.y, dd));
-        }
+    }
+    // statistics of the reconstructed row x^ = 2^e c and D = dO^ . O, from the codes:
+    // sums over the decoded codes, scaled by 2^e (2^2e) once at the end (exact)
+    const float back = ue8m0_to_f32((uint32_t)(e + 127));
+    float ss = 0.f, mx = 0.f, dd = 0.f;
+    uint32_t cmax = 0;
+    if (STATS || WITH_D) {
+      float2 ss2 = make_float2(0.f, 0.f), dd2 = make_float2(0.f, 0.f);
+      const uint4 oraw = WITH_D ? load8(o, r) : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oraw);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint16_t c2 = (uint16_t)(packed[j >> 1] >> (16 * (j & 1)));
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2, __NV_E4M3);
+        const float2 f = __half22float2(__half2(hr));
+        if (STATS) ss2 = ffma2(f, f, ss2);
+        if (WITH_D) dd2 = ffma2(f, __bfloat1622float2(ov[j]), dd2);
       }
+      if (STATS) {
+        ss = ss2.x + ss2.y;
+        cmax = __vmaxu4(packed[0] & 0x7F7F7F7Fu, packed[1] & 0x7F7F7F7Fu);   // |code| orders like |value|
+        cmax = max(max(cmax & 0xFFu, (cmax >> 8) & 0xFFu), max((cmax >> 16) & 0xFFu, cmax >> 24));
+      }
+      if (WITH_D) dd = dd2.x + dd2.y;
     }
     if (inrange) {
       const int64_t row = r0 + r;
@@ -145,50 +169,86 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
       for (int o2 = kLpr / 2; o2 > 0; o2 >>= 1) {
         if (STATS) {
           ss += __shfl_xor_sync(0xffffffffu, ss, o2);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+          cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o2));
         }
         if (WITH_D) dd += __shfl_xor_sync(0xffffffffu, dd, o2);
       }
+      if (STATS) mx = e4m3_to_f32((uint8_t)cmax) * back;
     }
     if (inrange && (lane % kLpr) == 0) {
       const int64_t row = r0 + r;
-      if (STATS) stats[row * H + h] = make_float2(sqrtf(ss), mx);
-      if (WITH_D) dvec[(int64_t)h * T + row] = dd;
+      if (STATS) stats[row * H + h] = make_float2(sqrtf(ss) * back, mx);
+      if (WITH_D && !tail) mdo = fmaxf(mdo, sqrtf(ss) * back);
+      if (WITH_D) dvec[(int64_t)h * T + row] = dd * back;
       if (PER_TOKEN) scales[row * H + h] = (uint8_t)(e + 127);
     }
   }
   if (!PER_TOKEN && lane < nrows) scales[(int64_t)(r0 + lane) * H + h] = (uint8_t)(tail ? 127 : e_block + 127);
+  if (WITH_D && !PER_TOKEN && maxima && !tail) {
+    // dQ boost inputs of (document, query head): max ||dO^_i||, max ||V^_j||, max |K^_jd|
+    // over the block's rows, folded into the document maxima (non-negative floats
+    // order like their bit patterns)
+    const int hk = h / (H / hkv);
+    float mv = 0.f, mk = 0.f;
+    if (lane < nrows) {
+      const int64_t row = r0 + lane;
+      mv = v_stats[row * hkv + hk].x;
+      mk = k_stats[row * hkv + hk].y;
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      mdo = fmaxf(mdo, __shfl_xor_sync(0xffffffffu, mdo, o2));
+      mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o2));
+      mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o2));
+    }
+    if (lane == 0) {
+      int* mx3 = reinterpret_cast<int*>(maxima) + ((int64_t)doc * H + h) * 3;
+      atomicMax(mx3 + 0, __float_as_int(mdo));
+      atomicMax(mx3 + 1, __float_as_int(mv));
+      atomicMax(mx3 + 2, __float_as_int(mk));
+    }
+  }
 }
+
+struct PrepExtra {          // backward prep only
+  const float* k_stats;
+  const float* v_stats;
+  int hkv;
+  float* maxima;            // [N, H, 3], zeroed by the caller
+};
 
 template <int D, bool PT, bool ST, bool WD>
 cudaError_t launch_q(const void* x, int T, int H, const int32_t* cu, int N, const void* plan, void* codes,
-                     void* scales, float* stats, const void* o, float* dvec, void* dq_acc, cudaStream_t s) {
+                     void* scales, float* stats, const void* o, float* dvec, void* dq_acc, const PrepExtra& px,
+                     cudaStream_t s) {
   const int64_t units = PT ? (T + 31) / 32 : (int64_t)T / 32 + N + 1;
   const int64_t warps = units * H;
+  constexpr int kWarps = QShape<WD>::kWarps;
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   quantize_kernel<D, PT, ST, WD><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), T, H, cu, N, static_cast<const int*>(plan),
       static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), reinterpret_cast<float2*>(stats),
-      static_cast<const __nv_bfloat16*>(o), dvec, static_cast<__half*>(dq_acc));
+      static_cast<const __nv_bfloat16*>(o), dvec, static_cast<__half*>(dq_acc),
+      reinterpret_cast<const float2*>(px.k_stats), reinterpret_cast<const float2*>(px.v_stats), px.hkv, px.maxima);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t dispatch(const void* x, int T, int H, const int32_t* cu, int N, const void* plan, int per_token,
                      void* codes, void* scales, float* stats, const void* o, float* dvec, void* dq_acc,
-                     cudaStream_t s) {
+                     const PrepExtra& px, cudaStream_t s) {
   const bool st = stats != nullptr, wd = o != nullptr;
   if (wd) {
-    if (per_token) return launch_q<D, true, true, true>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
-    return launch_q<D, false, true, true>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+    if (per_token) return launch_q<D, true, true, true>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, px, s);
+    return launch_q<D, false, true, true>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, px, s);
   }
   if (per_token) {
-    if (st) return launch_q<D, true, true, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
-    return launch_q<D, true, false, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+    if (st) return launch_q<D, true, true, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, px, s);
+    return launch_q<D, true, false, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, px, s);
   }
-  if (st) return launch_q<D, false, true, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
-  return launch_q<D, false, false, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, s);
+  if (st) return launch_q<D, false, true, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, px, s);
+  return launch_q<D, false, false, false>(x, T, H, cu, N, plan, codes, scales, stats, o, dvec, dq_acc, px, s);
 }
 
 // NVFP4 score operand (step a2, the mixed route; FLAMIA technical review section
@@ -247,12 +307,16 @@ cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, voi
   return cudaGetLastError();
 }
 
-// o / dvec / dq_acc non-null selects the backward-prep variant (stats required).
+// o / dvec non-null selects the backward-prep variant (stats required); with the
+// token-block rule it also zeroes dq_acc (if non-null) and folds the dQ boost
+// inputs into maxima (if non-null; k_stats / v_stats of the hkv K/V heads).
 cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
                             int per_token, void* codes, void* scales, float* stats, const void* o, float* dvec,
-                            void* dq_acc, cudaStream_t s) {
-  if (D == 128) return dispatch<128>(x, T, H, cu, N, plan, per_token, codes, scales, stats, o, dvec, dq_acc, s);
-  if (D == 64) return dispatch<64>(x, T, H, cu, N, plan, per_token, codes, scales, stats, o, dvec, dq_acc, s);
+                            void* dq_acc, cudaStream_t s, const float* k_stats, const float* v_stats, int hkv,
+                            float* maxima) {
+  const PrepExtra px{k_stats, v_stats, hkv, maxima};
+  if (D == 128) return dispatch<128>(x, T, H, cu, N, plan, per_token, codes, scales, stats, o, dvec, dq_acc, px, s);
+  if (D == 64) return dispatch<64>(x, T, H, cu, N, plan, per_token, codes, scales, stats, o, dvec, dq_acc, px, s);
   return cudaErrorInvalidValue;
 }
 
