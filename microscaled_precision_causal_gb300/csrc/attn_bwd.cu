@@ -44,13 +44,21 @@ namespace {
 constexpr int kQStages = 2;
 // Compute warpgroups: each owns 32 of the 128 query columns of a step (as 4 / kWG
 // chunks of 32) and 32 of the head-dim columns of dQ / dK / dV.
+// Warpgroups: 0 = control (TMA producer, MMA issuer, TMEM allocator, row data),
+// 1 .. kWG = compute (P^ and dS^), kWG + 1 = dQ readout.  The control and readout
+// warpgroups hand registers to the compute warpgroups (setmaxnreg):
+// kRegLow x 256 + kRegHigh x kCompute = kLaunchRegs x kThreads.
 template <int D>
 struct BwdShape {
   static constexpr int kWG = D == 128 ? 4 : 2;
   static constexpr int kChunksPerWG = 4 / kWG;
-  static constexpr int kCols = D / kWG;                     // head-dim columns per warpgroup (32)
+  static constexpr int kCols = D / kWG;                     // head-dim columns per slice (32)
   static constexpr int kCompute = 128 * kWG;
-  static constexpr int kThreads = 128 + kCompute;
+  static constexpr int kThreads = 128 + kCompute + 128;
+  static constexpr int kLaunchRegs = (65536 / kThreads) & ~7;   // 80 at d = 128, 128 at d = 64
+  static constexpr int kRegLow = D == 128 ? 48 : 64;
+  static constexpr int kRegHigh = D == 128 ? 96 : 192;
+  static_assert(kRegLow * 256 + kRegHigh * kCompute == kLaunchRegs * kThreads, "register split");
 };
 
 struct BwdParams {
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_full, kCompute);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, kCompute);
+    mbar_init(dq_empty, 128);
     mbar_init(acc_full, 1);
     mbar_init(sf_ready, 128);
     fence_mbar_init();
@@ -171,6 +179,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool compute_wg = warp >= 4 && warp < 4 + 4 * kWG;
   const uint32_t tbase = *tmem_slot;
   constexpr uint32_t kS = 0, kP = 128, kDV = 256, kDK = 384;
   constexpr uint32_t kSF = kS + 104;        // 24 block-scale words, valid once S^T was read
@@ -178,6 +187,8 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   constexpr uint32_t kAtom = 8 * D;
   float* rowbuf = reinterpret_cast<float*>(smem + L::kRow);
 
+  if (warp < 4) {
+  setmaxnreg_dec<BwdShape<D>::kRegLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -327,8 +338,10 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       }
       mbar_arrive(&row_full[b]);
     }
-  } else if (warp >= 4) {
+  }
+  } else if (compute_wg) {
     // ------------------------------------------------------------ compute (warps 4 .. 4 + 4 kWG - 1)
+    setmaxnreg_inc<BwdShape<D>::kRegHigh>();
     const int wg = (warp - 4) >> 2;                    // query columns [32 kCPW wg, 32 kCPW (wg + 1))
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;                 // key row (TMEM lane) for S / dP; query row for dQ
@@ -347,41 +360,9 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     uint8_t* Esm = smem + L::kE;
     uint8_t* sPt = smem + L::kPt;
     uint8_t* sDS = smem + L::kDS;
-    uint8_t* sb = smem + L::kStage + wg * 2 * L::kStageBytes;   // this warpgroup's two staging buffers
     bool ok = true;
-    // mixed route: scale words of the score MMA, written by warpgroup 0 into the first
-    // 16 dP columns before every score MMA, replicated over the four lane quarters
-    // (lane 32q + l, column c holds row 32c + l): K~ rows (A, fixed) and the Q~ rows of
-    // the step's query tile (B); per row and instruction one word of four E4M3 scales
-    uint2 k4w[4] = {}, q4w[4] = {};
-    auto load_sf_rows = [&](const uint8_t* base, int64_t tok0, int H, int hh_, uint2 (&w4)[4]) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int64_t tok = tok0 + 32 * c + lane;
-        w4[c] = tok < p.T ? *reinterpret_cast<const uint2*>(base + (tok * H + hh_) * (D / 16)) : make_uint2(0u, 0u);
-      }
-    };
-    auto step_qsf = [&](int kk) {
-      load_sf_rows(p.q4_scales, (int64_t)doc_start + (u + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles, q4w);
-    };
-    auto store_score_sf = [&]() {
-      tmem_st4(lane_base + kP + 0, k4w[0].x, k4w[1].x, k4w[2].x, k4w[3].x);
-      tmem_st4(lane_base + kP + 4, k4w[0].y, k4w[1].y, k4w[2].y, k4w[3].y);
-      tmem_st4(lane_base + kP + 8, q4w[0].x, q4w[1].x, q4w[2].x, q4w[3].x);
-      tmem_st4(lane_base + kP + 12, q4w[0].y, q4w[1].y, q4w[2].y, q4w[3].y);
-    };
-    if (MIXED && wg == 0) {
-      load_sf_rows(p.k4_scales, (int64_t)doc_start + u * kTile, p.hkv, hk, k4w);
-      step_qsf(0);
-      store_score_sf();
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(sf_ready);
-      if (nsteps > 1) step_qsf(1);
-    }
     for (int k = 0; k < nsteps; ++k) {
-      const int hh = k / qtiles, t = u + k % qtiles;
-      const int h = hk * g + hh;
+      const int t = u + k % qtiles;
       const bool diag = (t == u);
       const int b = k & 1;
       const float* rb = rowbuf + b * (L::kRowBuf / 4);
@@ -389,7 +370,6 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
-      const float boost_step = rb[258];    // read before the row buffer is released below
       // P = 2^(x - LSE log2 e) for this warpgroup's query chunks
       float pr[kCPW][32];
 #pragma unroll
@@ -566,56 +546,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&row_empty[b]);
       mbar_arrive(p_full);
-      // dQ partial of this step: thread index = query row, this warpgroup's kCols columns
-      ok = named_bar_and(1, kCompute, mbar_wait(dq_full, k & 1, status));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        // read this warpgroup's columns of the dQ partial, release the TMEM columns,
-        // stage c * partial as fp16 in shared memory, then reduce-add it into the
-        // fp16 accumulator (rows outside the document are skipped).
-        const int ql = t * kTile + j;
-        const bool qv = ql < doc_len;
-        const float cb = qv ? boost_step : 0.f;
-        uint32_t v[32];
-        tmem_ld32(lane_base + kP + wg * kCols, v);
-        tmem_ld_wait();
-        if (MIXED && wg == 0 && k + 1 < nsteps) {
-          store_score_sf();                   // q4w holds the rows of step k + 1
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        if (MIXED && wg == 0 && k + 2 < nsteps) step_qsf(k + 2);
-        const float2 cb2 = make_float2(cb, cb);
-        constexpr int kRowBytes = kCols * 2;                // 64: one staged row of fp16
-        constexpr int kChunks = kRowBytes / 16;             // 16-byte units per staged row
-        uint8_t* sbk = sb + (k & 1) * L::kStageBytes;       // double-buffered staging
-#pragma unroll
-        for (int c16 = 0; c16 < kChunks; ++c16) {
-          uint32_t hw[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = fmul2(make_float2(__uint_as_float(v[8 * c16 + 2 * q]), __uint_as_float(v[8 * c16 + 2 * q + 1])), cb2);
-            __half2 h2 = __floats2half2_rn(f.x, f.y);
-            hw[q] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          *reinterpret_cast<uint4*>(sbk + dq_chunk_byte(j, 16 * c16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2 + wg, 128);
-        if ((threadIdx.x & 127) == 0) {
-          // one bulk fp16 reduce-add of the whole staged slice into the tile's accumulator
-          // chunk (rows past the document end were staged as zeros); the wait leaves at
-          // most this copy reading shared memory, so the other buffer is free next step
-          __half* dst = p.dq_acc + dq_chunk_elems(pv.tile_prefix[doc] + t, h, wg, p.hq, D);
-          bulk_reduce_add_f16(dst, smem_u32(sbk), L::kStageBytes);
-          bulk_commit();
-          bulk_wait_read<1>();
-        }
-      }
     }
-    if ((threadIdx.x & 127) == 0) bulk_wait_all();
     if (ok) ok = named_bar_and(1, kCompute, mbar_wait(acc_full, 0, status));
     if (ok) {
       tc_fence_after();
@@ -640,6 +571,100 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         }
       }
     }
+  } else {
+    // ------------------------------------------------------------ dQ readout (the last warpgroup)
+    setmaxnreg_dec<BwdShape<D>::kRegLow>();
+    // Per step: wait for the dQ partial, read it slice by slice (32 head-dim columns,
+    // thread = query row), release the TMEM columns, stage c * partial as fp16 in the
+    // slice's swizzled SMEM buffer and reduce each slice into its accumulator chunk
+    // with one bulk fp16 reduce-add (rows past the document end are staged as zeros).
+    const int quarter = warp & 3;
+    const int i = quarter * 32 + lane;                 // query row of the dQ partial (TMEM lane)
+    const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+    const bool elected = (threadIdx.x & 127) == 0;
+    // mixed route: scale words of the score MMA, written into the first 16 dP columns
+    // before every score MMA, replicated over the four lane quarters (lane 32q + l,
+    // column c holds row 32c + l): K~ rows (A, fixed) and the Q~ rows of the step's
+    // query tile (B); per row and instruction one word of four E4M3 scales
+    uint2 k4w[4] = {}, q4w[4] = {};
+    auto load_sf_rows = [&](const uint8_t* base, int64_t tok0, int H, int hh_, uint2 (&w4)[4]) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t tok = tok0 + 32 * c + lane;
+        w4[c] = tok < p.T ? *reinterpret_cast<const uint2*>(base + (tok * H + hh_) * (D / 16)) : make_uint2(0u, 0u);
+      }
+    };
+    auto step_qsf = [&](int kk) {
+      load_sf_rows(p.q4_scales, (int64_t)doc_start + (u + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles, q4w);
+    };
+    auto store_score_sf = [&]() {
+      tmem_st4(lane_base + kP + 0, k4w[0].x, k4w[1].x, k4w[2].x, k4w[3].x);
+      tmem_st4(lane_base + kP + 4, k4w[0].y, k4w[1].y, k4w[2].y, k4w[3].y);
+      tmem_st4(lane_base + kP + 8, q4w[0].x, q4w[1].x, q4w[2].x, q4w[3].x);
+      tmem_st4(lane_base + kP + 12, q4w[0].y, q4w[1].y, q4w[2].y, q4w[3].y);
+    };
+    if (MIXED) {
+      load_sf_rows(p.k4_scales, (int64_t)doc_start + u * kTile, p.hkv, hk, k4w);
+      step_qsf(0);
+      store_score_sf();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(sf_ready);
+      if (nsteps > 1) step_qsf(1);
+    }
+    constexpr int kRowBytes = kCols * 2;               // 64: one staged row of fp16
+    constexpr int kChunks = kRowBytes / 16;            // 16-byte units per staged row
+    bool ok = true;
+    for (int k = 0; k < nsteps && !STRICT; ++k) {
+      const int hh = k / qtiles, t = u + k % qtiles;
+      const int h = hk * g + hh;
+      const bool qv = t * kTile + i < doc_len;
+      const float cb = qv ? p.boost[(int64_t)doc * p.hq + h] : 0.f;
+      const float2 cb2 = make_float2(cb, cb);
+      ok = named_bar_and(6, 128, mbar_wait(dq_full, k & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kWG; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + kP + 32 * c, v);
+        tmem_ld_wait();
+        if (c == kWG - 1) {                  // the whole partial is in registers or SMEM
+          if (MIXED && k + 1 < nsteps) {
+            store_score_sf();                // q4w holds the rows of step k + 1
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          mbar_arrive(dq_empty);
+        }
+        uint8_t* sbk = smem + L::kStage + (2 * c + (k & 1)) * L::kStageBytes;
+#pragma unroll
+        for (int c16 = 0; c16 < kChunks; ++c16) {
+          uint32_t hw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = fmul2(make_float2(__uint_as_float(v[8 * c16 + 2 * q]), __uint_as_float(v[8 * c16 + 2 * q + 1])), cb2);
+            __half2 h2 = __floats2half2_rn(f.x, f.y);
+            hw[q] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(sbk + dq_chunk_byte(i, 16 * c16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+      }
+      if (MIXED && k + 2 < nsteps) step_qsf(k + 2);
+      fence_proxy_async_smem();
+      named_bar_sync(6, 128);
+      if (elected) {
+        // one bulk fp16 reduce-add per slice; the wait leaves at most this step's copies
+        // reading shared memory, so the other buffers are free next step
+        const int64_t tile = pv.tile_prefix[doc] + t;
+        for (int c = 0; c < kWG; ++c)
+          bulk_reduce_add_f16(p.dq_acc + dq_chunk_elems(tile, h, c, p.hq, D),
+                              smem_u32(smem + L::kStage + (2 * c + (k & 1)) * L::kStageBytes), L::kStageBytes);
+        bulk_commit();
+        bulk_wait_read<1>();
+      }
+    }
+    if (elected) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -1138,6 +1163,12 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_kernel<D, STRICT, MIXED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // the warpgroups' register split (setmaxnreg) assumes this launch allocation;
+  // with any other the increase could never be granted, so refuse to launch
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D, STRICT, MIXED>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != BwdShape<D>::kLaunchRegs) return cudaErrorInvalidConfiguration;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
   attn_bwd_kernel<D, STRICT, MIXED>
       <<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
