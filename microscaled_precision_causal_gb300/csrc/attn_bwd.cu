@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   uint64_t* dq_empty = s_full + 4;
   uint64_t* acc_full = s_full + 5;
   uint64_t* sf_ready = s_full + 6;            // mixed: score scale words of step 0 written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
+  uint64_t* pt_full = s_full + 7;             // P^ tile and the dV scale words written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 8);
   int* status = const_cast<int*>(p.plan) + kPlanStatus;
 
   const int n_items = p.plan[kPlanBwdItems];
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     mbar_init(dq_empty, 128);
     mbar_init(acc_full, 1);
     mbar_init(sf_ready, 128);
+    mbar_init(pt_full, 128);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -250,27 +252,31 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       }
       for (int k = 0; k < nsteps && ok; ++k) {
         const int st = k % kQStages;
-        ok = mbar_wait(p_full, k & 1, status);
+        const uint32_t qa = sq + st * L::kTileBytes, da = sdo + st * L::kTileBytes;
+        // dV as soon as P^ is in SMEM: it runs while the compute warpgroups build dS^
+        ok = mbar_wait(pt_full, k & 1, status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t qa = sq + st * L::kTileBytes, da = sdo + st * L::kTileBytes;
-        if (!STRICT) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major);
-            // first, so that its readout overlaps the dV and dK products
-            mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
-                     smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
-                     tbase + kSF + 16, tbase + kSF + 20, s > 0);
-          }
-          mma_commit(dq_full);
-        }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
           mma_mxf8(tbase + kDV, smem_desc(spt + 32 * s, 16, 1024, kSwizzle128B),
                    smem_desc(da + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
                    tbase + kSF + 0, tbase + kSF + 4, (k > 0 || s > 0));
+        }
+        ok = mbar_wait(p_full, k & 1, status);
+        if (!ok) break;
+        tc_fence_after();
+        if (!STRICT) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major);
+            // before dK, so that its readout overlaps the dK product
+            mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
+                     smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
+                     tbase + kSF + 16, tbase + kSF + 20, s > 0);
+          }
+          mma_commit(dq_full);
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
@@ -313,8 +319,9 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         const int ql = t * kTile + i;
         const bool qv = ql < doc_len;
         const int64_t qtok = (int64_t)doc_start + ql;
-        rb[i] = qv ? -p.lse[(int64_t)h * p.T + qtok] * 1.4426950408889634f : -INFINITY;
-        rb[128 + i] = qv ? -p.dvec[(int64_t)h * p.T + qtok] : 0.f;
+        // the P boost 2^8 rides in the exponent; dP - D is scaled by 2^-8 to compensate
+        rb[i] = qv ? fmaf(-p.lse[(int64_t)h * p.T + qtok], 1.4426950408889634f, 8.0f) : -INFINITY;
+        rb[128 + i] = qv ? -p.dvec[(int64_t)h * p.T + qtok] * (1.0f / 256.0f) : 0.f;
       }
       if (lane == 8 && !STRICT) rb[258] = p.boost[(int64_t)doc * p.hq + h];   // dQ boost of (document, query head)
       if (STRICT) {
@@ -370,7 +377,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
-      // P = 2^(x - LSE log2 e) for this warpgroup's query chunks
+      // 2^8 P = 2^(x - LSE log2 e + 8) for this warpgroup's query chunks
       float pr[kCPW][32];
 #pragma unroll
       for (int cc = 0; cc < kCPW; ++cc) {
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         tmem_ld32(lane_base + kS + 32 * c, vs);
         tmem_ld_wait();
         const float fS = MIXED ? p.scale_log2 : p.scale_log2 * sk_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[c]));
-        const float2 fS2 = make_float2(fS, fS), b2 = make_float2(256.f, 256.f);
+        const float2 fS2 = make_float2(fS, fS);
         const float4* nl4 = reinterpret_cast<const float4*>(rb + 32 * c);   // -LSE * log2(e)
         const float4* sq4 = reinterpret_cast<const float4*>(rb + 260 + 32 * c);   // strict: s_Q per query
         uint32_t pk[8];
@@ -405,10 +412,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
             p1.y = il + 3 >= j ? p1.y : 0.f;
           }
           pr[cc][i] = p0.x; pr[cc][i + 1] = p0.y; pr[cc][i + 2] = p1.x; pr[cc][i + 3] = p1.y;
-          if (!STRICT) {
-            const float2 q0 = fmul2(p0, b2), q1 = fmul2(p1, b2);
-            pk[i >> 2] = (uint32_t)e4m3x2(q0.x, q0.y) | ((uint32_t)e4m3x2(q1.x, q1.y) << 16);
-          }
+          if (!STRICT) pk[i >> 2] = (uint32_t)e4m3x2(p0.x, p0.y) | ((uint32_t)e4m3x2(p1.x, p1.y) << 16);
         }
         if (STRICT) {
           // dV operand with dO's per-token scale folded in: 2^8 P s_dO(i), one round-up
@@ -419,8 +423,8 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             const float4 sd = sd4[i >> 2];
-            const float2 a0 = fmul2(fmul2(make_float2(pr[cc][i], pr[cc][i + 1]), make_float2(sd.x, sd.y)), b2);
-            const float2 a1 = fmul2(fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), make_float2(sd.z, sd.w)), b2);
+            const float2 a0 = fmul2(make_float2(pr[cc][i], pr[cc][i + 1]), make_float2(sd.x, sd.y));
+            const float2 a1 = fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), make_float2(sd.z, sd.w));
             pf[i] = a0.x; pf[i + 1] = a0.y; pf[i + 2] = a1.x; pf[i + 3] = a1.y;
             gmax = fmax3(gmax, fmaxf(a0.x, a0.y), fmaxf(a1.x, a1.y));
           }
@@ -434,16 +438,32 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
+      fence_proxy_async_smem();                // P^ (and, strict, its row exponents) published below
       ok = named_bar_and(1, kCompute, mbar_wait(dp_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
+      if (wg == 0) {
+        // scale words of dV += P^^T dO (S^T has been read by every warpgroup): A = P^
+        // (1.0; strict: its per-key-row exponents), B = dO per query chunk (strict: 1.0)
+        if (STRICT) {
+          tmem_st1(lane_base + kSF + 0 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 64 + j * 4));
+          tmem_st4(lane_base + kSF + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+          const uint32_t bw = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
+          tmem_st4(lane_base + kSF + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          tmem_st4(lane_base + kSF + 4, bw, bw, bw, bw);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(pt_full);
+      }
 #pragma unroll
       for (int cc = 0; cc < kCPW; ++cc) {
         const int c = kCPW * wg + cc;
         uint32_t vp[32];
         tmem_ld32(lane_base + kP + 32 * c, vp);
         tmem_ld_wait();
-        const float fP = sv_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[4 + c]));
+        const float fP = (1.0f / 256.0f) * sv_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[4 + c]));
         const float2 fP2 = make_float2(fP, fP);
         const float4* nd4 = reinterpret_cast<const float4*>(rb + 128 + 32 * c);   // -D
         const float4* sd4 = reinterpret_cast<const float4*>(rb + 388 + 32 * c);   // strict: s_dO
@@ -495,15 +515,9 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
       if (STRICT) {
         // A-operand scales are per key row: row j's word sits in lane j, column
         // (base + j / 32), i.e. this warp's quarter; B operands (dO, Q) are folded.
-        if (wg == 0 || wg == 1 % kWG) {
-          if (wg == 0) {
-            tmem_st1(lane_base + kSF + 0 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 64 + j * 4));
-            tmem_st4(lane_base + kSF + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          }
-          if (wg == 1 % kWG) {
-            tmem_st1(lane_base + kSF + 8 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 576 + j * 4));
-            tmem_st4(lane_base + kSF + 12, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          }
+        if (wg == 1 % kWG) {      // dK: A per key row, B (Q) folded
+          tmem_st1(lane_base + kSF + 8 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 576 + j * 4));
+          tmem_st4(lane_base + kSF + 12, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
           tmem_st_wait();
         }
         fence_proxy_async_smem();
@@ -513,18 +527,16 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         continue;                            // dQ comes from the deterministic dQ kernel
       }
       {
-        // block-scale words of the three MXF8 MMAs, one operand pair per warpgroup
+        // block-scale words of the dK and dQ MMAs (dV's were written after P^), one
+        // operand pair per warpgroup
         const uint8_t* E = Esm;               // E[key block][query chunk]
         const int pair0 = wg, pair1 = wg + kWG;   // pairs 0 = dV, 1 = dK, 2 = dQ
 #pragma unroll
         for (int pi = 0; pi < 2; ++pi) {
           const int pair = pi == 0 ? pair0 : pair1;
-          if (pair > 2) continue;
+          if (pair == 0 || pair > 2) continue;
           uint32_t a[4], bw;
-          if (pair == 0) {          // dV: A = P^ (scale 1), B = dO per query chunk
-            a[0] = a[1] = a[2] = a[3] = 0x7F7F7F7Fu;
-            bw = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
-          } else if (pair == 1) {   // dK: A row = key in block cc, byte = query chunk; B = Q per query chunk
+          if (pair == 1) {          // dK: A row = key in block cc, byte = query chunk; B = Q per query chunk
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
               a[cc] = (uint32_t)E[cc * 4 + 0] | (uint32_t)E[cc * 4 + 1] << 8 | (uint32_t)E[cc * 4 + 2] << 16 |
