@@ -226,6 +226,21 @@ def traffic_for(kernel_file, workload):
     return {"bytes_per_flop": per_unit, "workload": rec.get("workload")}
 
 
+def quantizer_roofline(w, mode, ms, hbm_gbs):
+    """Algorithmic bytes of the Q/K/V quantization (token-block codes, scale bytes,
+    the K/V row stats; mixed: also the NVFP4 copies of Q and K and the per-token V
+    copy) over its measured time (the three or six launches of one step)."""
+    T, hq, hkv, d = w.total_tokens, w.hq, w.hkv, w.d
+    per = lambda H: T * H * d * (2 + 1) + T * H          # bf16 in, E4M3 out, one scale byte per row
+    total = per(hq) + 2 * per(hkv) + 2 * T * hkv * 8     # + (||x^||, max |x^|) of K and V
+    if mode == "mixed":
+        nv = lambda H: T * H * d * (2 + 0.5) + T * H * d / 16
+        total += nv(hq) + nv(hkv) + per(hkv)
+    gbs = total / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
+            "bytes_per_step": total, "ms": ms, "traffic": None}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -266,9 +281,13 @@ def run_ours(args, rank, world, local_rank):
     o_plain = F.Options()
     ctypes.pointer(o_plain)[0] = att.opts
 
-    def step(o_fwd=None, o_bwd=None):
+    def step(o_fwd=None, o_bwd=None, qev=None):
         att.plan_build(cu)
+        if qev:
+            qev[0].record(stream)
         att.quantize(x["q"], x["k"], x["v"], cu)
+        if qev:
+            qev[1].record(stream)
         att.opts = o_fwd or o_plain
         att.forward(cu)
         att.opts = o_bwd or o_plain
@@ -293,6 +312,7 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.3)
 
     per_step = [(make_opts(2), make_opts(8)) for _ in range(args.steps)]
+    qevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -303,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.steps):
         flush.zero_()                      # L2 flush between timed steps (outside the events)
         starts[i].record(stream)
-        step(per_step[i][0][2], per_step[i][1][2])
+        step(per_step[i][0][2], per_step[i][1][2], qevs[i])
         ends[i].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -314,6 +334,7 @@ def run_ours(args, rank, world, local_rank):
     kb = [b[0][4].elapsed_time(b[0][5]) for _, b in per_step]
     kbp = [b[0][0].elapsed_time(b[0][1]) for _, b in per_step]
     kfin = [b[0][6].elapsed_time(b[0][7]) for _, b in per_step]
+    kq = [q0.elapsed_time(q1) for q0, q1 in qevs]
     total_ms = float(sum(ms))
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -372,8 +393,9 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "flushed between timed steps (256 MiB write); step inputs 256 MiB > L2",
                    "frac_of_fp8_peak": value / world / fp8_peak,
                    "fp8_peak_tflops": fp8_peak, "peak_source": pk["src"] + " (2 x bf16 burst)"},
-        "phases_ms": {"fwd_kernel": kf_ms, "bwd_kernel": kb_ms, "bwd_prep": float(np.mean(kbp)),
-                      "bwd_finalise": float(np.mean(kfin))},
+        "phases_ms": {"quantize_qkv": float(np.mean(kq)), "fwd_kernel": kf_ms, "bwd_kernel": kb_ms,
+                      "bwd_prep": float(np.mean(kbp)), "bwd_finalise": float(np.mean(kfin))},
+        "quantizer_roofline": quantizer_roofline(w, args.mode, float(np.mean(kq)), pk["hbm"]),
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp8_peak, "traffic": traffic,
                      "per_unit": "FLOPs per launch = %s * head_dim * hq * visible pairs" % ("10" if "bwd" in dom else "4")},

@@ -39,7 +39,10 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
                     float2* __restrict__ stats, const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec,
                     __half* __restrict__ dq_acc, const float2* __restrict__ k_stats,
                     const float2* __restrict__ v_stats, int hkv, float* __restrict__ maxima) {
-  constexpr int kLpr = D / 8;          // lanes per token row (16 bytes each)
+  // Each lane owns 32 elements of a row as four 16-byte vectors, vector j at column
+  // j * 8 kLpr + 8 (lane % kLpr): a load instruction reads kRpi rows x 16 kLpr
+  // contiguous bytes, and per-row reductions take log2(kLpr) shuffle levels.
+  constexpr int kLpr = D / 32;         // lanes per token row
   constexpr int kRpi = 32 / kLpr;      // rows per iteration
   constexpr int kIters = 32 / kRpi;    // 32 rows per warp
   const int lane = threadIdx.x & 31;
@@ -76,10 +79,11 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
     tail = true;
   }
   const int sub = lane / kLpr;            // row within an iteration
-  const int cb = (lane % kLpr) * 8;       // first of the 8 elements this lane owns
+  const int seg = lane % kLpr;
+  auto col_of = [&](int j) { return j * 8 * kLpr + 8 * seg; };
   auto live = [&](int r) { return r < nrows && !tail && (!PER_TOKEN || r0 + r < valid); };
-  auto load8 = [&](const __nv_bfloat16* base, int r) {
-    return live(r) ? __ldg(reinterpret_cast<const uint4*>(base + ((int64_t)(r0 + r) * H + h) * D + cb))
+  auto load8 = [&](const __nv_bfloat16* base, int r, int j) {
+    return live(r) ? __ldg(reinterpret_cast<const uint4*>(base + ((int64_t)(r0 + r) * H + h) * D + col_of(j)))
                    : make_uint4(0, 0, 0, 0);
   };
   auto absmax8 = [](const uint4& w) {
@@ -94,77 +98,82 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
   };
 
   float mdo = 0.f;        // backward prep: max ||dO^_i|| over the block's rows
-  // pass 1 (token blocks): amax over the whole block; the block stays in
-  // registers for pass 2 (32 rows x 16 bytes per lane)
+  // pass 1 (token blocks): amax over the whole block; the plain quantizer keeps the
+  // block in registers for pass 2 (32 rows x 64 bytes per lane)
   int e_block = 0;
-  uint4 w[kHold ? kIters : 1];
+  uint4 w[kHold ? kIters : 1][4];
   if (!PER_TOKEN) {
-    uint4 w1[kHold ? 1 : kIters];
-#pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-      if (kHold) w[kHold ? it : 0] = load8(x, it * kRpi + sub);
-      else w1[kHold ? 0 : it] = load8(x, it * kRpi + sub);
-    }
     float a = 0.f;
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) a = fmaxf(a, absmax8(kHold ? w[kHold ? it : 0] : w1[kHold ? 0 : it]));
+    for (int it = 0; it < kIters; ++it) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 x4 = load8(x, it * kRpi + sub, j);
+        if (kHold) w[kHold ? it : 0][j] = x4;
+        a = fmaxf(a, absmax8(x4));
+      }
+    }
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o2));
     e_block = roundup_exp(a);
   }
-#pragma unroll(kHold ? kIters : 2)
+#pragma unroll(kHold ? kIters : 1)
   for (int it = 0; it < kIters; ++it) {
     const int r = it * kRpi + sub;
     const bool inrange = r < nrows;
-    const uint4 raw = kHold ? w[kHold ? it : 0] : load8(x, r);
+    uint4 raw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) raw[j] = kHold ? w[kHold ? it : 0][j] : load8(x, r, j);
     int e = e_block;
     if (PER_TOKEN) {
-      float m = absmax8(raw);
+      float m = fmaxf(fmaxf(absmax8(raw[0]), absmax8(raw[1])), fmaxf(absmax8(raw[2]), absmax8(raw[3])));
 #pragma unroll
       for (int o2 = kLpr / 2; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
       e = roundup_exp(m);
     }
     const float s = exp2i(-e);
-    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    uint32_t packed[2];
+    const float back = ue8m0_to_f32((uint32_t)(e + 127));
+    float2 ss2 = make_float2(0.f, 0.f), dd2 = make_float2(0.f, 0.f);
+    uint32_t cmax4 = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(v[j]);
-      const uint16_t c2 = e4m3x2(f.x * s, f.y * s);
-      if (j & 1) packed[j >> 1] |= (uint32_t)c2 << 16; else packed[j >> 1] = c2;
-    }
-    // statistics of the reconstructed row x^ = 2^e c and D = dO^ . O, from the codes:
-    // sums over the decoded codes, scaled by 2^e (2^2e) once at the end (exact)
-    const float back = ue8m0_to_f32((uint32_t)(e + 127));
-    float ss = 0.f, mx = 0.f, dd = 0.f;
-    uint32_t cmax = 0;
-    if (STATS || WITH_D) {
-      float2 ss2 = make_float2(0.f, 0.f), dd2 = make_float2(0.f, 0.f);
-      const uint4 oraw = WITH_D ? load8(o, r) : make_uint4(0, 0, 0, 0);
-      const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oraw);
+      const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+      uint32_t packed[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint16_t c2 = (uint16_t)(packed[j >> 1] >> (16 * (j & 1)));
-        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2, __NV_E4M3);
-        const float2 f = __half22float2(__half2(hr));
-        if (STATS) ss2 = ffma2(f, f, ss2);
-        if (WITH_D) dd2 = ffma2(f, __bfloat1622float2(ov[j]), dd2);
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(v[q]);
+        const uint16_t c2 = e4m3x2(f.x * s, f.y * s);
+        if (q & 1) packed[q >> 1] |= (uint32_t)c2 << 16; else packed[q >> 1] = c2;
       }
-      if (STATS) {
-        ss = ss2.x + ss2.y;
-        cmax = __vmaxu4(packed[0] & 0x7F7F7F7Fu, packed[1] & 0x7F7F7F7Fu);   // |code| orders like |value|
-        cmax = max(max(cmax & 0xFFu, (cmax >> 8) & 0xFFu), max((cmax >> 16) & 0xFFu, cmax >> 24));
+      // statistics of the reconstructed row x^ = 2^e c and D = dO^ . O, from the codes:
+      // sums over the decoded codes, scaled by 2^e (2^2e) once at the end (exact)
+      if (STATS || WITH_D) {
+        const uint4 oraw = WITH_D ? load8(o, r, j) : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oraw);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint16_t c2 = (uint16_t)(packed[q >> 1] >> (16 * (q & 1)));
+          const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2, __NV_E4M3);
+          const float2 f = __half22float2(__half2(hr));
+          if (STATS) ss2 = ffma2(f, f, ss2);
+          if (WITH_D) dd2 = ffma2(f, __bfloat1622float2(ov[q]), dd2);
+        }
+        if (STATS) cmax4 = __vmaxu4(cmax4, __vmaxu4(packed[0] & 0x7F7F7F7Fu, packed[1] & 0x7F7F7F7Fu));
       }
-      if (WITH_D) dd = dd2.x + dd2.y;
+      if (inrange) {
+        const int64_t row = r0 + r;
+        const int col = col_of(j);
+        *reinterpret_cast<uint2*>(codes + (row * H + h) * D + col) = make_uint2(packed[0], packed[1]);
+        if (WITH_D && !PER_TOKEN && !tail && dq_acc)      // zero the row's slice of its accumulator chunk
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(dq_acc + dq_chunk_elems(dq_tile0, h, col / 32, H, D)) +
+                                    dq_chunk_byte(dq_row0 + r, (col % 32) * 2)) = make_uint4(0, 0, 0, 0);
+      }
     }
-    if (inrange) {
-      const int64_t row = r0 + r;
-      *reinterpret_cast<uint2*>(codes + (row * H + h) * D + cb) = make_uint2(packed[0], packed[1]);
-      if (WITH_D && !PER_TOKEN && !tail && dq_acc)      // zero the row's slice of its accumulator chunk
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(dq_acc + dq_chunk_elems(dq_tile0, h, cb / 32, H, D)) +
-                                  dq_chunk_byte(dq_row0 + r, (cb % 32) * 2)) = make_uint4(0, 0, 0, 0);
-    }
+    float ss = 0.f, mx = 0.f, dd = 0.f;
     if (STATS || WITH_D) {
+      ss = ss2.x + ss2.y;
+      dd = dd2.x + dd2.y;
+      uint32_t cmax = max(max(cmax4 & 0xFFu, (cmax4 >> 8) & 0xFFu), max((cmax4 >> 16) & 0xFFu, cmax4 >> 24));
 #pragma unroll
       for (int o2 = kLpr / 2; o2 > 0; o2 >>= 1) {
         if (STATS) {
@@ -173,9 +182,9 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
         }
         if (WITH_D) dd += __shfl_xor_sync(0xffffffffu, dd, o2);
       }
-      if (STATS) mx = e4m3_to_f32((uint8_t)cmax) * back;
+      if (STATS) mx = e4m3_to_f32((uint8_t)cmax) * back;   // |code| orders like |value|
     }
-    if (inrange && (lane % kLpr) == 0) {
+    if (inrange && seg == 0) {
       const int64_t row = r0 + r;
       if (STATS) stats[row * H + h] = make_float2(sqrtf(ss) * back, mx);
       if (WITH_D && !tail) mdo = fmaxf(mdo, sqrtf(ss) * back);
