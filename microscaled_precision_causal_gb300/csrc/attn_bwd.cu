@@ -1172,15 +1172,12 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   const int64_t grid = max_items * hkv;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
   constexpr int smem = BwdSmem<D, MIXED>::kAlloc;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_bwd_kernel<D, STRICT, MIXED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int regs = 0;
+  cudaError_t e = prepare_kernel<attn_bwd_kernel<D, STRICT, MIXED>>(smem, &regs);
   if (e != cudaSuccess) return e;
   // the warpgroups' register split (setmaxnreg) assumes this launch allocation;
   // with any other the increase could never be granted, so refuse to launch
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D, STRICT, MIXED>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != BwdShape<D>::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (regs != BwdShape<D>::kLaunchRegs) return cudaErrorInvalidConfiguration;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
   attn_bwd_kernel<D, STRICT, MIXED>
       <<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
@@ -1210,7 +1207,7 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
     dp.scale = scale;
     dp.dq = static_cast<__nv_bfloat16*>(dq);
     constexpr int dsmem = DqSmem<D>::kAlloc;
-    e = cudaFuncSetAttribute(attn_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
+    e = prepare_kernel<attn_dq_kernel<D>>(dsmem);
     if (e != cudaSuccess) return e;
     const int64_t dgrid = ((int64_t)T / (kTile * kItemTiles) + N + 1) * hq;
     if (dgrid > 0x7FFFFFFF) return cudaErrorInvalidValue;

@@ -517,8 +517,7 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
   const int64_t grid = max_items * hq;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
   constexpr int smem = FwdSmem<D>::kAlloc;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_fwd_kernel<D, STRICT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = prepare_kernel<attn_fwd_kernel<D, STRICT>>(smem);
   if (e != cudaSuccess) return e;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
   attn_fwd_kernel<D, STRICT><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);

@@ -519,8 +519,7 @@ cudaError_t launch_coop_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const int64_t grid = max_items * p.hq;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
   constexpr int smem = CoopSmem<D, MIXED>::kAlloc;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_fwd_coop_kernel<D, MIXED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = prepare_kernel<attn_fwd_coop_kernel<D, MIXED>>(smem);
   if (e != cudaSuccess) return e;
   attn_fwd_coop_kernel<D, MIXED><<<(unsigned)grid, kCThreads, smem, stream>>>(tq, tk, tv, tvt, p);
   return cudaGetLastError();

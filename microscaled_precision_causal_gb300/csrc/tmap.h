@@ -4,9 +4,35 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace flamia {
+
+// Per-device one-time kernel set-up: the dynamic shared-memory limit and the
+// register count the launch relies on are settled on the first call on each
+// device, so that later calls -- including calls captured into a CUDA graph --
+// only launch.
+template <auto Kernel>
+inline cudaError_t prepare_kernel(int smem_bytes, int* num_regs = nullptr) {
+  static std::atomic<unsigned long long> ready{0};
+  static int regs[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(ready.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, Kernel);
+    if (e != cudaSuccess) return e;
+    regs[dev & 63] = fa.numRegs;
+    ready.fetch_or(bit, std::memory_order_release);
+  }
+  if (num_regs) *num_regs = regs[dev & 63];
+  return cudaSuccess;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

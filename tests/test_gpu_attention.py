@@ -189,3 +189,36 @@ def test_gpu_tracks_unquantized_attention_like_the_oracle():
     for n in ("dq", "dk", "dv"):
         cg, cor = cosine(g[n], ref_g[n]), cosine(o[n], ref_g[n])
         assert cg > 0.995 and abs(cg - cor) < 5e-4, (n, cg, cor)
+
+
+def test_training_call_replays_from_a_cuda_graph():
+    """The calls need no host synchronisation and allocate nothing, so the whole
+    training call (plan, quantize, forward, backward) can be captured into one CUDA
+    graph ([EN] section 6: graph-capturable, row capacity independent of the
+    document lengths). Replays match the eager call (dQ up to the order of its
+    fp16 reductions)."""
+    import torch
+    import microscaled_precision_causal_gb300 as F
+    from gpu_harness import to_device_bf16, cu_tensor
+    lengths, hq, hkv, d = [300, 77, 129], 4, 2, 128
+    T = sum(lengths) + 7
+    inp = W.make_inputs(W.custom([T], hq, hkv, d, seed=19))
+    x = {n: to_device_bf16(inp[n]) for n in inp}
+    cu = cu_tensor(lengths)
+    att = F.FlamiaAttention(T, len(lengths), hq, hkv, d)
+    att.training_call(x["q"], x["k"], x["v"], x["do"], cu)
+    torch.cuda.synchronize()
+    eager = {n: getattr(att, n).clone() for n in ("out", "lse", "dq", "dk", "dv")}
+    for t in (att.out, att.dq, att.dk, att.dv):
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        att.training_call(x["q"], x["k"], x["v"], x["do"], cu)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert att.device_status() == 0
+    for n in ("out", "lse", "dk", "dv"):
+        assert torch.equal(getattr(att, n), eager[n]), n
+    a, b = att.dq.float().cpu().numpy(), eager["dq"].float().cpu().numpy()
+    assert norm_max_err(a, b) < 2e-3
