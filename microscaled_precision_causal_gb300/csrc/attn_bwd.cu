@@ -12,27 +12,34 @@
 //          (section 3: the 32x32 square serves both contraction axes)
 //   dV  += E4M3(2^8 P)^T dO^ / 2^8     (MXF8, dO's scale per 32 queries)
 //   dK  += dS^^T Q^                    (MXF8, dS block and Q scales per 32 queries)
-//   dQp  = dS^ K^                      (MXF8, same dS codes read transposed)
+//   dQp  = dS^ K^                      (MXF8, same dS codes read transposed; at
+//                                       d = 128 computed as dQp^T = K^T dS^^T in two
+//                                       64-query halves)
 //   dQacc += fp16(c * dQp)             (section 4, boosted FP16 partials; staged in
-//                                       shared memory, reduce-added with coalesced
-//                                       16-byte red.global.add.f16x2)
+//                                       shared memory, added into the accumulator
+//                                       with bulk fp16 reduce copies)
 //
 // One CTA per (document-local 128-key tile, kv head); it visits every query
 // head of the kv head's group and every query tile at or after the key tile.
-// Roles (640 threads at d = 128, 384 at d = 64):
+// Roles (768 threads at d = 128, 512 at d = 64):
 //   warp 0      TMA producer (K, V once; Q and dO codes per step)
 //   warp 1      MMA issuer (one thread)
 //   warp 2      TMEM allocator
 //   warp 3      per-query row data of the next steps (LSE, D, chunk scales) into SMEM
-//   warps 4..    compute warpgroups (four at d = 128, two at d = 64): each owns
+//   warps 4..   compute warpgroups (four at d = 128, two at d = 64): each owns
 //               32 of the 128 query columns of a step and 32 of the head-dim
-//               columns of the dQ partial and the dK / dV accumulators
-// Thread = key row while building P^ and dS^ codes, = query row while reading
-// the dQ partial.  TMEM: S^T [0,128) (its last 24 columns carry the block-scale
-// words of the three MXF8 MMAs once S^T has been read), dP^T / dQ partial
-// [128,256), dV [256, 256+D), dK [384, 384+D).  Per step the MMA thread issues
-// dV, dK, dQ(k), then S^T(k+1) straight away and dP^T(k+1) once the dQ partial
-// has been read, so the exponentials of step k+1 overlap the dP MMA.
+//               columns of the dK / dV accumulators
+//   last WG     dQ readout: TMEM -> fp16 staging -> bulk reduce into the accumulator
+// Thread = key row while building P^ and dS^ codes.  TMEM: S^T [0,128), dP^T
+// [128,256), dV [256, 256+D), dK [384, 384+D).  At d = 128 the dQ^T halves take
+// dP^T's first 64 columns once dS^ is built; at d = 64 the dQ partial has
+// [320, 384).  Block-scale words: dV's in S^T's columns [104, 112) (written once
+// S^T has been read), dK's and dQ's in dP^T's columns [104, 124) (written once
+// dP^T has been read; at d = 64 dQ's in [448, 456)).  Per step the MMA thread
+// issues dV(k) as soon as P^ is in SMEM, then S^T(k+1) (the exponentials of the
+// next step overlap the dS^ work of this one), then dK(k), dQ(k) and dP^T(k+1)
+// once the dQ columns have been read.  The mixed route's S~ MMA (NVFP4) takes its
+// scale words from dP^T's first 16 columns and so is issued late, after dQ.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -45,20 +52,25 @@ constexpr int kQStages = 2;
 // Compute warpgroups: each owns 32 of the 128 query columns of a step (as 4 / kWG
 // chunks of 32) and 32 of the head-dim columns of dQ / dK / dV.
 // Warpgroups: 0 = control (TMA producer, MMA issuer, TMEM allocator, row data),
-// 1 .. kWG = compute (P^ and dS^), kWG + 1 = dQ readout.  The control and readout
-// warpgroups hand registers to the compute warpgroups (setmaxnreg):
-// kRegLow x 256 + kRegHigh x kCompute = kLaunchRegs x kThreads.
-template <int D>
+// 1 .. kWG = compute (P^ and dS^), then kRO dQ readout warpgroups (two at d = 128
+// outside the strict options, each reading 32 of a dQ^T half's 64 columns).  The
+// control and readout warpgroups hand registers to the compute warpgroups
+// (setmaxnreg); the per-role totals fit the launch allocation:
+// kRegCtl x 128 + kRegRead x 128 kRO + kRegHigh x kCompute <= kLaunchRegs x kThreads.
+template <int D, bool STRICT = false>
 struct BwdShape {
   static constexpr int kWG = D == 128 ? 4 : 2;
   static constexpr int kChunksPerWG = 4 / kWG;
   static constexpr int kCols = D / kWG;                     // head-dim columns per slice (32)
   static constexpr int kCompute = 128 * kWG;
-  static constexpr int kThreads = 128 + kCompute + 128;
-  static constexpr int kLaunchRegs = (65536 / kThreads) & ~7;   // 80 at d = 128, 128 at d = 64
-  static constexpr int kRegLow = D == 128 ? 48 : 64;
-  static constexpr int kRegHigh = D == 128 ? 96 : 192;
-  static_assert(kRegLow * 256 + kRegHigh * kCompute == kLaunchRegs * kThreads, "register split");
+  static constexpr int kRO = D == 128 && !STRICT ? 2 : 1;
+  static constexpr int kThreads = 128 + kCompute + 128 * kRO;
+  static constexpr int kLaunchRegs = (65536 / kThreads) & ~7;   // 72 / 80 at d = 128, 128 at d = 64
+  static constexpr int kRegCtl = D == 128 ? 48 : 64;
+  static constexpr int kRegRead = D == 128 ? (kRO == 2 ? 48 : 80) : 64;
+  static constexpr int kRegHigh = D == 128 ? 88 : 192;
+  static_assert(kRegCtl * 128 + kRegRead * 128 * kRO + kRegHigh * kCompute <= kLaunchRegs * kThreads,
+                "register split");
 };
 
 struct BwdParams {
@@ -97,6 +109,7 @@ struct BwdSmem {
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents (+ strict per-row exponents)
   static constexpr int kStageBytes = kTile * BwdShape<D>::kCols * 2;   // one warpgroup's fp16 slice of the dQ tile
   static constexpr int kStage = (kE + 64 + 1024 + 1023) & ~1023;   // [warpgroup][2 buffers]
+  static_assert(D != 128 || 2 * BwdShape<D>::kWG * kStageBytes == 2 * 32768, "two 32 KB dQ^T staging buffers");
   static constexpr int kScoreBytes = kTile * D / 2;           // mixed route: one E2M1 score-operand tile
   static constexpr int kK4 = kStage + 2 * BwdShape<D>::kWG * kStageBytes;
   static constexpr int kQ4 = kK4 + (MIXED ? kScoreBytes : 0);          // [kQStages]
@@ -110,7 +123,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 }
 
 template <int D, bool STRICT, bool MIXED>
-__global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
+__global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_q4, const __grid_constant__ CUtensorMap tm_k4,
@@ -118,8 +131,9 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   static_assert(!(STRICT && MIXED), "the strict options and the mixed route are separate");
   static_assert(!MIXED || D == 128, "the mixed route is built for head_dim 128");
   using L = BwdSmem<D, MIXED>;
-  constexpr int kWG = BwdShape<D>::kWG, kCPW = BwdShape<D>::kChunksPerWG, kCols = BwdShape<D>::kCols;
-  constexpr int kCompute = BwdShape<D>::kCompute;
+  using Shape = BwdShape<D, STRICT>;
+  constexpr int kWG = Shape::kWG, kCPW = Shape::kChunksPerWG, kCols = Shape::kCols;
+  constexpr int kCompute = Shape::kCompute, kRO = Shape::kRO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -168,9 +182,9 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_full, kCompute);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, 128 * kRO);
     mbar_init(acc_full, 1);
-    mbar_init(sf_ready, 128);
+    mbar_init(sf_ready, 128 * kRO);
     mbar_init(pt_full, 128);
     fence_mbar_init();
   }
@@ -184,13 +198,22 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   const bool compute_wg = warp >= 4 && warp < 4 + 4 * kWG;
   const uint32_t tbase = *tmem_slot;
   constexpr uint32_t kS = 0, kP = 128, kDV = 256, kDK = 384;
-  constexpr uint32_t kSF = kS + 104;        // 24 block-scale words, valid once S^T was read
+  // dQ: at d = 128 (default and mixed routes) dQ^T = K^T dS^T in two 64-query halves
+  // into the first 64 dP columns (TMEM is full: S, dP, dV, dK); at d = 64 the
+  // query-major dQ partial sits in free columns.  Block-scale words: dV's in the S
+  // columns (written after P), dK's and dQ's in the dP columns (written after dS),
+  // so S of the next step can be issued right after dV.
+  constexpr bool kDQT = D == 128 && !STRICT;
+  constexpr uint32_t kDQ = D == 128 ? kP : 320;
+  constexpr uint32_t kSFV = kS + 104;       // dV: A 4 words, B 4 words
+  constexpr uint32_t kSFK = kP + 104;       // dK: A 4, B 4
+  constexpr uint32_t kSFQ = D == 128 ? kP + 112 : 448;   // dQ: A 4, B 4 (d = 128: B lo 4, B hi 4)
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
   constexpr uint32_t kAtom = 8 * D;
   float* rowbuf = reinterpret_cast<float*>(smem + L::kRow);
 
   if (warp < 4) {
-  setmaxnreg_dec<BwdShape<D>::kRegLow>();
+  setmaxnreg_dec<Shape::kRegCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -213,98 +236,149 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sk = smem_u32(smem + L::kK), sv = smem_u32(smem + L::kV), sq = smem_u32(smem + L::kQ),
-                     sdo = smem_u32(smem + L::kDO), spt = smem_u32(smem + L::kPt), sds = smem_u32(smem + L::kDS);
+    // The warp runs the loop converged (every lane waits); the elected lane issues
+    // the MMAs and the commits (a commit tracks the MMAs of its own thread).
+    const bool leader = elect_one();
+    {
+      // operand descriptors: every tile sits at a compile-time offset from the aligned
+      // SMEM base, so each descriptor is one add on base16
+      constexpr uint32_t kDS64 = kDQT ? kSwizzle64B : kSwizzle128B;
+      constexpr uint32_t kDSR = kDQT ? 512 : 1024;       // dS^ 8-row group stride
+      const uint32_t base16 = (smem_u32(smem) & 0x3FFFFu) >> 4;
+      // base16 re-read at every use, so that the compiler does not hoist the ~20
+      // descriptor words out of the step loop into the issuer's few registers
+      auto b16 = [&]() {
+        uint32_t x;
+        asm volatile("mov.b32 %0, %1;" : "=r"(x) : "r"(base16));
+        return x;
+      };
+      auto k_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kK + o, 16, kAtom, kLayout); };        // S^T: A
+      auto k_mn = [&](uint32_t o) { return sdesc_at(b16(), L::kK + o, kAtom, kAtom, kLayout); };       // dQ: B, dQ^T: A
+      auto v_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kV + o, 16, kAtom, kLayout); };        // dP^T: A
+      auto q_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kQ + o, 16, kAtom, kLayout); };        // S^T: B
+      auto q_mn = [&](uint32_t o) { return sdesc_at(b16(), L::kQ + o, kAtom, kAtom, kLayout); };       // dK: B
+      auto do_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kDO + o, 16, kAtom, kLayout); };      // dP^T: B
+      auto do_mn = [&](uint32_t o) { return sdesc_at(b16(), L::kDO + o, kAtom, kAtom, kLayout); };     // dV: B
+      auto pt_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kPt + o, 16, 1024, kSwizzle128B); };  // dV: A
+      // dS^: dK's A (keys x queries, K-major) and dQ's operand read query-major (at d = 128
+      // two 64-query SW64 tiles, the B operands of the dQ^T halves)
+      auto ds_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kDS + o, 16, kDSR, kDS64); };
+      auto ds_mn = [&](uint32_t o) { return sdesc_at(b16(), L::kDS + o, kDSR, kDSR, kDS64); };
       auto issue_s = [&](int st) {
         if constexpr (MIXED) {
           // S^T = K~ Q~^T from the NVFP4 copies (64 E2M1 elements per instruction); the
-          // scale words sit in the first 16 dP columns, free once the dQ partial was read
-          const uint32_t k4 = smem_u32(smem + L::kK4), q4 = smem_u32(smem + L::kQ4) + st * L::kScoreBytes;
+          // scale words sit in dP columns 0-7 (K~) and 32-39 (Q~), free once the dQ^T
+          // high half was read
 #pragma unroll
           for (int s = 0; s < 2; ++s)
-            mma_nvf4(tbase + kS, smem_desc(k4 + 32 * s, 16, 8 * 64, kSwizzle64B),
-                     smem_desc(q4 + 32 * s, 16, 8 * 64, kSwizzle64B), idesc_nvf4(128, 128), tbase + kP + 4 * s,
-                     tbase + kP + 8 + 4 * s, s > 0);
+            if (leader) mma_nvf4(tbase + kS, sdesc_at(b16(), L::kK4 + 32 * s, 16, 8 * 64, kSwizzle64B),
+                     sdesc_at(b16(), L::kQ4 + st * L::kScoreBytes + 32 * s, 16, 8 * 64, kSwizzle64B),
+                     idesc_nvf4(128, 128), tbase + kP + 4 * s, tbase + kP + 32 + 4 * s, s > 0);
         } else {
-          const uint32_t qa = sq + st * L::kTileBytes;
 #pragma unroll
           for (int s = 0; s < D / 32; ++s)
-            mma_f8(tbase + kS, smem_desc(sk + 32 * s, 16, kAtom, kLayout), smem_desc(qa + 32 * s, 16, kAtom, kLayout),
-                   idesc_f8(128, 128, 0, 0), s > 0);
+            if (leader) mma_f8(tbase + kS, k_kmaj(32 * s), q_kmaj(st * L::kTileBytes + 32 * s), idesc_f8(128, 128, 0, 0), s > 0);
         }
       };
       auto issue_dp = [&](int st) {
-        const uint32_t da = sdo + st * L::kTileBytes;
 #pragma unroll
         for (int s = 0; s < D / 32; ++s)
-          mma_f8(tbase + kP, smem_desc(sv + 32 * s, 16, kAtom, kLayout), smem_desc(da + 32 * s, 16, kAtom, kLayout),
-                 idesc_f8(128, 128, 0, 0), s > 0);
+          if (leader) mma_f8(tbase + kP, v_kmaj(32 * s), do_kmaj(st * L::kTileBytes + 32 * s), idesc_f8(128, 128, 0, 0), s > 0);
       };
-      bool ok = mbar_wait(kv_full, 0, status) && mbar_wait(&qd_full[0], 0, status);
-      if (ok && MIXED) ok = mbar_wait(sf_ready, 0, status);
+      // dQ^T = K^T dS^T per 64-query half (A: K keys x d read d-major; B: the half's
+      // dS^ tile, queries contiguous)
+      auto issue_dqt = [&](int hf) {
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (leader) mma_mxf8(tbase + kDQ, k_mn(s * 32 * D), ds_mn(hf * 8192 + s * 32 * 64), idesc_mxf8(128, 64, 1, 1, s, s),
+                   tbase + kSFQ, tbase + kSFQ + 4 + 4 * hf, s > 0);
+        if (leader) mma_commit(dq_full);
+      };
+      bool ok = warp_wait(kv_full, 0, status) && warp_wait(&qd_full[0], 0, status);
+      if (ok && MIXED) ok = warp_wait(sf_ready, 0, status);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        mma_commit(s_full);
+        if (leader) mma_commit(s_full);
         issue_dp(0);
-        mma_commit(dp_full);
+        if (leader) mma_commit(dp_full);
       }
       for (int k = 0; k < nsteps && ok; ++k) {
         const int st = k % kQStages;
-        const uint32_t qa = sq + st * L::kTileBytes, da = sdo + st * L::kTileBytes;
-        // dV as soon as P^ is in SMEM: it runs while the compute warpgroups build dS^
-        ok = mbar_wait(pt_full, k & 1, status);
+        const int st1 = (k + 1) % kQStages;
+        const bool more = k + 1 < nsteps;
+        // dV as soon as P^ is in SMEM; then (not mixed) S of the next step, which runs
+        // while the compute warpgroups build dS^
+        ok = warp_wait(pt_full, k & 1, status);
         if (!ok) break;
         tc_fence_after();
+        {
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
-          mma_mxf8(tbase + kDV, smem_desc(spt + 32 * s, 16, 1024, kSwizzle128B),
-                   smem_desc(da + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
-                   tbase + kSF + 0, tbase + kSF + 4, (k > 0 || s > 0));
+          for (int s = 0; s < 4; ++s)
+            // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
+            if (leader) mma_mxf8(tbase + kDV, pt_kmaj(32 * s), do_mn(st * L::kTileBytes + s * 32 * D), idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFV,
+                     tbase + kSFV + 4, (k > 0 || s > 0));
         }
-        ok = mbar_wait(p_full, k & 1, status);
-        if (!ok) break;
-        tc_fence_after();
-        if (!STRICT) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            // dQ partial = dS^ K (A: the same dS^ tile read query-major; B: K keys x d, MN-major);
-            // before dK, so that its readout overlaps the dK product
-            mma_mxf8(tbase + kP, smem_desc(sds + s * 32 * 128, 1024, 1024, kSwizzle128B),
-                     smem_desc(sk + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 1, 1, s, s),
-                     tbase + kSF + 16, tbase + kSF + 20, s > 0);
-          }
-          mma_commit(dq_full);
-        }
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          // dK += dS^^T Q
-          mma_mxf8(tbase + kDK, smem_desc(sds + 32 * s, 16, 1024, kSwizzle128B),
-                   smem_desc(qa + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
-                   tbase + kSF + 8, tbase + kSF + 12, (k > 0 || s > 0));
-        }
-        mma_commit(&qd_empty[st]);
-        if (k + 1 < nsteps) {
-          const int st1 = (k + 1) % kQStages;
-          ok = mbar_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
-          if (ok && MIXED) ok = mbar_wait(dq_empty, k & 1, status);   // score scale words of step k + 1 written
+        if (!MIXED && more) {
+          ok = warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
           if (!ok) break;
           tc_fence_after();
           issue_s(st1);
-          mma_commit(s_full);
-          if (!STRICT && !MIXED) {      // the dQ partial occupies the dP columns until it has been read
-            ok = mbar_wait(dq_empty, k & 1, status);
+          if (leader) mma_commit(s_full);
+        }
+        ok = warp_wait(p_full, k & 1, status);
+        if (!ok) break;
+        tc_fence_after();
+        // the low dQ^T half goes first so that its readout overlaps dK; the high half
+        // follows once the readout released the columns
+        if (kDQT) issue_dqt(0);
+        {
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            // dK += dS^^T Q (A: dS^ keys x queries K-major)
+            if (leader) mma_mxf8(tbase + kDK, ds_kmaj(kDQT ? (s >> 1) * 8192 + 32 * (s & 1) : 32 * s), q_mn(st * L::kTileBytes + s * 32 * D),
+                     idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFK, tbase + kSFK + 4, (k > 0 || s > 0));
+        }
+        if (leader) mma_commit(&qd_empty[st]);             // Q and dO of this step are no longer read
+        if (kDQT) {
+          ok = warp_wait(dq_empty, 0, status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dqt(1);
+        } else if (!STRICT) {
+          if (k > 0) {                         // the previous partial has been read
+            ok = warp_wait(dq_empty, (k - 1) & 1, status);
             if (!ok) break;
             tc_fence_after();
           }
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            // dQ partial = dS^ K (A: the dS^ tile read query-major; B: K keys x d, MN-major)
+            if (leader) mma_mxf8(tbase + kDQ, ds_mn(s * 32 * 128), k_mn(s * 32 * D), idesc_mxf8(128, D, 1, 1, s, s),
+                     tbase + kSFQ, tbase + kSFQ + 4, s > 0);
+          if (leader) mma_commit(dq_full);
+        }
+        if (more) {
+          if (kDQT) {                          // dP of the next step goes where the dQ^T halves were
+            ok = warp_wait(dq_empty, 1, status);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          if (MIXED) {                         // score scale words of step k + 1 were written with the release
+            ok = warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(st1);
+            if (leader) mma_commit(s_full);
+          }
           issue_dp(st1);
-          mma_commit(dp_full);
+          if (leader) mma_commit(dp_full);
         }
       }
-      mma_commit(acc_full);
-      if (!ok) mbar_wait(acc_full, 0, status);
+      if (leader) {
+        mma_commit(acc_full);
+        if (!ok) mbar_wait(acc_full, 0, status);   // nothing of ours still reads SMEM or TMEM
+      }
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ per-query row data
@@ -348,7 +422,7 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
   }
   } else if (compute_wg) {
     // ------------------------------------------------------------ compute (warps 4 .. 4 + 4 kWG - 1)
-    setmaxnreg_inc<BwdShape<D>::kRegHigh>();
+    setmaxnreg_inc<Shape::kRegHigh>();
     const int wg = (warp - 4) >> 2;                    // query columns [32 kCPW wg, 32 kCPW (wg + 1))
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;                 // key row (TMEM lane) for S / dP; query row for dQ
@@ -446,12 +520,12 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
         // scale words of dV += P^^T dO (S^T has been read by every warpgroup): A = P^
         // (1.0; strict: its per-key-row exponents), B = dO per query chunk (strict: 1.0)
         if (STRICT) {
-          tmem_st1(lane_base + kSF + 0 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 64 + j * 4));
-          tmem_st4(lane_base + kSF + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          tmem_st1(lane_base + kSFV + quarter, *reinterpret_cast<const uint32_t*>(Esm + 64 + j * 4));
+          tmem_st4(lane_base + kSFV + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
         } else {
           const uint32_t bw = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
-          tmem_st4(lane_base + kSF + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          tmem_st4(lane_base + kSF + 4, bw, bw, bw, bw);
+          tmem_st4(lane_base + kSFV + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          tmem_st4(lane_base + kSFV + 4, bw, bw, bw, bw);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -506,21 +580,25 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
           const float2 q1 = fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), sc2);
           pk[i >> 2] = (uint32_t)e4m3x2(q0.x, q0.y) | ((uint32_t)e4m3x2(q1.x, q1.y) << 16);
         }
-        *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        // d = 128 (not strict): two 64-query SW64 tiles, the B operands of the dQ^T halves
+        uint8_t* dsrow = kDQT ? sDS + (c >> 1) * 8192 + swz_offset(j, 32 * (c & 1), 64) : sDS + swz_offset(j, 32 * c, 128);
+        uint8_t* dsrow2 = kDQT ? sDS + (c >> 1) * 8192 + swz_offset(j, 32 * (c & 1) + 16, 64)
+                               : sDS + swz_offset(j, 32 * c + 16, 128);
+        *reinterpret_cast<uint4*>(dsrow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(dsrow2) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         if (STRICT) Esm[576 + j * 4 + c] = (uint8_t)(e + 127);
         else if (lane == 0) Esm[quarter * 4 + c] = (uint8_t)(e + 127);
       }
+      fence_proxy_async_smem();              // this thread's dS^ codes, for the MMAs
       named_bar_sync(1, kCompute);           // all block exponents written; S^T and dP^T fully read
       if (STRICT) {
         // A-operand scales are per key row: row j's word sits in lane j, column
         // (base + j / 32), i.e. this warp's quarter; B operands (dO, Q) are folded.
         if (wg == 1 % kWG) {      // dK: A per key row, B (Q) folded
-          tmem_st1(lane_base + kSF + 8 + quarter, *reinterpret_cast<const uint32_t*>(Esm + 576 + j * 4));
-          tmem_st4(lane_base + kSF + 12, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          tmem_st1(lane_base + kSFK + quarter, *reinterpret_cast<const uint32_t*>(Esm + 576 + j * 4));
+          tmem_st4(lane_base + kSFK + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
           tmem_st_wait();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&row_empty[b]);
         mbar_arrive(p_full);
@@ -549,12 +627,22 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
                       (uint32_t)E[3 * 4 + cc] << 24;
             bw = ksf;
           }
-          tmem_st4(lane_base + kSF + 8 * pair, a[0], a[1], a[2], a[3]);
-          tmem_st4(lane_base + kSF + 8 * pair + 4, bw, bw, bw, bw);
+          if (pair == 1) {
+            tmem_st4(lane_base + kSFK, a[0], a[1], a[2], a[3]);
+            tmem_st4(lane_base + kSFK + 4, bw, bw, bw, bw);
+          } else if (kDQT) {
+            // dQ^T: A = K^T (every d row: K's block scales), B = the half's dS^T rows
+            // (query n of half hf: the word of query chunk 2 hf + n / 32)
+            tmem_st4(lane_base + kSFQ, bw, bw, bw, bw);
+            tmem_st4(lane_base + kSFQ + 4, a[0], a[1], a[0], a[1]);
+            tmem_st4(lane_base + kSFQ + 8, a[2], a[3], a[2], a[3]);
+          } else {
+            tmem_st4(lane_base + kSFQ, a[0], a[1], a[2], a[3]);
+            tmem_st4(lane_base + kSFQ + 4, bw, bw, bw, bw);
+          }
         }
         tmem_st_wait();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&row_empty[b]);
       mbar_arrive(p_full);
@@ -562,30 +650,49 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     if (ok) ok = named_bar_and(1, kCompute, mbar_wait(acc_full, 0, status));
     if (ok) {
       tc_fence_after();
+      // dV and dK tiles: each thread stages its row's slice as bf16 in the (now idle) Q
+      // and dO buffers, 16-byte units of row j permuted by XOR with (j mod 8), then the
+      // compute warps copy whole rows of the document's keys out with coalesced stores
+      constexpr int kRowB = D * 2, kUnits = kRowB / 16;
+      static_assert(kQStages * L::kTileBytes == kTile * kRowB, "a stage pair holds one bf16 tile");
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = (which == 0 ? kDV : kDK) + wg * kCols;
         const float mul = which == 0 ? (1.0f / 256.0f) : p.scale;
-        __nv_bfloat16* orow = (which == 0 ? p.dv : p.dk) + (ktok * p.hkv + hk) * D + wg * kCols;
+        uint8_t* stg = smem + (which == 0 ? L::kQ : L::kDO) + j * kRowB;
         uint32_t v[32];
         tmem_ld32(lane_base + col, v);
         tmem_ld_wait();
-        if (key_valid) {
-          uint32_t pk[16];
+        uint32_t pk[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]) * mul, __uint_as_float(v[2 * q + 1]) * mul);
-            pk[q] = *reinterpret_cast<uint32_t*>(&b2);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int q = 0; q < 16; ++q) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]) * mul, __uint_as_float(v[2 * q + 1]) * mul);
+          pk[q] = *reinterpret_cast<uint32_t*>(&b2);
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int unit = (wg * kCols * 2) / 16 + q;
+          *reinterpret_cast<uint4*>(stg + ((unit ^ (j & 7)) << 4)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      named_bar_sync(1, kCompute);
+      const int rows = min(kTile, doc_len - u * kTile);
+      const int64_t row0 = (int64_t)doc_start + u * kTile;
+      for (int idx = threadIdx.x - 128; idx < 2 * rows * kUnits; idx += kCompute) {
+        const int which = idx >= rows * kUnits;
+        const int rem = idx - which * rows * kUnits;
+        const int r = rem / kUnits, unit = rem % kUnits;
+        const uint4 val = *reinterpret_cast<const uint4*>(smem + (which == 0 ? L::kQ : L::kDO) + r * kRowB +
+                                                          ((unit ^ (r & 7)) << 4));
+        __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + ((row0 + r) * p.hkv + hk) * D + unit * 8;
+        *reinterpret_cast<uint4*>(dst) = val;
       }
     }
   } else {
     // ------------------------------------------------------------ dQ readout (the last warpgroup)
-    setmaxnreg_dec<BwdShape<D>::kRegLow>();
+    if constexpr (Shape::kRegRead < Shape::kLaunchRegs) setmaxnreg_dec<Shape::kRegRead>();
+    else setmaxnreg_inc<Shape::kRegRead>();
+    const int ro = (warp - 4 - 4 * kWG) >> 2;         // readout warpgroup
     // Per step: wait for the dQ partial, read it slice by slice (32 head-dim columns,
     // thread = query row), release the TMEM columns, stage c * partial as fp16 in the
     // slice's swizzled SMEM buffer and reduce each slice into its accumulator chunk
@@ -593,36 +700,36 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;                 // query row of the dQ partial (TMEM lane)
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
-    const bool elected = (threadIdx.x & 127) == 0;
-    // mixed route: scale words of the score MMA, written into the first 16 dP columns
-    // before every score MMA, replicated over the four lane quarters (lane 32q + l,
-    // column c holds row 32c + l): K~ rows (A, fixed) and the Q~ rows of the step's
-    // query tile (B); per row and instruction one word of four E4M3 scales
-    uint2 k4w[4] = {}, q4w[4] = {};
-    auto load_sf_rows = [&](const uint8_t* base, int64_t tok0, int H, int hh_, uint2 (&w4)[4]) {
+    const bool elected = ro == 0 && (threadIdx.x & 127) == 0;
+    // mixed route: scale words of the score MMA, written into dP columns before every
+    // score MMA, replicated over the four lane quarters (lane 32q + l, column c holds
+    // row 32c + l); per row and instruction one word of four E4M3 scales.  Readout
+    // warpgroup 0 holds the K~ rows' words (A, fixed, columns 0-7), warpgroup 1 the
+    // Q~ rows' words of the next step's query tile (B, columns 32-39): each writes
+    // only into the dQ^T columns it has itself just read.
+    uint2 sfw[4] = {};
+    auto load_sf_rows = [&](const uint8_t* base, int64_t tok0, int H, int hh_) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int64_t tok = tok0 + 32 * c + lane;
-        w4[c] = tok < p.T ? *reinterpret_cast<const uint2*>(base + (tok * H + hh_) * (D / 16)) : make_uint2(0u, 0u);
+        sfw[c] = tok < p.T ? *reinterpret_cast<const uint2*>(base + (tok * H + hh_) * (D / 16)) : make_uint2(0u, 0u);
       }
     };
-    auto step_qsf = [&](int kk) {
-      load_sf_rows(p.q4_scales, (int64_t)doc_start + (u + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles, q4w);
+    auto step_qsf = [&](int kk) {       // warpgroup 1: the Q~ rows of step kk
+      load_sf_rows(p.q4_scales, (int64_t)doc_start + (u + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles);
     };
     auto store_score_sf = [&]() {
-      tmem_st4(lane_base + kP + 0, k4w[0].x, k4w[1].x, k4w[2].x, k4w[3].x);
-      tmem_st4(lane_base + kP + 4, k4w[0].y, k4w[1].y, k4w[2].y, k4w[3].y);
-      tmem_st4(lane_base + kP + 8, q4w[0].x, q4w[1].x, q4w[2].x, q4w[3].x);
-      tmem_st4(lane_base + kP + 12, q4w[0].y, q4w[1].y, q4w[2].y, q4w[3].y);
+      tmem_st4(lane_base + kP + 32 * ro, sfw[0].x, sfw[1].x, sfw[2].x, sfw[3].x);
+      tmem_st4(lane_base + kP + 32 * ro + 4, sfw[0].y, sfw[1].y, sfw[2].y, sfw[3].y);
     };
     if (MIXED) {
-      load_sf_rows(p.k4_scales, (int64_t)doc_start + u * kTile, p.hkv, hk, k4w);
-      step_qsf(0);
+      if (ro == 0) load_sf_rows(p.k4_scales, (int64_t)doc_start + u * kTile, p.hkv, hk);
+      else step_qsf(0);
       store_score_sf();
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(sf_ready);
-      if (nsteps > 1) step_qsf(1);
+      if (ro == 1 && nsteps > 1) step_qsf(1);
     }
     constexpr int kRowBytes = kCols * 2;               // 64: one staged row of fp16
     constexpr int kChunks = kRowBytes / 16;            // 16-byte units per staged row
@@ -630,53 +737,101 @@ __global__ void __launch_bounds__(BwdShape<D>::kThreads, 1)
     for (int k = 0; k < nsteps && !STRICT; ++k) {
       const int hh = k / qtiles, t = u + k % qtiles;
       const int h = hk * g + hh;
-      const bool qv = t * kTile + i < doc_len;
-      const float cb = qv ? p.boost[(int64_t)doc * p.hq + h] : 0.f;
-      const float2 cb2 = make_float2(cb, cb);
-      ok = named_bar_and(6, 128, mbar_wait(dq_full, k & 1, status));
-      if (!ok) break;
-      tc_fence_after();
+      const float cb = p.boost[(int64_t)doc * p.hq + h];
+      const int qvalid = doc_len - t * kTile;          // query rows of the tile inside the document
+      if constexpr (kDQT) {
+        // dQ^T: thread = head-dim row d = i; per 64-query half this warpgroup reads its
+        // 32 query columns and packs them into four 16-byte units of the staged chunk
+        // (queries past the document end as 0)
+        uint8_t* srow = smem + L::kStage + (k & 1) * (2 * 16384) + i * 128;
+        const uint32_t sw = (uint32_t)(i & 7);
 #pragma unroll 1
-      for (int c = 0; c < kWG; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + kP + 32 * c, v);
-        tmem_ld_wait();
-        if (c == kWG - 1) {                  // the whole partial is in registers or SMEM
-          if (MIXED && k + 1 < nsteps) {
-            store_score_sf();                // q4w holds the rows of step k + 1
+        for (int hf = 0; hf < 2; ++hf) {
+          ok = named_bar_and(6, 128 * kRO, mbar_wait(dq_full, hf, status));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t v[32];
+          tmem_ld32(lane_base + kDQ + 32 * ro, v);
+          tmem_ld_wait();
+          if (MIXED && hf == 1 && k + 1 < nsteps) {
+            store_score_sf();                // warpgroup 1: the Q~ rows of step k + 1
             tmem_st_wait();
           }
           tc_fence_before();
-          mbar_arrive(dq_empty);
-        }
-        uint8_t* sbk = smem + L::kStage + (2 * c + (k & 1)) * L::kStageBytes;
+          mbar_arrive(dq_empty);             // the columns are in registers
+          const int nq = qvalid - hf * 64 - 32 * ro;   // valid queries among the 32
+          const float2 cb2 = make_float2(cb, cb);
 #pragma unroll
-        for (int c16 = 0; c16 < kChunks; ++c16) {
-          uint32_t hw[4];
+          for (int uu = 0; uu < 4; ++uu) {
+            uint32_t w[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = fmul2(make_float2(__uint_as_float(v[8 * c16 + 2 * q]), __uint_as_float(v[8 * c16 + 2 * q + 1])), cb2);
-            __half2 h2 = __floats2half2_rn(f.x, f.y);
-            hw[q] = *reinterpret_cast<uint32_t*>(&h2);
+            for (int e = 0; e < 4; ++e) {
+              const int q = 8 * uu + 2 * e;
+              float2 f = fmul2(make_float2(__uint_as_float(v[q]), __uint_as_float(v[q + 1])), cb2);
+              if (nq < 32) {
+                f.x = q < nq ? f.x : 0.f;
+                f.y = q + 1 < nq ? f.y : 0.f;
+              }
+              __half2 h2 = __floats2half2_rn(f.x, f.y);
+              w[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            const uint32_t unit = (uint32_t)(4 * ro + uu);
+            *reinterpret_cast<uint4*>(srow + hf * 16384 + ((unit ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *reinterpret_cast<uint4*>(sbk + dq_chunk_byte(i, 16 * c16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+        if (!ok) break;
+      } else {
+        const bool qv = i < qvalid;
+        const float2 cb2 = make_float2(qv ? cb : 0.f, qv ? cb : 0.f);
+        ok = named_bar_and(6, 128, mbar_wait(dq_full, k & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kWG; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + kDQ + 32 * c, v);
+          tmem_ld_wait();
+          if (c == kWG - 1) {                // the whole partial is in registers or SMEM
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+          }
+          uint8_t* sbk = smem + L::kStage + (2 * c + (k & 1)) * L::kStageBytes;
+#pragma unroll
+          for (int c16 = 0; c16 < kChunks; ++c16) {
+            uint32_t hw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 f = fmul2(make_float2(__uint_as_float(v[8 * c16 + 2 * q]), __uint_as_float(v[8 * c16 + 2 * q + 1])), cb2);
+              __half2 h2 = __floats2half2_rn(f.x, f.y);
+              hw[q] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(sbk + dq_chunk_byte(i, 16 * c16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          }
         }
       }
-      if (MIXED && k + 2 < nsteps) step_qsf(k + 2);
+      if (MIXED && ro == 1 && k + 2 < nsteps) step_qsf(k + 2);
       fence_proxy_async_smem();
-      named_bar_sync(6, 128);
+      named_bar_sync(6, 128 * kRO);
       if (elected) {
-        // one bulk fp16 reduce-add per slice; the wait leaves at most this step's copies
-        // reading shared memory, so the other buffers are free next step
+        // bulk fp16 reduce-adds of the staged tile (d = 128: one 32 KB chunk; d = 64: one
+        // per slice); the wait leaves at most this step's copies reading shared memory,
+        // so the other buffer is free next step
         const int64_t tile = pv.tile_prefix[doc] + t;
-        for (int c = 0; c < kWG; ++c)
-          bulk_reduce_add_f16(p.dq_acc + dq_chunk_elems(tile, h, c, p.hq, D),
-                              smem_u32(smem + L::kStage + (2 * c + (k & 1)) * L::kStageBytes), L::kStageBytes);
+        if constexpr (kDQT) {
+          bulk_reduce_add_f16(p.dq_acc + dqt_chunk_elems(tile, h, p.hq),
+                              smem_u32(smem + L::kStage + (k & 1) * (2 * 16384)), 2 * 16384);
+        } else {
+          for (int c = 0; c < kWG; ++c)
+            bulk_reduce_add_f16(p.dq_acc + dq_chunk_elems(tile, h, c, p.hq, D),
+                                smem_u32(smem + L::kStage + (2 * c + (k & 1)) * L::kStageBytes), L::kStageBytes);
+        }
         bulk_commit();
         bulk_wait_read<1>();
       }
     }
-    if (elected) bulk_wait_all();
+    // shared memory stays valid until the copies have read it; their global adds
+    // complete before the kernel does (the finalize kernel runs after it)
+    if (elected) bulk_wait_read<0>();
   }
   tc_fence_before();
   __syncthreads();
@@ -745,6 +900,55 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const __half* acc, con
     }
   }
   // rows outside every document
+  const int64_t tq = (int64_t)(T - valid) * hq * kVpr, tk = (int64_t)(T - valid) * hkv * kVpr;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < tq + 2 * tk;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < tq) reinterpret_cast<uint4*>(dq)[(int64_t)valid * hq * kVpr + i] = make_uint4(0, 0, 0, 0);
+    else if (i < tq + tk) reinterpret_cast<uint4*>(dk)[(int64_t)valid * hkv * kVpr + (i - tq)] = make_uint4(0, 0, 0, 0);
+    else reinterpret_cast<uint4*>(dv)[(int64_t)valid * hkv * kVpr + (i - tq - tk)] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// d = 128 (default and mixed routes): as dq_finalize_kernel for the head-dim-major
+// dQ^T chunks.  Thread = (query half, head-dim row d): it reads its row's 16-byte
+// units and writes each query's element, a warp covering 32 consecutive d of one
+// output row per store.
+__global__ void __launch_bounds__(256) dqt_finalize_kernel(const __half* acc, const int32_t* cu, const int* plan,
+                                                           const float* boost, int N, int T, int hq, int hkv,
+                                                           float scale, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                                                           __nv_bfloat16* dv) {
+  constexpr int D = 128;
+  const bool bad = plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS;
+  const int valid = bad ? 0 : plan[kPlanValid];
+  const int ntiles = bad ? 0 : plan[kPlanTiles];
+  const PlanView pv = plan_view(plan, T, N);
+  const int hf = threadIdx.x >> 7, d = threadIdx.x & 127;
+  const int64_t units = (int64_t)ntiles * hq;
+  for (int64_t un = blockIdx.x; un < units; un += gridDim.x) {
+    const int tile = (int)(un / hq), h = (int)(un % hq);
+    const int doc = upper_doc(pv.tile_prefix, N, tile);
+    const int t = tile - pv.tile_prefix[doc];
+    const int s0 = cu[doc];
+    const int rows = min(kTile, cu[doc + 1] - s0 - t * kTile);
+    const float mul = scale / boost[(int64_t)doc * hq + h];
+    const uint8_t* chunk = reinterpret_cast<const uint8_t*>(acc + dqt_chunk_elems(tile, h, hq));
+    __nv_bfloat16* out = dq + (((int64_t)s0 + t * kTile + hf * 64) * hq + h) * D + d;
+#pragma unroll 2
+    for (int u = 0; u < 8; ++u) {
+      const int q0 = hf * 64 + u * 8;
+      if (q0 >= rows) break;
+      const uint4 in = *reinterpret_cast<const uint4*>(chunk + dqt_chunk_byte(hf, d, u));
+      const __half2* hv = reinterpret_cast<const __half2*>(&in);
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        const float2 f = __half22float2(hv[e2]);
+        const int q = q0 + 2 * e2;
+        if (q < rows) out[(int64_t)(u * 8 + 2 * e2) * hq * D] = __float2bfloat16_rn(f.x * mul);
+        if (q + 1 < rows) out[(int64_t)(u * 8 + 2 * e2 + 1) * hq * D] = __float2bfloat16_rn(f.y * mul);
+      }
+    }
+  }
+  constexpr int kVpr = D / 8;
   const int64_t tq = (int64_t)(T - valid) * hq * kVpr, tk = (int64_t)(T - valid) * hkv * kVpr;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < tq + 2 * tk;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -1177,15 +1381,18 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   if (e != cudaSuccess) return e;
   // the warpgroups' register split (setmaxnreg) assumes this launch allocation;
   // with any other the increase could never be granted, so refuse to launch
-  if (regs != BwdShape<D>::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (regs != BwdShape<D, STRICT>::kLaunchRegs) return cudaErrorInvalidConfiguration;
   if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
   attn_bwd_kernel<D, STRICT, MIXED>
-      <<<(unsigned)grid, BwdShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
+      <<<(unsigned)grid, BwdShape<D, STRICT>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
   e = cudaGetLastError();
   if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
   if (ev && ev[2]) cudaEventRecord(static_cast<cudaEvent_t>(ev[2]), stream);
-  if (!STRICT) {
+  if (!STRICT && D == 128) {
+    dqt_finalize_kernel<<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
+                                                     hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
+  } else if (!STRICT) {
     dq_finalize_kernel<D><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
                                                        hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
   } else {

@@ -40,9 +40,9 @@ struct PlanView {
 };
 
 __host__ __device__ inline int64_t plan_capacity(int64_t T, int N) { return T / kTile + N + 1; }
-// fp16 dQ accumulator of the default backward (workspace-internal layout): one
-// contiguous 8 KB chunk per (document tile, query head, 32-column slice of the
-// head dim), tile = tile_prefix[doc] + document-local tile index.  A chunk holds
+// fp16 dQ accumulator of the default backward at head_dim 64 (workspace-internal
+// layout): one contiguous 8 KB chunk per (document tile, query head, 32-column
+// slice of the head dim), tile = tile_prefix[doc] + document-local tile index.  A chunk holds
 // the tile's 128 rows of 32 fp16 (64 bytes each) with the 16-byte units of every
 // row permuted by the 64-byte TMA/UMMA swizzle, the layout in which the backward
 // stages a slice in shared memory and reduces it with one bulk copy.
@@ -53,6 +53,17 @@ __host__ __device__ inline size_t dq_chunk_elems(int64_t tile, int h, int slice,
 __host__ __device__ inline uint32_t dq_chunk_byte(int r, int col_byte) {
   const uint32_t lin = (uint32_t)r * 64u + (uint32_t)col_byte;
   return lin ^ (((lin >> 7) & 3u) << 4);
+}
+// At head_dim 128 (default and mixed routes) the backward produces dQ^T, so the
+// accumulator is head-dim-major: one contiguous 32 KB chunk per (document tile,
+// query head) of [query half hf][head-dim row d][64 queries] fp16, the eight
+// 16-byte units of each 128-byte row permuted by XOR with (d mod 8).
+__host__ __device__ inline size_t dqt_chunk_elems(int64_t tile, int h, int hq) {
+  return ((size_t)tile * hq + h) * (size_t)(kTile * 128);
+}
+// Byte offset of 16-byte unit `unit` (queries 64 hf + 8 unit .. + 7) of row d.
+__host__ __device__ inline uint32_t dqt_chunk_byte(int hf, int d, int unit) {
+  return (uint32_t)hf * 16384u + (uint32_t)d * 128u + ((uint32_t)(unit ^ (d & 7)) << 4);
 }
 __host__ __device__ inline size_t dq_acc_bytes(int64_t T, int N, int hq, int D) {
   return (size_t)plan_capacity(T, N) * hq * D * kTile * 2;
