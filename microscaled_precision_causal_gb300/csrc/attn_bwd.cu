@@ -377,41 +377,49 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ per-query row data
+    // Every global load of a step is issued into registers before the wait for the
+    // buffer and before any shared-memory store, so the latencies overlap each other
+    // and the wait instead of queueing behind stores the compiler cannot reorder.
     for (int k = 0; k < nsteps; ++k) {
       const int b = k & 1;
-      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&row_empty[b], ((k >> 1) - 1) & 1, status))) break;
       const int h = hk * g + k / qtiles, t = u + k % qtiles;
+      float lv[4], dv[4], sqv[4], sdv[4];
+      uint8_t scb = 127;
+      float bst = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ql = t * kTile + q * 32 + lane;
+        const bool qv = ql < doc_len;
+        const int64_t qtok = (int64_t)doc_start + ql;
+        lv[q] = qv ? __ldg(p.lse + (int64_t)h * p.T + qtok) : 0.f;
+        dv[q] = qv ? __ldg(p.dvec + (int64_t)h * p.T + qtok) : 0.f;
+        if (STRICT) {
+          sqv[q] = qv ? ue8m0_to_f32(__ldg(p.q_scales + qtok * p.hq + h)) : 1.0f;
+          sdv[q] = qv ? ue8m0_to_f32(__ldg(p.do_scales + qtok * p.hq + h)) : 1.0f;
+        }
+      }
+      if (lane < 8) {
+        const int ql = t * kTile + (lane & 3) * 32;
+        const uint8_t* src = lane < 4 ? p.q_scales : p.do_scales;
+        if (ql < doc_len) scb = __ldg(src + ((int64_t)doc_start + ql) * p.hq + h);
+      }
+      if (lane == 8 && !STRICT) bst = __ldg(p.boost + (int64_t)doc * p.hq + h);   // dQ boost of (document, query head)
+      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&row_empty[b], ((k >> 1) - 1) & 1, status))) break;
       float* rb = rowbuf + b * (L::kRowBuf / 4);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int i = q * 32 + lane;
-        const int ql = t * kTile + i;
-        const bool qv = ql < doc_len;
-        const int64_t qtok = (int64_t)doc_start + ql;
+        const bool qv = t * kTile + i < doc_len;
         // the P boost 2^8 rides in the exponent; dP - D is scaled by 2^-8 to compensate
-        rb[i] = qv ? fmaf(-p.lse[(int64_t)h * p.T + qtok], 1.4426950408889634f, 8.0f) : -INFINITY;
-        rb[128 + i] = qv ? -p.dvec[(int64_t)h * p.T + qtok] * (1.0f / 256.0f) : 0.f;
-      }
-      if (lane == 8 && !STRICT) rb[258] = p.boost[(int64_t)doc * p.hq + h];   // dQ boost of (document, query head)
-      if (STRICT) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i = q * 32 + lane;
-          const int ql = t * kTile + i;
-          const bool qv = ql < doc_len;
-          const int64_t qtok = (int64_t)doc_start + ql;
-          rb[260 + i] = qv ? ue8m0_to_f32(p.q_scales[qtok * p.hq + h]) : 1.0f;
-          rb[388 + i] = qv ? ue8m0_to_f32(p.do_scales[qtok * p.hq + h]) : 1.0f;
+        rb[i] = qv ? fmaf(-lv[q], 1.4426950408889634f, 8.0f) : -INFINITY;
+        rb[128 + i] = qv ? -dv[q] * (1.0f / 256.0f) : 0.f;
+        if (STRICT) {
+          rb[260 + i] = sqv[q];
+          rb[388 + i] = sdv[q];
         }
       }
-      if (lane < 8) {
-        const int c = lane & 3;
-        const int ql = t * kTile + c * 32;
-        const bool qv = ql < doc_len;
-        const int64_t qtok = (int64_t)doc_start + ql;
-        const uint8_t* src = lane < 4 ? p.q_scales : p.do_scales;
-        reinterpret_cast<uint8_t*>(rb + 256)[lane] = qv ? src[qtok * p.hq + h] : (uint8_t)127;
-      }
+      if (lane == 8 && !STRICT) rb[258] = bst;
+      if (lane < 8) reinterpret_cast<uint8_t*>(rb + 256)[lane] = scb;
       mbar_arrive(&row_full[b]);
     }
   }
