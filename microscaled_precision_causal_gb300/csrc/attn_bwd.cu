@@ -31,17 +31,15 @@
 //               columns of the dK / dV accumulators
 //   last WG     dQ readout: TMEM -> fp16 staging -> bulk reduce into the accumulator
 // Thread = key row while building P^ and dS^ codes.  TMEM: S^T [0,128), dP^T
-// [128,256), dV [256, 256+D), dK [384, 384+D).  At d = 128 TMEM is full, so dQ^T
-// takes dP^T's columns once dS^ is built; at d = 64 the dQ partial has [320, 384).
-// Block-scale words: dV's in S^T's columns [104, 112) (written once S^T has been
-// read), dK's in dP^T's [104, 112) (written once dP^T has been read), dQ's in S^T's
-// [112, 120) at d = 128 and in [448, 456) at d = 64.  Per step the MMA warp issues
-// dV(k) as soon as P^ is in SMEM, then dK(k) and dQ(k) once dS^ is; S^T(k+1) follows
-// dV(k) at d = 64 and dQ^T(k) at d = 128 (either way the exponentials of the next
-// step wait only for MMAs, not for the dQ readout), and dP^T(k+1) follows once the
-// dQ columns have been read, in time for the next dS^.  The mixed route's S~ MMA
-// (NVFP4) takes its scale words from dP^T's columns and so is issued after the
-// readout too.
+// [128,256), dV [256, 256+D), dK [384, 384+D).  At d = 128 the dQ^T halves take
+// dP^T's first 64 columns once dS^ is built; at d = 64 the dQ partial has
+// [320, 384).  Block-scale words: dV's in S^T's columns [104, 112) (written once
+// S^T has been read), dK's and dQ's in dP^T's columns [104, 124) (written once
+// dP^T has been read; at d = 64 dQ's in [448, 456)).  Per step the MMA thread
+// issues dV(k) as soon as P^ is in SMEM, then S^T(k+1) (the exponentials of the
+// next step overlap the dS^ work of this one), then dK(k), dQ(k) and dP^T(k+1)
+// once the dQ columns have been read.  The mixed route's S~ MMA (NVFP4) takes its
+// scale words from dP^T's first 16 columns and so is issued late, after dQ.
 #include <type_traits>
 
 #include "common.cuh"
@@ -202,17 +200,16 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   const bool compute_wg = warp >= 4 && warp < 4 + 4 * kWG;
   const uint32_t tbase = *tmem_slot;
   constexpr uint32_t kS = 0, kP = 128, kDV = 256, kDK = 384;
-  // dQ: at d = 128 (default and mixed routes) TMEM is full (S, dP, dV, dK), so dQ^T =
-  // K^T dS^T takes the dP columns once dS^ is built, and the next S^T is issued right
-  // after it; at d = 64 the query-major dQ partial has free columns and the next S^T
-  // goes right after dV.  Block-scale words: dV's in S^T's columns (written after P),
-  // dK's in dP^T's (written after dS, read before dQ^T overwrites them), d = 128 dQ's
-  // in S^T's (written after dS, read before the next S^T overwrites them).
+  // dQ: at d = 128 (default and mixed routes) dQ^T = K^T dS^T in two 64-query halves
+  // into the first 64 dP columns (TMEM is full: S, dP, dV, dK); at d = 64 the
+  // query-major dQ partial sits in free columns.  Block-scale words: dV's in the S
+  // columns (written after P), dK's and dQ's in the dP columns (written after dS),
+  // so S of the next step can be issued right after dV.
   constexpr bool kDQT = D == 128 && !STRICT;
   constexpr uint32_t kDQ = D == 128 ? kP : 320;
   constexpr uint32_t kSFV = kS + 104;       // dV: A 4 words, B 4 words
   constexpr uint32_t kSFK = kP + 104;       // dK: A 4, B 4
-  constexpr uint32_t kSFQ = D == 128 ? kS + 112 : 448;   // dQ: A 4, B 4
+  constexpr uint32_t kSFQ = D == 128 ? kP + 112 : 448;   // dQ: A 4, B 4 (d = 128: B lo 4, B hi 4)
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
   constexpr uint32_t kAtom = 8 * D;
   float* rowbuf = reinterpret_cast<float*>(smem + L::kRow);
@@ -247,6 +244,8 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     {
       // operand descriptors: every tile sits at a compile-time offset from the aligned
       // SMEM base, so each descriptor is one add on base16
+      constexpr uint32_t kDS64 = kDQT ? kSwizzle64B : kSwizzle128B;
+      constexpr uint32_t kDSR = kDQT ? 512 : 1024;       // dS^ 8-row group stride
       const uint32_t base16 = (smem_u32(smem) & 0x3FFFFu) >> 4;
       // base16 re-read at every use, so that the compiler does not hoist the ~20
       // descriptor words out of the step loop into the issuer's few registers
@@ -263,18 +262,20 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       auto do_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kDO + o, 16, kAtom, kLayout); };      // dP^T: B
       auto do_mn = [&](uint32_t o) { return sdesc_at(b16(), L::kDO + o, kAtom, kAtom, kLayout); };     // dV: B
       auto pt_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kPt + o, 16, 1024, kSwizzle128B); };  // dV: A
-      // dS^ [key][query]: dK's A (K-major) and dQ's operand read query-major
-      auto ds_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kDS + o, 16, 1024, kSwizzle128B); };
-      auto ds_mn = [&](uint32_t o) { return sdesc_at(b16(), L::kDS + o, 1024, 1024, kSwizzle128B); };
+      // dS^: dK's A (keys x queries, K-major) and dQ's operand read query-major (at d = 128
+      // two 64-query SW64 tiles, the B operands of the dQ^T halves)
+      auto ds_kmaj = [&](uint32_t o) { return sdesc_at(b16(), L::kDS + o, 16, kDSR, kDS64); };
+      auto ds_mn = [&](uint32_t o) { return sdesc_at(b16(), L::kDS + o, kDSR, kDSR, kDS64); };
       auto issue_s = [&](int st) {
         if constexpr (MIXED) {
           // S^T = K~ Q~^T from the NVFP4 copies (64 E2M1 elements per instruction); the
-          // scale words sit in dP columns 0-7 (K~) and 64-71 (Q~), free once dQ^T was read
+          // scale words sit in dP columns 0-7 (K~) and 32-39 (Q~), free once the dQ^T
+          // high half was read
 #pragma unroll
           for (int s = 0; s < 2; ++s)
             if (leader) mma_nvf4(tbase + kS, sdesc_at(b16(), L::kK4 + 32 * s, 16, 8 * 64, kSwizzle64B),
                      sdesc_at(b16(), L::kQ4 + st * L::kScoreBytes + 32 * s, 16, 8 * 64, kSwizzle64B),
-                     idesc_nvf4(128, 128), tbase + kP + 4 * s, tbase + kP + 64 + 4 * s, s > 0);
+                     idesc_nvf4(128, 128), tbase + kP + 4 * s, tbase + kP + 32 + 4 * s, s > 0);
         } else {
 #pragma unroll
           for (int s = 0; s < D / 32; ++s)
@@ -285,6 +286,15 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
 #pragma unroll
         for (int s = 0; s < D / 32; ++s)
           if (leader) mma_f8(tbase + kP, v_kmaj(32 * s), do_kmaj(st * L::kTileBytes + 32 * s), idesc_f8(128, 128, 0, 0), s > 0);
+      };
+      // dQ^T = K^T dS^T per 64-query half (A: K keys x d read d-major; B: the half's
+      // dS^ tile, queries contiguous)
+      auto issue_dqt = [&](int hf) {
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (leader) mma_mxf8(tbase + kDQ, k_mn(s * 32 * D), ds_mn(hf * 8192 + s * 32 * 64), idesc_mxf8(128, 64, 1, 1, s, s),
+                   tbase + kSFQ, tbase + kSFQ + 4 + 4 * hf, s > 0);
+        if (leader) mma_commit(dq_full);
       };
       bool ok = warp_wait(kv_full, 0, status) && warp_wait(&qd_full[0], 0, status);
       if (ok && MIXED) ok = warp_wait(sf_ready, 0, status);
@@ -299,17 +309,19 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         const int st = k % kQStages;
         const int st1 = (k + 1) % kQStages;
         const bool more = k + 1 < nsteps;
-        // dV as soon as P^ is in SMEM; at d = 64 and under the strict options S of the next
-        // step follows straight away (it runs while the compute warpgroups build dS^)
+        // dV as soon as P^ is in SMEM; then (not mixed) S of the next step, which runs
+        // while the compute warpgroups build dS^
         ok = warp_wait(pt_full, k & 1, status);
         if (!ok) break;
         tc_fence_after();
+        {
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-          // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
-          if (leader) mma_mxf8(tbase + kDV, pt_kmaj(32 * s), do_mn(st * L::kTileBytes + s * 32 * D),
-                               idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFV, tbase + kSFV + 4, (k > 0 || s > 0));
-        if (!kDQT && more) {
+          for (int s = 0; s < 4; ++s)
+            // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
+            if (leader) mma_mxf8(tbase + kDV, pt_kmaj(32 * s), do_mn(st * L::kTileBytes + s * 32 * D), idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFV,
+                     tbase + kSFV + 4, (k > 0 || s > 0));
+        }
+        if (!MIXED && more) {
           ok = warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
           if (!ok) break;
           tc_fence_after();
@@ -319,27 +331,22 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         ok = warp_wait(p_full, k & 1, status);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          // dK += dS^^T Q (A: dS^ keys x queries K-major)
-          if (leader) mma_mxf8(tbase + kDK, ds_kmaj(32 * s), q_mn(st * L::kTileBytes + s * 32 * D),
-                               idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFK, tbase + kSFK + 4, (k > 0 || s > 0));
-        if (leader) mma_commit(&qd_empty[st]);             // Q and dO of this step are no longer read
-        if (kDQT) {
+        // the low dQ^T half goes first so that its readout overlaps dK; the high half
+        // follows once the readout released the columns
+        if (kDQT) issue_dqt(0);
+        {
 #pragma unroll
           for (int s = 0; s < 4; ++s)
-            // dQ^T = K^T dS^^T (A: K keys x d read d-major; B: dS^ keys x queries, queries
-            // contiguous) into the dP columns, which dS^ no longer needs
-            if (leader) mma_mxf8(tbase + kDQ, k_mn(s * 32 * D), ds_mn(s * 32 * 128), idesc_mxf8(128, 128, 1, 1, s, s),
-                                 tbase + kSFQ, tbase + kSFQ + 4, s > 0);
-          if (leader) mma_commit(dq_full);
-          if (!MIXED && more) {                // S of the next step, while dQ^T is read out
-            ok = warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(st1);
-            if (leader) mma_commit(s_full);
-          }
+            // dK += dS^^T Q (A: dS^ keys x queries K-major)
+            if (leader) mma_mxf8(tbase + kDK, ds_kmaj(kDQT ? (s >> 1) * 8192 + 32 * (s & 1) : 32 * s), q_mn(st * L::kTileBytes + s * 32 * D),
+                     idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFK, tbase + kSFK + 4, (k > 0 || s > 0));
+        }
+        if (leader) mma_commit(&qd_empty[st]);             // Q and dO of this step are no longer read
+        if (kDQT) {
+          ok = warp_wait(dq_empty, 0, status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dqt(1);
         } else if (!STRICT) {
           if (k > 0) {                         // the previous partial has been read
             ok = warp_wait(dq_empty, (k - 1) & 1, status);
@@ -350,12 +357,12 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           for (int s = 0; s < 4; ++s)
             // dQ partial = dS^ K (A: the dS^ tile read query-major; B: K keys x d, MN-major)
             if (leader) mma_mxf8(tbase + kDQ, ds_mn(s * 32 * 128), k_mn(s * 32 * D), idesc_mxf8(128, D, 1, 1, s, s),
-                                 tbase + kSFQ, tbase + kSFQ + 4, s > 0);
+                     tbase + kSFQ, tbase + kSFQ + 4, s > 0);
           if (leader) mma_commit(dq_full);
         }
         if (more) {
-          if (kDQT) {                          // dP of the next step goes where dQ^T was
-            ok = warp_wait(dq_empty, k & 1, status);
+          if (kDQT) {                          // dP of the next step goes where the dQ^T halves were
+            ok = warp_wait(dq_empty, 1, status);
             if (!ok) break;
             tc_fence_after();
           }
@@ -589,8 +596,12 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           const float2 q1 = fmul2(make_float2(pr[cc][i + 2], pr[cc][i + 3]), sc2);
           pk[i >> 2] = (uint32_t)e4m3x2(q0.x, q0.y) | ((uint32_t)e4m3x2(q1.x, q1.y) << 16);
         }
-        *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(sDS + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        // d = 128 (not strict): two 64-query SW64 tiles, the B operands of the dQ^T halves
+        uint8_t* dsrow = kDQT ? sDS + (c >> 1) * 8192 + swz_offset(j, 32 * (c & 1), 64) : sDS + swz_offset(j, 32 * c, 128);
+        uint8_t* dsrow2 = kDQT ? sDS + (c >> 1) * 8192 + swz_offset(j, 32 * (c & 1) + 16, 64)
+                               : sDS + swz_offset(j, 32 * c + 16, 128);
+        *reinterpret_cast<uint4*>(dsrow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(dsrow2) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         if (STRICT) Esm[576 + j * 4 + c] = (uint8_t)(e + 127);
         else if (lane == 0) Esm[quarter * 4 + c] = (uint8_t)(e + 127);
       }
@@ -636,10 +647,11 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
             tmem_st4(lane_base + kSFK, a[0], a[1], a[2], a[3]);
             tmem_st4(lane_base + kSFK + 4, bw, bw, bw, bw);
           } else if (kDQT) {
-            // dQ^T: A = K^T (every d row: K's block scales), B = dS^T rows (query n: the
-            // word of query chunk n / 32)
+            // dQ^T: A = K^T (every d row: K's block scales), B = the half's dS^T rows
+            // (query n of half hf: the word of query chunk 2 hf + n / 32)
             tmem_st4(lane_base + kSFQ, bw, bw, bw, bw);
-            tmem_st4(lane_base + kSFQ + 4, a[0], a[1], a[2], a[3]);
+            tmem_st4(lane_base + kSFQ + 4, a[0], a[1], a[0], a[1]);
+            tmem_st4(lane_base + kSFQ + 8, a[2], a[3], a[2], a[3]);
           } else {
             tmem_st4(lane_base + kSFQ, a[0], a[1], a[2], a[3]);
             tmem_st4(lane_base + kSFQ + 4, bw, bw, bw, bw);
@@ -709,7 +721,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     // score MMA, replicated over the four lane quarters (lane 32q + l, column c holds
     // row 32c + l); per row and instruction one word of four E4M3 scales.  Readout
     // warpgroup 0 holds the K~ rows' words (A, fixed, columns 0-7), warpgroup 1 the
-    // Q~ rows' words of the next step's query tile (B, columns 64-71): each writes
+    // Q~ rows' words of the next step's query tile (B, columns 32-39): each writes
     // only into the dQ^T columns it has itself just read.
     uint2 sfw[4] = {};
     auto load_sf_rows = [&](const uint8_t* base, int64_t tok0, int H, int hh_) {
@@ -723,8 +735,8 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       load_sf_rows(p.q4_scales, (int64_t)doc_start + (u + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles);
     };
     auto store_score_sf = [&]() {
-      tmem_st4(lane_base + kP + 64 * ro, sfw[0].x, sfw[1].x, sfw[2].x, sfw[3].x);
-      tmem_st4(lane_base + kP + 64 * ro + 4, sfw[0].y, sfw[1].y, sfw[2].y, sfw[3].y);
+      tmem_st4(lane_base + kP + 32 * ro, sfw[0].x, sfw[1].x, sfw[2].x, sfw[3].x);
+      tmem_st4(lane_base + kP + 32 * ro + 4, sfw[0].y, sfw[1].y, sfw[2].y, sfw[3].y);
     };
     if (MIXED) {
       if (ro == 0) load_sf_rows(p.k4_scales, (int64_t)doc_start + u * kTile, p.hkv, hk);
@@ -744,29 +756,27 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       const float cb = p.boost[(int64_t)doc * p.hq + h];
       const int qvalid = doc_len - t * kTile;          // query rows of the tile inside the document
       if constexpr (kDQT) {
-        // dQ^T: thread = head-dim row d = i; readout warpgroup ro reads the 64 query
-        // columns of half ro, 32 at a time, and packs each into four 16-byte units of
-        // its row of the staged chunk (queries past the document end as 0)
-        uint8_t* srow = smem + L::kStage + (k & 1) * (2 * 16384) + ro * 16384 + i * 128;
+        // dQ^T: thread = head-dim row d = i; per 64-query half this warpgroup reads its
+        // 32 query columns and packs them into four 16-byte units of the staged chunk
+        // (queries past the document end as 0)
+        uint8_t* srow = smem + L::kStage + (k & 1) * (2 * 16384) + i * 128;
         const uint32_t sw = (uint32_t)(i & 7);
-        ok = named_bar_and(6, 128 * kRO, mbar_wait(dq_full, k & 1, status));
-        if (!ok) break;
-        tc_fence_after();
-        const float2 cb2 = make_float2(cb, cb);
 #pragma unroll 1
-        for (int gq = 0; gq < 2; ++gq) {
+        for (int hf = 0; hf < 2; ++hf) {
+          ok = named_bar_and(6, 128 * kRO, mbar_wait(dq_full, hf, status));
+          if (!ok) break;
+          tc_fence_after();
           uint32_t v[32];
-          tmem_ld32(lane_base + kDQ + 64 * ro + 32 * gq, v);
+          tmem_ld32(lane_base + kDQ + 32 * ro, v);
           tmem_ld_wait();
-          if (gq == 1) {
-            if (MIXED && k + 1 < nsteps) {
-              store_score_sf();              // into this warpgroup's own (read) columns
-              tmem_st_wait();
-            }
-            tc_fence_before();
-            mbar_arrive(dq_empty);           // this warpgroup's columns are read
+          if (MIXED && hf == 1 && k + 1 < nsteps) {
+            store_score_sf();                // warpgroup 1: the Q~ rows of step k + 1
+            tmem_st_wait();
           }
-          const int nq = qvalid - 64 * ro - 32 * gq;   // valid queries among the 32
+          tc_fence_before();
+          mbar_arrive(dq_empty);             // the columns are in registers
+          const int nq = qvalid - hf * 64 - 32 * ro;   // valid queries among the 32
+          const float2 cb2 = make_float2(cb, cb);
           auto stage = [&](auto tail) {                  // built twice: the mask only at a document end
             constexpr bool kTail = decltype(tail)::value;
 #pragma unroll
@@ -783,8 +793,8 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
                 __half2 h2 = __floats2half2_rn(f.x, f.y);
                 w[e] = *reinterpret_cast<uint32_t*>(&h2);
               }
-              const uint32_t unit = (uint32_t)(4 * gq + uu);
-              *reinterpret_cast<uint4*>(srow + ((unit ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              const uint32_t unit = (uint32_t)(4 * ro + uu);
+              *reinterpret_cast<uint4*>(srow + hf * 16384 + ((unit ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
           };
           if (nq < 32) stage(std::true_type{});
