@@ -13,7 +13,8 @@
 // One CTA per (work item, query head): a work item is up to two document-local
 // 128-query tiles (Algorithm 2 step 03).  Roles (384 threads):
 //   warp 0      TMA producer: both Q tiles once, then K/V tiles through a ring
-//   warp 1      MMA issuer (one thread): S_w = Q_w K^T and O_w += P^_w V
+//   warp 1      MMA issuer (converged warp, one elected lane issues): S_w = Q_w K^T
+//               and O_w += P^_w V
 //   warp 2      TMEM allocator
 //   warps 4-7   softmax warpgroup 0 (query tile t0), thread = query row
 //   warps 8-11  softmax warpgroup 1 (query tile t0 + 1)
@@ -23,6 +24,8 @@
 // The block-scale words of the PV MMA live in the last 8 columns of the
 // warpgroup's S region (written after S was read; the next S MMA is issued
 // after the PV MMA by the same thread, and tcgen05 MMAs run in issue order).
+#include <type_traits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -175,62 +178,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, status);
-      const uint32_t sq = smem_u32(smem + L::kQ), sk = smem_u32(smem + L::kK), sv = smem_u32(smem + L::kV),
-                     sp = smem_u32(smem + L::kP);
+    // The warp runs the loop converged (every lane waits); the elected lane issues
+    // the MMAs and the commits.  Every tile sits at a compile-time offset from the
+    // aligned SMEM base, so each descriptor is one add on base16 (re-read at every
+    // use so that the compiler does not hoist the descriptor words into registers).
+    const bool leader = elect_one();
+    {
+      const uint32_t base16 = (smem_u32(smem) & 0x3FFFFu) >> 4;
+      auto b16 = [&]() {
+        uint32_t x;
+        asm volatile("mov.b32 %0, %1;" : "=r"(x) : "r"(base16));
+        return x;
+      };
+      bool ok = warp_wait(q_full, 0, status);
       auto issue_s = [&](int w, int u) {
         const int st = u % kStages;
-        const uint32_t qa = sq + w * L::kTileBytes, ka = sk + st * L::kTileBytes;
 #pragma unroll
-        for (int s = 0; s < D / 32; ++s) {
-          mma_f8(tbase + kSCol[w], smem_desc(qa + 32 * s, 16, kAtom, kLayout),
-                 smem_desc(ka + 32 * s, 16, kAtom, kLayout), idesc_f8(128, 128, 0, 0), s > 0);
-        }
+        for (int s = 0; s < D / 32; ++s)
+          if (leader)
+            mma_f8(tbase + kSCol[w], sdesc_at(b16(), L::kQ + w * L::kTileBytes + 32 * s, 16, kAtom, kLayout),
+                   sdesc_at(b16(), L::kK + st * L::kTileBytes + 32 * s, 16, kAtom, kLayout), idesc_f8(128, 128, 0, 0),
+                   s > 0);
       };
       auto issue_pv = [&](int w, int u) {
         const int st = u % kStages;
-        const uint32_t pa = sp + w * kTile * kTile, va = sv + st * L::kTileBytes;
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          mma_mxf8(tbase + kOCol[w], smem_desc(pa + 32 * s, 16, 1024, kSwizzle128B),
-                   smem_desc(va + s * 32 * kRowBytes, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
-                   tbase + kSCol[w] + 120, tbase + kSCol[w] + 124, (u > 0 || s > 0));
-        }
+        for (int s = 0; s < 4; ++s)
+          if (leader)
+            mma_mxf8(tbase + kOCol[w], sdesc_at(b16(), L::kP + w * kTile * kTile + 32 * s, 16, 1024, kSwizzle128B),
+                     sdesc_at(b16(), L::kV + st * L::kTileBytes + s * 32 * kRowBytes, kAtom, kAtom, kLayout),
+                     idesc_mxf8(128, D, 0, 1, s, s), tbase + kSCol[w] + 120, tbase + kSCol[w] + 124, (u > 0 || s > 0));
       };
-      if (ok) ok = mbar_wait(&kv_full[0], 0, status);
+      if (ok) ok = warp_wait(&kv_full[0], 0, status);
       if (ok) {
         tc_fence_after();
         for (int w = 0; w < ntq; ++w) {
           issue_s(w, 0);
-          mma_commit(&s_full[w]);
+          if (leader) mma_commit(&s_full[w]);
         }
         for (int u = 0; u < nkv && ok; ++u) {
           bool next_loaded = false;
           for (int w = 0; w < ntq && ok; ++w) {
             if (u >= nk_w[w]) continue;
-            ok = mbar_wait(&p_full[w], u & 1, status);
+            ok = warp_wait(&p_full[w], u & 1, status);
             if (!ok) break;
             tc_fence_after();
             issue_pv(w, u);
             if (u + 1 < nk_w[w]) {
               if (!next_loaded) {
                 const int st = (u + 1) % kStages;
-                ok = mbar_wait(&kv_full[st], ((u + 1) / kStages) & 1, status);
+                ok = warp_wait(&kv_full[st], ((u + 1) / kStages) & 1, status);
                 if (!ok) break;
                 tc_fence_after();
                 next_loaded = true;
               }
               issue_s(w, u + 1);
-              mma_commit(&s_full[w]);
+              if (leader) mma_commit(&s_full[w]);
             } else {
-              mma_commit(&o_full[w]);
+              if (leader) mma_commit(&o_full[w]);
             }
           }
-          mma_commit(&kv_empty[u % kStages]);
+          if (leader) mma_commit(&kv_empty[u % kStages]);
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // timed out: make sure nothing we issued is still running before TMEM is freed
         mma_commit(&o_full[0]);
         mbar_wait(&o_full[0], 0, status);
@@ -399,8 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A scale of row r is read from lane r, column (base + r / 32): this warp's quarter
           tmem_st1(s_addr + 120 + quarter, sfa);
         } else {
-        // pass 2: boosted weights 2^(x - m + 8), their E4M3 codes into the P tile
+        // pass 2: boosted weights 2^(x - m + 8), their E4M3 codes into the P tile (the
+        // loop is built twice: the causal mask only on the diagonal tile)
         float2 acc2 = make_float2(0.f, 0.f);
+        auto pass2 = [&](auto diag_tile) {
+          constexpr bool kDiag = decltype(diag_tile)::value;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t v[32];
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float2 x1 = ffma2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), f2, n2);
             float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
             float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
-            if (diag) {
+            if (kDiag) {
               const int kc = g * 32 + j;
               p0.x = kc <= r ? p0.x : 0.f;
               p0.y = kc + 1 <= r ? p0.y : 0.f;
@@ -429,6 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g + 16, 128)) =
               make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
+        };
+        if (diag) pass2(std::true_type{});
+        else pass2(std::false_type{});
         lsum += acc2.x + acc2.y;
         }
         m = m_new;
