@@ -99,6 +99,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkv = ntq > 1 ? t0 + 2 : t0 + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool tab_ok = STRICT ? nkv * 32 <= L::kMaxTabTiles : nkv <= L::kMaxTabTiles;
+  const bool run = !STRICT || tab_ok;
+  constexpr int kEarly = kStages;                 // K/V tiles whose loads start in the prologue
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kStages; ++i) {
@@ -111,6 +114,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_full[w], 1);
     }
     fence_mbar_init();
+    if (run) {
+      // the producer's first loads start before the scale table and the CTA barrier
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(q_full, ntq * L::kTileBytes);
+      for (int w = 0; w < ntq; ++w)
+        tma_load_3d(smem + L::kQ + w * L::kTileBytes, &tm_q, q_full, 0, h, doc_start + (t0 + w) * kTile);
+      for (int u = 0; u < nkv && u < kEarly; ++u) {
+        mbar_arrive_expect_tx(&kv_full[u], 2 * L::kTileBytes);
+        tma_load_3d(smem + L::kK + u * L::kTileBytes, &tm_k, &kv_full[u], 0, hk, doc_start + u * kTile);
+        tma_load_3d(smem + L::kV + u * L::kTileBytes, &tm_v, &kv_full[u], 0, hk, doc_start + u * kTile);
+      }
+    }
   }
   if (warp == 2) {
     tmem_alloc(tmem_slot, 512);
@@ -119,8 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // K / V block-scale bytes of every key tile of the item (one byte per 32-key
   // group, 127 past the document end), staged once so the softmax loop reads
   // them from shared memory
+  // (each thread's global loads are issued before its shared-memory stores)
   uint32_t* scale_tab = reinterpret_cast<uint32_t*>(smem + L::kScaleTab);
-  const bool tab_ok = STRICT ? nkv * 32 <= L::kMaxTabTiles : nkv <= L::kMaxTabTiles;
   if (STRICT && tab_ok) {
     // strict: per-token scale bytes of every key of the item, 128 K then 128 V per tile
     uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
@@ -129,8 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kl = uu * kTile + j;
       const int64_t ktok = (int64_t)doc_start + kl;
       const bool kv = kl < doc_len;
-      tb[uu * 256 + j] = kv ? p.k_scales[ktok * p.hkv + hk] : (uint8_t)127;
-      tb[uu * 256 + 128 + j] = kv ? p.v_scales[ktok * p.hkv + hk] : (uint8_t)127;
+      const uint8_t kb = kv ? __ldg(p.k_scales + ktok * p.hkv + hk) : (uint8_t)127;
+      const uint8_t vb = kv ? __ldg(p.v_scales + ktok * p.hkv + hk) : (uint8_t)127;
+      tb[uu * 256 + j] = kb;
+      tb[uu * 256 + 128 + j] = vb;
     }
   } else if (STRICT && threadIdx.x == 0) {
     atomicOr(status, FLAMIA_DEV_CAPACITY);         // document too long for the strict per-key table
@@ -142,8 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kl = uu * kTile + gg * 32;
       const int64_t ktok = (int64_t)doc_start + kl;
       const bool kv = kl < doc_len;
-      tb[uu * 8 + gg] = kv ? p.k_scales[ktok * p.hkv + hk] : (uint8_t)127;
-      tb[uu * 8 + 4 + gg] = kv ? p.v_scales[ktok * p.hkv + hk] : (uint8_t)127;
+      const uint8_t kb = kv ? __ldg(p.k_scales + ktok * p.hkv + hk) : (uint8_t)127;
+      const uint8_t vb = kv ? __ldg(p.v_scales + ktok * p.hkv + hk) : (uint8_t)127;
+      tb[uu * 8 + gg] = kb;
+      tb[uu * 8 + 4 + gg] = vb;
     }
   }
   tc_fence_before();
@@ -156,19 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
   constexpr uint32_t kAtom = 8 * D;
 
-  const bool run = !STRICT || tab_ok;
   if (!run) {
     // strict call on a document longer than the per-key table: nothing is computed
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(q_full, ntq * L::kTileBytes);
-      for (int w = 0; w < ntq; ++w)
-        tma_load_3d(smem + L::kQ + w * L::kTileBytes, &tm_q, q_full, 0, h, doc_start + (t0 + w) * kTile);
-      for (int u = 0; u < nkv; ++u) {
+      for (int u = kEarly; u < nkv; ++u) {      // Q and the first kEarly K/V tiles: prologue
         const int st = u % kStages;
         if (u >= kStages && !mbar_wait(&kv_empty[st], ((u / kStages) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTileBytes);
