@@ -189,6 +189,21 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     mbar_init(sf_ready, 128 * kRO);
     mbar_init(pt_full, 128);
     fence_mbar_init();
+    // the producer's first loads (K, V and the first kQStages steps' Q, dO) start
+    // before the TMEM allocation and the CTA barrier
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
+    tma_load_3d(smem + L::kK, &tm_k, kv_full, 0, hk, doc_start + u * kTile);
+    tma_load_3d(smem + L::kV, &tm_v, kv_full, 0, hk, doc_start + u * kTile);
+    if (MIXED) tma_load_3d(smem + L::kK4, &tm_k4, kv_full, 0, hk, doc_start + u * kTile);
+    for (int k = 0; k < nsteps && k < kQStages; ++k) {
+      const int h = hk * g + k / qtiles, t = u + k % qtiles;
+      mbar_arrive_expect_tx(&qd_full[k], 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
+      tma_load_3d(smem + L::kQ + k * L::kTileBytes, &tm_q, &qd_full[k], 0, h, doc_start + t * kTile);
+      tma_load_3d(smem + L::kDO + k * L::kTileBytes, &tm_do, &qd_full[k], 0, h, doc_start + t * kTile);
+      if (MIXED) tma_load_3d(smem + L::kQ4 + k * L::kScoreBytes, &tm_q4, &qd_full[k], 0, h, doc_start + t * kTile);
+    }
   }
   if (warp == 2) {
     tmem_alloc(tmem_slot, 512);
@@ -219,15 +234,9 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
-      tma_load_3d(smem + L::kK, &tm_k, kv_full, 0, hk, doc_start + u * kTile);
-      tma_load_3d(smem + L::kV, &tm_v, kv_full, 0, hk, doc_start + u * kTile);
-      if (MIXED) tma_load_3d(smem + L::kK4, &tm_k4, kv_full, 0, hk, doc_start + u * kTile);
-      for (int k = 0; k < nsteps; ++k) {
+      for (int k = kQStages; k < nsteps; ++k) {     // K, V and the first kQStages steps: prologue
         const int st = k % kQStages;
-        if (k >= kQStages && !mbar_wait(&qd_empty[st], ((k / kQStages) - 1) & 1, status)) break;
+        if (!mbar_wait(&qd_empty[st], ((k / kQStages) - 1) & 1, status)) break;
         const int h = hk * g + k / qtiles, t = u + k % qtiles;
         mbar_arrive_expect_tx(&qd_full[st], 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
         tma_load_3d(smem + L::kQ + st * L::kTileBytes, &tm_q, &qd_full[st], 0, h, doc_start + t * kTile);
