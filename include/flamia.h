@@ -155,9 +155,11 @@ typedef struct flamia_qtensor {
  *   [4]  number of 32-token blocks            [5]  number of 128-token tiles
  *   [6]  number of forward items              [7]  number of backward items
  *   [8]  capacity (items)                     [16 ...] blk_prefix[num_seqs+1]
- *   then tile_prefix[num_seqs+1], then (16-byte aligned) forward items as
- *   int4 {doc, first query tile, query tile count, cost} x capacity, then
- *   backward items as int4 {doc, key tile, cost, 0} x capacity.
+ *   then tile_prefix[num_seqs+1] and item_prefix[num_seqs+1], then (16-byte
+ *   aligned) forward items as int4 {doc, first query tile, query tile count,
+ *   cost} x capacity, then backward items as int4 {doc, key tile, cost, 0} x
+ *   capacity, then each backward item's document as int2 {first token, length}
+ *   x capacity, the same for each forward item, then the sort scratch.
  * Ownership: caller-allocated device memory of flamia_plan_bytes() bytes,
  * 16-byte aligned; it must stay valid until every call using it completed. */
 size_t flamia_plan_bytes(int64_t total_tokens, int num_seqs);

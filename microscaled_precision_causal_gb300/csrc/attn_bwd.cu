@@ -161,9 +161,10 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   if (item_idx >= n_items) return;
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.bwd_items[item_idx];
+  const int2 span = pv.bwd_span[item_idx];      // loaded alongside the item (no dependent load)
   const int doc = item.x, u = item.y;
-  const int doc_start = p.cu[doc];
-  const int doc_len = p.cu[doc + 1] - doc_start;
+  const int doc_start = span.x;
+  const int doc_len = span.y;
   const int nt = (doc_len + kTile - 1) / kTile;
   const int g = p.hq / p.hkv;
   const int qtiles = nt - u;
@@ -1126,9 +1127,10 @@ __global__ void __launch_bounds__(256, 1)
   if (item_idx >= n_items) return;
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.fwd_items[item_idx];
+  const int2 span = pv.fwd_span[item_idx];      // loaded alongside the item (no dependent load)
   const int doc = item.x, t0 = item.y, ntq = item.z;
-  const int doc_start = p.cu[doc];
-  const int doc_len = p.cu[doc + 1] - doc_start;
+  const int doc_start = span.x;
+  const int doc_len = span.y;
   const int hk = h / (p.hq / p.hkv);
   // pairs (query tile w, key tile u), w-major, u = 0 .. t0 + w
   const int npairs = ntq == 1 ? t0 + 1 : 2 * t0 + 3;

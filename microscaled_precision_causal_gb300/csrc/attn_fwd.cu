@@ -91,9 +91,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (item_idx >= n_items) return;
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.fwd_items[item_idx];
+  const int2 span = pv.fwd_span[item_idx];      // loaded alongside the item (no dependent load)
   const int doc = item.x, t0 = item.y, ntq = item.z;
-  const int doc_start = p.cu[doc];
-  const int doc_len = p.cu[doc + 1] - doc_start;
+  const int doc_start = span.x;
+  const int doc_len = span.y;
   const int hk = h / (p.hq / p.hkv);
   const int nk_w[2] = {t0 + 1, ntq > 1 ? t0 + 2 : 0};
   const int nkv = ntq > 1 ? t0 + 2 : t0 + 1;

@@ -36,6 +36,8 @@ struct PlanView {
   const int* item_prefix;   // [N+1] cumulative ceil(L/256)
   const int4* fwd_items;    // [cap] {doc, tile0, ntiles, cost}
   const int4* bwd_items;    // [cap] {doc, ktile, cost, 0}
+  const int2* bwd_span;     // [cap] the backward item's document: {first token, length}
+  const int2* fwd_span;     // [cap] the forward item's document: {first token, length}
   unsigned long long* sort_keys;  // [pow2(cap)]
 };
 
@@ -76,7 +78,7 @@ __host__ __device__ inline int64_t pow2_ceil(int64_t x) {
 __host__ __device__ inline int64_t plan_prefix_words(int N) { return ((int64_t)kPlanHeaderWords + 3 * (N + 1) + 3) & ~3LL; }
 __host__ __device__ inline size_t plan_bytes(int64_t T, int N) {
   const int64_t cap = plan_capacity(T, N);
-  return (size_t)plan_prefix_words(N) * 4 + (size_t)cap * 32 + (size_t)pow2_ceil(cap) * 8 + 16;
+  return (size_t)plan_prefix_words(N) * 4 + (size_t)cap * 48 + (size_t)pow2_ceil(cap) * 8 + 16;
 }
 __host__ __device__ inline PlanView plan_view(const void* plan, int64_t T, int N) {
   PlanView v;
@@ -89,7 +91,9 @@ __host__ __device__ inline PlanView plan_view(const void* plan, int64_t T, int N
   int4* items = (int4*)(w + plan_prefix_words(N));
   v.fwd_items = items;
   v.bwd_items = items + cap;
-  v.sort_keys = (unsigned long long*)(items + 2 * cap);
+  v.bwd_span = (const int2*)(items + 2 * cap);
+  v.fwd_span = v.bwd_span + cap;
+  v.sort_keys = (unsigned long long*)(v.fwd_span + cap);
   return v;
 }
 

@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
   int* item_prefix = const_cast<int*>(pv.item_prefix);
   int4* fwd = const_cast<int4*>(pv.fwd_items);
   int4* bwd = const_cast<int4*>(pv.bwd_items);
+  int2* bwd_span = const_cast<int2*>(pv.bwd_span);
+  int2* fwd_span = const_cast<int2*>(pv.fwd_span);
   const int cap = (int)plan_capacity(T, N);
 
   if (threadIdx.x == 0) {
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
       const int t0 = (i - item_prefix[doc]) * kItemTiles;
       const int cnt = min(kItemTiles, nt - t0);
       fwd[r] = make_int4(doc, t0, cnt, (int)(kCostMax - (unsigned)(keys[r] >> 32)));
+      fwd_span[r] = make_int2(cu[doc], cu[doc + 1] - cu[doc]);
     }
     __syncthreads();
   }
@@ -193,6 +196,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
       const int i = (int)(keys[r] & 0xFFFFFFFFull);
       const int doc = upper_doc(tile_prefix, N, i);
       bwd[r] = make_int4(doc, i - tile_prefix[doc], (int)(kCostMax - (unsigned)(keys[r] >> 32)), 0);
+      bwd_span[r] = make_int2(cu[doc], cu[doc + 1] - cu[doc]);
     }
   }
 }
