@@ -47,7 +47,37 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return before;
 }
 
+// Bitonic sort of n <= blockDim.x keys (n a power of two): one key per thread in a
+// register; partners closer than a warp are exchanged with shuffles, the others
+// through shared memory.  Ascending.
+__device__ void bitonic_sort_regs(unsigned long long* keys, int n) {
+  const int i = threadIdx.x;
+  unsigned long long a = i < n ? keys[i] : ~0ull;
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      unsigned long long b;
+      if (j >= 32) {
+        __syncthreads();                       // every read of the previous round done
+        if (i < n) keys[i] = a;
+        __syncthreads();
+        b = i < n ? keys[i ^ j] : a;
+      } else {
+        b = __shfl_xor_sync(0xffffffffu, a, j);
+      }
+      const bool up = (i & k) == 0, lower = (i & j) == 0;
+      a = (lower == up) ? (a < b ? a : b) : (a < b ? b : a);
+    }
+  }
+  __syncthreads();
+  if (i < n) keys[i] = a;
+  __syncthreads();
+}
+
 __device__ void bitonic_sort(unsigned long long* keys, int n) {  // n is a power of two
+  if (n <= (int)blockDim.x) {
+    bitonic_sort_regs(keys, n);
+    return;
+  }
   for (int k = 2; k <= n; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int i = threadIdx.x; i < n; i += blockDim.x) {
