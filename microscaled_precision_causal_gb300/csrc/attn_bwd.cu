@@ -120,10 +120,6 @@ struct BwdSmem {
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 template <int D, bool STRICT, bool MIXED>
 __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1128,7 +1124,7 @@ __global__ void __launch_bounds__(256, 1)
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.fwd_items[item_idx];
   const int2 span = pv.fwd_span[item_idx];      // loaded alongside the item (no dependent load)
-  const int doc = item.x, t0 = item.y, ntq = item.z;
+  const int t0 = item.y, ntq = item.z;
   const int doc_start = span.x;
   const int doc_len = span.y;
   const int hk = h / (p.hq / p.hkv);

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.fwd_items[item_idx];
   const int2 span = pv.fwd_span[item_idx];      // loaded alongside the item (no dependent load)
-  const int doc = item.x, t0 = item.y, ntq = item.z;
+  const int t0 = item.y, ntq = item.z;
   const int doc_start = span.x;
   const int doc_len = span.y;
   const int hk = h / (p.hq / p.hkv);
@@ -473,17 +473,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&p_full[w]);
       }
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[w], 0, status));
+      // warpgroup-wide: the epilogue below synchronises the warpgroup's four warps
+      ok = named_bar_and(2 + w, 128, ok && mbar_wait(&o_full[w], 0, status));
       if (ok) {
         tc_fence_after();
+        // O = bf16(acc / l): 64 columns per pass, staged row by row in this warpgroup's P^
+        // tile (every PV MMA that read it is done), 16-byte units of row r permuted by
+        // XOR with (r mod 8), then copied out as whole 128-byte row segments
         const float inv = 1.0f / lsum;
-        __nv_bfloat16* orow = p.out + (tok * p.hq + h) * D;
+        const int tr = threadIdx.x & 127;
+        const int vrows = doc_len - t * kTile;          // rows of the tile inside the document
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(o_addr + 32 * c, v);
-          tmem_ld_wait();
-          if (row_valid) {
+        for (int half = 0; half < D / 64; ++half) {
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(o_addr + 64 * half + 32 * c, v);
+            tmem_ld_wait();
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -491,10 +497,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                         __uint_as_float(v[2 * j + 1]) * inv);
               pk[j] = *reinterpret_cast<uint32_t*>(&b2);
             }
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(sP + r * 128 + (((4 * c + j) ^ (r & 7)) << 4)) =
+                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
+          named_bar_sync(2 + w, 128);
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int idx = it * 128 + tr, row = idx >> 3, unit = idx & 7;
+            const uint4 val = *reinterpret_cast<const uint4*>(sP + row * 128 + ((unit ^ (row & 7)) << 4));
+            if (row < vrows)
+              *reinterpret_cast<uint4*>(p.out + (((int64_t)doc_start + t * kTile + row) * p.hq + h) * D + 64 * half +
+                                        8 * unit) = val;
+          }
+          named_bar_sync(2 + w, 128);                  // before the next pass overwrites the tile
         }
         if (row_valid) p.lse[(int64_t)h * p.T + tok] = (m + __log2f(lsum) - 8.0f) * 0.69314718055994531f;
       }

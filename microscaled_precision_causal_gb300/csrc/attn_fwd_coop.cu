@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.fwd_items[item_idx];
   const int2 span = pv.fwd_span[item_idx];      // loaded alongside the item (no dependent load)
-  const int doc = item.x, t0 = item.y, ntq = item.z;
+  const int t0 = item.y, ntq = item.z;
   const int doc_start = span.x;
   const int doc_len = span.y;
   const int hk = h / (p.hq / p.hkv);

@@ -87,6 +87,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
+// Named barrier over `n` threads (warp multiples) with id `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 // Named barrier over `n` threads that also ANDs a predicate across them, so a
 // group leaves a loop together when any member's bounded wait expired.
 __device__ __forceinline__ bool named_bar_and(int id, int n, bool pred) {
