@@ -18,6 +18,7 @@
 #include <cuda_fp4.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace flamia {
 
@@ -38,7 +39,7 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
                     const int* __restrict__ plan, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                     float2* __restrict__ stats, const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec,
                     __half* __restrict__ dq_acc, const float2* __restrict__ k_stats,
-                    const float2* __restrict__ v_stats, int hkv, float* __restrict__ maxima) {
+                    const float2* __restrict__ v_stats, int hkv, float* __restrict__ maxima, int64_t nwork) {
   // Each lane owns 32 elements of a row as four 16-byte vectors, vector j at column
   // j * 8 kLpr + 8 (lane % kLpr): a load instruction reads kRpi rows x 16 kLpr
   // contiguous bytes, and per-row reductions take log2(kLpr) shuffle levels.
@@ -48,40 +49,93 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
   const int lane = threadIdx.x & 31;
   constexpr int kWarps = QShape<WITH_D>::kWarps;
   constexpr bool kHold = !PER_TOKEN && !WITH_D;   // block held in registers for pass 2
-  const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const int h = (int)(gw % H);
-  const int64_t unit = gw / H;
   const PlanView pv = plan_view(plan, T, N);
   const int valid = plan[kPlanValid];
   const int nblk = plan[kPlanBlocks];
-
-  // rows [r0, r0 + nrows) of this warp; tail rows (no document) get zeros
-  int r0, nrows;
-  bool tail = false;
-  int64_t dq_tile0 = 0;   // backward prep: accumulator tile of the block's document tile
-  int dq_row0 = 0;
-  int doc = -1;
-  if (PER_TOKEN) {
-    r0 = (int)(unit * 32);
-    if (r0 >= T) return;
-    nrows = min(32, T - r0);
-  } else if (unit < nblk) {
-    doc = upper_doc(pv.blk_prefix, N, (int)unit);
-    const int s0 = cu[doc], s1 = cu[doc + 1];
-    r0 = s0 + ((int)unit - pv.blk_prefix[doc]) * kBlock;
-    nrows = min(kBlock, s1 - r0);
-    dq_tile0 = pv.tile_prefix[doc] + (r0 - s0) / kTile;
-    dq_row0 = (r0 - s0) % kTile;
-  } else {
-    r0 = valid + (int)(unit - nblk) * 32;
-    if (r0 >= T) return;
-    nrows = min(32, T - r0);
-    tail = true;
-  }
   const int sub = lane / kLpr;            // row within an iteration
   const int seg = lane % kLpr;
   auto col_of = [&](int j) { return j * 8 * kLpr + 8 * seg; };
-  auto live = [&](int r) { return r < nrows && !tail && (!PER_TOKEN || r0 + r < valid); };
+
+  // Work unit gw = (32-row block, head); the warps walk the units with a grid stride.
+  // Rows [r0, r0 + nrows); tail rows (no document) get zeros.
+  struct QUnit {
+    int h, r0, nrows, doc, dq_row0;
+    bool tail, skip;
+    int64_t dq_tile0;     // backward prep: accumulator tile of the block's document tile
+  };
+  auto unit_setup = [&](int64_t gw) {
+    QUnit U;
+    U.h = (int)(gw % H);
+    const int64_t unit = gw / H;
+    U.tail = false;
+    U.skip = gw >= nwork;
+    U.dq_tile0 = 0;
+    U.dq_row0 = 0;
+    U.doc = -1;
+    U.r0 = 0;
+    U.nrows = 0;
+    if (U.skip) return U;
+    if (PER_TOKEN) {
+      U.r0 = (int)(unit * 32);
+      U.skip = U.r0 >= T;
+      U.nrows = min(32, T - U.r0);
+    } else if (unit < nblk) {
+      U.doc = upper_doc(pv.blk_prefix, N, (int)unit);
+      const int s0 = cu[U.doc], s1 = cu[U.doc + 1];
+      U.r0 = s0 + ((int)unit - pv.blk_prefix[U.doc]) * kBlock;
+      U.nrows = min(kBlock, s1 - U.r0);
+      U.dq_tile0 = pv.tile_prefix[U.doc] + (U.r0 - s0) / kTile;
+      U.dq_row0 = (U.r0 - s0) % kTile;
+    } else {
+      U.r0 = valid + (int)(unit - nblk) * 32;
+      U.skip = U.r0 >= T;
+      U.nrows = min(32, T - U.r0);
+      U.tail = true;
+    }
+    return U;
+  };
+  auto live_u = [&](const QUnit& U, int r) { return r < U.nrows && !U.tail && (!PER_TOKEN || U.r0 + r < valid); };
+  // register-held variant: the next unit's block is prefetched into this lane's own
+  // shared-memory slots (16 x 16 bytes, zero-filled where no row) with cp.async
+  __shared__ uint4 pf_buf[kHold ? kWarps : 1][kHold ? kIters * 4 : 1][32];
+  auto prefetch = [&](const QUnit& U) {
+#pragma unroll
+    for (int it = 0; it < kIters; ++it)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = it * kRpi + sub;
+        const bool lv = !U.skip && live_u(U, r);
+        const __nv_bfloat16* src = x + ((int64_t)(lv ? U.r0 + r : 0) * H + U.h) * D + col_of(j);
+        const uint32_t dst = smem_u32(&pf_buf[kHold ? (threadIdx.x >> 5) : 0][kHold ? it * 4 + j : 0][lane]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(lv ? 16 : 0) : "memory");
+      }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  const int64_t stride = (int64_t)gridDim.x * kWarps;
+  int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  QUnit nextU;
+  if constexpr (kHold) {
+    nextU = unit_setup(gw);
+    prefetch(nextU);
+  }
+  for (; gw < nwork; gw += stride) {
+  // (the other variants launch one warp per unit and leave after one pass)
+  const QUnit U = kHold ? nextU : unit_setup(gw);
+  uint4 w[kHold ? kIters : 1][4];
+  if constexpr (kHold) {
+    nextU = unit_setup(gw + stride);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+#pragma unroll
+    for (int it = 0; it < kIters; ++it)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[kHold ? it : 0][j] = pf_buf[kHold ? (threadIdx.x >> 5) : 0][kHold ? it * 4 + j : 0][lane];
+    if (!nextU.skip) prefetch(nextU);          // this lane's slots were just read
+  }
+  if (U.skip) continue;
+  const int h = U.h, r0 = U.r0, nrows = U.nrows, doc = U.doc, dq_row0 = U.dq_row0;
+  const bool tail = U.tail;
+  const int64_t dq_tile0 = U.dq_tile0;
+  auto live = [&](int r) { return live_u(U, r); };
   auto load8 = [&](const __nv_bfloat16* base, int r, int j) {
     return live(r) ? __ldg(reinterpret_cast<const uint4*>(base + ((int64_t)(r0 + r) * H + h) * D + col_of(j)))
                    : make_uint4(0, 0, 0, 0);
@@ -101,15 +155,13 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
   // pass 1 (token blocks): amax over the whole block; the plain quantizer keeps the
   // block in registers for pass 2 (32 rows x 64 bytes per lane)
   int e_block = 0;
-  uint4 w[kHold ? kIters : 1][4];
   if (!PER_TOKEN) {
     float a = 0.f;
 #pragma unroll
     for (int it = 0; it < kIters; ++it) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 x4 = load8(x, it * kRpi + sub, j);
-        if (kHold) w[kHold ? it : 0][j] = x4;
+        const uint4 x4 = kHold ? w[kHold ? it : 0][j] : load8(x, it * kRpi + sub, j);
         a = fmaxf(a, absmax8(x4));
       }
     }
@@ -217,6 +269,9 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
       atomicMax(mx3 + 2, __float_as_int(mk));
     }
   }
+  if constexpr (!kHold) break;
+  }  // work units
+  if (kHold) asm volatile("cp.async.wait_group 0;" ::: "memory");   // no copy outlives the block
 }
 
 struct PrepExtra {          // backward prep only
@@ -233,13 +288,23 @@ cudaError_t launch_q(const void* x, int T, int H, const int32_t* cu, int N, cons
   const int64_t units = PT ? (T + 31) / 32 : (int64_t)T / 32 + N + 1;
   const int64_t warps = units * H;
   constexpr int kWarps = QShape<WD>::kWarps;
-  const int64_t blocks = (warps + kWarps - 1) / kWarps;
-  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  int64_t blocks = (warps + kWarps - 1) / kWarps;
+  // the register-held variant walks several units per warp (its next block prefetched);
+  // the others keep one unit per warp
+  if (!PT && !WD) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cudaErrorInvalidValue;
+    const int64_t resident = (int64_t)sms * QShape<WD>::kMinBlocks;
+    if (blocks > resident) blocks = resident;
+  }
+  if (blocks > 0x7FFFFFFF || blocks < 1) return cudaErrorInvalidValue;
   quantize_kernel<D, PT, ST, WD><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), T, H, cu, N, static_cast<const int*>(plan),
       static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), reinterpret_cast<float2*>(stats),
       static_cast<const __nv_bfloat16*>(o), dvec, static_cast<__half*>(dq_acc),
-      reinterpret_cast<const float2*>(px.k_stats), reinterpret_cast<const float2*>(px.v_stats), px.hkv, px.maxima);
+      reinterpret_cast<const float2*>(px.k_stats), reinterpret_cast<const float2*>(px.v_stats), px.hkv, px.maxima,
+      warps);
   return cudaGetLastError();
 }
 
