@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         issue_dp(0);
         if (leader) mma_commit(dp_full);
       }
+      bool acc_committed = false;
       for (int k = 0; k < nsteps && ok; ++k) {
         const int st = k % kQStages;
         const int st1 = (k + 1) % kQStages;
@@ -348,6 +349,12 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
                      idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFK, tbase + kSFK + 4, (k > 0 || s > 0));
         }
         if (leader) mma_commit(&qd_empty[st]);             // Q and dO of this step are no longer read
+        // last step: dK and dV are complete once the MMAs so far are, so the compute
+        // warpgroups' epilogue starts while the last dQ partial is computed and read
+        if (!more) {
+          if (leader) mma_commit(acc_full);
+          acc_committed = true;
+        }
         if (kDQT) {
           ok = warp_wait(dq_empty, 0, status);
           if (!ok) break;
@@ -383,9 +390,11 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           if (leader) mma_commit(dp_full);
         }
       }
-      if (leader) {
-        mma_commit(acc_full);
-        if (!ok) mbar_wait(acc_full, 0, status);   // nothing of ours still reads SMEM or TMEM
+      if (!ok && leader) {
+        // a wait ran out: commit (unless the last step did) and wait, so that nothing
+        // of ours still reads SMEM or TMEM
+        if (!acc_committed) mma_commit(acc_full);
+        mbar_wait(acc_full, 0, status);
       }
     }
   } else if (warp == 3) {
