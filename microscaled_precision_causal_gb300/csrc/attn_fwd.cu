@@ -85,13 +85,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 2);
   int* status = const_cast<int*>(p.plan) + kPlanStatus;
 
-  const int n_items = p.plan[kPlanFwdItems];
   const int item_idx = blockIdx.x / p.hq;
   const int h = blockIdx.x % p.hq;
-  if (item_idx >= n_items) return;
+  // the item, its document span and the item count in one round trip: the grid never
+  // exceeds the plan capacity, so the first two reads stay inside the plan also for a
+  // CTA without an item
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.fwd_items[item_idx];
-  const int2 span = pv.fwd_span[item_idx];      // loaded alongside the item (no dependent load)
+  const int2 span = pv.fwd_span[item_idx];
+  const int n_items = p.plan[kPlanFwdItems];
+  if (item_idx >= n_items) return;
   const int t0 = item.y, ntq = item.z;
   const int doc_start = span.x;
   const int doc_len = span.y;
@@ -135,39 +138,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   // K / V block-scale bytes of every key tile of the item (one byte per 32-key
-  // group, 127 past the document end), staged once so the softmax loop reads
+  // group, 127 past the document end), staged once by the two softmax warpgroups
+  // after the CTA barrier (while the first tiles load) so the softmax loop reads
   // them from shared memory
   // (each thread's global loads are issued before its shared-memory stores)
   uint32_t* scale_tab = reinterpret_cast<uint32_t*>(smem + L::kScaleTab);
-  if (STRICT && tab_ok) {
-    // strict: per-token scale bytes of every key of the item, 128 K then 128 V per tile
-    uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
-    for (int i = threadIdx.x; i < nkv * kTile; i += kThreads) {
-      const int uu = i >> 7, j = i & 127;
-      const int kl = uu * kTile + j;
-      const int64_t ktok = (int64_t)doc_start + kl;
-      const bool kv = kl < doc_len;
-      const uint8_t kb = kv ? __ldg(p.k_scales + ktok * p.hkv + hk) : (uint8_t)127;
-      const uint8_t vb = kv ? __ldg(p.v_scales + ktok * p.hkv + hk) : (uint8_t)127;
-      tb[uu * 256 + j] = kb;
-      tb[uu * 256 + 128 + j] = vb;
+  auto stage_scale_table = [&](int first, int stride) {
+    if (STRICT && tab_ok) {
+      // strict: per-token scale bytes of every key of the item, 128 K then 128 V per tile
+      uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
+      for (int i = first; i < nkv * kTile; i += stride) {
+        const int uu = i >> 7, j = i & 127;
+        const int kl = uu * kTile + j;
+        const int64_t ktok = (int64_t)doc_start + kl;
+        const bool kv = kl < doc_len;
+        const uint8_t kb = kv ? __ldg(p.k_scales + ktok * p.hkv + hk) : (uint8_t)127;
+        const uint8_t vb = kv ? __ldg(p.v_scales + ktok * p.hkv + hk) : (uint8_t)127;
+        tb[uu * 256 + j] = kb;
+        tb[uu * 256 + 128 + j] = vb;
+      }
     }
-  } else if (STRICT && threadIdx.x == 0) {
+    if (!STRICT && tab_ok) {
+      uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
+      for (int i = first; i < nkv * 4; i += stride) {
+        const int uu = i >> 2, gg = i & 3;
+        const int kl = uu * kTile + gg * 32;
+        const int64_t ktok = (int64_t)doc_start + kl;
+        const bool kv = kl < doc_len;
+        const uint8_t kb = kv ? __ldg(p.k_scales + ktok * p.hkv + hk) : (uint8_t)127;
+        const uint8_t vb = kv ? __ldg(p.v_scales + ktok * p.hkv + hk) : (uint8_t)127;
+        tb[uu * 8 + gg] = kb;
+        tb[uu * 8 + 4 + gg] = vb;
+      }
+    }
+  };
+  if (STRICT && !tab_ok && threadIdx.x == 0)
     atomicOr(status, FLAMIA_DEV_CAPACITY);         // document too long for the strict per-key table
-  }
-  if (!STRICT && tab_ok) {
-    uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
-    for (int i = threadIdx.x; i < nkv * 4; i += kThreads) {
-      const int uu = i >> 2, gg = i & 3;
-      const int kl = uu * kTile + gg * 32;
-      const int64_t ktok = (int64_t)doc_start + kl;
-      const bool kv = kl < doc_len;
-      const uint8_t kb = kv ? __ldg(p.k_scales + ktok * p.hkv + hk) : (uint8_t)127;
-      const uint8_t vb = kv ? __ldg(p.v_scales + ktok * p.hkv + hk) : (uint8_t)127;
-      tb[uu * 8 + gg] = kb;
-      tb[uu * 8 + 4 + gg] = vb;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -264,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
+    stage_scale_table(threadIdx.x - 128, 256);
+    named_bar_sync(1, 256);
     const int w = (warp - 4) >> 2;        // warpgroup = query tile t0 + w
     if (w < ntq) {
       const int quarter = warp & 3;
@@ -473,45 +481,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&p_full[w]);
       }
-      // warpgroup-wide: the epilogue below synchronises the warpgroup's four warps
+      // warpgroup-wide, so that the four warps leave together on a timeout
       ok = named_bar_and(2 + w, 128, ok && mbar_wait(&o_full[w], 0, status));
       if (ok) {
         tc_fence_after();
-        // O = bf16(acc / l): 64 columns per pass, staged row by row in this warpgroup's P^
-        // tile (every PV MMA that read it is done), 16-byte units of row r permuted by
-        // XOR with (r mod 8), then copied out as whole 128-byte row segments
+        // O = bf16(acc / l) straight from registers: 32 columns per TMEM load, written as
+        // two 32-byte stores of the thread's row (16-byte ones if O is only 16-byte
+        // aligned); the SM's store path drains them while the warpgroup leaves
         const float inv = 1.0f / lsum;
-        const int tr = threadIdx.x & 127;
-        const int vrows = doc_len - t * kTile;          // rows of the tile inside the document
+        const bool al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
+        __nv_bfloat16* orow = p.out + (tok * p.hq + h) * D;
 #pragma unroll 1
-        for (int half = 0; half < D / 64; ++half) {
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            tmem_ld32(o_addr + 64 * half + 32 * c, v);
-            tmem_ld_wait();
-            uint32_t pk[16];
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(o_addr + 32 * c, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]) * inv,
-                                                        __uint_as_float(v[2 * j + 1]) * inv);
-              pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]) * inv,
+                                                      __uint_as_float(v[2 * j + 1]) * inv);
+            pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          if (row_valid) {
+            __nv_bfloat16* dst = orow + 32 * c;
+            if (al32) {
+              st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+              st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(sP + r * 128 + (((4 * c + j) ^ (r & 7)) << 4)) =
-                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
-          named_bar_sync(2 + w, 128);
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int idx = it * 128 + tr, row = idx >> 3, unit = idx & 7;
-            const uint4 val = *reinterpret_cast<const uint4*>(sP + row * 128 + ((unit ^ (row & 7)) << 4));
-            if (row < vrows)
-              *reinterpret_cast<uint4*>(p.out + (((int64_t)doc_start + t * kTile + row) * p.hq + h) * D + 64 * half +
-                                        8 * unit) = val;
-          }
-          named_bar_sync(2 + w, 128);                  // before the next pass overwrites the tile
         }
         if (row_valid) p.lse[(int64_t)h * p.T + tok] = (m + __log2f(lsum) - 8.0f) * 0.69314718055994531f;
       }
