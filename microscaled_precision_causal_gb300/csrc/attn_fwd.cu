@@ -10,8 +10,10 @@
 //   O  += P^ V^ with V's token-block scale per 32 keys (MXF8 block-scaled MMA),
 //   O   = bf16(O / l), LSE = m + ln l.
 //
-// One CTA per (work item, query head): a work item is up to two document-local
-// 128-query tiles (Algorithm 2 step 03).  Roles (384 threads):
+// The MXFP8 route runs attn_fwd_persist_kernel below: one CTA per SM walks the
+// (work item, query head) units in boustrophedon order (Algorithm 2 step 05).  The
+// strict options run attn_fwd_kernel: one CTA per unit.  A work item is up to two
+// document-local 128-query tiles (Algorithm 2 step 03).  Roles (384 threads):
 //   warp 0      TMA producer: both Q tiles once, then K/V tiles through a ring
 //   warp 1      MMA issuer (converged warp, one elected lane issues): S_w = Q_w K^T
 //               and O_w += P^_w V
@@ -527,6 +529,435 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Persistent forward of the MXFP8 route: one CTA per SM walks the (work item,
+// query head) units of the cost-sorted work list in boustrophedon order -- in
+// round r, CTA c takes unit r G + c when r is even and r G + G - 1 - c when r is
+// odd (G CTAs) -- the assignment of the review's Algorithm 2 (step 05).  Nothing
+// drains between units: the producer loads the next unit's Q tiles into the
+// second Q buffer and its K/V tiles into the ring while the current unit still
+// runs, the MMA warp issues the next unit's first QK^T as soon as its tiles have
+// landed, and a warpgroup's epilogue (O = acc / l, LSE) overlaps the other
+// warpgroup's last tiles and the next unit's first score MMAs.  A warpgroup reads
+// its O accumulator before it hands in the first P^ tile of its next unit, so the
+// first PV MMA of that unit (which overwrites O) never races the epilogue.
+// Roles and TMEM columns are those of attn_fwd_kernel; the K/V block-scale words
+// of the next tile are loaded into registers one tile ahead.
+// Register split (setmaxnreg): the control warpgroup (producer, MMA warp) keeps 120
+// registers, the two softmax warpgroups take 192; the shares add up to the launch
+// allocation of 168 per thread, and the launch is refused with any other allocation
+// (the increase could then never be granted).
+constexpr int kPersistLaunchRegs = (65536 / kThreads) & ~7;
+constexpr int kPersistRegCtl = 120;
+constexpr int kPersistRegSoftmax = 192;
+static_assert(kPersistRegCtl * 128 + kPersistRegSoftmax * 256 <= kPersistLaunchRegs * kThreads, "register split");
+
+template <int D>
+struct PersistSmem {
+  static constexpr int kTileBytes = kTile * D;
+  static constexpr int kQ = 0;                                   // [2 buffers][2 query tiles]
+  static constexpr int kK = kQ + 4 * kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kP = kV + kStages * kTileBytes;            // [2 warpgroups]
+  static constexpr int kMaxTabTiles = 1024;                       // per key tile: K word, V word
+  static constexpr int kTab = kP + 2 * kTile * kTile;             // [2 warpgroups][kMaxTabTiles]
+  static constexpr int kBar = kTab + 2 * kMaxTabTiles * 8;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+// One unit of the forward work: query tiles t0 (.. t0 + ntq - 1) of a document for
+// query head h; nk[w] key tiles are visible to the query tile of warpgroup w.
+struct FwdUnit {
+  int h, hk, t0, ntq, doc_start, doc_len, nkv;
+  int nk0, nk1;
+  __device__ __forceinline__ int nk(int w) const { return w ? nk1 : nk0; }
+};
+
+__device__ __forceinline__ FwdUnit fwd_unit(const PlanView& pv, int i, int hq, int hkv) {
+  FwdUnit U;
+  const int item_idx = i / hq;
+  U.h = i % hq;
+  U.hk = U.h / (hq / hkv);
+  const int4 item = pv.fwd_items[item_idx];
+  const int2 span = pv.fwd_span[item_idx];
+  U.t0 = item.y;
+  U.ntq = item.z;
+  U.doc_start = span.x;
+  U.doc_len = span.y;
+  U.nk0 = U.t0 + 1;
+  U.nk1 = U.ntq > 1 ? U.t0 + 2 : 0;
+  U.nkv = U.ntq > 1 ? U.t0 + 2 : U.t0 + 1;
+  return U;
+}
+
+// Unit of round r for CTA c of G (boustrophedon).
+__device__ __forceinline__ int snake_unit(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = PersistSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars + 0;                  // [2 Q buffers]
+  uint64_t* q_empty = bars + 2;                 // [2]
+  uint64_t* kv_full = bars + 4;                 // [kStages]
+  uint64_t* kv_empty = kv_full + kStages;       // [kStages]
+  uint64_t* s_full = kv_empty + kStages;        // [2 warpgroups]
+  uint64_t* p_full = s_full + 2;                // [2]
+  uint64_t* o_full = p_full + 2;                // [2]
+  uint64_t* drain = o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* status = const_cast<int*>(p.plan) + kPlanStatus;
+
+  const PlanView pv = plan_view(p.plan, p.T, p.N);
+  const int n_units = p.plan[kPlanFwdItems] * p.hq;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int rounds = (n_units + G - 1) / G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_full[i], 1);
+    }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  constexpr uint32_t kSCol[2] = {0, 256};
+  constexpr uint32_t kOCol[2] = {128, 384};
+  constexpr uint32_t kRowBytes = D;
+  constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
+  constexpr uint32_t kAtom = 8 * D;
+  if (warp < 4) setmaxnreg_dec<kPersistRegCtl>();
+  else setmaxnreg_inc<kPersistRegSoftmax>();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int qn = 0;        // units loaded so far (Q buffer qn & 1)
+      int kvc = 0;       // K/V tiles loaded so far (ring stage kvc % kStages)
+      bool ok = true;
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int i = snake_unit(r, c, G);
+        if (i >= n_units) continue;
+        const FwdUnit U = fwd_unit(pv, i, p.hq, p.hkv);
+        const int qb = qn & 1;
+        if (qn >= 2 && !mbar_wait(&q_empty[qb], ((qn >> 1) - 1) & 1, status)) break;
+        mbar_arrive_expect_tx(&q_full[qb], U.ntq * L::kTileBytes);
+        for (int w = 0; w < U.ntq; ++w)
+          tma_load_3d(smem + L::kQ + (2 * qb + w) * L::kTileBytes, &tm_q, &q_full[qb], 0, U.h,
+                      U.doc_start + (U.t0 + w) * kTile);
+        ++qn;
+        for (int u = 0; u < U.nkv; ++u, ++kvc) {
+          const int st = kvc % kStages;
+          if (kvc >= kStages && !mbar_wait(&kv_empty[st], ((kvc / kStages) - 1) & 1, status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTileBytes);
+          tma_load_3d(smem + L::kK + st * L::kTileBytes, &tm_k, &kv_full[st], 0, U.hk, U.doc_start + u * kTile);
+          tma_load_3d(smem + L::kV + st * L::kTileBytes, &tm_v, &kv_full[st], 0, U.hk, U.doc_start + u * kTile);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = elect_one();
+    const uint32_t base16 = (smem_u32(smem) & 0x3FFFFu) >> 4;
+    auto b16 = [&]() {
+      uint32_t x;
+      asm volatile("mov.b32 %0, %1;" : "=r"(x) : "r"(base16));
+      return x;
+    };
+    auto issue_s = [&](int w, int qb, int st) {
+#pragma unroll
+      for (int s = 0; s < D / 32; ++s)
+        if (leader)
+          mma_f8(tbase + kSCol[w], sdesc_at(b16(), L::kQ + (2 * qb + w) * L::kTileBytes + 32 * s, 16, kAtom, kLayout),
+                 sdesc_at(b16(), L::kK + st * L::kTileBytes + 32 * s, 16, kAtom, kLayout), idesc_f8(128, 128, 0, 0),
+                 s > 0);
+    };
+    auto issue_pv = [&](int w, int st, bool acc) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        if (leader)
+          mma_mxf8(tbase + kOCol[w], sdesc_at(b16(), L::kP + w * kTile * kTile + 32 * s, 16, 1024, kSwizzle128B),
+                   sdesc_at(b16(), L::kV + st * L::kTileBytes + s * 32 * kRowBytes, kAtom, kAtom, kLayout),
+                   idesc_mxf8(128, D, 0, 1, s, s), tbase + kSCol[w] + 120, tbase + kSCol[w] + 124, acc || s > 0);
+    };
+    int qn = 0, kvc = 0;
+    int pcnt0 = 0, pcnt1 = 0;   // P^ tiles handed in by each warpgroup so far
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int i = snake_unit(r, c, G);
+      if (i >= n_units) continue;
+      const FwdUnit U = fwd_unit(pv, i, p.hq, p.hkv);
+      const int qb = qn & 1;
+      ok = warp_wait(&q_full[qb], (qn >> 1) & 1, status) &&
+           warp_wait(&kv_full[kvc % kStages], (kvc / kStages) & 1, status);
+      if (!ok) break;
+      tc_fence_after();
+      for (int w = 0; w < U.ntq; ++w) {
+        issue_s(w, qb, kvc % kStages);
+        if (leader) mma_commit(&s_full[w]);
+      }
+      for (int u = 0; u < U.nkv && ok; ++u) {
+        const int st = (kvc + u) % kStages;
+        const int st1 = (kvc + u + 1) % kStages;
+        bool next_loaded = false;
+        for (int w = 0; w < U.ntq && ok; ++w) {
+          if (u >= U.nk(w)) continue;
+          ok = warp_wait(&p_full[w], (w ? pcnt1 : pcnt0) & 1, status);
+          if (w) ++pcnt1;
+          else ++pcnt0;
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(w, st, u > 0);
+          if (u + 1 < U.nk(w)) {
+            if (!next_loaded) {
+              ok = warp_wait(&kv_full[st1], ((kvc + u + 1) / kStages) & 1, status);
+              if (!ok) break;
+              tc_fence_after();
+              next_loaded = true;
+            }
+            issue_s(w, qb, st1);
+            if (leader) mma_commit(&s_full[w]);
+          } else {
+            if (leader) mma_commit(&o_full[w]);
+          }
+        }
+        if (leader) mma_commit(&kv_empty[st]);
+      }
+      if (leader) mma_commit(&q_empty[qb]);
+      kvc += U.nkv;
+      ++qn;
+    }
+    if (!ok && leader) {
+      // timed out: make sure nothing we issued is still running before TMEM is freed
+      mma_commit(drain);
+      mbar_wait(drain, 0, status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int w = (warp - 4) >> 2;        // warpgroup = query tile t0 + w of each unit
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;    // row within the tile (= TMEM lane)
+    const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_addr = lane_base + kSCol[w], o_addr = lane_base + kOCol[w];
+    uint8_t* sP = smem + L::kP + w * kTile * kTile;
+    const bool al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
+    int scnt = 0, ocnt = 0;               // S tiles and units of this warpgroup so far
+    bool ok = true;
+    for (int rr = 0; rr < rounds && ok; ++rr) {
+      const int i = snake_unit(rr, c, G);
+      if (i >= n_units) continue;
+      const FwdUnit U = fwd_unit(pv, i, p.hq, p.hkv);
+      if (w >= U.ntq) continue;
+      const int t = U.t0 + w;
+      const int qrow_local = t * kTile + r;
+      const bool row_valid = qrow_local < U.doc_len;
+      const int64_t tok = (int64_t)U.doc_start + qrow_local;
+      const float fq = p.scale_log2 * scale_of(p.q_scales, tok, p.hq, U.h, row_valid);
+      const int nk = U.nk(w);
+      // K and V block-scale bytes of every key tile of the unit (one per 32-key group,
+      // 127 past the document end), staged in this warpgroup's own table (tiles past
+      // its capacity read them from global memory); each thread's loads come before
+      // its stores.  The warpgroup barrier of the previous epilogue separates the last
+      // reads of the old table from these stores.
+      uint32_t* tab = reinterpret_cast<uint32_t*>(smem + L::kTab) + w * (2 * L::kMaxTabTiles);
+      uint8_t* tb = reinterpret_cast<uint8_t*>(tab);
+      const int ntab = min(nk, L::kMaxTabTiles);
+      auto scale_bytes = [&](int uu, int g, uint32_t& kb, uint32_t& vb) {
+        const int kl = uu * kTile + g * 32;
+        const bool kv = kl < U.doc_len;
+        const int64_t ktok = (int64_t)U.doc_start + kl;
+        kb = kv ? __ldg(p.k_scales + ktok * p.hkv + U.hk) : 127u;
+        vb = kv ? __ldg(p.v_scales + ktok * p.hkv + U.hk) : 127u;
+      };
+      for (int e = r; e < ntab * 4; e += 128) {
+        uint32_t kb, vb;
+        scale_bytes(e >> 2, e & 3, kb, vb);
+        tb[(e >> 2) * 8 + (e & 3)] = (uint8_t)kb;
+        tb[(e >> 2) * 8 + 4 + (e & 3)] = (uint8_t)vb;
+      }
+      named_bar_sync(2 + w, 128);
+      float m = -INFINITY, lsum = 0.f;
+      for (int u = 0; u < nk; ++u) {
+        uint32_t kw = 0, vsf = 0;
+        if (u < ntab) {
+          const uint2 kv2 = *reinterpret_cast<const uint2*>(tab + 2 * u);
+          kw = kv2.x;
+          vsf = kv2.y;
+        } else {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t kb, vb;
+            scale_bytes(u, g, kb, vb);
+            kw |= kb << (8 * g);
+            vsf |= vb << (8 * g);
+          }
+        }
+        float fk[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) fk[g] = fq * ue8m0_to_f32((kw >> (8 * g)) & 0xFFu);
+        const bool diag = (u == t);
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], scnt & 1, status));
+        ++scnt;
+        if (!ok) break;
+        tc_fence_after();
+        // pass 1: row max of x = S * log2(e) over visible keys (the column factor is a
+        // positive power of two times a constant, so max(v * f) = f * max(v))
+        float mx = -INFINITY;
+        if (!diag) {
+          float cm[4];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tmem_ld32_max(s_addr + 32 * g, v, cm[g]);
+            tmem_ld_wait();
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) mx = fmaxf(mx, cm[g] * fk[g]);
+        } else {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + 32 * g, v);
+            tmem_ld_wait();
+            float b = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) b = (g * 32 + j) <= r ? fmaxf(b, __uint_as_float(v[j])) : b;
+            mx = fmaxf(mx, b * fk[g]);
+          }
+        }
+        const float m_new = fmaxf(m, mx);
+        const float alpha = fast_exp2(m - m_new);   // 0 on the first tile
+        // rescale the running O row when the max moved (warp-uniform decision)
+        if (u > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(o_addr + 32 * cc, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            tmem_st32(o_addr + 32 * cc, v);
+          }
+          tmem_st_wait();
+        }
+        lsum *= alpha;
+        const float neg = 8.0f - m_new;
+        // pass 2: boosted weights 2^(x - m + 8) and their E4M3 codes into the P tile
+        // (built twice: the causal mask only on the diagonal tile)
+        float2 acc2 = make_float2(0.f, 0.f);
+        auto pass2 = [&](auto diag_tile) {
+          constexpr bool kDiag = decltype(diag_tile)::value;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + 32 * g, v);
+            tmem_ld_wait();
+            uint32_t packed[8];
+            const float2 f2 = make_float2(fk[g], fk[g]), n2 = make_float2(neg, neg);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float2 x0 = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), f2, n2);
+              float2 x1 = ffma2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), f2, n2);
+              float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+              float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+              if (kDiag) {
+                const int kc = g * 32 + j;
+                p0.x = kc <= r ? p0.x : 0.f;
+                p0.y = kc + 1 <= r ? p0.y : 0.f;
+                p1.x = kc + 2 <= r ? p1.x : 0.f;
+                p1.y = kc + 3 <= r ? p1.y : 0.f;
+              }
+              acc2 = fadd2(acc2, fadd2(p0, p1));
+              packed[j >> 2] = (uint32_t)e4m3x2(p0.x, p0.y) | ((uint32_t)e4m3x2(p1.x, p1.y) << 16);
+            }
+            *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g, 128)) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            *reinterpret_cast<uint4*>(sP + swz_offset(r, 32 * g + 16, 128)) =
+                make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        };
+        if (diag) pass2(std::true_type{});
+        else pass2(std::false_type{});
+        lsum += acc2.x + acc2.y;
+        m = m_new;
+        // block-scale words of the PV MMA: P^ scale 1.0, V's token-block scales
+        tmem_st4(s_addr + 120, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_st4(s_addr + 124, vsf, vsf, vsf, vsf);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[w]);
+      }
+      // warpgroup-wide, so that the four warps leave together on a timeout
+      ok = named_bar_and(2 + w, 128, ok && mbar_wait(&o_full[w], ocnt & 1, status));
+      ++ocnt;
+      if (!ok) break;
+      tc_fence_after();
+      // O = bf16(acc / l) straight from registers (two 32-byte stores per 32 columns;
+      // 16-byte ones if O is only 16-byte aligned).  These TMEM loads complete before
+      // this warpgroup hands in the first P^ tile of its next unit, which is what the
+      // next unit's first (overwriting) PV MMA waits for.
+      const float inv = 1.0f / lsum;
+      __nv_bfloat16* orow = p.out + (tok * p.hq + U.h) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(o_addr + 32 * cc, v);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]) * inv, __uint_as_float(v[2 * j + 1]) * inv);
+          pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        if (row_valid) {
+          __nv_bfloat16* dst = orow + 32 * cc;
+          if (al32) {
+            st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+            st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      }
+      if (row_valid) p.lse[(int64_t)U.h * p.T + tok] = (m + __log2f(lsum) - 8.0f) * 0.69314718055994531f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
 // Rows outside every document: O = 0, LSE = +inf.
 template <int D>
 __global__ void fwd_tail_kernel(const int* plan, int T, int hq, __nv_bfloat16* out, float* lse) {
@@ -567,11 +998,28 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
   const int64_t max_items = (int64_t)T / (kTile * kItemTiles) + N + 1;
   const int64_t grid = max_items * hq;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  constexpr int smem = FwdSmem<D>::kAlloc;
-  cudaError_t e = prepare_kernel<attn_fwd_kernel<D, STRICT>>(smem);
-  if (e != cudaSuccess) return e;
-  if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
-  attn_fwd_kernel<D, STRICT><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  cudaError_t e;
+  if constexpr (STRICT) {
+    constexpr int smem = FwdSmem<D>::kAlloc;
+    e = prepare_kernel<attn_fwd_kernel<D, STRICT>>(smem);
+    if (e != cudaSuccess) return e;
+    if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
+    attn_fwd_kernel<D, STRICT><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  } else {
+    // persistent: one CTA per SM (fewer when there are fewer units than SMs)
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    constexpr int smem = PersistSmem<D>::kAlloc;
+    int regs = 0;
+    e = prepare_kernel<attn_fwd_persist_kernel<D>>(smem, &regs);
+    if (e != cudaSuccess) return e;
+    if (regs != kPersistLaunchRegs) return cudaErrorInvalidConfiguration;
+    const unsigned pgrid = (unsigned)(grid < sms ? grid : sms);
+    if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
+    attn_fwd_persist_kernel<D><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  }
   e = cudaGetLastError();
   if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
   if (e != cudaSuccess) return e;
