@@ -99,13 +99,16 @@ __global__ void __launch_bounds__(kCThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_full + 4);
   int* status = const_cast<int*>(p.plan) + kPlanStatus;
 
-  const int n_items = p.plan[kPlanFwdItems];
   const int item_idx = blockIdx.x / p.hq;
   const int h = blockIdx.x % p.hq;
-  if (item_idx >= n_items) return;
+  // the item, its document span and the item count in one round trip: the grid never
+  // exceeds the plan capacity, so the first two reads stay inside the plan also for a
+  // CTA without an item
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int4 item = pv.fwd_items[item_idx];
-  const int2 span = pv.fwd_span[item_idx];      // loaded alongside the item (no dependent load)
+  const int2 span = pv.fwd_span[item_idx];
+  const int n_items = p.plan[kPlanFwdItems];
+  if (item_idx >= n_items) return;
   const int t0 = item.y, ntq = item.z;
   const int doc_start = span.x;
   const int doc_len = span.y;
@@ -481,6 +484,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
         const float l = xsum[r] + xsum[128 + r];
         const float inv = 1.0f / l;
         __nv_bfloat16* orow = p.out + (tok * p.hq + h) * D + oc0;
+        const bool al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 #pragma unroll 1
         for (int c = 0; c < kOCols / 32; ++c) {
           uint32_t v[32];
@@ -494,9 +498,15 @@ __global__ void __launch_bounds__(kCThreads, 1)
                                                         __uint_as_float(v[2 * j + 1]) * inv);
               pk[j] = *reinterpret_cast<uint32_t*>(&b2);
             }
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+            __nv_bfloat16* dst = orow + 32 * c;
+            if (al32) {                  // two 32-byte stores; 16-byte ones if O is only 16-byte aligned
+              st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+              st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
           }
         }
         if (wg == 0 && row_valid) p.lse[(int64_t)h * p.T + tok] = (m + __log2f(l) - 8.0f) * 0.69314718055994531f;
