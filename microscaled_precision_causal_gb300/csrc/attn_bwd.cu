@@ -946,43 +946,79 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const __half* acc, con
 }
 
 // d = 128 (default and mixed routes): as dq_finalize_kernel for the head-dim-major
-// dQ^T chunks.  Thread = (query half, head-dim row d): it reads its row's 16-byte
-// units and writes each query's element, a warp covering 32 consecutive d of one
-// output row per store.
+// dQ^T chunks, transposed through shared memory.  Persistent CTAs walk the
+// (document tile, query head) chunks; each 32 KB chunk is copied into one of two
+// shared-memory buffers with cp.async while the previous one is converted, so two
+// chunks per CTA are in flight.  Thread = (query row q, head-dim half): it gathers
+// the row's 64 values from the chunk (a warp reads 32 consecutive queries of one
+// head-dim row, 64 contiguous bytes) and writes them as 32-byte stores of the
+// row-major dQ row (16-byte ones if dQ is only 16-byte aligned).
+constexpr int kDqtFinalizeSmem = 2 * 32768;
+
 __global__ void __launch_bounds__(256) dqt_finalize_kernel(const __half* acc, const int32_t* cu, const int* plan,
                                                            const float* boost, int N, int T, int hq, int hkv,
                                                            float scale, __nv_bfloat16* dq, __nv_bfloat16* dk,
                                                            __nv_bfloat16* dv) {
   constexpr int D = 128;
+  extern __shared__ __align__(16) uint8_t fsm[];
   const bool bad = plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS;
   const int valid = bad ? 0 : plan[kPlanValid];
   const int ntiles = bad ? 0 : plan[kPlanTiles];
   const PlanView pv = plan_view(plan, T, N);
-  const int hf = threadIdx.x >> 7, d = threadIdx.x & 127;
   const int64_t units = (int64_t)ntiles * hq;
-  for (int64_t un = blockIdx.x; un < units; un += gridDim.x) {
+  const bool al32 = (reinterpret_cast<uintptr_t>(dq) & 31) == 0;
+  auto issue = [&](int64_t un, int buf) {      // this thread's eight 16-byte pieces of the chunk
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(acc + dqt_chunk_elems(un / hq, (int)(un % hq), hq));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int off = (k * 256 + (int)threadIdx.x) * 16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(fsm + buf * 32768 + off)),
+                   "l"(src + off)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  const int q = threadIdx.x & 127, half = threadIdx.x >> 7;
+  int buf = 0;
+  if ((int64_t)blockIdx.x < units) issue(blockIdx.x, 0);
+  for (int64_t un = blockIdx.x; un < units; un += gridDim.x, buf ^= 1) {
+    const bool more = un + gridDim.x < units;
+    if (more) issue(un + gridDim.x, buf ^ 1);   // that buffer was released by the barrier closing the last pass
+    if (more) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     const int tile = (int)(un / hq), h = (int)(un % hq);
     const int doc = upper_doc(pv.tile_prefix, N, tile);
     const int t = tile - pv.tile_prefix[doc];
     const int s0 = cu[doc];
     const int rows = min(kTile, cu[doc + 1] - s0 - t * kTile);
-    const float mul = scale / boost[(int64_t)doc * hq + h];
-    const uint8_t* chunk = reinterpret_cast<const uint8_t*>(acc + dqt_chunk_elems(tile, h, hq));
-    __nv_bfloat16* out = dq + (((int64_t)s0 + t * kTile + hf * 64) * hq + h) * D + d;
-#pragma unroll 2
-    for (int u = 0; u < 8; ++u) {
-      const int q0 = hf * 64 + u * 8;
-      if (q0 >= rows) break;
-      const uint4 in = *reinterpret_cast<const uint4*>(chunk + dqt_chunk_byte(hf, d, u));
-      const __half2* hv = reinterpret_cast<const __half2*>(&in);
+    if (q < rows) {
+      const float mul = scale / boost[(int64_t)doc * hq + h];
+      const uint8_t* base = fsm + buf * 32768 + (q >> 6) * 16384 + (q & 7) * 2;
+      const int unit = (q & 63) >> 3;
+      __nv_bfloat16* orow = dq + (((int64_t)s0 + t * kTile + q) * hq + h) * D + half * 64;
 #pragma unroll
-      for (int e2 = 0; e2 < 4; ++e2) {
-        const float2 f = __half22float2(hv[e2]);
-        const int q = q0 + 2 * e2;
-        if (q < rows) out[(int64_t)(u * 8 + 2 * e2) * hq * D] = __float2bfloat16_rn(f.x * mul);
-        if (q + 1 < rows) out[(int64_t)(u * 8 + 2 * e2 + 1) * hq * D] = __float2bfloat16_rn(f.y * mul);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int d = half * 64 + c * 16 + 2 * j;
+          const float a = __half2float(*reinterpret_cast<const __half*>(base + d * 128 + ((unit ^ (d & 7)) << 4)));
+          const float b =
+              __half2float(*reinterpret_cast<const __half*>(base + (d + 1) * 128 + ((unit ^ ((d + 1) & 7)) << 4)));
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(a * mul, b * mul);
+          pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        __nv_bfloat16* dst = orow + c * 16;
+        if (al32) {
+          st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
       }
     }
+    __syncthreads();
   }
   constexpr int kVpr = D / 8;
   const int64_t tq = (int64_t)(T - valid) * hq * kVpr, tk = (int64_t)(T - valid) * hkv * kVpr;
@@ -1427,8 +1463,15 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   if (e != cudaSuccess) return e;
   if (ev && ev[2]) cudaEventRecord(static_cast<cudaEvent_t>(ev[2]), stream);
   if (!STRICT && D == 128) {
-    dqt_finalize_kernel<<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
-                                                     hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
+    e = prepare_kernel<dqt_finalize_kernel>(kDqtFinalizeSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    dqt_finalize_kernel<<<3 * sms, 256, kDqtFinalizeSmem, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan,
+                                                                    boost, N, T, hq, hkv, scale,
+                                                                    static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
   } else if (!STRICT) {
     dq_finalize_kernel<D><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
                                                        hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
