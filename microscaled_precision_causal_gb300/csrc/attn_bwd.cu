@@ -105,7 +105,7 @@ struct BwdSmem {
   static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query]
   static constexpr int kDS = kPt + kTile * kTile;             // dS^ codes, [key][query]
   static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
-  // per-query row data: -lse2[128], -D[128], chunk scale bytes[8] + dQ boost (4 words),
+  // per-query row data: -lse2[128], -D[128], chunk scale bytes[8] (4 words reserved),
   // then (strict) s_Q[128] and s_dO[128] as floats
   static constexpr int kRowBuf = (128 * 2 + 4 + 128 * 2) * 4;
   static constexpr int kE = kRow + 2 * kRowBuf;               // 16 block exponents (+ strict per-row exponents)
@@ -407,7 +407,6 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       const int h = hk * g + k / qtiles, t = u + k % qtiles;
       float lv[4], dv[4], sqv[4], sdv[4];
       uint8_t scb = 127;
-      float bst = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int ql = t * kTile + q * 32 + lane;
@@ -425,7 +424,6 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         const uint8_t* src = lane < 4 ? p.q_scales : p.do_scales;
         if (ql < doc_len) scb = __ldg(src + ((int64_t)doc_start + ql) * p.hq + h);
       }
-      if (lane == 8 && !STRICT) bst = __ldg(p.boost + (int64_t)doc * p.hq + h);   // dQ boost of (document, query head)
       if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&row_empty[b], ((k >> 1) - 1) & 1, status))) break;
       float* rb = rowbuf + b * (L::kRowBuf / 4);
 #pragma unroll
@@ -440,7 +438,6 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           rb[388 + i] = sdv[q];
         }
       }
-      if (lane == 8 && !STRICT) rb[258] = bst;
       if (lane < 8) reinterpret_cast<uint8_t*>(rb + 256)[lane] = scb;
       mbar_arrive(&row_full[b]);
     }
