@@ -222,3 +222,25 @@ def test_training_call_replays_from_a_cuda_graph():
         assert torch.equal(getattr(att, n), eager[n]), n
     a, b = att.dq.float().cpu().numpy(), eager["dq"].float().cpu().numpy()
     assert norm_max_err(a, b) < 2e-3
+
+
+@pytest.mark.gpu
+def test_forward_document_longer_than_the_scale_table():
+    """A document of more than 1024 key tiles (131,972 tokens): each forward softmax
+    warpgroup stages the K/V scale bytes of at most 1024 key tiles in shared memory and
+    reads those of later tiles from global memory; the last query tiles use both, the
+    first tile only the table.  O and LSE of those tiles against the oracle."""
+    L = 1024 * 128 + 900
+    lengths = [300, L]
+    w = W.Workload("long_document", tuple(lengths), 1, 1, 64, seed=11)
+    inp = W.make_inputs(w, tensors=("q", "k", "v"))
+    g = run_gpu(inp, lengths, 1, 1, 64, with_bwd=False)
+    assert g["status"] == 0
+    s0 = lengths[0]
+    sub = {n: inp[n][s0:s0 + L] for n in ("q", "k", "v")}
+    nt = -(-L // 128)
+    o = run_oracle(sub, [L], 1, 1, 64, with_bwd=False, q_tiles={0: [0, nt - 2, nt - 1]})
+    rows = np.r_[0:128, (nt - 2) * 128:L]
+    e = norm_max_err(g["o"][s0:s0 + L][rows], o["o"][rows])
+    assert e <= TOL, f"o: {e:.3e}"
+    assert np.max(np.abs(g["lse"][:, s0:s0 + L][:, rows] - o["lse"][:, rows])) < 1e-3
