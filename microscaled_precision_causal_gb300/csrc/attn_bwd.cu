@@ -293,6 +293,14 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         for (int s = 0; s < D / 32; ++s)
           if (leader) mma_f8(tbase + kP, v_kmaj(32 * s), do_kmaj(st * L::kTileBytes + 32 * s), idesc_f8(128, 128, 0, 0), s > 0);
       };
+      // dP^T for the queries of one 64-query half qh (columns kP + 64 qh ..)
+      auto issue_dp_half = [&](int st, int qh) {
+#pragma unroll
+        for (int s = 0; s < D / 32; ++s)
+          if (leader)
+            mma_f8(tbase + kP + 64 * qh, v_kmaj(32 * s), do_kmaj(st * L::kTileBytes + qh * 64 * D + 32 * s),
+                   idesc_f8(128, 64, 0, 0), s > 0);
+      };
       // dQ^T = K^T dS^T per 64-query half (A: K keys x d read d-major; B: the half's
       // dS^ tile, queries contiguous)
       auto issue_dqt = [&](int hf) {
@@ -360,6 +368,10 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_dqt(1);
+          // the next step's dP^T for queries 64..127 goes into the columns the dQ^T halves
+          // do not use (the scale words there were read by the dK and dQ^T MMAs issued
+          // before it), so only the other half waits for the readout of the high half
+          if (!MIXED && more) issue_dp_half(st1, 1);
         } else if (!STRICT) {
           if (k > 0) {                         // the previous partial has been read
             ok = warp_wait(dq_empty, (k - 1) & 1, status);
@@ -386,7 +398,8 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
             issue_s(st1);
             if (leader) mma_commit(s_full);
           }
-          issue_dp(st1);
+          if (kDQT && !MIXED) issue_dp_half(st1, 0);
+          else issue_dp(st1);
           if (leader) mma_commit(dp_full);
         }
       }
