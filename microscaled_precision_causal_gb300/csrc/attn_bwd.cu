@@ -483,9 +483,14 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       const int b = k & 1;
       const float* rb = rowbuf + b * (L::kRowBuf / 4);
       const uint8_t* cs = reinterpret_cast<const uint8_t*>(rb + 256);
-      // per warp: no warpgroup needs another's data before the barrier that closes P^
-      // (the block exponents of the last step were all read before that barrier)
-      ok = __all_sync(0xffffffffu, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
+      // default and mixed routes: per warp, since no warpgroup needs another's data before
+      // the barrier that closes P^ (the block exponents of the last step were all read
+      // before that barrier); the strict options keep the warpgroups in step here, which
+      // measured faster for their per-key folds
+      if constexpr (STRICT)
+        ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
+      else
+        ok = __all_sync(0xffffffffu, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
       // 2^8 P = 2^(x - LSE log2 e + 8) for this warpgroup's query chunks
