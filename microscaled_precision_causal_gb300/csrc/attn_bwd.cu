@@ -491,7 +491,12 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       else
         ok = __all_sync(0xffffffffu, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
-      if (!ok) break;
+      if (!ok) {
+        // a warp whose wait ran out still meets the barrier that closes P^ (with a false
+        // vote), so that the other compute warps learn of it there and none is left waiting
+        if constexpr (!STRICT) named_bar_and(1, kCompute, false);
+        break;
+      }
       tc_fence_after();
       // 2^8 P = 2^(x - LSE log2 e + 8) for this warpgroup's query chunks
       float pr[kCPW][32];
