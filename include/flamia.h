@@ -260,7 +260,9 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
  * are rejected with FLAMIA_ERR_WORKSPACE before anything is launched.  The
  * first call on each device resolves the array's address (cudaGetSymbolAddress,
  * with that device current) and caches it: make that first call before any
- * stream capture.  The call allocates nothing.  All calls share the array:
+ * stream capture.  The cached address is only valid for the device's current
+ * context: after cudaDeviceReset on that device do not call this function
+ * again in the same process.  The call allocates nothing.  All calls share the array:
  * calls whose GPU work overlaps race and give wrong results; the fp16 dQ
  * accumulator is cleared by every call. */
 #define FLAMIA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)

@@ -12,7 +12,10 @@
 //
 // Set-up: the first call on each device (with that device current) resolves
 // the array's device address with cudaGetSymbolAddress and caches it; make
-// that first call before any stream capture.  The call itself allocates
+// that first call before any stream capture.  The cached address belongs to
+// the device's current context: after cudaDeviceReset (or anything else that
+// destroys and re-creates the primary context) the array may move, so a
+// process that resets a device must not call this entry point on it again.  The call itself allocates
 // nothing (no cudaMalloc / cudaFree, no allocating library routine).
 //
 // Sharing: every call uses the same array, which keeps the previous call's
@@ -41,9 +44,6 @@ extern "C" int flamia_bwd_static_scratch(const flamia_qtensor* q, const flamia_q
                                          int hkv, int head_dim, int causal, float softmax_scale,
                                          const flamia_options* opt, const void* plan, void* dq_bf16, void* dk_bf16,
                                          void* dv_bf16, void* stream) {
-  if (total_tokens < 0 || num_seqs < 0 || hq <= 0 || hkv <= 0) return FLAMIA_ERR_INVALID_ARG;
-  const size_t need = flamia_bwd_workspace_bytes(total_tokens, num_seqs, hq, hkv, head_dim);
-  if (need == 0 || need > kScratchBytes) return FLAMIA_ERR_WORKSPACE;  // problem too large for the static scratch
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLAMIA_ERR_CUDA;
   void* ptr = g_scratch_ptr[dev].load(std::memory_order_acquire);
@@ -51,6 +51,9 @@ extern "C" int flamia_bwd_static_scratch(const flamia_qtensor* q, const flamia_q
     if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess || !ptr) return FLAMIA_ERR_CUDA;
     g_scratch_ptr[dev].store(ptr, std::memory_order_release);
   }
+  // flamia_bwd checks every argument first and the workspace size last, so a bad
+  // argument returns the same code as there, and only a problem larger than the
+  // array returns FLAMIA_ERR_WORKSPACE (before anything is launched).
   return flamia_bwd(q, k, v, out_bf16, lse, dout_bf16, cu_seqlens, num_seqs, total_tokens, hq, hkv, head_dim, causal,
                     softmax_scale, opt, plan, dq_bf16, dk_bf16, dv_bf16, ptr, kScratchBytes, stream);
 }

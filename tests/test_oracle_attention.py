@@ -455,3 +455,132 @@ def test_mixed_and_strict_are_separate():
     q, k, v, do, cu = _inputs([40], 1, 1, 16, seed=43)
     with pytest.raises(ValueError):
         O.run_training_call(q, k, v, do, cu, 1, 1, opts=O.Options(mixed=True, strict=True))
+
+
+# ------------------------------------------------------------ dS block quantizer (reading C-9)
+#
+# [EN] section 3 ("the analogous region is a 32 by 32 square") and section 5 (the
+# 32 by 32 maxima of dS); [KO] section 3.3: dS is quantized with one round-up
+# exponent per document-local 32x32 block (query block x key block).  The pins
+# below fix the grouping, the exponent rule and the treatment of masked (zero)
+# entries from values worked out by hand, and each plausible slip (one exponent
+# per row, 32x128 blocks, one exponent per tile, the floor rule, an exponent off
+# by one) is planted on the CPU and shown to fail them.
+
+def _ds_hand_example():
+    """A 64x64 dS tile (query rows 128..191, key columns 0..63 of a document)
+    holding a few entries; every expected value below was worked out by hand
+    from the E4M3 grid (3 mantissa bits, subnormal step 2**-9, max 448)."""
+    x = np.zeros((64, 64))
+    want = np.zeros((64, 64))
+    # block (0, 0): amax 448 -> e = 0
+    x[3, 5], want[3, 5] = 448.0, 448.0
+    x[0, 1], want[0, 1] = 5 * 2.0 ** -9, 5 * 2.0 ** -9          # subnormal code 5, exact
+    x[0, 7], want[0, 7] = 100.5, 104.0                          # grid step 8 in [64, 128)
+    x[2, 2], want[2, 2] = -0.296875, -0.3125                    # 9.5 steps of 2**-5: tie -> even
+    # block (0, 1): amax 900 = 1.7578 * 2**9 -> e = 2 (448 * 2 = 896 < 900)
+    x[0, 40], want[0, 40] = 900.0, 896.0                        # 225 -> 224 (step 16)
+    x[1, 33], want[1, 33] = 5 * 2.0 ** -9, 2.0 ** -7            # 1.25 subnormal steps -> 1, times 4
+    x[5, 50], want[5, 50] = 5.25, 5.0                           # 1.3125: tie between 1.25 and 1.375
+    x[7, 45], want[7, 45] = 6 * 2.0 ** -9, 2.0 ** -6            # 1.5 subnormal steps -> 2, times 4
+    # block (1, 0): amax 1 -> e = -8 (448 / 256 = 1.75 >= 1 > 448 / 512)
+    x[40, 2], want[40, 2] = 1.0, 1.0
+    x[33, 0], want[33, 0] = 5 * 2.0 ** -17, 5 * 2.0 ** -17      # 5 * 2**-9 after scaling: exact
+    x[63, 31], want[63, 31] = 25 * 2.0 ** -13, 0.0029296875     # 0.78125: tie -> 0.75, / 256
+    # block (1, 1): no entry (masked keys) -> all zero
+    return x, want
+
+
+def _ds_blocks_pins(fn):
+    """Every check the 32x32 dS block rule must pass, run against ``fn``."""
+    x, want = _ds_hand_example()
+    got = fn(x, 128, 0)
+    assert np.array_equal(got, want), np.argwhere(got != want)[:4]
+    rng = np.random.default_rng(50)
+    for R, C, qoff, koff in ((128, 128, 0, 0), (97, 128, 256, 128), (128, 45, 384, 0), (3, 5, 128, 256)):
+        ds = rng.standard_normal((R, C)) * np.exp2(rng.integers(-12, 12, (R, C)))
+        ds[rng.random((R, C)) < 0.2] = 0.0                      # masked entries are exact zeros
+        ds[: min(R, 32), : min(C, 32)] *= 2.0 ** 10              # one block far above the others
+        out = fn(ds, qoff, koff)
+        assert np.all(out[ds == 0] == 0)
+        for r0 in range(0, R, 32):
+            for c0 in range(0, C, 32):
+                blk = ds[r0:r0 + 32, c0:c0 + 32]
+                ob = out[r0:r0 + 32, c0:c0 + 32]
+                # locality: the block's result depends on that block alone
+                assert np.array_equal(ob, fn(blk, 0, 0))
+                amax = np.abs(blk).max()
+                if amax == 0:
+                    continue
+                # the exponent from an independent closed form (amax = f 2**k, f in [0.5, 1))
+                f, k = np.frexp(amax)
+                e = k - 9 + (f > 0.875)
+                assert 224.0 < amax * 2.0 ** -e <= 448.0
+                # every value sits on the E4M3 grid of that exponent, within half a step
+                y = ob * 2.0 ** -e
+                yb = np.abs(blk) * 2.0 ** -e
+                step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6))), -6) - 3)
+                assert np.all(np.abs(y / step - np.round(y / step)) == 0)
+                assert np.all(np.abs(np.abs(y) - yb) <= step / 2)
+                # scaling the block by 2**j scales its result exactly (away from the subnormals)
+                big = np.abs(blk) * 2.0 ** -e >= 2.0 ** -6
+                assert np.array_equal(fn(blk * 8.0, 0, 0)[big], ob[big] * 8.0)
+
+
+def test_ds_block_quantizer_pins():
+    _ds_blocks_pins(O.flamia_oracle._quantize_ds_blocks)
+
+
+def _mutant_per_row(dS, qoff, koff):
+    e = O.roundup_exponent(np.abs(dS).max(axis=1))[:, None]
+    return O.e4m3_round(dS * np.exp2(-e)) * np.exp2(e)
+
+
+def _mutant_wide_blocks(dS, qoff, koff):          # 32 x 128 blocks
+    out = np.zeros_like(dS)
+    for r0 in range(0, dS.shape[0], 32):
+        blk = dS[r0:r0 + 32]
+        e = O.roundup_exponent(np.abs(blk).max())
+        out[r0:r0 + 32] = O.e4m3_round(blk * 2.0 ** -e) * 2.0 ** e
+    return out
+
+
+def _mutant_per_tile(dS, qoff, koff):
+    e = O.roundup_exponent(np.abs(dS).max())
+    return O.e4m3_round(dS * 2.0 ** -e) * 2.0 ** e
+
+
+def _mutant_rule(rule_shift, use_floor=False):
+    def fn(dS, qoff, koff):
+        out = np.zeros_like(dS)
+        for r0 in range(0, dS.shape[0], 32):
+            for c0 in range(0, dS.shape[1], 32):
+                blk = dS[r0:r0 + 32, c0:c0 + 32]
+                amax = np.abs(blk).max()
+                e = (O.floor_exponent(amax) if use_floor else O.roundup_exponent(amax)) + rule_shift
+                out[r0:r0 + 32, c0:c0 + 32] = O.e4m3_round(blk * 2.0 ** -e) * 2.0 ** e
+        return out
+    return fn
+
+
+@pytest.mark.parametrize("mutant", [_mutant_per_row, _mutant_wide_blocks, _mutant_per_tile,
+                                    _mutant_rule(1), _mutant_rule(-1), _mutant_rule(0, use_floor=True)],
+                         ids=["per_row", "32x128", "per_tile", "exp_plus_1", "exp_minus_1", "floor_rule"])
+def test_ds_block_pins_reject_planted_mistakes(mutant):
+    with pytest.raises(AssertionError):
+        _ds_blocks_pins(mutant)
+
+
+def test_backward_uses_the_block_quantized_ds_for_dq_and_dk(monkeypatch):
+    """Swapping the 32x32 rule for the per-row slip changes both dQ and dK of the
+    training call: the block-quantized dS feeds both products (dK through its
+    transpose, which the 32x32 square allows)."""
+    lengths, hq, hkv, d = [150], 1, 1, 16
+    q, k, v, do, cu = _inputs(lengths, hq, hkv, d, seed=51)
+    do[:, :, :] *= np.exp2(np.random.default_rng(52).integers(-9, 9, (150, 1, 1)))   # spread the row scales
+    base = _train(q, k, v, do, cu, hq, hkv)
+    monkeypatch.setattr(O.flamia_oracle, "_quantize_ds_blocks", _mutant_per_row)
+    pert = _train(q, k, v, do, cu, hq, hkv)
+    assert not np.array_equal(base["dq"], pert["dq"])
+    assert not np.array_equal(base["dk"], pert["dk"])
+    assert np.array_equal(base["dv"], pert["dv"])          # dV does not use dS

@@ -265,3 +265,41 @@ def test_nvfp4_quantizer_pins():
     assert cosine(xh, x) > 0.97
     # the group maximum reconstructs within one E2M1 step of its scaled value
     assert np.all(np.abs(np.abs(xh.reshape(9, 2, 2, 16)).max(-1) - amax) <= 1.0 * s + 1e-12)
+
+
+def test_nvfp4_hand_worked_groups():
+    """Five 16-element groups whose scales and codes were worked out by hand from
+    reading C-7 (s = E4M3(amax / 6), raised to 2**-9 for a non-zero group that
+    would round to 0; codes = E2M1(x / s), ties to the even code, saturating):
+    a scale tie that rounds down, one that rounds up, the 2**-9 floor, an
+    all-zero group, and a scale that saturates at 448 (so the codes saturate at
+    6 s).  Every input is exact in bf16."""
+    groups = [
+        # amax 6.375: 6.375 / 6 = 1.0625, tie between 1 and 1.125 -> 1 (even); 6.375 saturates to 6
+        ([6.375, 1.3125, -2.625, 0.1875, 0.25, 0.75, 1.25, 2.5, 5.0, -0.75],
+         1.0, 0x38, [6.0, 1.5, -3.0, 0.0, 0.0, 1.0, 1.0, 2.0, 4.0, -1.0], [7, 3, 13, 0, 0, 2, 2, 4, 6, 10]),
+        # amax 7.125: 7.125 / 6 = 1.1875, tie between 1.125 and 1.25 -> 1.25 (even);
+        # 7.125 / 1.25 = 5.7 -> 6; -3.125 / 1.25 = -2.5, tie -> -2; 0.625 / 1.25 = 0.5
+        ([7.125, -3.125, 0.625], 1.25, 0x3A, [7.5, -2.5, 0.625], [7, 12, 1]),
+        # amax 1.5 * 2**-10: amax / 6 = 2**-12 rounds to 0 in E4M3 -> floor 2**-9;
+        # 0.75 steps -> 1 (tie to even), -0.25 steps -> -0 (tie to even)
+        ([1.5 * 2.0 ** -10, -2.0 ** -11], 2.0 ** -9, 0x01, [2.0 ** -9, -0.0], [2, 8]),
+        # all zero: scale code 0, codes 0
+        ([], 0.0, 0x00, [], []),
+        # amax 2944 = 1.4375 * 2**11: 2944 / 6 = 490.7 saturates to 448; 2944 / 448 = 6.57 -> 6
+        ([2944.0, -1344.0], 448.0, 0x7E, [2688.0, -1344.0], [7, 13]),
+    ]
+    x = np.zeros((1, 1, 16 * len(groups)))
+    for gi, (vals, *_rest) in enumerate(groups):
+        x[0, 0, 16 * gi:16 * gi + len(vals)] = vals
+    assert np.array_equal(O.bf16_round(x), x)
+    codes, sc = O.quantize_nvfp4(x)
+    xh = O.dequantize_nvfp4(codes, sc)
+    for gi, (vals, s, s_code, recon, cds) in enumerate(groups):
+        assert sc[0, 0, gi] == s_code and O.e4m3_decode(sc[0, 0, gi]) == s, gi
+        n = len(vals)
+        seg = slice(16 * gi, 16 * gi + n)
+        assert np.array_equal(xh[0, 0, seg], recon), (gi, xh[0, 0, seg])
+        assert np.array_equal(np.signbit(xh[0, 0, seg]), np.signbit(np.array(recon, float))), gi
+        assert list(codes[0, 0, seg]) == cds, (gi, list(codes[0, 0, seg]))
+        assert np.all(codes[0, 0, 16 * gi + n:16 * (gi + 1)] == 0), gi
