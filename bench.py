@@ -54,7 +54,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA-graph replays")
+    ap.add_argument("--rounds", type=int, default=4, help="the timed steps are split into this many rounds")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
+    ap.add_argument("--secondary-steps", type=int, default=30)
     return ap.parse_args()
 
 
@@ -211,94 +213,293 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- our arm
 
+# The other workloads of the pages' shapes, timed in the same run after the headline
+# (parity cases in the tests; here for their throughput): (workload, route).
+SECONDARY = (
+    ("causal_b1_h2_s256_d64", "default"),
+    ("gqa_b4_s8192_hq32_hkv8_d128", "default"),
+    ("mixed_nvfp4_gqa_b4_s8192", "mixed"),
+    ("strict_packed_4x8192_h16_t3", "strict"),
+    ("strict_packed_4x8192_h16_t3", "default"),
+)
+EX2_PER_CLK_PER_SM = 32      # MUFU ex2 issue rate of B300-class SMs ([EN] section 7; probe in the design notes)
+
+
 def kernel_source_sha(name):
     with open(os.path.join(ROOT, "microscaled_precision_causal_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def traffic_for(kernel_file, workload):
+def traffic_record(kernel_file, workload):
+    """DRAM bytes per launch of a kernel from profiles/traffic.json (one ncu capture),
+    valid only while the kernel's source is unchanged and for the same workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path)).get(kernel_file)
-    if not rec or rec.get("source_sha256") != kernel_source_sha(kernel_file):
+    if not rec or rec.get("source_sha256") != kernel_source_sha(kernel_file) or rec.get("workload") != workload:
         return None
-    per_unit = rec["dram_bytes_per_launch"] / rec["flops_per_launch"]
-    return {"bytes_per_flop": per_unit, "workload": rec.get("workload")}
+    return rec
 
 
-def quantizer_roofline(w, mode, ms, hbm_gbs):
-    """Algorithmic bytes of the Q/K/V quantization (token-block codes, scale bytes,
-    the K/V row stats; mixed: also the NVFP4 copies of Q and K and the per-token V
-    copy) over its measured time (the three or six launches of one step)."""
+def quantizer_bytes(w, mode):
+    """Algorithmic bytes of the Q/K/V quantization of one step: bf16 in, E4M3 codes and one
+    scale byte per row out, plus the K/V row stats; mixed: also the NVFP4 copies of Q and K
+    and the per-token V copy."""
     T, hq, hkv, d = w.total_tokens, w.hq, w.hkv, w.d
-    per = lambda H: T * H * d * (2 + 1) + T * H          # bf16 in, E4M3 out, one scale byte per row
-    total = per(hq) + 2 * per(hkv) + 2 * T * hkv * 8     # + (||x^||, max |x^|) of K and V
+    per = lambda H: T * H * d * (2 + 1) + T * H
+    total = per(hq) + 2 * per(hkv) + 2 * T * hkv * 8
     if mode == "mixed":
         nv = lambda H: T * H * d * (2 + 0.5) + T * H * d / 16
         total += nv(hq) + nv(hkv) + per(hkv)
-    gbs = total / (ms * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
-            "bytes_per_step": total, "ms": ms, "traffic": None}
+    return total
+
+
+def measure_fp8_peak(dev):
+    """Dense E4M3 GEMM throughput of this GPU: torch._scaled_mm at 8192^3 (per-tensor
+    scales, bf16 out), best of 10 after warm-up, CUDA events.  None if unavailable."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            mm()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
+
+
+def timing_event(torch_mod):
+    """A timing event that, recorded inside a stream capture, becomes a graph node."""
+    try:
+        return torch_mod.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+class WorkloadRun:
+    """One workload on one route: buffers, the captured training call, and its timings."""
+
+    def __init__(self, F, w, mode, dev, flush):
+        import torch
+        self.torch, self.F, self.w, self.mode, self.dev, self.flush = torch, F, w, mode, dev, flush
+        self.T, self.N = w.total_tokens, len(w.lengths)
+        self.pairs = W.visible_pair_count(w.lengths)
+        self.flops = 14.0 * w.d * w.hq * self.pairs
+        inp = W.make_inputs(w)
+        self.host = {n: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for n, b in inp.items()}
+        self.x = {n: t.to(dev) for n, t in self.host.items()}
+        self.cu_host = torch.tensor(w.cu_seqlens, dtype=torch.int32).pin_memory()
+        self.cu = self.cu_host.to(dev)
+        self.att = F.FlamiaAttention(self.T, self.N, w.hq, w.hkv, w.d, device=dev, strict=mode == "strict",
+                                     mixed=mode == "mixed")
+        self.stream = torch.cuda.current_stream(dev)
+        self.o_plain = F.Options()
+        import ctypes
+        ctypes.pointer(self.o_plain)[0] = self.att.opts
+
+    def step(self, o_fwd=None, o_bwd=None, qev=None):
+        att, cu = self.att, self.cu
+        att.plan_build(cu)
+        cur = self.torch.cuda.current_stream()     # the capture stream while a graph is captured
+        if qev:
+            qev[0].record(cur)
+        att.quantize(self.x["q"], self.x["k"], self.x["v"], cu)
+        if qev:
+            qev[1].record(cur)
+        att.opts = o_fwd or self.o_plain
+        att.forward(cu)
+        att.opts = o_bwd or self.o_plain
+        att.backward(self.x["do"], cu)
+        att.opts = self.o_plain
+
+    def _opts_with_events(self, n):
+        import ctypes
+        torch = self.torch
+        evs = [timing_event(torch) for _ in range(n)]
+        if any(e is None for e in evs):
+            return None
+        for e in evs:
+            e.record(self.stream)          # creates the underlying cudaEvent_t
+        arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
+        o = self.F.Options()
+        ctypes.pointer(o)[0] = self.att.opts
+        o.timing_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+        return evs, arr, o
+
+    def warm_and_capture(self, warmup):
+        torch = self.torch
+        for _ in range(max(warmup, 3)):
+            self.step()
+        torch.cuda.synchronize()
+        assert self.att.device_status() == 0, "device status error during warm-up"
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step()
+        torch.cuda.synchronize()
+        for _ in range(max(warmup, 3)):
+            self.graph.replay()
+        torch.cuda.synchronize()
+
+    def phases(self, n):
+        """Per-kernel times inside a CUDA graph of the step: the library's timing hook and
+        two events around the Q/K/V quantization are captured as event-record nodes; each
+        replay follows an L2 flush and is read before the next one."""
+        torch = self.torch
+        ef, eb = self._opts_with_events(2), self._opts_with_events(8)
+        qev = [timing_event(torch), timing_event(torch)]
+        if ef is None or eb is None or qev[0] is None:
+            return None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(ef[2], eb[2], qev)
+        torch.cuda.synchronize()
+        rows = []
+        for i in range(n + 2):
+            self.flush.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            if i >= 2:
+                e, b = ef[0], eb[0]
+                rows.append(dict(quantize_qkv=qev[0].elapsed_time(qev[1]), fwd_kernel=e[0].elapsed_time(e[1]),
+                                 bwd_prep=b[0].elapsed_time(b[1]), bwd_boost=b[2].elapsed_time(b[3]),
+                                 bwd_kernel=b[4].elapsed_time(b[5]), bwd_finalise=b[6].elapsed_time(b[7])))
+        assert self.att.device_status() == 0, "device status error during the phase replays"
+        del g
+        return {k: float(np.median([r[k] for r in rows])) for k in rows[0]}
+
+    def timed(self, steps, rounds, world):
+        """`steps` graph replays, each after an L2 flush (outside its events), bracketed
+        by a barrier and a synchronize; per-round mean, median over rounds."""
+        torch = self.torch
+        import torch.distributed as dist
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(steps):
+            self.flush.zero_()
+            starts[i].record(self.stream)
+            self.graph.replay()
+            ends[i].record(self.stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t1 = time.time()
+        ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
+        assert self.att.device_status() == 0, "device status error during the timed steps"
+        per_round = [float(c.mean()) for c in np.array_split(ms, max(1, rounds))]
+        return dict(mean=float(ms.mean()), median_of_rounds=float(np.median(per_round)), rounds=per_round,
+                    t_wall=(t0, t1))
+
+    def e2e(self, steps):
+        """The training call through the public API with host buffers: pinned inputs in and
+        results out inside the timed region.  The copies run on a second stream: dO comes
+        in while the forward runs and O goes out while the backward runs (Q, K, V and
+        cu_seqlens before the forward, dQ, dK, dV after the backward)."""
+        torch, att, x, host, stream = self.torch, self.att, self.x, self.host, self.stream
+        out_host = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in
+                    (("o", att.out), ("dq", att.dq), ("dk", att.dk), ("dv", att.dv))}
+        h2d = sum(t.numel() * t.element_size() for t in host.values()) + self.cu_host.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        copy_stream = torch.cuda.Stream(self.dev)
+        ev_qkv, ev_do, ev_fwd, ev_bwd, ev_out = (torch.cuda.Event() for _ in range(5))
+        res = []
+        for i in range(steps + 1):
+            self.flush.zero_()
+            e0.record(stream)
+            copy_stream.wait_event(e0)
+            with torch.cuda.stream(copy_stream):
+                self.cu.copy_(self.cu_host, non_blocking=True)
+                for n in ("q", "k", "v"):
+                    x[n].copy_(host[n], non_blocking=True)
+                ev_qkv.record(copy_stream)
+                x["do"].copy_(host["do"], non_blocking=True)
+                ev_do.record(copy_stream)
+            stream.wait_event(ev_qkv)
+            att.plan_build(self.cu)
+            att.quantize(x["q"], x["k"], x["v"], self.cu)
+            att.forward(self.cu)
+            ev_fwd.record(stream)
+            stream.wait_event(ev_do)
+            att.backward(x["do"], self.cu)
+            ev_bwd.record(stream)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(ev_fwd)
+                out_host["o"].copy_(att.out, non_blocking=True)
+                copy_stream.wait_event(ev_bwd)
+                for n, t in (("dq", att.dq), ("dk", att.dk), ("dv", att.dv)):
+                    out_host[n].copy_(t, non_blocking=True)
+                ev_out.record(copy_stream)
+            stream.wait_event(ev_out)
+            e1.record(stream)
+            e1.synchronize()
+            if i > 0:
+                res.append(e0.elapsed_time(e1))
+        return float(np.median(res)), h2d, d2h
+
+    def kernel_roofline(self, ph, fp8_peak):
+        d, hq = self.w.d, self.w.hq
+        f_fwd, f_bwd = 4.0 * d * hq * self.pairs, 10.0 * d * hq * self.pairs
+        if ph["bwd_kernel"] >= ph["fwd_kernel"]:
+            name, ms, flops, src = "attn_bwd_kernel", ph["bwd_kernel"], f_bwd, "attn_bwd.cu"
+        else:
+            name, ms, flops, src = "attn_fwd_kernel", ph["fwd_kernel"], f_fwd, "attn_fwd.cu"
+        ach = flops / (ms * 1e-3) / 1e12
+        rec = traffic_record(src, self.w.name) if self.mode == "default" else None
+        traffic = rec["dram_bytes_per_launch"] if rec else None
+        return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": ach / fp8_peak, "traffic": traffic, "algorithmic_flops": flops,
+                "per_unit": "FLOPs per launch = %s * head_dim * hq * visible pairs" % ("10" if "bwd" in name else "4")}
+
+    def release(self):
+        del self.graph
+        self.att = self.x = self.host = None
+        self.torch.cuda.empty_cache()
+
+
+def exp_ceiling(d, sms, sm_mhz):
+    """Upper bounds set by the MUFU exponentials: one ex2 per visible pair in the forward
+    and one in the backward, against 4d (forward), 10d (backward) and 14d (call) FLOPs."""
+    rate = EX2_PER_CLK_PER_SM * sms * sm_mhz * 1e6          # ex2 per second
+    return {"ex2_per_clk_per_sm": EX2_PER_CLK_PER_SM, "sms": sms, "sm_mhz": sm_mhz,
+            "fwd_tflops": 4.0 * d * rate / 1e12, "bwd_tflops": 10.0 * d * rate / 1e12,
+            "call_tflops": 7.0 * d * rate / 1e12}
 
 
 def run_ours(args, rank, world, local_rank):
     import torch
-    import torch.distributed as dist
     from microscaled_precision_causal_gb300 import build as _b
     _b.build()
     import microscaled_precision_causal_gb300 as F
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.WORKLOADS[args.workload]
-    T, N, hq, hkv, d = w.total_tokens, len(w.lengths), w.hq, w.hkv, w.d
-    pairs = W.visible_pair_count(w.lengths)
-    flops_step = 14.0 * d * hq * pairs
-    flops_fwd, flops_bwd = 4.0 * d * hq * pairs, 10.0 * d * hq * pairs
-
-    inp = W.make_inputs(w)
-    host = {n: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for n, b in inp.items()}
-    x = {n: t.to(dev) for n, t in host.items()}
-    cu_host = torch.tensor(w.cu_seqlens, dtype=torch.int32).pin_memory()
-    cu = cu_host.to(dev)
-    att = F.FlamiaAttention(T, N, hq, hkv, d, device=dev, strict=args.mode == "strict",
-                            mixed=args.mode == "mixed")
+    pk = peaks()
+    fp8_meas = measure_fp8_peak(dev) if rank == 0 else None
+    fp8_peak = max(fp8_meas or 0.0, 2.0 * pk["bf16"])
+    fp8_src = ("measured E4M3 _scaled_mm 8192^3 burst" if fp8_meas and fp8_meas >= 2.0 * pk["bf16"]
+               else "2 x %s bf16 burst (nominal FP8/BF16 ratio)" % pk["src"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    import ctypes
-
-    def make_opts(n):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for e in evs:
-            e.record(stream)          # creates the underlying cudaEvent_t
-        arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
-        o = F.Options()
-        ctypes.pointer(o)[0] = att.opts          # the mode's flags and operands
-        o.timing_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
-        return evs, arr, o
-
-    o_plain = F.Options()
-    ctypes.pointer(o_plain)[0] = att.opts
-
-    def step(o_fwd=None, o_bwd=None, qev=None):
-        att.plan_build(cu)
-        if qev:
-            qev[0].record(stream)
-        att.quantize(x["q"], x["k"], x["v"], cu)
-        if qev:
-            qev[1].record(stream)
-        att.opts = o_fwd or o_plain
-        att.forward(cu)
-        att.opts = o_bwd or o_plain
-        att.backward(x["do"], cu)
-        att.opts = o_plain
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    assert att.device_status() == 0, "device status error during warm-up"
+    w = W.WORKLOADS[args.workload]
+    run = WorkloadRun(F, w, args.mode, dev, flush)
+    run.warm_and_capture(args.warmup)
 
     gpu_index = local_rank
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -311,151 +512,88 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_clocks:
         sampler.start()
         time.sleep(0.3)
-
-    # Per-kernel phases: eager steps with the timing_events hook (a bounded sample).
-    n_ph = min(args.steps, 50)
-    per_step = [(make_opts(2), make_opts(8)) for _ in range(n_ph)]
-    qevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_ph)]
-    for i in range(n_ph):
-        flush.zero_()
-        step(per_step[i][0][2], per_step[i][1][2], qevs[i])
-    torch.cuda.synchronize()
-    # The whole step (plan, quantize, forward, backward) as one CUDA graph: the same
-    # launches, replayed without host launch gaps ([EN] Appendix D times CUDA graphs).
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        torch.cuda.synchronize()
-        for _ in range(max(args.warmup, 3)):
-            graph.replay()
-        torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ph = run.phases(min(args.steps, 30))
+    tm = run.timed(args.steps, args.rounds, world)
+    ms_step = tm["median_of_rounds"]
     if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()                      # L2 flush between timed steps (outside the events)
-        starts[i].record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    t_wall1 = time.time()
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kf = [f[0][0].elapsed_time(f[0][1]) for f, _ in per_step]
-    kb = [b[0][4].elapsed_time(b[0][5]) for _, b in per_step]
-    kbp = [b[0][0].elapsed_time(b[0][1]) for _, b in per_step]
-    kfin = [b[0][6].elapsed_time(b[0][7]) for _, b in per_step]
-    kq = [q0.elapsed_time(q1) for q0, q1 in qevs]
-    total_ms = float(sum(ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    assert att.device_status() == 0, "device status error during the timed steps"
-
-    # end to end: pinned host inputs -> device, the training call, results -> pinned host
-    out_host = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in
-                (("o", att.out), ("dq", att.dq), ("dk", att.dk), ("dv", att.dv))}
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + cu_host.numel() * 4
-    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # The copies run on a second stream so that they overlap the compute they do not
-    # feed: dO comes in while the forward runs and O goes out while the backward runs
-    # (Q, K, V and cu_seqlens before the forward, dQ, dK, dV after the backward).  More
-    # copy streams were measured slower: the host link is the limit, not the engines.
-    copy_stream = torch.cuda.Stream(dev)
-    ev_qkv, ev_do, ev_fwd, ev_bwd, ev_out = (torch.cuda.Event() for _ in range(5))
-    e2e_ms = []
-    for i in range(args.e2e_steps + 1):
-        flush.zero_()
-        e0.record(stream)
-        copy_stream.wait_event(e0)
-        with torch.cuda.stream(copy_stream):
-            cu.copy_(cu_host, non_blocking=True)
-            for n in ("q", "k", "v"):
-                x[n].copy_(host[n], non_blocking=True)
-            ev_qkv.record(copy_stream)
-            x["do"].copy_(host["do"], non_blocking=True)
-            ev_do.record(copy_stream)
-        stream.wait_event(ev_qkv)
-        att.plan_build(cu)
-        att.quantize(x["q"], x["k"], x["v"], cu)
-        att.forward(cu)
-        ev_fwd.record(stream)
-        stream.wait_event(ev_do)
-        att.backward(x["do"], cu)
-        ev_bwd.record(stream)
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(ev_fwd)
-            out_host["o"].copy_(att.out, non_blocking=True)
-            copy_stream.wait_event(ev_bwd)
-            for n, t in (("dq", att.dq), ("dk", att.dk), ("dv", att.dv)):
-                out_host[n].copy_(t, non_blocking=True)
-            ev_out.record(copy_stream)
-        stream.wait_event(ev_out)
-        e1.record(stream)
-        e1.synchronize()
-        if i > 0:
-            e2e_ms.append(e0.elapsed_time(e1))
-    e2e_mean = float(np.mean(e2e_ms))
+        ms_step = float(t.item())
+    e2e_ms, h2d, d2h = run.e2e(args.e2e_steps)
     if world > 1:
-        t = torch.tensor([e2e_mean], device=dev)
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_mean = float(t.item())
-
+        e2e_ms = float(t.item())
     lines = sampler.stop() if not args.no_clocks else None
-    clocks = ClockSampler.summarize(lines, t_wall0, t_wall1) if lines else None
+    clocks = ClockSampler.summarize(lines, *tm["t_wall"]) if lines else None
     if rank != 0:
         return None
-
-    pk = peaks()
-    fp8_peak = 2.0 * pk["bf16"]          # FP8 dense = 2 x BF16 dense (4.5 / 2.25 nominal ratio)
-    kf_ms, kb_ms = float(np.mean(kf)), float(np.mean(kb))
-    if kb_ms >= kf_ms:
-        dom, dom_ms, dom_flops, dom_src = "attn_bwd_kernel", kb_ms, flops_bwd, "attn_bwd.cu"
-    else:
-        dom, dom_ms, dom_flops, dom_src = "attn_fwd_kernel", kf_ms, flops_fwd, "attn_fwd.cu"
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    tr = traffic_for(dom_src, w.name)
-    traffic = tr["bytes_per_flop"] * dom_flops if tr else None
-    value = world * flops_step / (total_ms / args.steps * 1e-3) / 1e12
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = clocks["sm_mhz"] if clocks else 2070.0
+    value = world * run.flops / (ms_step * 1e-3) / 1e12
+    q_ms = ph["quantize_qkv"] if ph else None
+    qb = quantizer_bytes(w, args.mode)
+    qrec = traffic_record("quantize.cu", w.name) if args.mode == "default" else None
     res = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": w.name, "mode": args.mode, "cuda_graph": graph is not None, "total_tokens": T, "num_docs": N, "hq": hq, "hkv": hkv, "head_dim": d,
-                   "visible_pairs": pairs, "flops_per_step": flops_step,
+        "config": {"workload": w.name, "mode": args.mode, "cuda_graph": True, "total_tokens": run.T,
+                   "num_docs": run.N, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d, "visible_pairs": run.pairs,
+                   "flops_per_step": run.flops,
                    "l2": "flushed between timed steps (256 MiB write); step inputs 256 MiB > L2",
-                   "frac_of_fp8_peak": value / world / fp8_peak,
-                   "fp8_peak_tflops": fp8_peak, "peak_source": pk["src"] + " (2 x bf16 burst)"},
-        "phases_ms": {"quantize_qkv": float(np.mean(kq)), "fwd_kernel": kf_ms, "bwd_kernel": kb_ms,
-                      "bwd_prep": float(np.mean(kbp)), "bwd_finalise": float(np.mean(kfin))},
-        "quantizer_roofline": quantizer_roofline(w, args.mode, float(np.mean(kq)), pk["hbm"]),
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": traffic,
-                     "per_unit": "FLOPs per launch = %s * head_dim * hq * visible pairs" % ("10" if "bwd" in dom else "4")},
-        "e2e": {"value": world * flops_step / (e2e_mean * 1e-3) / 1e12, "unit": "TFLOPS",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
+                   "timing": "%d graph replays in %d rounds; ms_per_step = median of the round means "
+                             "(mean %.4f ms)" % (args.steps, args.rounds, tm["mean"]),
+                   "frac_of_fp8_peak": value / world / fp8_peak, "fp8_peak_tflops": fp8_peak,
+                   "fp8_peak_source": fp8_src, "fp8_measured_tflops": fp8_meas},
+        "phases_ms": ph,
+        "roofline": run.kernel_roofline(ph, fp8_peak) if ph else None,
+        "exp_ceiling": exp_ceiling(w.d, sms, sm_mhz),
+        "quantizer_roofline": ({"bound": "hbm", "achieved": qb / (q_ms * 1e-3) / 1e9, "peak": pk["hbm"],
+                                "unit": "GB/s", "frac": qb / (q_ms * 1e-3) / 1e9 / pk["hbm"],
+                                "bytes_per_step": qb, "ms": q_ms,
+                                "traffic": qrec["dram_bytes_per_launch"] * 3 if qrec else None,
+                                "measured": "inside the CUDA graph (event-record nodes), median of replays"}
+                               if ph else None),
+        "e2e": {"value": world * run.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "copies": "pinned host buffers; a second stream brings dO in during the forward and takes O out "
                           "during the backward"},
         "gpu_launches": LAUNCHES_PER_STEP[args.mode] * args.steps,
         "clocks": clocks,
     }
+    run.release()
     if not args.no_cpu_baseline:
         s = oracle_sample(w, args.cpu_seconds, mode=args.mode)
         res["cpu_baseline"] = {
             "value": s["tflops"], "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle",
             "sample": (f"oracle fwd+bwd (fp64 numpy) on the first {s['tokens']} tokens of the longest document, "
                        f"{s['heads']} query heads: {s['seconds']:.1f} s")}
+    if not args.no_secondary and world == 1:
+        res["workloads"] = {}
+        for wname, mode in SECONDARY:
+            if wname == w.name and mode == args.mode:
+                continue
+            ws = W.WORKLOADS[wname]
+            r = WorkloadRun(F, ws, mode, dev, flush)
+            r.warm_and_capture(3)
+            p2 = r.phases(10)
+            t2 = r.timed(args.secondary_steps, 3, 1)
+            v2 = r.flops / (t2["median_of_rounds"] * 1e-3) / 1e12
+            ent = {"mode": mode, "value": v2, "unit": "TFLOPS", "ms_per_step": t2["median_of_rounds"],
+                   "rounds_ms": t2["rounds"], "frac_of_fp8_peak": v2 / fp8_peak, "phases_ms": p2,
+                   "roofline": r.kernel_roofline(p2, fp8_peak) if p2 else None,
+                   "exp_ceiling_call_tflops": exp_ceiling(ws.d, sms, sm_mhz)["call_tflops"]}
+            r.release()
+            if not args.no_cpu_baseline:
+                s = oracle_sample(ws, args.cpu_seconds / 3, mode=mode)
+                ent["cpu_baseline"] = {"value": s["tflops"], "unit": "TFLOPS", "cores": blas_threads(),
+                                       "kind": "oracle",
+                                       "sample": f"first {s['tokens']} tokens, {s['heads']} query heads: "
+                                                 f"{s['seconds']:.1f} s"}
+            res["workloads"][f"{wname}/{mode}"] = ent
     return res
 
 

@@ -104,6 +104,16 @@ typedef struct flamia_options {
   void* const* timing_events;
   /* Mixed route operands (required when mixed_nvfp4 = 1, else ignored). */
   const struct flamia_mixed_operands* mixed;
+  /* Diagnostic output of flamia_bwd (NULL = off), for checking the centred
+     softmax gradient (FLAMIA review section 2, "The softmax gradient is a
+     centered product"; section 5, "An error decomposition for the centering
+     term"): device float [2, hq, T, T], caller-zeroed.  Slice 0 receives the
+     recomputed P_ij = exp(S_ij - LSE_i) and slice 1 dS_ij = P_ij (dP_ij - D_i),
+     both fp32 before any quantization, at [query token][key token] for every
+     visible pair (other entries are left untouched).  Default route only
+     (not strict, not mixed) and total_tokens <= 1024, else
+     FLAMIA_ERR_UNSUPPORTED.  A slower build of the backward kernel runs. */
+  float* debug_p_ds;
 } flamia_options;
 
 /* Operands of the mixed NVFP4/FP8 route (FLAMIA review section 2, "The mixed

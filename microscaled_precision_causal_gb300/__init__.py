@@ -40,7 +40,8 @@ class Options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "p_boost_log2", "bwd_p_boost_log2", "dq_headroom_log2", "strict_per_token", "strict_row_ds",
         "strict_causal_dq", "mixed_nvfp4", "deterministic")] + [("timing_events", ctypes.POINTER(ctypes.c_void_p)),
-                                                                 ("mixed", ctypes.c_void_p)]
+                                                                 ("mixed", ctypes.c_void_p),
+                                                                 ("debug_p_ds", ctypes.c_void_p)]
 
 
 class QTensor(ctypes.Structure):
@@ -283,6 +284,14 @@ class FlamiaAttention:
 
     def device_status(self, stream=None) -> int:
         return flamia_get_device_status(self.plan, stream)
+
+    def bwd_dvec(self):
+        """View into the backward workspace: D = rowsum(dO^ o O), float [hq, T], of the last backward call."""
+        import torch
+        T, H, d = self.T, self.hq, self.d
+        rnd = lambda x: (x + 255) // 256 * 256
+        off = rnd(rnd(rnd(T * H * d) + T * H) + T * H * 8)
+        return self.workspace[off:off + T * H * 4].view(torch.float32).view(H, T)
 
     def bwd_dout_codes(self):
         """Views into the backward workspace: (dO codes, dO scale bytes) of the last backward call."""

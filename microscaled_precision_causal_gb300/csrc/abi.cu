@@ -30,7 +30,7 @@ cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, co
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
                        void* const* ev, bool strict, const void* q4c, const void* q4s, const void* k4c,
-                       const void* k4s);
+                       const void* k4s, float* dbg);
 }  // namespace flamia
 
 using namespace flamia;
@@ -92,7 +92,7 @@ int check_qt(const flamia_qtensor* t, bool need_stats) {
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA; }
 
 inline void record(void* const* ev, int i, cudaStream_t s) {
-  if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+  if (ev) record_timing_event(ev[i], s);
 }
 
 float resolve_scale(float s, int d) { return s > 0.f ? s : 1.0f / std::sqrt((float)d); }
@@ -222,6 +222,9 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
       !aligned16(dv_bf16) || (reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FLAMIA_ERR_MISALIGNED;
   if (is_mixed(opt) && head_dim != 128) return FLAMIA_ERR_UNSUPPORTED;
+  float* dbg = opt ? opt->debug_p_ds : nullptr;
+  if (dbg && (is_mixed(opt) || is_strict(opt) || total_tokens > 1024)) return FLAMIA_ERR_UNSUPPORTED;
+  if (dbg && (reinterpret_cast<uintptr_t>(dbg) & 3u)) return FLAMIA_ERR_MISALIGNED;
   const BwdWorkspace w = bwd_layout(total_tokens, num_seqs, hq, head_dim);
   if (workspace_bytes < w.total) return FLAMIA_ERR_WORKSPACE;
   if (total_tokens == 0) return FLAMIA_OK;
@@ -262,7 +265,7 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
                    is_mixed(opt) ? opt->mixed->q_codes_e2m1 : nullptr,
                    is_mixed(opt) ? opt->mixed->q_scales_e4m3 : nullptr,
                    is_mixed(opt) ? opt->mixed->k_codes_e2m1 : nullptr,
-                   is_mixed(opt) ? opt->mixed->k_scales_e4m3 : nullptr);
+                   is_mixed(opt) ? opt->mixed->k_scales_e4m3 : nullptr, dbg);
   return cuda_status(e);
 }
 

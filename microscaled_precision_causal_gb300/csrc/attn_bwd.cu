@@ -93,6 +93,7 @@ struct BwdParams {
   __half* dq_acc;          // fp16 accumulator chunks (dq_chunk_elems layout)
   __nv_bfloat16* dk;       // [T, hkv, D]
   __nv_bfloat16* dv;
+  float* dbg;              // diagnostic build only: fp32 P and dS, [2, hq, T, T]
 };
 
 template <int D, bool MIXED>
@@ -120,7 +121,9 @@ struct BwdSmem {
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-template <int D, bool STRICT, bool MIXED>
+// DBG: a diagnostic build that also writes the fp32 P and dS of every visible pair
+// (default route, small problems); the production builds carry none of its code.
+template <int D, bool STRICT, bool MIXED, bool DBG = false>
 __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
                     const BwdParams p) {
   static_assert(!(STRICT && MIXED), "the strict options and the mixed route are separate");
   static_assert(!MIXED || D == 128, "the mixed route is built for head_dim 128");
+  static_assert(!DBG || (!STRICT && !MIXED), "the diagnostic build covers the default route");
   using L = BwdSmem<D, MIXED>;
   using Shape = BwdShape<D, STRICT>;
   constexpr int kWG = Shape::kWG, kCPW = Shape::kChunksPerWG, kCols = Shape::kCols;
@@ -476,6 +480,16 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     uint8_t* Esm = smem + L::kE;
     uint8_t* sPt = smem + L::kPt;
     uint8_t* sDS = smem + L::kDS;
+    // diagnostic build: row j's 32 values of query chunk c (slice 0 = P, 1 = dS)
+    auto dbg_store = [&](int which, int kstep, int c, const float* vals, float mul) {
+      const int h = hk * g + kstep / qtiles, tq = u + kstep % qtiles;
+      if (!key_valid) return;
+#pragma unroll 1
+      for (int i = 0; i < 32; ++i) {
+        const int ql = tq * kTile + 32 * c + i;
+        if (ql < doc_len) p.dbg[(((int64_t)which * p.hq + h) * p.T + doc_start + ql) * p.T + ktok] = vals[i] * mul;
+      }
+    };
     bool ok = true;
     for (int k = 0; k < nsteps; ++k) {
       const int t = u + k % qtiles;
@@ -541,6 +555,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         };
         if (diag) p_math(std::true_type{});
         else p_math(std::false_type{});
+        if constexpr (DBG) dbg_store(0, k, c, pr[cc], 1.0f / 256.0f);
         if (STRICT) {
           // dV operand with dO's per-token scale folded in: 2^8 P s_dO(i), one round-up
           // exponent per (key row, 32-query chunk)
@@ -619,6 +634,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           amax = fmax3(amax, fabsf(d0.x), fabsf(d0.y));
           amax = fmax3(amax, fabsf(d1.x), fabsf(d1.y));
         }
+        if constexpr (DBG) dbg_store(1, k, c, pr[cc], 1.0f);
         if (!STRICT) {      // 32 x 32 block: the warp's 32 key rows
 #pragma unroll
           for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
@@ -1426,12 +1442,13 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int D, bool STRICT, bool MIXED>
+template <int D, bool STRICT, bool MIXED, bool DBG = false>
 cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                          const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                          const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
-                         void* const* ev, const void* q4c, const void* q4s, const void* k4c, const void* k4s) {
+                         void* const* ev, const void* q4c, const void* q4s, const void* k4c, const void* k4s,
+                         float* dbg) {
   CUtensorMap tq, tk, tv, tdo, tq4, tk4;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
@@ -1467,23 +1484,24 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   p.dq_acc = static_cast<__half*>(dq_acc);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dbg = dbg;
   const int64_t max_items = (int64_t)T / kTile + N + 1;
   const int64_t grid = max_items * hkv;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
   constexpr int smem = BwdSmem<D, MIXED>::kAlloc;
   int regs = 0;
-  cudaError_t e = prepare_kernel<attn_bwd_kernel<D, STRICT, MIXED>>(smem, &regs);
+  cudaError_t e = prepare_kernel<attn_bwd_kernel<D, STRICT, MIXED, DBG>>(smem, &regs);
   if (e != cudaSuccess) return e;
   // the warpgroups' register split (setmaxnreg) assumes this launch allocation;
   // with any other the increase could never be granted, so refuse to launch
   if (regs != BwdShape<D, STRICT>::kLaunchRegs) return cudaErrorInvalidConfiguration;
-  if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
-  attn_bwd_kernel<D, STRICT, MIXED>
+  if (ev) record_timing_event(ev[0], stream);
+  attn_bwd_kernel<D, STRICT, MIXED, DBG>
       <<<(unsigned)grid, BwdShape<D, STRICT>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
   e = cudaGetLastError();
-  if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
+  if (ev) record_timing_event(ev[1], stream);
   if (e != cudaSuccess) return e;
-  if (ev && ev[2]) cudaEventRecord(static_cast<cudaEvent_t>(ev[2]), stream);
+  if (ev) record_timing_event(ev[2], stream);
   if (!STRICT && D == 128) {
     e = prepare_kernel<dqt_finalize_kernel>(kDqtFinalizeSmem);
     if (e != cudaSuccess) return e;
@@ -1526,7 +1544,7 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
     bwd_tail_kernel<D><<<152, 256, 0, stream>>>(p.plan, T, hq, hkv, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
   }
   e = cudaGetLastError();
-  if (ev && ev[3]) cudaEventRecord(static_cast<cudaEvent_t>(ev[3]), stream);
+  if (ev) record_timing_event(ev[3], stream);
   return e;
 }
 
@@ -1552,10 +1570,13 @@ cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, co
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
                        void* const* ev, bool strict, const void* q4c, const void* q4s, const void* k4c,
-                       const void* k4s) {
+                       const void* k4s, float* dbg) {
 #define FLAMIA_BWD_ARGS qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan, \
-                        dq_acc, dq, dk, dv, stream, ev, q4c, q4s, k4c, k4s
+                        dq_acc, dq, dk, dv, stream, ev, q4c, q4s, k4c, k4s, dbg
   const bool mixed = q4c != nullptr;
+  if (dbg && (mixed || strict)) return cudaErrorInvalidValue;
+  if (dbg && D == 128) return launch_bwd_d<128, false, false, true>(FLAMIA_BWD_ARGS);
+  if (dbg && D == 64) return launch_bwd_d<64, false, false, true>(FLAMIA_BWD_ARGS);
   if (D == 128 && mixed) return launch_bwd_d<128, false, true>(FLAMIA_BWD_ARGS);
   if (mixed) return cudaErrorInvalidValue;
   if (D == 128 && strict) return launch_bwd_d<128, true, false>(FLAMIA_BWD_ARGS);

@@ -1003,7 +1003,7 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
     constexpr int smem = FwdSmem<D>::kAlloc;
     e = prepare_kernel<attn_fwd_kernel<D, STRICT>>(smem);
     if (e != cudaSuccess) return e;
-    if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
+    if (ev) record_timing_event(ev[0], stream);
     attn_fwd_kernel<D, STRICT><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   } else {
     // persistent: one CTA per SM (fewer when there are fewer units than SMs)
@@ -1017,11 +1017,11 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
     if (e != cudaSuccess) return e;
     if (regs != kPersistLaunchRegs) return cudaErrorInvalidConfiguration;
     const unsigned pgrid = (unsigned)(grid < sms ? grid : sms);
-    if (ev && ev[0]) cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), stream);
+    if (ev) record_timing_event(ev[0], stream);
     attn_fwd_persist_kernel<D><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
   }
   e = cudaGetLastError();
-  if (ev && ev[1]) cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), stream);
+  if (ev) record_timing_event(ev[1], stream);
   if (e != cudaSuccess) return e;
   fwd_tail_kernel<D><<<152, 256, 0, stream>>>(static_cast<const int*>(plan), T, hq, static_cast<__nv_bfloat16*>(out),
                                               lse);

@@ -164,4 +164,16 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
   return __half2float(__half(h));
 }
 
+// Record a caller's timing event on `s`.  Inside a stream capture the record is
+// captured as an event-record node (cudaEventRecordExternal), so every replay of
+// the graph records it again and the events time the graph's launches too.
+inline void record_timing_event(void* ev, cudaStream_t s) {
+  if (!ev) return;
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
 }  // namespace flamia

@@ -504,6 +504,9 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
     diag = dict(rowsum_ds=np.zeros((hq, T)), rowmax_ds=np.zeros((hq, T)),
                 rowsum_p=np.zeros((hq, T)), rowsum_pdp=np.zeros((hq, T)),
                 ds_nonzero=0, dsq_zero=0) if diagnostics else None
+    if diagnostics and T <= 2048:      # every pair's P and dS before quantization, [hq, query, key]
+        diag["p_full"] = np.zeros((hq, T, T))
+        diag["ds_full"] = np.zeros((hq, T, T))
     kv_heads = range(hkv) if kv_heads is None else kv_heads
     if opts.strict:   # per-token scales s_X = 2**e of the strict per-token quantization
         Q_scale, K_scale, dO_scale = (np.asarray(tok_scales[n], np.float64) for n in ("q", "k", "do"))
@@ -565,6 +568,9 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                                                                      np.abs(dS).max(1))
                             diag["rowsum_p"][h, r0:r1] += P.sum(1)
                             diag["rowsum_pdp"][h, r0:r1] += (P * dP).sum(1)
+                            if "p_full" in diag:
+                                diag["p_full"][h, r0:r1, c0:c1] = P
+                                diag["ds_full"][h, r0:r1, c0:c1] = dS
                             if q:
                                 nz = dS != 0
                                 diag["ds_nonzero"] += int(nz.sum())

@@ -90,3 +90,20 @@ def test_strict_options_come_as_a_set(flamia):
         for f in flags:
             setattr(o, f, 1)
         assert fwd(o) == want, flags
+
+
+def test_backward_diagnostic_output_limits(flamia):
+    """The fp32 P / dS diagnostic output of flamia_bwd is refused outside its
+    scope (strict options, more than 1024 tokens) before any CUDA call."""
+    L, F = flamia.lib(), flamia
+    q = F.QTensor(16, 16, 16)
+
+    def bwd(o, T):
+        return L.flamia_bwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), 256, 256, 256, 256, 1, T, 4, 2, 128, 1,
+                            0.0, ctypes.byref(o), 256, 256, 256, 256, 256, 1 << 30, None)
+    o = F.default_options()
+    o.debug_p_ds = 256
+    assert bwd(o, 2000) == -2
+    for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq"):
+        setattr(o, f, 1)
+    assert bwd(o, 100) == -2
