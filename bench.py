@@ -128,9 +128,9 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle sample
 
-def oracle_opts(mode):
+def oracle_opts(mode, window=(-1, 0)):
     import oracle as O
-    return O.Options(strict=mode == "strict", mixed=mode == "mixed")
+    return O.Options(strict=mode == "strict", mixed=mode == "mixed", window=tuple(window))
 
 
 def oracle_sample(w, budget_s, max_tokens=None, mode="default"):
@@ -148,10 +148,11 @@ def oracle_sample(w, budget_s, max_tokens=None, mode="default"):
         S = min(S, L)
         sub = {n: v[:S, :(G * g if n in ("q", "do") else G)] for n, v in vals.items()}
         t0 = time.perf_counter()
-        O.run_training_call(sub["q"], sub["k"], sub["v"], sub["do"], [0, S], G * g, G, opts=oracle_opts(mode))
+        O.run_training_call(sub["q"], sub["k"], sub["v"], sub["do"], [0, S], G * g, G,
+                            opts=oracle_opts(mode, w.window))
         dt = time.perf_counter() - t0
         spent += dt
-        flops = 14.0 * w.d * G * g * S * (S + 1) / 2
+        flops = 14.0 * w.d * G * g * W.visible_pair_count([S], w.window)
         best = dict(tokens=S, heads=G * g, seconds=dt, flops=flops, tflops=flops / dt / 1e12)
         if spent + 2.5 * dt > budget_s:
             break
@@ -191,14 +192,14 @@ def run_reference(args, rank, world):
     inp = W.make_inputs(W.custom([S], Hs, Hs // g, w.d, dist=w.dist, seed=w.seed))
     vals = {n: W.bf16_bits_to_f32(b).astype(np.float64) for n, b in inp.items()}
     step = lambda: O.run_training_call(vals["q"], vals["k"], vals["v"], vals["do"], [0, S], Hs, Hs // g,
-                                       opts=oracle_opts(args.mode))
+                                       opts=oracle_opts(args.mode, w.window))
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     dt = (time.perf_counter() - t0) / args.steps
-    flops = 14.0 * w.d * Hs * S * (S + 1) / 2
+    flops = 14.0 * w.d * Hs * W.visible_pair_count([S], w.window)
     value = flops / dt / 1e12
     sample = f"oracle fwd+bwd (fp64 numpy) on the first {S} tokens of the longest document, {Hs} query heads"
     return {
@@ -221,6 +222,8 @@ SECONDARY = (
     ("mixed_nvfp4_gqa_b4_s8192", "mixed"),
     ("strict_packed_4x8192_h16_t3", "strict"),
     ("strict_packed_4x8192_h16_t3", "default"),
+    ("noncausal_packed_16k_h16_d128", "default"),
+    ("noncausal_b2_s8192_h16_d128", "default"),
 )
 EX2_PER_CLK_PER_SM = 32      # MUFU ex2 issue rate of B300-class SMs ([EN] section 7; probe in the design notes)
 
@@ -297,7 +300,7 @@ class WorkloadRun:
         import torch
         self.torch, self.F, self.w, self.mode, self.dev, self.flush = torch, F, w, mode, dev, flush
         self.T, self.N = w.total_tokens, len(w.lengths)
-        self.pairs = W.visible_pair_count(w.lengths)
+        self.pairs = W.visible_pair_count(w.lengths, w.window)
         self.flops = 14.0 * w.d * w.hq * self.pairs
         inp = W.make_inputs(w)
         self.host = {n: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for n, b in inp.items()}
@@ -305,7 +308,7 @@ class WorkloadRun:
         self.cu_host = torch.tensor(w.cu_seqlens, dtype=torch.int32).pin_memory()
         self.cu = self.cu_host.to(dev)
         self.att = F.FlamiaAttention(self.T, self.N, w.hq, w.hkv, w.d, device=dev, strict=mode == "strict",
-                                     mixed=mode == "mixed")
+                                     mixed=mode == "mixed", causal=w.causal, window=w.window)
         self.stream = torch.cuda.current_stream(dev)
         self.o_plain = F.Options()
         import ctypes
@@ -540,7 +543,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": w.name, "mode": args.mode, "cuda_graph": True, "total_tokens": run.T,
+        "config": {"workload": w.name, "mode": args.mode, "causal": w.causal, "window": list(w.window),
+                   "cuda_graph": True, "total_tokens": run.T,
                    "num_docs": run.N, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d, "visible_pairs": run.pairs,
                    "flops_per_step": run.flops,
                    "l2": "flushed between timed steps (256 MiB write); step inputs 256 MiB > L2",
@@ -582,7 +586,7 @@ def run_ours(args, rank, world, local_rank):
             p2 = r.phases(10)
             t2 = r.timed(args.secondary_steps, 3, 1)
             v2 = r.flops / (t2["median_of_rounds"] * 1e-3) / 1e12
-            ent = {"mode": mode, "value": v2, "unit": "TFLOPS", "ms_per_step": t2["median_of_rounds"],
+            ent = {"mode": mode, "causal": ws.causal, "value": v2, "unit": "TFLOPS", "ms_per_step": t2["median_of_rounds"],
                    "rounds_ms": t2["rounds"], "frac_of_fp8_peak": v2 / fp8_peak, "phases_ms": p2,
                    "roofline": r.kernel_roofline(p2, fp8_peak) if p2 else None,
                    "exp_ceiling_call_tflops": exp_ceiling(ws.d, sms, sm_mhz)["call_tflops"]}

@@ -31,6 +31,13 @@ class Workload:
     dist: str = "normal"      # "normal" | "student_t3" | "normal_outliers"
     seed: int = 0
     description: str = ""
+    # visible keys: query i sees key j of its document iff i - left <= j <= i + right
+    # (-1: no limit); causal (-1, 0), noncausal (-1, -1)
+    window: tuple = (-1, 0)
+
+    @property
+    def causal(self) -> bool:
+        return self.window[1] == 0
 
     @property
     def total_tokens(self) -> int:
@@ -71,14 +78,23 @@ def _workloads():
     w["strict_packed_4x8192_h16_t3"] = Workload(
         "strict_packed_4x8192_h16_t3", (8192,) * 4, 16, 16, 128, dist="student_t3",
         description="4 documents of 8192, H=16, d=128, Student-t(3) inputs, strict options")
+    # the noncausal calls the pages time beside the causal ones (packed rows, and the
+    # batched 2 x 8192 case)
+    w["noncausal_packed_16k_h16_d128"] = Workload(
+        "noncausal_packed_16k_h16_d128", tuple(packed_lengths(16384, 128, 4096, 0)), 16, 16, 128,
+        window=(-1, -1), description="packed varlen MHA as packed_16k_h16_d128, noncausal")
+    w["noncausal_b2_s8192_h16_d128"] = Workload(
+        "noncausal_b2_s8192_h16_d128", (8192,) * 2, 16, 16, 128, window=(-1, -1),
+        description="batched noncausal, B=2, seq 8192, H=16, d=128")
     return w
 
 
 WORKLOADS = _workloads()
 
 
-def custom(lengths, hq, hkv, d, dist="normal", seed=0, name="custom") -> Workload:
-    return Workload(name, tuple(int(x) for x in lengths), int(hq), int(hkv), int(d), dist, int(seed))
+def custom(lengths, hq, hkv, d, dist="normal", seed=0, name="custom", window=(-1, 0)) -> Workload:
+    return Workload(name, tuple(int(x) for x in lengths), int(hq), int(hkv), int(d), dist, int(seed),
+                    window=tuple(window))
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -120,6 +136,17 @@ def make_inputs(w: Workload, seed: Optional[int] = None, tensors=("q", "k", "v",
     return out
 
 
-def visible_pair_count(lengths) -> int:
-    """Number of (query, key) pairs a causal mask admits: sum n(n+1)/2."""
-    return int(sum(int(n) * (int(n) + 1) // 2 for n in lengths))
+def visible_pair_count(lengths, window=(-1, 0)) -> int:
+    """Number of (query, key) pairs the mask admits (the FLOP count's unit):
+    sum n(n+1)/2 for causal calls, sum n^2 for noncausal ones, and for a window
+    (left, right) the sum over rows i of |[max(0, i - left), min(n - 1, i + right)]|."""
+    left, right = window
+    if left < 0 and right == 0:
+        return int(sum(int(n) * (int(n) + 1) // 2 for n in lengths))
+    total = 0
+    for n in lengths:
+        i = np.arange(int(n), dtype=np.int64)
+        lo = np.zeros_like(i) if left < 0 else np.maximum(i - left, 0)
+        hi = np.full_like(i, int(n) - 1) if right < 0 else np.minimum(i + right, int(n) - 1)
+        total += int((hi - lo + 1).sum())
+    return total

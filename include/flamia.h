@@ -42,7 +42,8 @@ extern "C" {
 /* ----------------------------------------------------------- status codes */
 #define FLAMIA_OK 0
 #define FLAMIA_ERR_INVALID_ARG (-1)   /* null pointer, negative size, bad count */
-#define FLAMIA_ERR_UNSUPPORTED (-2)   /* head_dim not 64/128, hq % hkv != 0, causal == 0, too many tokens */
+#define FLAMIA_ERR_UNSUPPORTED (-2)   /* head_dim not 64/128, hq % hkv != 0, too many tokens, a window with
+                                         the strict options or the mixed route */
 #define FLAMIA_ERR_MISALIGNED (-3)    /* a tensor pointer is not 16-byte aligned */
 #define FLAMIA_ERR_WORKSPACE (-4)     /* workspace / plan buffer too small */
 #define FLAMIA_ERR_CUDA (-5)          /* a CUDA launch or driver call failed */
@@ -114,6 +115,28 @@ typedef struct flamia_options {
      (not strict, not mixed) and total_tokens <= 1024, else
      FLAMIA_ERR_UNSUPPORTED.  A slower build of the backward kernel runs. */
   float* debug_p_ds;
+  /* Visible keys: query i sees key j of its document (document-local
+     positions) iff i - window_left <= j <= i + window_right; a negative value
+     means no limit on that side (default -1, -1).  With causal = 1 the right
+     bound is 0 whatever window_right holds, so the defaults give plain causal
+     attention and, with causal = 0, attention over the whole document (the
+     packed noncausal calls the FLAMIA review reports beside the causal ones,
+     section 8).  Other values give sliding windows.  The strict options and
+     the mixed route are causal only (a window there returns
+     FLAMIA_ERR_UNSUPPORTED).  Bounds of total_tokens or more count as no
+     limit. */
+  int window_left;
+  int window_right;
+  /* Q and K were quantized with flamia_quantize_hadamard (each token row
+     multiplied by H / 2^k, H the +-1 Sylvester Hadamard matrix of order
+     head_dim, k = ceil(log2(head_dim) / 2); FLAMIA review section 3,
+     "Rotation, range, and the alternative").  The exact score is unchanged up
+     to the factor head_dim / 4^k, which the call folds into the softmax scale;
+     the same rotated codes serve the gradient products, and dQ and dK are
+     rotated back (by the same map) before their bf16 rounding.  V and dO are
+     not rotated.  Default 0; the strict options and the mixed route do not
+     take it (FLAMIA_ERR_UNSUPPORTED). */
+  int rotate;
 } flamia_options;
 
 /* Operands of the mixed NVFP4/FP8 route (FLAMIA review section 2, "The mixed
@@ -136,7 +159,8 @@ typedef struct flamia_mixed_operands {
 } flamia_mixed_operands;
 
 /* Fill *opt with the defaults above (p_boost_log2 = 8, bwd_p_boost_log2 = 8,
-   dq_headroom_log2 = 14, everything else 0 / NULL). */
+   dq_headroom_log2 = 14, window_left = window_right = -1, everything else
+   0 / NULL). */
 void flamia_default_options(flamia_options* opt);
 
 /* ----------------------------------------------------------- quantized tensor view */
@@ -175,6 +199,14 @@ typedef struct flamia_qtensor {
 size_t flamia_plan_bytes(int64_t total_tokens, int num_seqs);
 int flamia_plan_build(const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, void* plan,
                       size_t plan_bytes, void* stream);
+/* The same plan with costs for the given visible-key window (causal, and
+   window_left / window_right as in flamia_options): forward items cost the key
+   tiles their query tiles see, backward items the query tiles that see them.
+   flamia_plan_build equals causal = 1 with no left bound.  The item sets do not
+   depend on the window, so any plan of the same cu_seqlens gives correct
+   results; a plan built for the call's own window orders the work best. */
+int flamia_plan_build_window(const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int causal,
+                             int window_left, int window_right, void* plan, size_t plan_bytes, void* stream);
 
 /* ----------------------------------------------------------- quantizer (a1)
  * Token-block MXFP8 quantizer (FLAMIA review section 3, "Why one shared
@@ -195,6 +227,21 @@ int flamia_plan_build(const int32_t* cu_seqlens, int num_seqs, int64_t total_tok
 int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int heads, int head_dim,
                                const int32_t* cu_seqlens, int num_seqs, const void* plan, int per_token,
                                void* codes_e4m3, void* scales_ue8m0, float* stats, void* stream);
+
+/* ----------------------------------------------------------- rotated quantizer
+ * flamia_quantize_tokenblock of x H / 2^k instead of x (Korean review section
+ * 3.4: rotation, block statistics, codes and scales in one pass), for Q and K
+ * of calls with opt->rotate = 1.  H is the +-1 Sylvester Hadamard matrix of
+ * order head_dim and k = ceil(log2(head_dim) / 2) (H / 2^k is orthonormal at
+ * 64 and H H / 256 = I / 2 at 128).  Each row is rotated in fp32 by the fast
+ * Walsh-Hadamard butterflies, strides 1, 2, ..., head_dim / 2 in increasing
+ * order, (a, b) -> (a + b, a - b); then the power of two.  Codes, scale bytes
+ * and stats follow the token-block rule on the rotated values and are
+ * bit-exact with the oracle.  Arguments as flamia_quantize_tokenblock without
+ * per_token. */
+int flamia_quantize_hadamard(const void* x_bf16, int64_t total_tokens, int heads, int head_dim,
+                             const int32_t* cu_seqlens, int num_seqs, const void* plan, void* codes_e4m3,
+                             void* scales_ue8m0, float* stats, void* stream);
 
 /* ----------------------------------------------------------- NVFP4 quantizer (a2)
  * Score operands of the mixed route (FLAMIA review section 2: E2M1 codes and
@@ -225,9 +272,12 @@ int flamia_quantize_nvfp4(const void* x_bf16, int64_t total_tokens, int heads, i
  *   P^  = E4M3(2^8 p), O += P^ V^ / 2^8 (MXFP8 block-scaled MMA, V's token-
  *         block scale per 32 keys),
  * then O = bf16(O / l) and LSE = m + ln l (natural log).
+ * With causal = 0 (or a window in opt) the key tiles are those the query
+ * tile's window sees, and every tile holding a hidden pair or keys past the
+ * document end is masked element by element.
  * q, k, v: quantized views (stats unused here).  out: bf16 [T, hq, head_dim];
- * lse: float [hq, T].  causal must be 1.  softmax_scale <= 0 selects
- * 1/sqrt(head_dim).  opt may be NULL (defaults). */
+ * lse: float [hq, T].  causal: 1 (keys up to the query) or 0.  softmax_scale
+ * <= 0 selects 1/sqrt(head_dim).  opt may be NULL (defaults). */
 int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v,
                const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int hq, int hkv, int head_dim,
                int causal, float softmax_scale, const flamia_options* opt, const void* plan, void* out_bf16,

@@ -27,7 +27,8 @@ DEV_BAD_CU_SEQLENS, DEV_TIMEOUT, DEV_CAPACITY = 1, 2, 4
 EXPORTED = (
     "flamia_default_options", "flamia_plan_bytes", "flamia_plan_build", "flamia_quantize_tokenblock",
     "flamia_fwd", "flamia_bwd_workspace_bytes", "flamia_bwd", "flamia_get_device_status",
-    "flamia_status_string", "flamia_bwd_static_scratch", "flamia_quantize_nvfp4",
+    "flamia_status_string", "flamia_bwd_static_scratch", "flamia_quantize_nvfp4", "flamia_plan_build_window",
+    "flamia_quantize_hadamard",
 )
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -41,7 +42,10 @@ class Options(ctypes.Structure):
         "p_boost_log2", "bwd_p_boost_log2", "dq_headroom_log2", "strict_per_token", "strict_row_ds",
         "strict_causal_dq", "mixed_nvfp4", "deterministic")] + [("timing_events", ctypes.POINTER(ctypes.c_void_p)),
                                                                  ("mixed", ctypes.c_void_p),
-                                                                 ("debug_p_ds", ctypes.c_void_p)]
+                                                                 ("debug_p_ds", ctypes.c_void_p),
+                                                                 ("window_left", ctypes.c_int),
+                                                                 ("window_right", ctypes.c_int),
+                                                                 ("rotate", ctypes.c_int)]
 
 
 class QTensor(ctypes.Structure):
@@ -72,6 +76,7 @@ def lib():
         "flamia_default_options": (None, [op]),
         "flamia_plan_bytes": (sz, [i64, i32]),
         "flamia_plan_build": (i32, [vp, i32, i64, vp, sz, vp]),
+        "flamia_plan_build_window": (i32, [vp, i32, i64, i32, i32, i32, vp, sz, vp]),
         "flamia_quantize_tokenblock": (i32, [vp, i64, i32, i32, vp, i32, vp, i32, vp, vp, vp, vp]),
         "flamia_fwd": (i32, [qp, qp, qp, vp, i32, i64, i32, i32, i32, i32, f32, op, vp, vp, vp, vp]),
         "flamia_bwd_workspace_bytes": (sz, [i64, i32, i32, i32, i32]),
@@ -82,6 +87,7 @@ def lib():
         "flamia_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_int), vp]),
         "flamia_status_string": (ctypes.c_char_p, [i32]),
         "flamia_quantize_nvfp4": (i32, [vp, i64, i32, i32, vp, vp, vp]),
+        "flamia_quantize_hadamard": (i32, [vp, i64, i32, i32, vp, i32, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -134,12 +140,25 @@ def flamia_plan_build(cu_seqlens, num_seqs: int, total_tokens: int, plan, stream
                                    _stream(stream)), "flamia_plan_build")
 
 
+def flamia_plan_build_window(cu_seqlens, num_seqs: int, total_tokens: int, causal: int, window_left: int,
+                             window_right: int, plan, stream=None):
+    _check(lib().flamia_plan_build_window(_ptr(cu_seqlens), num_seqs, total_tokens, int(causal), window_left,
+                                          window_right, _ptr(plan), plan.numel() * plan.element_size(),
+                                          _stream(stream)), "flamia_plan_build_window")
+
+
 def flamia_quantize_tokenblock(x, cu_seqlens, num_seqs: int, plan, codes, scales, stats=None, per_token: bool = False,
                                stream=None):
     T, H, d = x.shape
     _check(lib().flamia_quantize_tokenblock(_ptr(x), T, H, d, _ptr(cu_seqlens), num_seqs, _ptr(plan), int(per_token),
                                             _ptr(codes), _ptr(scales), _ptr(stats), _stream(stream)),
            "flamia_quantize_tokenblock")
+
+
+def flamia_quantize_hadamard(x, cu_seqlens, num_seqs: int, plan, codes, scales, stats=None, stream=None):
+    T, H, d = x.shape
+    _check(lib().flamia_quantize_hadamard(_ptr(x), T, H, d, _ptr(cu_seqlens), num_seqs, _ptr(plan), _ptr(codes),
+                                          _ptr(scales), _ptr(stats), _stream(stream)), "flamia_quantize_hadamard")
 
 
 def flamia_quantize_nvfp4(x, codes, scales, stream=None):
@@ -194,16 +213,22 @@ def flamia_get_device_status(plan, stream=None) -> int:
 # ---------------------------------------------------------------- training call
 
 class FlamiaAttention:
-    """Buffers and calls for one packed causal attention layout.
+    """Buffers and calls for one packed attention layout.
 
     All tensors live on one CUDA device; the object owns the plan, the
     quantized Q/K/V views and the backward workspace (allocated once through
-    torch, reused across calls: nothing is allocated per call)."""
+    torch, reused across calls: nothing is allocated per call).  causal=False
+    gives attention over the whole document; window = (left, right) limits the
+    visible keys to i - left <= j <= i + right (-1: no limit; causal calls use
+    right = 0)."""
 
     def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, device="cuda",
-                 strict: bool = False, mixed: bool = False):
+                 strict: bool = False, mixed: bool = False, causal: bool = True, window=(-1, -1),
+                 rotate: bool = False):
         import torch
         self.T, self.N, self.hq, self.hkv, self.d = total_tokens, num_seqs, hq, hkv, head_dim
+        self.causal = 1 if causal else 0
+        self.window = (int(window[0]), int(window[1]))
         self.device = torch.device(device)
         dev = self.device
         u8 = torch.uint8
@@ -224,6 +249,9 @@ class FlamiaAttention:
         ws = flamia_bwd_workspace_bytes(total_tokens, num_seqs, hq, hkv, head_dim)
         self.workspace = torch.empty(ws, dtype=u8, device=dev)
         self.opts = default_options()
+        self.opts.window_left, self.opts.window_right = self.window
+        self.rotate = bool(rotate)      # Q and K rotated by the Hadamard map before quantization
+        self.opts.rotate = int(self.rotate)
         self.strict = bool(strict)
         if self.strict:   # per-token operand scales, per-query-row dS exponents, causal dQ boost, deterministic dQ
             for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq", "deterministic"):
@@ -247,13 +275,22 @@ class FlamiaAttention:
                 qtensor(self.v_codes, self.v_scales, self.v_stats))
 
     def plan_build(self, cu_seqlens, stream=None):
-        flamia_plan_build(cu_seqlens, self.N, self.T, self.plan, stream)
+        if self.causal and self.window[0] < 0:
+            flamia_plan_build(cu_seqlens, self.N, self.T, self.plan, stream)
+        else:
+            flamia_plan_build_window(cu_seqlens, self.N, self.T, self.causal, self.window[0], self.window[1], self.plan,
+                                     stream)
 
     def quantize(self, q, k, v, cu_seqlens, stream=None):
         pt = self.strict
-        flamia_quantize_tokenblock(q, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, None, pt, stream)
-        flamia_quantize_tokenblock(k, cu_seqlens, self.N, self.plan, self.k_codes, self.k_scales, self.k_stats, pt,
-                                   stream)
+        if self.rotate:
+            flamia_quantize_hadamard(q, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, None, stream)
+            flamia_quantize_hadamard(k, cu_seqlens, self.N, self.plan, self.k_codes, self.k_scales, self.k_stats,
+                                     stream)
+        else:
+            flamia_quantize_tokenblock(q, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, None, pt, stream)
+            flamia_quantize_tokenblock(k, cu_seqlens, self.N, self.plan, self.k_codes, self.k_scales, self.k_stats,
+                                       pt, stream)
         flamia_quantize_tokenblock(v, cu_seqlens, self.N, self.plan, self.v_codes, self.v_scales, self.v_stats, pt,
                                    stream)
         if self.mixed:
@@ -265,13 +302,14 @@ class FlamiaAttention:
     def forward(self, cu_seqlens, softmax_scale: float = 0.0, stream=None):
         q, k, v = self.views()
         flamia_fwd(q, k, v, cu_seqlens, self.N, self.T, self.hq, self.hkv, self.d, self.plan, self.out, self.lse,
-                   softmax_scale, self.opts, stream=stream)
+                   softmax_scale, self.opts, causal=self.causal, stream=stream)
         return self.out, self.lse
 
     def backward(self, dout, cu_seqlens, softmax_scale: float = 0.0, stream=None):
         q, k, v = self.views()
         flamia_bwd(q, k, v, self.out, self.lse, dout, cu_seqlens, self.N, self.T, self.hq, self.hkv, self.d, self.plan,
-                   self.dq, self.dk, self.dv, self.workspace, softmax_scale, self.opts, stream=stream)
+                   self.dq, self.dk, self.dv, self.workspace, softmax_scale, self.opts, causal=self.causal,
+                   stream=stream)
         return self.dq, self.dk, self.dv
 
     def training_call(self, q, k, v, dout, cu_seqlens, softmax_scale: float = 0.0, stream=None, build_plan=True):

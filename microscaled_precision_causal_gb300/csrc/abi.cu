@@ -8,15 +8,18 @@
 #include "common.cuh"
 
 namespace flamia {
-cudaError_t launch_plan(const int32_t* cu, int N, int T, void* plan, cudaStream_t s);
+cudaError_t launch_plan(const int32_t* cu, int N, int T, Window win, void* plan, cudaStream_t s);
 cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
                             int per_token, void* codes, void* scales, float* stats, const void* o, float* dvec,
                             void* dq_acc, cudaStream_t s, const float* k_stats = nullptr,
                             const float* v_stats = nullptr, int hkv = 1, float* maxima = nullptr);
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict);
+                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict,
+                       Window win);
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, void* scales, cudaStream_t s);
+cudaError_t launch_quantize_rot(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
+                                void* codes, void* scales, float* stats, cudaStream_t s);
 cudaError_t launch_fwd_coop(int D, int mixed, const void* qc, const void* qs, const void* kc, const void* ks,
                             const void* vc, const void* vs, const void* q4c, const void* q4s, const void* k4c,
                             const void* k4s, const void* vtc, const void* vts, const int32_t* cu, int N, int T, int hq,
@@ -30,7 +33,7 @@ cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, co
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
                        void* const* ev, bool strict, const void* q4c, const void* q4s, const void* k4c,
-                       const void* k4s, float* dbg);
+                       const void* k4s, float* dbg, Window win, bool rot);
 }  // namespace flamia
 
 using namespace flamia;
@@ -97,6 +100,23 @@ inline void record(void* const* ev, int i, cudaStream_t s) {
 
 float resolve_scale(float s, int d) { return s > 0.f ? s : 1.0f / std::sqrt((float)d); }
 
+// The call's visible-key window: causal forces the right bound to 0; negative
+// values and bounds of T or more mean no limit (-1).
+Window resolve_window(int causal, int left, int right, int64_t T) {
+  Window w;
+  w.left = (left < 0 || (int64_t)left >= T) ? -1 : left;
+  w.right = causal ? 0 : ((right < 0 || (int64_t)right >= T) ? -1 : right);
+  return w;
+}
+Window call_window(const flamia_options* o, int causal, int64_t T) {
+  return resolve_window(causal, o ? o->window_left : -1, o ? o->window_right : -1, T);
+}
+inline bool is_causal_window(Window w) { return w.left < 0 && w.right == 0; }
+
+bool is_rotated(const flamia_options* o) { return o && o->rotate; }
+// Rotated operands: S = (d / 4^k) Q~ K~^T, folded into the softmax scale.
+float score_scale(float s, int d, bool rot) { return rot ? s * (d == 128 ? 2.0f : 1.0f) : s; }
+
 struct BwdWorkspace {
   size_t do_codes, do_scales, do_stats, dvec, boost, maxima, dq_acc, total;
 };
@@ -124,6 +144,9 @@ void flamia_default_options(flamia_options* opt) {
   opt->p_boost_log2 = 8;
   opt->bwd_p_boost_log2 = 8;
   opt->dq_headroom_log2 = 14;
+  opt->window_left = -1;
+  opt->window_right = -1;
+  opt->rotate = 0;
 }
 
 size_t flamia_plan_bytes(int64_t total_tokens, int num_seqs) {
@@ -136,7 +159,19 @@ int flamia_plan_build(const int32_t* cu_seqlens, int num_seqs, int64_t total_tok
   int rc = check_common(total_tokens, num_seqs, cu_seqlens, plan);
   if (rc) return rc;
   if (plan_bytes_ < plan_bytes(total_tokens, num_seqs)) return FLAMIA_ERR_WORKSPACE;
-  return cuda_status(launch_plan(cu_seqlens, num_seqs, (int)total_tokens, plan, (cudaStream_t)stream));
+  return cuda_status(launch_plan(cu_seqlens, num_seqs, (int)total_tokens, resolve_window(1, -1, -1, total_tokens), plan,
+                                 (cudaStream_t)stream));
+}
+
+int flamia_plan_build_window(const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int causal,
+                             int window_left, int window_right, void* plan, size_t plan_bytes_, void* stream) {
+  int rc = check_common(total_tokens, num_seqs, cu_seqlens, plan);
+  if (rc) return rc;
+  if (causal != 0 && causal != 1) return FLAMIA_ERR_INVALID_ARG;
+  if (plan_bytes_ < plan_bytes(total_tokens, num_seqs)) return FLAMIA_ERR_WORKSPACE;
+  return cuda_status(launch_plan(cu_seqlens, num_seqs, (int)total_tokens,
+                                 resolve_window(causal, window_left, window_right, total_tokens), plan,
+                                 (cudaStream_t)stream));
 }
 
 int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int heads, int head_dim,
@@ -152,6 +187,20 @@ int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int hea
   return cuda_status(launch_quantize(x_bf16, (int)total_tokens, heads, head_dim, cu_seqlens, num_seqs, plan,
                                      per_token, codes_e4m3, scales_ue8m0, stats, nullptr, nullptr, nullptr,
                                      (cudaStream_t)stream));
+}
+
+int flamia_quantize_hadamard(const void* x_bf16, int64_t total_tokens, int heads, int head_dim,
+                             const int32_t* cu_seqlens, int num_seqs, const void* plan, void* codes_e4m3,
+                             void* scales_ue8m0, float* stats, void* stream) {
+  int rc = check_common(total_tokens, num_seqs, cu_seqlens, plan);
+  if (rc) return rc;
+  if (!x_bf16 || !codes_e4m3 || !scales_ue8m0 || heads <= 0) return FLAMIA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return FLAMIA_ERR_UNSUPPORTED;
+  if (!aligned16(x_bf16) || !aligned16(codes_e4m3) || (stats && (reinterpret_cast<uintptr_t>(stats) & 7u)))
+    return FLAMIA_ERR_MISALIGNED;
+  if (total_tokens == 0) return FLAMIA_OK;
+  return cuda_status(launch_quantize_rot(x_bf16, (int)total_tokens, heads, head_dim, cu_seqlens, num_seqs, plan,
+                                         codes_e4m3, scales_ue8m0, stats, (cudaStream_t)stream));
 }
 
 int flamia_quantize_nvfp4(const void* x_bf16, int64_t total_tokens, int heads, int head_dim, void* codes_e2m1,
@@ -175,12 +224,14 @@ int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (!rc) rc = check_qt(k, false);
   if (!rc) rc = check_qt(v, false);
   if (rc) return rc;
-  if (causal != 1) return FLAMIA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FLAMIA_ERR_INVALID_ARG;
+  const Window win = call_window(opt, causal, total_tokens);
+  if ((is_strict(opt) || is_mixed(opt)) && (!is_causal_window(win) || is_rotated(opt))) return FLAMIA_ERR_UNSUPPORTED;
   if (!out_bf16 || !lse) return FLAMIA_ERR_INVALID_ARG;
   if (!aligned16(out_bf16) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FLAMIA_ERR_MISALIGNED;
   if (is_mixed(opt) && head_dim != 128) return FLAMIA_ERR_UNSUPPORTED;
   if (total_tokens == 0) return FLAMIA_OK;
-  const float scale = resolve_scale(softmax_scale, head_dim);
+  const float scale = score_scale(resolve_scale(softmax_scale, head_dim), head_dim, is_rotated(opt));
   if (is_mixed(opt)) {
     const flamia_mixed_operands* m = opt->mixed;
     cudaStream_t s = (cudaStream_t)stream;
@@ -195,7 +246,7 @@ int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   }
   return cuda_status(launch_fwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, cu_seqlens,
                                 num_seqs, (int)total_tokens, hq, hkv, scale, plan, out_bf16, lse, (cudaStream_t)stream,
-                                opt ? opt->timing_events : nullptr, is_strict(opt)));
+                                opt ? opt->timing_events : nullptr, is_strict(opt), win));
 }
 
 size_t flamia_bwd_workspace_bytes(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim) {
@@ -216,14 +267,17 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   if (!rc) rc = check_qt(k, true);
   if (!rc) rc = check_qt(v, true);
   if (rc) return rc;
-  if (causal != 1) return FLAMIA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FLAMIA_ERR_INVALID_ARG;
+  const Window win = call_window(opt, causal, total_tokens);
+  if ((is_strict(opt) || is_mixed(opt)) && (!is_causal_window(win) || is_rotated(opt))) return FLAMIA_ERR_UNSUPPORTED;
   if (!out_bf16 || !lse || !dout_bf16 || !dq_bf16 || !dk_bf16 || !dv_bf16 || !workspace) return FLAMIA_ERR_INVALID_ARG;
   if (!aligned16(out_bf16) || !aligned16(dout_bf16) || !aligned16(dq_bf16) || !aligned16(dk_bf16) ||
       !aligned16(dv_bf16) || (reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FLAMIA_ERR_MISALIGNED;
   if (is_mixed(opt) && head_dim != 128) return FLAMIA_ERR_UNSUPPORTED;
   float* dbg = opt ? opt->debug_p_ds : nullptr;
-  if (dbg && (is_mixed(opt) || is_strict(opt) || total_tokens > 1024)) return FLAMIA_ERR_UNSUPPORTED;
+  if (dbg && (is_mixed(opt) || is_strict(opt) || is_rotated(opt) || !is_causal_window(win) || total_tokens > 1024))
+    return FLAMIA_ERR_UNSUPPORTED;
   if (dbg && (reinterpret_cast<uintptr_t>(dbg) & 3u)) return FLAMIA_ERR_MISALIGNED;
   const BwdWorkspace w = bwd_layout(total_tokens, num_seqs, hq, head_dim);
   if (workspace_bytes < w.total) return FLAMIA_ERR_WORKSPACE;
@@ -260,12 +314,13 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   record(ev, 3, s);
   if (e == cudaSuccess)
     e = launch_bwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, do_codes, do_scales, lse,
-                   dvec, boost, cu_seqlens, num_seqs, T, hq, hkv, resolve_scale(softmax_scale, head_dim), plan, dq_acc,
+                   dvec, boost, cu_seqlens, num_seqs, T, hq, hkv,
+                   score_scale(resolve_scale(softmax_scale, head_dim), head_dim, is_rotated(opt)), plan, dq_acc,
                    dq_bf16, dk_bf16, dv_bf16, s, ev ? ev + 4 : nullptr, strict,
                    is_mixed(opt) ? opt->mixed->q_codes_e2m1 : nullptr,
                    is_mixed(opt) ? opt->mixed->q_scales_e4m3 : nullptr,
                    is_mixed(opt) ? opt->mixed->k_codes_e2m1 : nullptr,
-                   is_mixed(opt) ? opt->mixed->k_scales_e4m3 : nullptr, dbg);
+                   is_mixed(opt) ? opt->mixed->k_scales_e4m3 : nullptr, dbg, win, is_rotated(opt));
   return cuda_status(e);
 }
 

@@ -94,6 +94,7 @@ struct BwdParams {
   __nv_bfloat16* dk;       // [T, hkv, D]
   __nv_bfloat16* dv;
   float* dbg;              // diagnostic build only: fp32 P and dS, [2, hq, T, T]
+  Window win;              // visible keys (causal: right = 0); strict and mixed are causal only
 };
 
 template <int D, bool MIXED>
@@ -123,7 +124,11 @@ struct BwdSmem {
 
 // DBG: a diagnostic build that also writes the fp32 P and dS of every visible pair
 // (default route, small problems); the production builds carry none of its code.
-template <int D, bool STRICT, bool MIXED, bool DBG = false>
+// WIN: a call with a window other than causal (noncausal, sliding); the causal
+// builds carry none of its code.  ROT: Q and K were rotated by H / 2^k before
+// quantization (H the +-1 Hadamard matrix, k = ceil(log2(D) / 2)); dK is rotated
+// back by the same map in the epilogue (dQ in its finalise kernel).
+template <int D, bool STRICT, bool MIXED, bool DBG = false, bool WIN = false, bool ROT = false>
 __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -132,6 +137,8 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   static_assert(!(STRICT && MIXED), "the strict options and the mixed route are separate");
   static_assert(!MIXED || D == 128, "the mixed route is built for head_dim 128");
   static_assert(!DBG || (!STRICT && !MIXED), "the diagnostic build covers the default route");
+  static_assert(!WIN || (!STRICT && !MIXED), "the strict options and the mixed route are causal");
+  static_assert(!ROT || (!STRICT && !MIXED && !DBG), "the rotation is built for the MXFP8 route");
   using L = BwdSmem<D, MIXED>;
   using Shape = BwdShape<D, STRICT>;
   constexpr int kWG = Shape::kWG, kCPW = Shape::kChunksPerWG, kCols = Shape::kCols;
@@ -167,7 +174,9 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   const int doc_len = span.y;
   const int nt = (doc_len + kTile - 1) / kTile;
   const int g = p.hq / p.hkv;
-  const int qtiles = nt - u;
+  // the query tiles that see this key tile under the call's window (causal: u .. nt - 1)
+  const int tlo = WIN ? win_tlo(u, p.win) : u;
+  const int qtiles = WIN ? win_thi(u, nt, p.win) - tlo + 1 : nt - u;
   const int nsteps = g * qtiles;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     tma_load_3d(smem + L::kV, &tm_v, kv_full, 0, hk, doc_start + u * kTile);
     if (MIXED) tma_load_3d(smem + L::kK4, &tm_k4, kv_full, 0, hk, doc_start + u * kTile);
     for (int k = 0; k < nsteps && k < kQStages; ++k) {
-      const int h = hk * g + k / qtiles, t = u + k % qtiles;
+      const int h = hk * g + k / qtiles, t = tlo + k % qtiles;
       mbar_arrive_expect_tx(&qd_full[k], 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
       tma_load_3d(smem + L::kQ + k * L::kTileBytes, &tm_q, &qd_full[k], 0, h, doc_start + t * kTile);
       tma_load_3d(smem + L::kDO + k * L::kTileBytes, &tm_do, &qd_full[k], 0, h, doc_start + t * kTile);
@@ -238,7 +247,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       for (int k = kQStages; k < nsteps; ++k) {     // K, V and the first kQStages steps: prologue
         const int st = k % kQStages;
         if (!mbar_wait(&qd_empty[st], ((k / kQStages) - 1) & 1, status)) break;
-        const int h = hk * g + k / qtiles, t = u + k % qtiles;
+        const int h = hk * g + k / qtiles, t = tlo + k % qtiles;
         mbar_arrive_expect_tx(&qd_full[st], 2 * L::kTileBytes + (MIXED ? L::kScoreBytes : 0));
         tma_load_3d(smem + L::kQ + st * L::kTileBytes, &tm_q, &qd_full[st], 0, h, doc_start + t * kTile);
         tma_load_3d(smem + L::kDO + st * L::kTileBytes, &tm_do, &qd_full[st], 0, h, doc_start + t * kTile);
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     // and the wait instead of queueing behind stores the compiler cannot reorder.
     for (int k = 0; k < nsteps; ++k) {
       const int b = k & 1;
-      const int h = hk * g + k / qtiles, t = u + k % qtiles;
+      const int h = hk * g + k / qtiles, t = tlo + k % qtiles;
       float lv[4], dv[4], sqv[4], sdv[4];
       uint8_t scb = 127;
 #pragma unroll
@@ -482,7 +491,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     uint8_t* sDS = smem + L::kDS;
     // diagnostic build: row j's 32 values of query chunk c (slice 0 = P, 1 = dS)
     auto dbg_store = [&](int which, int kstep, int c, const float* vals, float mul) {
-      const int h = hk * g + kstep / qtiles, tq = u + kstep % qtiles;
+      const int h = hk * g + kstep / qtiles, tq = tlo + kstep % qtiles;
       if (!key_valid) return;
 #pragma unroll 1
       for (int i = 0; i < 32; ++i) {
@@ -492,8 +501,10 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     };
     bool ok = true;
     for (int k = 0; k < nsteps; ++k) {
-      const int t = u + k % qtiles;
-      const bool diag = (t == u);
+      const int t = tlo + k % qtiles;
+      // tiles with a hidden pair (causal: the diagonal one) or keys past the document end
+      // take the masked variant of the weight loop
+      const bool diag = WIN ? win_masked(t, u, doc_len, p.win) : t == u;
       const int b = k & 1;
       const float* rb = rowbuf + b * (L::kRowBuf / 4);
       const uint8_t* cs = reinterpret_cast<const uint8_t*>(rb + 256);
@@ -528,6 +539,14 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         // the causal mask only on the diagonal tile: the loop is built twice
         auto p_math = [&](auto diag_tile) {
           constexpr bool kDiag = decltype(diag_tile)::value;
+          // windowed calls, masked variant: this key row is seen by the tile's queries
+          // [qlim, qhim] (causal calls: the queries at or after the key)
+          int qlim = 0, qhim = 0;
+          if constexpr (kDiag && WIN) {
+            const int kj = u * kTile + j;
+            qlim = !key_valid ? kTile : (p.win.right < 0 ? 0 : kj - p.win.right - t * kTile);
+            qhim = !key_valid ? -1 : (p.win.left < 0 ? kTile : kj + p.win.left - t * kTile);
+          }
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 nl = nl4[i >> 2];
@@ -544,10 +563,17 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
           if (kDiag) {
             const int il = 32 * c + i;
-            p0.x = il >= j ? p0.x : 0.f;
-            p0.y = il + 1 >= j ? p0.y : 0.f;
-            p1.x = il + 2 >= j ? p1.x : 0.f;
-            p1.y = il + 3 >= j ? p1.y : 0.f;
+            if constexpr (WIN) {
+              p0.x = (il >= qlim && il <= qhim) ? p0.x : 0.f;
+              p0.y = (il + 1 >= qlim && il + 1 <= qhim) ? p0.y : 0.f;
+              p1.x = (il + 2 >= qlim && il + 2 <= qhim) ? p1.x : 0.f;
+              p1.y = (il + 3 >= qlim && il + 3 <= qhim) ? p1.y : 0.f;
+            } else {
+              p0.x = il >= j ? p0.x : 0.f;
+              p0.y = il + 1 >= j ? p0.y : 0.f;
+              p1.x = il + 2 >= j ? p1.x : 0.f;
+              p1.y = il + 3 >= j ? p1.y : 0.f;
+            }
           }
           pr[cc][i] = p0.x; pr[cc][i + 1] = p0.y; pr[cc][i + 2] = p1.x; pr[cc][i + 3] = p1.y;
           if (!STRICT) pk[i >> 2] = (uint32_t)e4m3x2(p0.x, p0.y) | ((uint32_t)e4m3x2(p1.x, p1.y) << 16);
@@ -727,11 +753,38 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = (which == 0 ? kDV : kDK) + wg * kCols;
-        const float mul = which == 0 ? (1.0f / 256.0f) : p.scale;
+        float mul = which == 0 ? (1.0f / 256.0f) : p.scale;
         uint8_t* stg = smem + (which == 0 ? L::kQ : L::kDO) + j * kRowB;
         uint32_t v[32];
-        tmem_ld32(lane_base + col, v);
-        tmem_ld_wait();
+        if (ROT && which == 1) {
+          // rotated operands: this warpgroup's 32 columns of dK_rot H / 2^k.  H = H_kWG x
+          // H_32: combine the row's kWG slices with the signs of H_kWG's row wg, then
+          // the 32-point butterflies (strides 1 .. 16) in registers.
+          float acc[32];
+#pragma unroll 1
+          for (int s2 = 0; s2 < kWG; ++s2) {
+            tmem_ld32(lane_base + kDK + s2 * kCols, v);
+            tmem_ld_wait();
+            const float sg = (__popc(wg & s2) & 1) ? -1.0f : 1.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = s2 == 0 ? sg * __uint_as_float(v[i]) : fmaf(sg, __uint_as_float(v[i]), acc[i]);
+          }
+#pragma unroll
+          for (int st = 1; st < 32; st <<= 1)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (!(i & st)) {
+                const float a = acc[i], b = acc[i + st];
+                acc[i] = a + b;
+                acc[i + st] = a - b;
+              }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[i]);
+          mul *= D == 128 ? 0.0625f : 0.125f;   // 2^-k
+        } else {
+          tmem_ld32(lane_base + col, v);
+          tmem_ld_wait();
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -785,7 +838,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       }
     };
     auto step_qsf = [&](int kk) {       // warpgroup 1: the Q~ rows of step kk
-      load_sf_rows(p.q4_scales, (int64_t)doc_start + (u + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles);
+      load_sf_rows(p.q4_scales, (int64_t)doc_start + (tlo + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles);
     };
     auto store_score_sf = [&]() {
       tmem_st4(lane_base + kP + 32 * ro, sfw[0].x, sfw[1].x, sfw[2].x, sfw[3].x);
@@ -804,7 +857,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     constexpr int kChunks = kRowBytes / 16;            // 16-byte units per staged row
     bool ok = true;
     for (int k = 0; k < nsteps && !STRICT; ++k) {
-      const int hh = k / qtiles, t = u + k % qtiles;
+      const int hh = k / qtiles, t = tlo + k % qtiles;
       const int h = hk * g + hh;
       const float cb = p.boost[(int64_t)doc * p.hq + h];
       const int qvalid = doc_len - t * kTile;          // query rows of the tile inside the document
@@ -938,7 +991,7 @@ __global__ void boost_from_max_kernel(const float* maxima, const int* plan, int 
 // dQ = bf16(scale * acc / c), read from the accumulator chunks one (document
 // tile, query head) at a time; then the rows outside every document of dQ, dK
 // and dV are zeroed.
-template <int D>
+template <int D, bool ROT = false>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(const __half* acc, const int32_t* cu, const int* plan,
                                                           const float* boost, int N, int T, int hq, int hkv,
                                                           float scale, __nv_bfloat16* dq, __nv_bfloat16* dk,
@@ -956,6 +1009,48 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const __half* acc, con
     const int s0 = cu[doc];
     const int rows = min(kTile, cu[doc + 1] - s0 - t * kTile);
     const float mul = scale / boost[(int64_t)doc * hq + h];
+    if constexpr (ROT) {
+      // rotated operands: thread = query row, the row's D values through the D-point
+      // butterflies (strides 1 .. D / 2), times 2^-k
+      for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+        float z[D];
+#pragma unroll
+        for (int c = 0; c < D; c += kVec) {
+          const __half* chunk = acc + dq_chunk_elems(tile, h, c / 32, hq, D);
+          const uint4 in = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(chunk) +
+                                                           dq_chunk_byte(r, (c % 32) * 2));
+          const __half2* hv = reinterpret_cast<const __half2*>(&in);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(hv[q]);
+            z[c + 2 * q] = f.x;
+            z[c + 2 * q + 1] = f.y;
+          }
+        }
+#pragma unroll
+        for (int st = 1; st < D; st <<= 1)
+#pragma unroll
+          for (int i = 0; i < D; ++i)
+            if (!(i & st)) {
+              const float a = z[i], b = z[i + st];
+              z[i] = a + b;
+              z[i + st] = a - b;
+            }
+        const float m2 = mul * (D == 128 ? 0.0625f : 0.125f);
+#pragma unroll
+        for (int c = 0; c < D; c += kVec) {
+          uint4 out;
+          uint32_t* ov = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(z[c + 2 * q] * m2, z[c + 2 * q + 1] * m2);
+            ov[q] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(dq + (((int64_t)s0 + t * kTile + r) * hq + h) * D + c) = out;
+        }
+      }
+      continue;
+    }
     for (int i = threadIdx.x; i < rows * kVpr; i += blockDim.x) {
       const int r = i / kVpr, col = (i % kVpr) * kVec;
       const __half* chunk = acc + dq_chunk_elems(tile, h, col / 32, hq, D);
@@ -993,6 +1088,7 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const __half* acc, con
 // row-major dQ row (16-byte ones if dQ is only 16-byte aligned).
 constexpr int kDqtFinalizeSmem = 2 * 32768;
 
+template <bool ROT = false>
 __global__ void __launch_bounds__(256) dqt_finalize_kernel(const __half* acc, const int32_t* cu, const int* plan,
                                                            const float* boost, int N, int T, int hq, int hkv,
                                                            float scale, __nv_bfloat16* dq, __nv_bfloat16* dk,
@@ -1035,16 +1131,35 @@ __global__ void __launch_bounds__(256) dqt_finalize_kernel(const __half* acc, co
       const uint8_t* base = fsm + buf * 32768 + (q >> 6) * 16384 + (q & 7) * 2;
       const int unit = (q & 63) >> 3;
       __nv_bfloat16* orow = dq + (((int64_t)s0 + t * kTile + q) * hq + h) * D + half * 64;
+      auto val = [&](int d) {
+        return __half2float(*reinterpret_cast<const __half*>(base + d * 128 + ((unit ^ (d & 7)) << 4)));
+      };
+      // rotated operands: this thread's half of the row times H / 16 (H = H_2 x H_64: the
+      // half's sign on the other half, then the 64-point butterflies, strides 1 .. 32)
+      float z[ROT ? 64 : 1];
+      if constexpr (ROT) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) z[c] = half ? val(c) - val(c + 64) : val(c) + val(c + 64);
+#pragma unroll
+        for (int st = 1; st < 64; st <<= 1)
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (!(i & st)) {
+              const float a = z[i], b = z[i + st];
+              z[i] = a + b;
+              z[i + st] = a - b;
+            }
+      }
+      const float m2 = ROT ? mul * 0.0625f : mul;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int d = half * 64 + c * 16 + 2 * j;
-          const float a = __half2float(*reinterpret_cast<const __half*>(base + d * 128 + ((unit ^ (d & 7)) << 4)));
-          const float b =
-              __half2float(*reinterpret_cast<const __half*>(base + (d + 1) * 128 + ((unit ^ ((d + 1) & 7)) << 4)));
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(a * mul, b * mul);
+          const float a = ROT ? z[ROT ? c * 16 + 2 * j : 0] : val(d);
+          const float b = ROT ? z[ROT ? c * 16 + 2 * j + 1 : 0] : val(d + 1);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(a * m2, b * m2);
           pk[j] = *reinterpret_cast<uint32_t*>(&b2);
         }
         __nv_bfloat16* dst = orow + c * 16;
@@ -1442,13 +1557,13 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int D, bool STRICT, bool MIXED, bool DBG = false>
+template <int D, bool STRICT, bool MIXED, bool DBG = false, bool WIN = false, bool ROT = false>
 cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const void* doc_codes, const void* dos, const float* lse, const float* dvec,
                          const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                          const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
                          void* const* ev, const void* q4c, const void* q4s, const void* k4c, const void* k4s,
-                         float* dbg) {
+                         float* dbg, Window win) {
   CUtensorMap tq, tk, tv, tdo, tq4, tk4;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
@@ -1485,35 +1600,36 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dbg = dbg;
+  p.win = win;
   const int64_t max_items = (int64_t)T / kTile + N + 1;
   const int64_t grid = max_items * hkv;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
   constexpr int smem = BwdSmem<D, MIXED>::kAlloc;
   int regs = 0;
-  cudaError_t e = prepare_kernel<attn_bwd_kernel<D, STRICT, MIXED, DBG>>(smem, &regs);
+  cudaError_t e = prepare_kernel<attn_bwd_kernel<D, STRICT, MIXED, DBG, WIN, ROT>>(smem, &regs);
   if (e != cudaSuccess) return e;
   // the warpgroups' register split (setmaxnreg) assumes this launch allocation;
   // with any other the increase could never be granted, so refuse to launch
   if (regs != BwdShape<D, STRICT>::kLaunchRegs) return cudaErrorInvalidConfiguration;
   if (ev) record_timing_event(ev[0], stream);
-  attn_bwd_kernel<D, STRICT, MIXED, DBG>
+  attn_bwd_kernel<D, STRICT, MIXED, DBG, WIN, ROT>
       <<<(unsigned)grid, BwdShape<D, STRICT>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
   e = cudaGetLastError();
   if (ev) record_timing_event(ev[1], stream);
   if (e != cudaSuccess) return e;
   if (ev) record_timing_event(ev[2], stream);
   if (!STRICT && D == 128) {
-    e = prepare_kernel<dqt_finalize_kernel>(kDqtFinalizeSmem);
+    e = prepare_kernel<dqt_finalize_kernel<ROT>>(kDqtFinalizeSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    dqt_finalize_kernel<<<3 * sms, 256, kDqtFinalizeSmem, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan,
+    dqt_finalize_kernel<ROT><<<3 * sms, 256, kDqtFinalizeSmem, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan,
                                                                     boost, N, T, hq, hkv, scale,
                                                                     static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
   } else if (!STRICT) {
-    dq_finalize_kernel<D><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
+    dq_finalize_kernel<D, ROT><<<4 * 152, 256, 0, stream>>>(static_cast<const __half*>(dq_acc), cu, p.plan, boost, N, T, hq,
                                                        hkv, scale, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
   } else {
     DqParams dp;
@@ -1570,13 +1686,25 @@ cudaError_t launch_bwd(int D, const void* qc, const void* qs, const void* kc, co
                        const float* boost, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
                        void* const* ev, bool strict, const void* q4c, const void* q4s, const void* k4c,
-                       const void* k4s, float* dbg) {
+                       const void* k4s, float* dbg, Window win, bool rot) {
 #define FLAMIA_BWD_ARGS qc, qs, kc, ks, vc, vs, doc_codes, dos, lse, dvec, boost, cu, N, T, hq, hkv, scale, plan, \
-                        dq_acc, dq, dk, dv, stream, ev, q4c, q4s, k4c, k4s, dbg
+                        dq_acc, dq, dk, dv, stream, ev, q4c, q4s, k4c, k4s, dbg, win
   const bool mixed = q4c != nullptr;
+  if ((strict || mixed) && (win.left >= 0 || win.right != 0)) return cudaErrorInvalidValue;   // causal only
   if (dbg && (mixed || strict)) return cudaErrorInvalidValue;
+  const bool causal = win.left < 0 && win.right == 0;
+  if (dbg && !causal) return cudaErrorInvalidValue;
   if (dbg && D == 128) return launch_bwd_d<128, false, false, true>(FLAMIA_BWD_ARGS);
   if (dbg && D == 64) return launch_bwd_d<64, false, false, true>(FLAMIA_BWD_ARGS);
+  if (rot && (mixed || strict || dbg)) return cudaErrorInvalidValue;
+  if (rot && D == 128)
+    return causal ? launch_bwd_d<128, false, false, false, false, true>(FLAMIA_BWD_ARGS)
+                  : launch_bwd_d<128, false, false, false, true, true>(FLAMIA_BWD_ARGS);
+  if (rot && D == 64)
+    return causal ? launch_bwd_d<64, false, false, false, false, true>(FLAMIA_BWD_ARGS)
+                  : launch_bwd_d<64, false, false, false, true, true>(FLAMIA_BWD_ARGS);
+  if (!causal && D == 128) return launch_bwd_d<128, false, false, false, true>(FLAMIA_BWD_ARGS);
+  if (!causal && D == 64) return launch_bwd_d<64, false, false, false, true>(FLAMIA_BWD_ARGS);
   if (D == 128 && mixed) return launch_bwd_d<128, false, true>(FLAMIA_BWD_ARGS);
   if (mixed) return cudaErrorInvalidValue;
   if (D == 128 && strict) return launch_bwd_d<128, true, false>(FLAMIA_BWD_ARGS);

@@ -49,6 +49,7 @@ struct FwdParams {
   float scale_log2;          // softmax scale * log2(e)
   __nv_bfloat16* out;
   float* lse;
+  Window win;                // visible keys (causal: right = 0); the strict kernel is causal only
 };
 
 template <int D>
@@ -566,14 +567,18 @@ struct PersistSmem {
 };
 
 // One unit of the forward work: query tiles t0 (.. t0 + ntq - 1) of a document for
-// query head h; nk[w] key tiles are visible to the query tile of warpgroup w.
+// query head h.  The query tile of warpgroup w sees key tiles [klo(w), khi(w)]; the
+// unit loads the union [ulo, ulo + nkv) once, in increasing order.
 struct FwdUnit {
-  int h, hk, t0, ntq, doc_start, doc_len, nkv;
-  int nk0, nk1;
-  __device__ __forceinline__ int nk(int w) const { return w ? nk1 : nk0; }
+  int h, hk, t0, ntq, doc_start, doc_len, nkv, ulo;
+  int klo0, klo1, khi0, khi1;
+  __device__ __forceinline__ int klo(int w) const { return w ? klo1 : klo0; }
+  __device__ __forceinline__ int khi(int w) const { return w ? khi1 : khi0; }
+  __device__ __forceinline__ int nk(int w) const { return w < ntq ? khi(w) - klo(w) + 1 : 0; }
 };
 
-__device__ __forceinline__ FwdUnit fwd_unit(const PlanView& pv, int i, int hq, int hkv) {
+template <bool WIN>
+__device__ __forceinline__ FwdUnit fwd_unit(const PlanView& pv, int i, int hq, int hkv, Window win) {
   FwdUnit U;
   const int item_idx = i / hq;
   U.h = i % hq;
@@ -584,16 +589,22 @@ __device__ __forceinline__ FwdUnit fwd_unit(const PlanView& pv, int i, int hq, i
   U.ntq = item.z;
   U.doc_start = span.x;
   U.doc_len = span.y;
-  U.nk0 = U.t0 + 1;
-  U.nk1 = U.ntq > 1 ? U.t0 + 2 : 0;
-  U.nkv = U.ntq > 1 ? U.t0 + 2 : U.t0 + 1;
+  const int nt = (U.doc_len + kTile - 1) / kTile;
+  U.klo0 = WIN ? win_klo(U.t0, win) : 0;
+  U.khi0 = WIN ? win_khi(U.t0, nt, win) : U.t0;
+  U.klo1 = U.ntq > 1 ? (WIN ? win_klo(U.t0 + 1, win) : 0) : U.klo0;
+  U.khi1 = U.ntq > 1 ? (WIN ? win_khi(U.t0 + 1, nt, win) : U.t0 + 1) : U.khi0;
+  U.ulo = U.klo0;                         // the later query tile's range starts and ends no earlier
+  U.nkv = (U.ntq > 1 ? U.khi1 : U.khi0) - U.ulo + 1;
   return U;
 }
 
 // Unit of round r for CTA c of G (boustrophedon).
 __device__ __forceinline__ int snake_unit(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
 
-template <int D>
+// WIN: a call with a window other than causal (noncausal, sliding); the causal
+// builds carry none of its code.
+template <int D, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -660,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < rounds && ok; ++r) {
         const int i = snake_unit(r, c, G);
         if (i >= n_units) continue;
-        const FwdUnit U = fwd_unit(pv, i, p.hq, p.hkv);
+        const FwdUnit U = fwd_unit<WIN>(pv, i, p.hq, p.hkv, p.win);
         const int qb = qn & 1;
         if (qn >= 2 && !mbar_wait(&q_empty[qb], ((qn >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&q_full[qb], U.ntq * L::kTileBytes);
@@ -675,8 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTileBytes);
-          tma_load_3d(smem + L::kK + st * L::kTileBytes, &tm_k, &kv_full[st], 0, U.hk, U.doc_start + u * kTile);
-          tma_load_3d(smem + L::kV + st * L::kTileBytes, &tm_v, &kv_full[st], 0, U.hk, U.doc_start + u * kTile);
+          const int ku = U.ulo + u;
+          tma_load_3d(smem + L::kK + st * L::kTileBytes, &tm_k, &kv_full[st], 0, U.hk, U.doc_start + ku * kTile);
+          tma_load_3d(smem + L::kV + st * L::kTileBytes, &tm_v, &kv_full[st], 0, U.hk, U.doc_start + ku * kTile);
         }
       }
     }
@@ -711,40 +723,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < rounds && ok; ++r) {
       const int i = snake_unit(r, c, G);
       if (i >= n_units) continue;
-      const FwdUnit U = fwd_unit(pv, i, p.hq, p.hkv);
+      const FwdUnit U = fwd_unit<WIN>(pv, i, p.hq, p.hkv, p.win);
       const int qb = qn & 1;
       ok = warp_wait(&q_full[qb], (qn >> 1) & 1, status) &&
            warp_wait(&kv_full[kvc % kStages], (kvc / kStages) & 1, status);
       if (!ok) break;
       tc_fence_after();
       for (int w = 0; w < U.ntq; ++w) {
+        if (U.klo(w) != U.ulo) continue;         // its first key tile comes later
         issue_s(w, qb, kvc % kStages);
         if (leader) mma_commit(&s_full[w]);
       }
-      for (int u = 0; u < U.nkv && ok; ++u) {
-        const int st = (kvc + u) % kStages;
-        const int st1 = (kvc + u + 1) % kStages;
+      for (int uu = 0; uu < U.nkv && ok; ++uu) {
+        const int u = U.ulo + uu;                // key tile (document-local index)
+        const int st = (kvc + uu) % kStages;
+        const int st1 = (kvc + uu + 1) % kStages;
         bool next_loaded = false;
+        auto load_next = [&]() {
+          if (!next_loaded) {
+            ok = warp_wait(&kv_full[st1], ((kvc + uu + 1) / kStages) & 1, status);
+            if (ok) tc_fence_after();
+            next_loaded = true;
+          }
+          return ok;
+        };
         for (int w = 0; w < U.ntq && ok; ++w) {
-          if (u >= U.nk(w)) continue;
+          if (u < U.klo(w) || u > U.khi(w)) continue;
           ok = warp_wait(&p_full[w], (w ? pcnt1 : pcnt0) & 1, status);
           if (w) ++pcnt1;
           else ++pcnt0;
           if (!ok) break;
           tc_fence_after();
-          issue_pv(w, st, u > 0);
-          if (u + 1 < U.nk(w)) {
-            if (!next_loaded) {
-              ok = warp_wait(&kv_full[st1], ((kvc + u + 1) / kStages) & 1, status);
-              if (!ok) break;
-              tc_fence_after();
-              next_loaded = true;
-            }
+          issue_pv(w, st, u > U.klo(w));
+          if (u + 1 <= U.khi(w)) {
+            if (!load_next()) break;
             issue_s(w, qb, st1);
             if (leader) mma_commit(&s_full[w]);
           } else {
             if (leader) mma_commit(&o_full[w]);
           }
+        }
+        // a warpgroup whose range starts at the next key tile gets its first S now
+        for (int w = 1; w < U.ntq && ok; ++w) {
+          if (U.klo(w) != u + 1) continue;
+          if (!load_next()) break;
+          issue_s(w, qb, st1);
+          if (leader) mma_commit(&s_full[w]);
         }
         if (leader) mma_commit(&kv_empty[st]);
       }
@@ -771,14 +795,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; rr < rounds && ok; ++rr) {
       const int i = snake_unit(rr, c, G);
       if (i >= n_units) continue;
-      const FwdUnit U = fwd_unit(pv, i, p.hq, p.hkv);
+      const FwdUnit U = fwd_unit<WIN>(pv, i, p.hq, p.hkv, p.win);
       if (w >= U.ntq) continue;
       const int t = U.t0 + w;
       const int qrow_local = t * kTile + r;
       const bool row_valid = qrow_local < U.doc_len;
       const int64_t tok = (int64_t)U.doc_start + qrow_local;
       const float fq = p.scale_log2 * scale_of(p.q_scales, tok, p.hq, U.h, row_valid);
-      const int nk = U.nk(w);
+      const int nk = U.nk(w), klo = U.klo(w);
       // K and V block-scale bytes of every key tile of the unit (one per 32-key group,
       // 127 past the document end), staged in this warpgroup's own table (tiles past
       // its capacity read them from global memory); each thread's loads come before
@@ -796,16 +820,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int e = r; e < ntab * 4; e += 128) {
         uint32_t kb, vb;
-        scale_bytes(e >> 2, e & 3, kb, vb);
+        scale_bytes(klo + (e >> 2), e & 3, kb, vb);
         tb[(e >> 2) * 8 + (e & 3)] = (uint8_t)kb;
         tb[(e >> 2) * 8 + 4 + (e & 3)] = (uint8_t)vb;
       }
       named_bar_sync(2 + w, 128);
       float m = -INFINITY, lsum = 0.f;
-      for (int u = 0; u < nk; ++u) {
+      for (int uu = 0; uu < nk; ++uu) {
+        const int u = klo + uu;                // key tile (document-local index)
         uint32_t kw = 0, vsf = 0;
-        if (u < ntab) {
-          const uint2 kv2 = *reinterpret_cast<const uint2*>(tab + 2 * u);
+        if (uu < ntab) {
+          const uint2 kv2 = *reinterpret_cast<const uint2*>(tab + 2 * uu);
           kw = kv2.x;
           vsf = kv2.y;
         } else {
@@ -820,7 +845,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float fk[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) fk[g] = fq * ue8m0_to_f32((kw >> (8 * g)) & 0xFFu);
-        const bool diag = (u == t);
+        // a tile with a hidden pair (causal: the diagonal one) or keys past the document
+        // end takes the masked variants, where this row sees the tile's keys [klim, khim]
+        const bool diag = WIN ? win_masked(t, u, U.doc_len, p.win) : u == t;
+        auto key_bounds = [&](int& klim, int& khim) {
+          if constexpr (WIN) {
+            const int qi = t * kTile + r;
+            klim = p.win.left < 0 ? 0 : qi - p.win.left - u * kTile;
+            khim = min(U.doc_len - 1 - u * kTile, p.win.right < 0 ? kTile : qi + p.win.right - u * kTile);
+          } else {                             // causal: the keys up to the query
+            klim = 0;
+            khim = r;
+          }
+        };
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], scnt & 1, status));
         ++scnt;
         if (!ok) break;
@@ -839,6 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int g = 0; g < 4; ++g) mx = fmaxf(mx, cm[g] * fk[g]);
         } else {
+          int klim, khim;
+          key_bounds(klim, khim);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint32_t v[32];
@@ -846,14 +885,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             float b = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) b = (g * 32 + j) <= r ? fmaxf(b, __uint_as_float(v[j])) : b;
+            for (int j = 0; j < 32; ++j)
+              b = (g * 32 + j >= klim && g * 32 + j <= khim) ? fmaxf(b, __uint_as_float(v[j])) : b;
             mx = fmaxf(mx, b * fk[g]);
           }
         }
         const float m_new = fmaxf(m, mx);
-        const float alpha = fast_exp2(m - m_new);   // 0 on the first tile
+        // 0 on the first tile; 1 while the row has seen no key (a window that starts
+        // further right), where m - m_new would be -inf - -inf
+        const float alpha = (WIN && m_new == -INFINITY) ? 1.0f : fast_exp2(m - m_new);
         // rescale the running O row when the max moved (warp-uniform decision)
-        if (u > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        if (uu > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t v[32];
@@ -872,6 +914,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 acc2 = make_float2(0.f, 0.f);
         auto pass2 = [&](auto diag_tile) {
           constexpr bool kDiag = decltype(diag_tile)::value;
+          int klim = 0, khim = 0;
+          if constexpr (kDiag) key_bounds(klim, khim);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint32_t v[32];
@@ -887,10 +931,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
               if (kDiag) {
                 const int kc = g * 32 + j;
-                p0.x = kc <= r ? p0.x : 0.f;
-                p0.y = kc + 1 <= r ? p0.y : 0.f;
-                p1.x = kc + 2 <= r ? p1.x : 0.f;
-                p1.y = kc + 3 <= r ? p1.y : 0.f;
+                p0.x = (kc >= klim && kc <= khim) ? p0.x : 0.f;
+                p0.y = (kc + 1 >= klim && kc + 1 <= khim) ? p0.y : 0.f;
+                p1.x = (kc + 2 >= klim && kc + 2 <= khim) ? p1.x : 0.f;
+                p1.y = (kc + 3 >= klim && kc + 3 <= khim) ? p1.y : 0.f;
               }
               acc2 = fadd2(acc2, fadd2(p0, p1));
               packed[j >> 2] = (uint32_t)e4m3x2(p0.x, p0.y) | ((uint32_t)e4m3x2(p1.x, p1.y) << 16);
@@ -976,7 +1020,7 @@ __global__ void fwd_tail_kernel(const int* plan, int T, int hq, __nv_bfloat16* o
 template <int D, bool STRICT>
 cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                         const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev) {
+                         const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, Window win) {
   CUtensorMap tq, tk, tv;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
@@ -995,6 +1039,7 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
+  p.win = win;
   const int64_t max_items = (int64_t)T / (kTile * kItemTiles) + N + 1;
   const int64_t grid = max_items * hq;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
@@ -1013,12 +1058,15 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
     if (e != cudaSuccess) return e;
     constexpr int smem = PersistSmem<D>::kAlloc;
     int regs = 0;
-    e = prepare_kernel<attn_fwd_persist_kernel<D>>(smem, &regs);
+    const bool causal = win.left < 0 && win.right == 0;
+    e = causal ? prepare_kernel<attn_fwd_persist_kernel<D, false>>(smem, &regs)
+               : prepare_kernel<attn_fwd_persist_kernel<D, true>>(smem, &regs);
     if (e != cudaSuccess) return e;
     if (regs != kPersistLaunchRegs) return cudaErrorInvalidConfiguration;
     const unsigned pgrid = (unsigned)(grid < sms ? grid : sms);
     if (ev) record_timing_event(ev[0], stream);
-    attn_fwd_persist_kernel<D><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    if (causal) attn_fwd_persist_kernel<D, false><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    else attn_fwd_persist_kernel<D, true><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
   }
   e = cudaGetLastError();
   if (ev) record_timing_event(ev[1], stream);
@@ -1044,13 +1092,15 @@ cudaError_t launch_fwd_tail(int D, const void* plan, int T, int hq, void* out, f
 
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict) {
-  if (D == 128 && strict)
-    return launch_fwd_d<128, true>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
-  if (D == 128) return launch_fwd_d<128, false>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
-  if (D == 64 && strict)
-    return launch_fwd_d<64, true>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
-  if (D == 64) return launch_fwd_d<64, false>(qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev);
+                       const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict,
+                       Window win) {
+#define FLAMIA_FWD_ARGS qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev, win
+  if (strict && (win.left >= 0 || win.right != 0)) return cudaErrorInvalidValue;   // the strict kernel is causal
+  if (D == 128 && strict) return launch_fwd_d<128, true>(FLAMIA_FWD_ARGS);
+  if (D == 128) return launch_fwd_d<128, false>(FLAMIA_FWD_ARGS);
+  if (D == 64 && strict) return launch_fwd_d<64, true>(FLAMIA_FWD_ARGS);
+  if (D == 64) return launch_fwd_d<64, false>(FLAMIA_FWD_ARGS);
+#undef FLAMIA_FWD_ARGS
   return cudaErrorInvalidValue;
 }
 

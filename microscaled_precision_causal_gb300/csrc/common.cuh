@@ -26,6 +26,8 @@ enum PlanWord : int {
   kPlanFwdItems = 6,
   kPlanBwdItems = 7,
   kPlanCapacity = 8,
+  kPlanWindowLeft = 9,      // the window the costs were computed for
+  kPlanWindowRight = 10,
   kPlanHeaderWords = 16,
 };
 
@@ -42,6 +44,44 @@ struct PlanView {
 };
 
 __host__ __device__ inline int64_t plan_capacity(int64_t T, int N) { return T / kTile + N + 1; }
+// ---------------------------------------------------------------- visible keys
+// Query i of a document sees key j of the same document (document-local
+// positions) iff i - left <= j <= i + right; a negative bound means no limit on
+// that side.  Causal calls use right = 0, noncausal calls (-1, -1) (the packed
+// noncausal calls of the FLAMIA review, section 8 and its Appendix H); other
+// values give sliding windows.
+struct Window {
+  int left, right;
+};
+// Key tiles [win_klo, win_khi] seen by some query of query tile t (nt tiles in
+// the document): the rows' visible ranges are consecutive, so the union runs
+// from the first row's first key to the last row's last key.
+__host__ __device__ inline int win_klo(int t, Window w) {
+  return w.left < 0 ? 0 : (t * kTile - w.left > 0 ? t * kTile - w.left : 0) / kTile;
+}
+__host__ __device__ inline int win_khi(int t, int nt, Window w) {
+  if (w.right < 0) return nt - 1;
+  const int h = (t * kTile + kTile - 1 + w.right) / kTile;
+  return h < nt - 1 ? h : nt - 1;
+}
+// Query tiles [win_tlo, win_thi] holding some query that sees a key of key tile u.
+__host__ __device__ inline int win_tlo(int u, Window w) {
+  return w.right < 0 ? 0 : (u * kTile - w.right > 0 ? u * kTile - w.right : 0) / kTile;
+}
+__host__ __device__ inline int win_thi(int u, int nt, Window w) {
+  if (w.left < 0) return nt - 1;
+  const int h = (u * kTile + kTile - 1 + w.left) / kTile;
+  return h < nt - 1 ? h : nt - 1;
+}
+// True when some (query, key) pair of query tile t x key tile u is hidden by the
+// window, or the key tile runs past the document end: the tile needs a mask.
+__host__ __device__ inline bool win_masked(int t, int u, int doc_len, Window w) {
+  if ((u + 1) * kTile > doc_len) return true;
+  if (w.right >= 0 && u * kTile + kTile - 1 > t * kTile + w.right) return true;
+  if (w.left >= 0 && u * kTile < t * kTile + kTile - 1 - w.left) return true;
+  return false;
+}
+
 // fp16 dQ accumulator of the default backward at head_dim 64 (workspace-internal
 // layout): one contiguous 8 KB chunk per (document tile, query head, 32-column
 // slice of the head dim), tile = tile_prefix[doc] + document-local tile index.  A chunk holds

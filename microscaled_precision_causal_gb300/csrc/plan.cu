@@ -11,6 +11,9 @@
 //      tiles) and backward key-tile items (cost = query tiles that see the
 //      key tile), each sorted by decreasing cost with ties in document, then
 //      tile order: a bitonic sort of 64-bit keys (cost descending, index).
+// "Visible" follows the call's (left, right) window (causal: keys up to the
+// query; noncausal: the whole document).  The costs only order the work; the
+// item sets are the same for every window.
 #include "common.cuh"
 
 namespace flamia {
@@ -98,7 +101,7 @@ __device__ void bitonic_sort(unsigned long long* keys, int n) {  // n is a power
 
 constexpr int kSmemKeys = 4096;   // sorts of up to this many keys run in shared memory
 
-__global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restrict__ cu, int N, int T,
+__global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restrict__ cu, int N, int T, Window win,
                                                         int* __restrict__ plan_words) {
   __shared__ unsigned long long smem_keys[kSmemKeys];
   __shared__ int warp_sums[32];
@@ -171,6 +174,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     plan_words[kPlanFwdItems] = (bad || over) ? 0 : nitem;
     plan_words[kPlanBwdItems] = (bad || over) ? 0 : ntile;
     plan_words[kPlanCapacity] = cap;
+    plan_words[kPlanWindowLeft] = win.left;
+    plan_words[kPlanWindowRight] = win.right;
   }
   if (bad || over) return;
   const unsigned long long kPad = ~0ull;
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
         const int t0 = (i - item_prefix[doc]) * kItemTiles;
         const int cnt = min(kItemTiles, nt - t0);
         int cost = 0;
-        for (int t = t0; t < t0 + cnt; ++t) cost += t + 1;
+        for (int t = t0; t < t0 + cnt; ++t) cost += win_khi(t, nt, win) - win_klo(t, win) + 1;
         key = ((unsigned long long)(kCostMax - (unsigned)cost) << 32) | (unsigned)i;
       }
       keys[i] = key;
@@ -215,7 +220,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
       if (i < ntile) {
         const int doc = upper_doc(tile_prefix, N, i);
         const int nt = tile_prefix[doc + 1] - tile_prefix[doc];
-        const int cost = nt - (i - tile_prefix[doc]);
+        const int u = i - tile_prefix[doc];
+        const int cost = win_thi(u, nt, win) - win_tlo(u, win) + 1;
         key = ((unsigned long long)(kCostMax - (unsigned)cost) << 32) | (unsigned)i;
       }
       keys[i] = key;
@@ -233,8 +239,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
 
 }  // namespace
 
-cudaError_t launch_plan(const int32_t* cu, int N, int T, void* plan, cudaStream_t s) {
-  plan_kernel<<<1, kThreads, 0, s>>>(cu, N, T, static_cast<int*>(plan));
+cudaError_t launch_plan(const int32_t* cu, int N, int T, Window win, void* plan, cudaStream_t s) {
+  plan_kernel<<<1, kThreads, 0, s>>>(cu, N, T, win, static_cast<int*>(plan));
   return cudaGetLastError();
 }
 

@@ -15,6 +15,14 @@
 // The backward-prep variant (review Algorithm 1 step 09) encodes dO once and,
 // in the same pass, computes D_i = dO^_i . O_i from the saved bf16 O and
 // zeroes the fp16 dQ accumulator rows it owns.
+//
+// The rotated variant (review section 3, "Rotation, range, and the
+// alternative"; Korean review section 3.4: rotation, block statistics, codes
+// and scales in one pass) first multiplies each token row by H / 2^k (H the
+// +-1 Sylvester Hadamard matrix, k = ceil(log2(d) / 2)) with the fast
+// Walsh-Hadamard butterflies in fp32, strides 1, 2, ..., d/2 in increasing
+// order: inside a lane's 16-byte vectors, then across the row's lanes
+// (shuffles), then across the lane's vectors.
 #include <cuda_fp4.h>
 
 #include "common.cuh"
@@ -27,14 +35,16 @@ namespace {
 // Launch shape: the plain quantizer holds its block in registers between the two
 // passes (4 warps, 3 blocks per SM); the backward prep streams dO and O and keeps
 // more warps in flight instead, re-reading the block from L1/L2 in pass 2.
-template <bool WITH_D>
+// The rotated variant streams its block twice (one unit per warp, more warps in
+// flight) instead of holding it next to the rotation's working values.
+template <bool WITH_D, bool ROT = false>
 struct QShape {
-  static constexpr int kWarps = WITH_D ? 8 : 4;
-  static constexpr int kMinBlocks = WITH_D ? 4 : 3;
+  static constexpr int kWarps = WITH_D || ROT ? 8 : 4;
+  static constexpr int kMinBlocks = WITH_D || ROT ? 4 : 3;
 };
 
-template <int D, bool PER_TOKEN, bool STATS, bool WITH_D>
-__global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::kMinBlocks)
+template <int D, bool PER_TOKEN, bool STATS, bool WITH_D, bool ROT = false>
+__global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_D, ROT>::kMinBlocks)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, const int32_t* __restrict__ cu, int N,
                     const int* __restrict__ plan, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                     float2* __restrict__ stats, const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec,
@@ -47,8 +57,9 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
   constexpr int kRpi = 32 / kLpr;      // rows per iteration
   constexpr int kIters = 32 / kRpi;    // 32 rows per warp
   const int lane = threadIdx.x & 31;
-  constexpr int kWarps = QShape<WITH_D>::kWarps;
-  constexpr bool kHold = !PER_TOKEN && !WITH_D;   // block held in registers for pass 2
+  constexpr int kWarps = QShape<WITH_D, ROT>::kWarps;
+  constexpr bool kHold = !PER_TOKEN && !WITH_D && !ROT;   // block held in registers for pass 2
+  static_assert(!ROT || (!PER_TOKEN && !WITH_D), "the rotation is fused into the token-block quantizer of Q and K");
   const PlanView pv = plan_view(plan, T, N);
   const int valid = plan[kPlanValid];
   const int nblk = plan[kPlanBlocks];
@@ -140,6 +151,57 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
     return live(r) ? __ldg(reinterpret_cast<const uint4*>(base + ((int64_t)(r0 + r) * H + h) * D + col_of(j)))
                    : make_uint4(0, 0, 0, 0);
   };
+  // the row's 32 values of this lane rotated by H / 2^k (fp32 butterflies, strides
+  // 1, 2, 4 in the vectors, 8 .. 4 kLpr across the lanes, 8 kLpr, 16 kLpr across vectors)
+  auto rotate = [&](const uint4 (&rw)[4], float (&v)[4][8]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&rw[j]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(b[q]);
+        v[j][2 * q] = f.x;
+        v[j][2 * q + 1] = f.y;
+      }
+#pragma unroll
+      for (int st = 1; st < 8; st <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (!(i & st)) {
+            const float a = v[j][i], c = v[j][i + st];
+            v[j][i] = __fadd_rn(a, c);
+            v[j][i + st] = __fsub_rn(a, c);
+          }
+    }
+#pragma unroll
+    for (int m = 1; m < kLpr; m <<= 1) {
+      const bool upper = (seg & m) != 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float o = __shfl_xor_sync(0xffffffffu, v[j][i], m);
+          v[j][i] = upper ? __fsub_rn(o, v[j][i]) : __fadd_rn(v[j][i], o);
+        }
+    }
+#pragma unroll
+    for (int st = 1; st < 4; st <<= 1)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (!(j & st)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float a = v[j][i], c = v[j + st][i];
+            v[j][i] = __fadd_rn(a, c);
+            v[j + st][i] = __fsub_rn(a, c);
+          }
+        }
+    constexpr float kNorm = D == 128 ? 0.0625f : 0.125f;    // 2^-k
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[j][i] *= kNorm;
+  };
   auto absmax8 = [](const uint4& w) {
     const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&w);
     float m = 0.f;
@@ -159,10 +221,22 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
     float a = 0.f;
 #pragma unroll
     for (int it = 0; it < kIters; ++it) {
+      if constexpr (ROT) {
+        float v[4][8];
+        uint4 rw[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 x4 = kHold ? w[kHold ? it : 0][j] : load8(x, it * kRpi + sub, j);
-        a = fmaxf(a, absmax8(x4));
+        for (int j = 0; j < 4; ++j) rw[j] = load8(x, it * kRpi + sub, j);
+        rotate(rw, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) a = fmax3(a, fabsf(v[j][i]), fabsf(v[j][i + 1]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 x4 = kHold ? w[kHold ? it : 0][j] : load8(x, it * kRpi + sub, j);
+          a = fmaxf(a, absmax8(x4));
+        }
       }
     }
 #pragma unroll
@@ -187,13 +261,16 @@ __global__ void __launch_bounds__(QShape<WITH_D>::kWarps * 32, QShape<WITH_D>::k
     const float back = ue8m0_to_f32((uint32_t)(e + 127));
     float2 ss2 = make_float2(0.f, 0.f), dd2 = make_float2(0.f, 0.f);
     uint32_t cmax4 = 0;
+    float rv[ROT ? 4 : 1][ROT ? 8 : 1];
+    if constexpr (ROT) rotate(raw, rv);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
       uint32_t packed[2];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(v[q]);
+        const float2 f = ROT ? make_float2(rv[ROT ? j : 0][ROT ? 2 * q : 0], rv[ROT ? j : 0][ROT ? 2 * q + 1 : 0])
+                             : __bfloat1622float2(v[q]);
         const uint16_t c2 = e4m3x2(f.x * s, f.y * s);
         if (q & 1) packed[q >> 1] |= (uint32_t)c2 << 16; else packed[q >> 1] = c2;
       }
@@ -281,25 +358,25 @@ struct PrepExtra {          // backward prep only
   float* maxima;            // [N, H, 3], zeroed by the caller
 };
 
-template <int D, bool PT, bool ST, bool WD>
+template <int D, bool PT, bool ST, bool WD, bool ROT = false>
 cudaError_t launch_q(const void* x, int T, int H, const int32_t* cu, int N, const void* plan, void* codes,
                      void* scales, float* stats, const void* o, float* dvec, void* dq_acc, const PrepExtra& px,
                      cudaStream_t s) {
   const int64_t units = PT ? (T + 31) / 32 : (int64_t)T / 32 + N + 1;
   const int64_t warps = units * H;
-  constexpr int kWarps = QShape<WD>::kWarps;
+  constexpr int kWarps = QShape<WD, ROT>::kWarps;
   int64_t blocks = (warps + kWarps - 1) / kWarps;
   // the register-held variant walks several units per warp (its next block prefetched);
   // the others keep one unit per warp
-  if (!PT && !WD) {
+  if (!PT && !WD && !ROT) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return cudaErrorInvalidValue;
-    const int64_t resident = (int64_t)sms * QShape<WD>::kMinBlocks;
+    const int64_t resident = (int64_t)sms * QShape<WD, ROT>::kMinBlocks;
     if (blocks > resident) blocks = resident;
   }
   if (blocks > 0x7FFFFFFF || blocks < 1) return cudaErrorInvalidValue;
-  quantize_kernel<D, PT, ST, WD><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
+  quantize_kernel<D, PT, ST, WD, ROT><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), T, H, cu, N, static_cast<const int*>(plan),
       static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), reinterpret_cast<float2*>(stats),
       static_cast<const __nv_bfloat16*>(o), dvec, static_cast<__half*>(dq_acc),
@@ -384,6 +461,25 @@ cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, voi
 // o / dvec non-null selects the backward-prep variant (stats required); with the
 // token-block rule it also zeroes dq_acc (if non-null) and folds the dQ boost
 // inputs into maxima (if non-null; k_stats / v_stats of the hkv K/V heads).
+// Hadamard-rotated token-block quantization of Q or K (stats optional).
+cudaError_t launch_quantize_rot(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
+                                void* codes, void* scales, float* stats, cudaStream_t s) {
+  const PrepExtra px{nullptr, nullptr, 1, nullptr};
+  if (D == 128 && stats)
+    return launch_q<128, false, true, false, true>(x, T, H, cu, N, plan, codes, scales, stats, nullptr, nullptr,
+                                                   nullptr, px, s);
+  if (D == 128)
+    return launch_q<128, false, false, false, true>(x, T, H, cu, N, plan, codes, scales, nullptr, nullptr, nullptr,
+                                                    nullptr, px, s);
+  if (D == 64 && stats)
+    return launch_q<64, false, true, false, true>(x, T, H, cu, N, plan, codes, scales, stats, nullptr, nullptr,
+                                                  nullptr, px, s);
+  if (D == 64)
+    return launch_q<64, false, false, false, true>(x, T, H, cu, N, plan, codes, scales, nullptr, nullptr, nullptr,
+                                                   nullptr, px, s);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
                             int per_token, void* codes, void* scales, float* stats, const void* o, float* dvec,
                             void* dq_acc, cudaStream_t s, const float* k_stats, const float* v_stats, int hkv,

@@ -39,11 +39,11 @@ import numpy as np
 __all__ = [
     "E4M3_MAX", "FP16_MAX", "e4m3_decode", "e4m3_round", "e4m3_encode", "e2m1_round", "e2m1_encode",
     "e2m1_decode", "bf16_round", "fp16_round", "ue8m0_decode",
-    "roundup_exponent", "floor_exponent", "quantize_tokenblock", "dequantize_tokenblock",
+    "roundup_exponent", "floor_exponent", "quantize_tokenblock", "dequantize_tokenblock", "hadamard_rotate", "hadamard_norm_log2",
     "quantize_nvfp4", "dequantize_nvfp4",
     "Options", "attention_forward", "attention_backward", "run_training_call",
     "dense_attention", "dense_attention_grads", "visible_pairs", "work_list",
-    "bwd_key_tile_list", "dq_boost", "causal_dq_boost", "doc_ranges",
+    "bwd_key_tile_list", "visible_keys", "key_tiles", "query_tiles", "dq_boost", "causal_dq_boost", "doc_ranges",
 ]
 
 E4M3_MAX = 448.0          # largest finite E4M3 magnitude ([FA] "Lower precision", format table)
@@ -234,6 +234,38 @@ def quantize_tokenblock(x, cu, block: int = 32, rule: str = "roundup"):
     return codes, sbytes
 
 
+def hadamard_norm_log2(d: int) -> int:
+    """k = ceil(log2(d) / 2): the rotation is H / 2**k (see :func:`hadamard_rotate`)."""
+    return (int(d).bit_length() - 1 + 1) // 2
+
+
+def hadamard_rotate(x, dtype=np.float32) -> np.ndarray:
+    """Rotation of the head dimension, reading C-18 ([EN] section 3 "Rotation,
+    range, and the alternative": an orthogonal normalized Hadamard matrix mixes
+    the last dimension before rounding, and the exact score is unchanged; [KO]
+    section 3.4: fused into the quantizer, on by default at head dim 128).
+
+    Returns x H~ along the last axis with H~ = H / 2**k, H the d x d Sylvester
+    Hadamard matrix (entries +-1, H H = d I) and k = ceil(log2(d) / 2), so the
+    scale is a power of two (d = 64: H~ is orthonormal; d = 128: H~ H~ = I / 2).
+    It is computed by the fast Walsh-Hadamard butterfly network: for strides
+    1, 2, ..., d/2 in increasing order every pair (i, i + stride) with that bit
+    of i clear becomes (a + b, a - b), each sum rounded to ``dtype`` (fp32 for
+    the quantized route: the codes of the rotated values are bit-exact); then
+    the power of two.  H~ is symmetric, so the same map undoes a rotation up to
+    the factor d / 4**k."""
+    y = np.asarray(x, np.float64).astype(dtype)
+    d = y.shape[-1]
+    lead = y.shape[:-1]
+    st = 1
+    while st < d:
+        v = y.reshape(lead + (d // (2 * st), 2, st))
+        a, b = v[..., 0, :], v[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(lead + (d,))
+        st *= 2
+    return (y * dtype(2.0 ** -hadamard_norm_log2(d))).astype(np.float64)
+
+
 def dequantize_tokenblock(codes, sbytes) -> np.ndarray:
     """X^ = s_X * c_X with s_X = 2**(byte - 127) per token and head."""
     return e4m3_decode(codes) * ue8m0_decode(sbytes)[:, :, None]
@@ -270,12 +302,55 @@ def dequantize_nvfp4(codes, scodes) -> np.ndarray:
 # behavior" and Algorithm 2.
 # --------------------------------------------------------------------------
 
-def visible_pairs(lengths) -> int:
-    """Visible (query, key) pairs of causal packed documents: sum n(n+1)/2."""
-    return int(sum(int(n) * (int(n) + 1) // 2 for n in lengths))
+def visible_pairs(lengths, window=(-1, 0)) -> int:
+    """Visible (query, key) pairs of packed documents: sum n(n+1)/2 for causal
+    calls; under a (left, right) window (see :func:`visible_keys`) the sum over
+    every query row of the length of its visible key range."""
+    if tuple(window) == (-1, 0):
+        return int(sum(int(n) * (int(n) + 1) // 2 for n in lengths))
+    total = 0
+    for n in lengths:
+        i = np.arange(int(n))
+        lo, hi = visible_keys(i, int(n), window)
+        total += int(np.maximum(hi - lo + 1, 0).sum())
+    return total
 
 
-def work_list(cu, tile: int = 128, item_tiles: int = 2, num_ctas: Optional[int] = None):
+def visible_keys(i, L: int, window=(-1, 0)):
+    """Document-local key range [lo, hi] that query i of a document of length L
+    sees.  window = (left, right): key j is visible iff i - left <= j <= i + right,
+    a negative bound meaning no limit on that side.  Causal calls use (-1, 0)
+    (keys up to the query), noncausal calls (-1, -1) (the whole document) --
+    the packed noncausal calls of [EN] section 8 / Appendix H; other values give
+    sliding windows.  Keys never leave the document."""
+    left, right = window
+    i = np.asarray(i)
+    lo = np.zeros_like(i) if left < 0 else np.maximum(i - left, 0)
+    hi = np.full_like(i, L - 1) if right < 0 else np.minimum(i + right, L - 1)
+    return lo, hi
+
+
+def key_tiles(t: int, L: int, window=(-1, 0), tile: int = 128) -> range:
+    """Key tiles holding a key that some query of query tile t sees: the rows'
+    ranges are consecutive, so their union runs from the first row's lo to the
+    last row's hi."""
+    first, last = t * tile, min(t * tile + tile, L) - 1
+    lo, _ = visible_keys(first, L, window)
+    _, hi = visible_keys(last, L, window)
+    return range(int(lo) // tile, int(hi) // tile + 1)
+
+
+def query_tiles(u: int, L: int, window=(-1, 0), tile: int = 128) -> range:
+    """Query tiles holding a query that sees some key of key tile u (query i sees
+    key j iff j - right <= i <= j + left)."""
+    left, right = window
+    first, last = u * tile, min(u * tile + tile, L) - 1
+    lo = 0 if right < 0 else max(first - right, 0)
+    hi = L - 1 if left < 0 else min(last + left, L - 1)
+    return range(lo // tile, hi // tile + 1)
+
+
+def work_list(cu, tile: int = 128, item_tiles: int = 2, num_ctas: Optional[int] = None, window=(-1, 0)):
     """Algorithm 2 of [EN] (steps 03-06) with reading C-11: items of up to
     ``item_tiles`` query tiles (256 queries) of one document; cost = number of
     visible key tiles summed over the item's query tiles (causal); sort by
@@ -289,7 +364,7 @@ def work_list(cu, tile: int = 128, item_tiles: int = 2, num_ctas: Optional[int] 
         ntile = -(-(t - s) // tile)
         for t0 in range(0, ntile, item_tiles):
             nt = min(item_tiles, ntile - t0)
-            cost = sum(tt + 1 for tt in range(t0, t0 + nt))
+            cost = sum(len(key_tiles(tt, t - s, window, tile)) for tt in range(t0, t0 + nt))
             items.append(dict(doc=n, tile0=t0, ntiles=nt, cost=cost))
     order = sorted(range(len(items)), key=lambda i: (-items[i]["cost"], i))
     out = [items[i] for i in order]
@@ -300,7 +375,7 @@ def work_list(cu, tile: int = 128, item_tiles: int = 2, num_ctas: Optional[int] 
     return out
 
 
-def bwd_key_tile_list(cu, tile: int = 128):
+def bwd_key_tile_list(cu, tile: int = 128, window=(-1, 0)):
     """Backward work ([EN] Algorithm 2 step 12): one item per document-local key
     tile, cost = number of query tiles that see it, sorted by decreasing cost
     (ties keep document order then key order)."""
@@ -308,7 +383,7 @@ def bwd_key_tile_list(cu, tile: int = 128):
     for n, (s, t) in enumerate(doc_ranges(cu)):
         ntile = -(-(t - s) // tile)
         for u in range(ntile):
-            items.append(dict(doc=n, ktile=u, cost=ntile - u))
+            items.append(dict(doc=n, ktile=u, cost=len(query_tiles(u, t - s, window, tile))))
     order = sorted(range(len(items)), key=lambda i: (-items[i]["cost"], i))
     return [items[i] for i in order]
 
@@ -333,12 +408,22 @@ class Options:
     tile: int = 128                # query and key tile (reading C-11)
     dq_headroom_log2: int = 14     # dQ boost target 2**14 (reading C-10)
     mixed: bool = False            # mixed route: NVFP4 score operands, diagonal per-key V (C-7, C-8)
+    window: tuple = (-1, 0)        # (left, right) visible-key window: causal (-1, 0), noncausal (-1, -1)
+    rotate: bool = False           # Hadamard rotation of Q and K before quantization (reading C-18)
 
 
-def _masked_scores(Qt, Ku, qpos, kpos, scale):
+def _masked_scores(Qt, Ku, qpos, kpos, scale, window=(-1, 0)):
+    """scale * Q K^T with the keys a query does not see set to -inf (positions of
+    one document; see visible_keys)."""
+    left, right = window
     S = scale * (Qt @ Ku.T)
-    S = np.where(kpos[None, :] > qpos[:, None], -np.inf, S)
-    return S
+    d = kpos[None, :] - qpos[:, None]
+    hidden = np.zeros(d.shape, bool)
+    if right >= 0:
+        hidden |= d > right
+    if left >= 0:
+        hidden |= d < -left
+    return np.where(hidden, -np.inf, S)
 
 
 def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] = None,
@@ -401,13 +486,15 @@ def attention_forward(Qh, Kh, Vh, cu, hq: int, hkv: int, scale: Optional[float] 
                 m = np.full(r1 - r0, -np.inf)
                 l = np.zeros(r1 - r0)
                 acc = np.zeros((r1 - r0, d))
-                for u in range(t + 1):
+                for u in key_tiles(t, s1 - s0, opts.window, tile):
                     c0, c1 = s0 + u * tile, min(s0 + (u + 1) * tile, s1)
-                    S = _masked_scores(Qt, Ks[c0:c1, hk], qpos, np.arange(c0, c1), scale)
+                    S = _masked_scores(Qt, Ks[c0:c1, hk], qpos, np.arange(c0, c1), scale, opts.window)
                     rowmax = S.max(axis=1)
                     m_new = np.where(rowmax > m + tau_nat, np.maximum(m, rowmax), m)
-                    alpha = np.where(np.isfinite(m), np.exp(m - m_new), 0.0)
-                    p = np.exp(S - m_new[:, None])
+                    with np.errstate(invalid="ignore"):
+                        alpha = np.where(np.isfinite(m), np.exp(m - m_new), 0.0)
+                    with np.errstate(invalid="ignore"):   # rows that have seen no key yet: p = 0
+                        p = np.where(np.isfinite(S), np.exp(S - m_new[:, None]), 0.0)
                     l = l * alpha + p.sum(axis=1)
                     Vt = Vh[c0:c1, hk]
                     if not opts.quantized:
@@ -454,7 +541,8 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                        kv_heads: Optional[Iterable[int]] = None,
                        k_tiles: Optional[Dict[int, Iterable[int]]] = None,
                        q_tiles: Optional[Dict[int, Iterable[int]]] = None,
-                       diagnostics: bool = False, tok_scales: Optional[dict] = None, score_ops=None):
+                       diagnostics: bool = False, tok_scales: Optional[dict] = None, score_ops=None,
+                       grad_map=None):
     """Backward of Algorithm 1 (steps 09-16).
 
     dOh: the reconstructed incoming gradient dO^ (encoded once, step 09);
@@ -487,7 +575,10 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
     uses the E4M3 copies as in the default route.
 
     k_tiles / q_tiles restrict which dK/dV key tiles and dQ query tiles are
-    produced (others stay zero); kv_heads restricts heads.
+    produced (others stay zero); kv_heads restricts heads.  grad_map (rotated
+    operands): applied along the head dimension to scale * accQ / c and to
+    scale * dK before the bf16 rounding, to bring them back to the caller's
+    basis.
     Returns dict with dq, dk, dv (and diagnostics when asked)."""
     Qh = np.asarray(Qh, np.float64); Kh = np.asarray(Kh, np.float64)
     Vh = np.asarray(Vh, np.float64); dOh = np.asarray(dOh, np.float64)
@@ -526,12 +617,12 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                 for u in range(ntile):
                     c0, c1 = s0 + u * tile, min(s0 + (u + 1) * tile, s1)
                     kpos = np.arange(c0, c1)
-                    for t in range(u, ntile):
+                    for t in query_tiles(u, s1 - s0, opts.window, tile):
                         if u not in ksel and t not in qsel and not diagnostics:
                             continue
                         r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
                         qpos = np.arange(r0, r1)
-                        S = _masked_scores(Qs[r0:r1, h], Ks[c0:c1, hk], qpos, kpos, scale)
+                        S = _masked_scores(Qs[r0:r1, h], Ks[c0:c1, hk], qpos, kpos, scale, opts.window)
                         P = np.exp(S - LSE[h, r0:r1][:, None])
                         dP = dOh[r0:r1, h] @ Vh[c0:c1, hk].T
                         dS = P * (dP - D[r0:r1, h][:, None])
@@ -579,8 +670,11 @@ def attention_backward(Qh, Kh, Vh, O, LSE, dOh, cu, hq: int, hkv: int,
                     r0, r1 = s0 + t * tile, min(s0 + (t + 1) * tile, s1)
                     ct = c[r0 - s0:r1 - s0, None] if np.ndim(c) else c
                     dQ[r0:r1, h] = scale * accQ[t] / ct
+    dK = scale * dK
+    if grad_map is not None:
+        dQ, dK = grad_map(dQ), grad_map(dK)
     out = dict(dq=bf16_round(dQ) if q else dQ,
-               dk=bf16_round(scale * dK) if q else scale * dK,
+               dk=bf16_round(dK) if q else dK,
                dv=bf16_round(dV) if q else dV)
     if diagnostics:
         out["diag"] = diag
@@ -648,7 +742,7 @@ def _quantize_ds_blocks(dS, qoff: int, koff: int, block: int = 32):
 # 1.2; [EN] section 2 "The contraction moves between forward and backward".
 # --------------------------------------------------------------------------
 
-def dense_attention(Q, K, V, cu, hq: int, hkv: int, scale: Optional[float] = None):
+def dense_attention(Q, K, V, cu, hq: int, hkv: int, scale: Optional[float] = None, window=(-1, 0)):
     """Masked softmax attention per document and head, whole score matrix at once.
     Returns (O [T,hq,d], LSE [hq,T])."""
     Q = np.asarray(Q, np.float64); K = np.asarray(K, np.float64); V = np.asarray(V, np.float64)
@@ -659,7 +753,7 @@ def dense_attention(Q, K, V, cu, hq: int, hkv: int, scale: Optional[float] = Non
     for s0, s1 in doc_ranges(cu):
         pos = np.arange(s0, s1)
         for h in range(hq):
-            S = _masked_scores(Q[s0:s1, h], K[s0:s1, h // g], pos, pos, scale)
+            S = _masked_scores(Q[s0:s1, h], K[s0:s1, h // g], pos, pos, scale, window)
             mx = S.max(1, keepdims=True)
             E = np.exp(S - mx)
             Z = E.sum(1, keepdims=True)
@@ -668,7 +762,7 @@ def dense_attention(Q, K, V, cu, hq: int, hkv: int, scale: Optional[float] = Non
     return O, LSE
 
 
-def dense_attention_grads(Q, K, V, dO, cu, hq: int, hkv: int, scale: Optional[float] = None):
+def dense_attention_grads(Q, K, V, dO, cu, hq: int, hkv: int, scale: Optional[float] = None, window=(-1, 0)):
     """Textbook gradients: dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij,
     dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q (GQA: summed over the
     query heads of a kv head).  Returns dict dq, dk, dv, ds_rowsum [hq,T]."""
@@ -683,7 +777,7 @@ def dense_attention_grads(Q, K, V, dO, cu, hq: int, hkv: int, scale: Optional[fl
         pos = np.arange(s0, s1)
         for h in range(hq):
             hk = h // g
-            S = _masked_scores(Q[s0:s1, h], K[s0:s1, hk], pos, pos, scale)
+            S = _masked_scores(Q[s0:s1, h], K[s0:s1, hk], pos, pos, scale, window)
             P = np.exp(S - S.max(1, keepdims=True))
             P /= P.sum(1, keepdims=True)
             dP = dO[s0:s1, h] @ V[s0:s1, hk].T
@@ -708,8 +802,22 @@ def run_training_call(q, k, v, do, cu, hq: int, hkv: int, scale: Optional[float]
     backward (sampled parity at large sizes).  Returns a dict with the codes,
     scale bytes, O, LSE, dq, dk, dv."""
     out = {}
+    if opts.rotate:
+        if opts.strict or opts.mixed:
+            raise ValueError("the rotation is built for the MXFP8 route")
+        # Q and K are rotated per token before quantization (Algorithm 1 step 02); the
+        # same codes serve the scores and the gradient products; the score scale takes the
+        # rotation's d / 4**k, and dQ, dK are rotated back by the same map
+        dt = np.float32 if opts.quantized else np.float64
+        d = np.asarray(q).shape[-1]
+        q, k = hadamard_rotate(q, dt), hadamard_rotate(k, dt)
+        out["q_rot"], out["k_rot"] = q, k
+        scale = (1.0 / math.sqrt(d) if scale is None else float(scale)) * 4.0 ** hadamard_norm_log2(d) / d
+        sel = dict(sel, grad_map=lambda y: hadamard_rotate(y, np.float64))
     if opts.strict and opts.mixed:
         raise ValueError("the strict options and the mixed route are separate configurations")
+    if (opts.strict or opts.mixed) and tuple(opts.window) != (-1, 0):
+        raise ValueError("the strict options and the mixed route are causal")
     if opts.quantized:
         blk = 1 if opts.strict else opts.block
         for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
@@ -746,6 +854,6 @@ def run_training_call(q, k, v, do, cu, hq: int, hkv: int, scale: Optional[float]
                                hq, hkv, scale, opts, kv_heads=sel.get("kv_heads"),
                                k_tiles=sel.get("k_tiles"), q_tiles=sel.get("bwd_q_tiles"),
                                diagnostics=sel.get("diagnostics", False), tok_scales=tok,
-                               score_ops=score_ops)
+                               score_ops=score_ops, grad_map=sel.get("grad_map"))
         out.update(g)
     return out

@@ -21,14 +21,18 @@ def cu_tensor(lengths, device="cuda"):
     return torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=device)
 
 
-def run_gpu(inputs, lengths, hq, hkv, d, total_tokens=None, with_bwd=True, scale=0.0, strict=False, mixed=False):
-    """inputs: dict of bf16 bit arrays (uint16) q, k, v[, do] of shape [T, H, d]."""
+def run_gpu(inputs, lengths, hq, hkv, d, total_tokens=None, with_bwd=True, scale=0.0, strict=False, mixed=False,
+            window=(-1, 0), rotate=False):
+    """inputs: dict of bf16 bit arrays (uint16) q, k, v[, do] of shape [T, H, d].  window:
+    (left, right) visible keys, causal when right == 0 (the oracle's convention)."""
     import torch
     import microscaled_precision_causal_gb300 as F
     T = inputs["q"].shape[0] if total_tokens is None else total_tokens
     N = len(lengths)
     cu = cu_tensor(lengths)
-    att = F.FlamiaAttention(T, N, hq, hkv, d, strict=strict, mixed=mixed)
+    causal = window[1] == 0
+    att = F.FlamiaAttention(T, N, hq, hkv, d, strict=strict, mixed=mixed, causal=causal, window=tuple(window),
+                            rotate=rotate)
     q, k, v = (to_device_bf16(inputs[n]) for n in ("q", "k", "v"))
     att.plan_build(cu)
     att.quantize(q, k, v, cu)

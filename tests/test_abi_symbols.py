@@ -55,7 +55,16 @@ def test_host_validation_without_gpu(flamia):
                             a["causal"], 0.0, ctypes.byref(a["opts"]), a["plan"], a["out"], a["lse"], None)
     assert fwd(args(d=96)) == -2                      # unsupported head dim
     assert fwd(args(hq=3)) == -2                      # hq % hkv != 0
-    assert fwd(args(causal=0)) == -2                  # non-causal: not built
+    assert fwd(args(causal=2)) == -1                  # causal is 0 or 1
+    strict_nc = F.default_options()
+    for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq"):
+        setattr(strict_nc, f, 1)
+    assert fwd(args(causal=0, opts=strict_nc)) == -2  # the strict options are causal only
+    sw = F.default_options(); sw.window_left = 64
+    for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq"):
+        setattr(sw, f, 1)
+    assert fwd(args(opts=sw)) == -2                   # ... and take no sliding window
+    assert (o.window_left, o.window_right) == (-1, -1)
     assert fwd(args(plan=0)) == -1                    # null plan
     assert fwd(args(out=258)) == -3                   # misaligned output
     bad = F.default_options(); bad.p_boost_log2 = 10
