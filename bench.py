@@ -34,10 +34,10 @@ import flamia_workloads as W  # noqa: E402
 
 METRIC = "causal packed MXFP8 attn fwd+bwd TFLOPS and % of GB300 dense FP8 peak"
 DEFAULT_WORKLOAD = "packed_16k_h16_d128"
-# kernels launched per step: plan, 3 quantize, fwd, fwd tail, dO prep, dQ boost, bwd, dQ finalise;
-# strict: the ordered dQ kernel and the zeroing of rows outside every document replace the
-# finalise; mixed: 3 more quantize launches (NVFP4 Q and K, per-token V)
-LAUNCHES_PER_STEP = {"default": 10, "strict": 11, "mixed": 13}
+# kernels launched per step: plan, Q/K/V quantize (one launch), fwd, fwd tail, dO prep, dQ boost,
+# bwd, dQ finalise; strict: the ordered dQ kernel and the zeroing of rows outside every document
+# replace the finalise; mixed: 3 more quantize launches (NVFP4 Q and K, per-token V)
+LAUNCHES_PER_STEP = {"default": 8, "strict": 9, "mixed": 11}
 L2_FLUSH_BYTES = 256 << 20
 
 

@@ -228,6 +228,16 @@ int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int hea
                                const int32_t* cu_seqlens, int num_seqs, const void* plan, int per_token,
                                void* codes_e4m3, void* scales_ue8m0, float* stats, void* stream);
 
+/* The three flamia_quantize_tokenblock calls of a training call (Q without
+ * stats, K and V with stats) in one launch.  q_bf16: [T, hq, head_dim]; k_bf16,
+ * v_bf16: [T, hkv, head_dim]; outputs as in flamia_quantize_tokenblock, with the
+ * same per_token rule for all three.  Results are those of the three separate
+ * calls. */
+int flamia_quantize_qkv(const void* q_bf16, const void* k_bf16, const void* v_bf16, int64_t total_tokens, int hq,
+                        int hkv, int head_dim, const int32_t* cu_seqlens, int num_seqs, const void* plan,
+                        int per_token, void* q_codes, void* q_scales, void* k_codes, void* k_scales, float* k_stats,
+                        void* v_codes, void* v_scales, float* v_stats, void* stream);
+
 /* ----------------------------------------------------------- rotated quantizer
  * flamia_quantize_tokenblock of x H / 2^k instead of x (Korean review section
  * 3.4: rotation, block statistics, codes and scales in one pass), for Q and K

@@ -28,7 +28,7 @@ EXPORTED = (
     "flamia_default_options", "flamia_plan_bytes", "flamia_plan_build", "flamia_quantize_tokenblock",
     "flamia_fwd", "flamia_bwd_workspace_bytes", "flamia_bwd", "flamia_get_device_status",
     "flamia_status_string", "flamia_bwd_static_scratch", "flamia_quantize_nvfp4", "flamia_plan_build_window",
-    "flamia_quantize_hadamard",
+    "flamia_quantize_hadamard", "flamia_quantize_qkv",
 )
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -88,6 +88,8 @@ def lib():
         "flamia_status_string": (ctypes.c_char_p, [i32]),
         "flamia_quantize_nvfp4": (i32, [vp, i64, i32, i32, vp, vp, vp]),
         "flamia_quantize_hadamard": (i32, [vp, i64, i32, i32, vp, i32, vp, vp, vp, vp, vp]),
+        "flamia_quantize_qkv": (i32, [vp, vp, vp, i64, i32, i32, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -153,6 +155,16 @@ def flamia_quantize_tokenblock(x, cu_seqlens, num_seqs: int, plan, codes, scales
     _check(lib().flamia_quantize_tokenblock(_ptr(x), T, H, d, _ptr(cu_seqlens), num_seqs, _ptr(plan), int(per_token),
                                             _ptr(codes), _ptr(scales), _ptr(stats), _stream(stream)),
            "flamia_quantize_tokenblock")
+
+
+def flamia_quantize_qkv(q, k, v, cu_seqlens, num_seqs: int, plan, q_codes, q_scales, k_codes, k_scales, k_stats,
+                        v_codes, v_scales, v_stats, per_token: bool = False, stream=None):
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    _check(lib().flamia_quantize_qkv(_ptr(q), _ptr(k), _ptr(v), T, hq, hkv, d, _ptr(cu_seqlens), num_seqs, _ptr(plan),
+                                     int(per_token), _ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales),
+                                     _ptr(k_stats), _ptr(v_codes), _ptr(v_scales), _ptr(v_stats), _stream(stream)),
+           "flamia_quantize_qkv")
 
 
 def flamia_quantize_hadamard(x, cu_seqlens, num_seqs: int, plan, codes, scales, stats=None, stream=None):
@@ -287,12 +299,11 @@ class FlamiaAttention:
             flamia_quantize_hadamard(q, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, None, stream)
             flamia_quantize_hadamard(k, cu_seqlens, self.N, self.plan, self.k_codes, self.k_scales, self.k_stats,
                                      stream)
-        else:
-            flamia_quantize_tokenblock(q, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, None, pt, stream)
-            flamia_quantize_tokenblock(k, cu_seqlens, self.N, self.plan, self.k_codes, self.k_scales, self.k_stats,
-                                       pt, stream)
-        flamia_quantize_tokenblock(v, cu_seqlens, self.N, self.plan, self.v_codes, self.v_scales, self.v_stats, pt,
-                                   stream)
+            flamia_quantize_tokenblock(v, cu_seqlens, self.N, self.plan, self.v_codes, self.v_scales, self.v_stats, pt,
+                                       stream)
+        else:             # Q, K and V in one launch
+            flamia_quantize_qkv(q, k, v, cu_seqlens, self.N, self.plan, self.q_codes, self.q_scales, self.k_codes,
+                                self.k_scales, self.k_stats, self.v_codes, self.v_scales, self.v_stats, pt, stream)
         if self.mixed:
             flamia_quantize_nvfp4(q, self.q4_codes, self.q4_scales, stream)
             flamia_quantize_nvfp4(k, self.k4_codes, self.k4_scales, stream)

@@ -20,6 +20,9 @@ cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, co
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, void* scales, cudaStream_t s);
 cudaError_t launch_quantize_rot(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
                                 void* codes, void* scales, float* stats, cudaStream_t s);
+cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, int T, int hq, int hkv, int D,
+                                const int32_t* cu, int N, const void* plan, int per_token, void* qc, void* qs,
+                                void* kc, void* ks, float* kst, void* vc, void* vs, float* vst, cudaStream_t s);
 cudaError_t launch_fwd_coop(int D, int mixed, const void* qc, const void* qs, const void* kc, const void* ks,
                             const void* vc, const void* vs, const void* q4c, const void* q4s, const void* k4c,
                             const void* k4s, const void* vtc, const void* vts, const int32_t* cu, int N, int T, int hq,
@@ -187,6 +190,25 @@ int flamia_quantize_tokenblock(const void* x_bf16, int64_t total_tokens, int hea
   return cuda_status(launch_quantize(x_bf16, (int)total_tokens, heads, head_dim, cu_seqlens, num_seqs, plan,
                                      per_token, codes_e4m3, scales_ue8m0, stats, nullptr, nullptr, nullptr,
                                      (cudaStream_t)stream));
+}
+
+int flamia_quantize_qkv(const void* q_bf16, const void* k_bf16, const void* v_bf16, int64_t total_tokens, int hq,
+                        int hkv, int head_dim, const int32_t* cu_seqlens, int num_seqs, const void* plan,
+                        int per_token, void* q_codes, void* q_scales, void* k_codes, void* k_scales, float* k_stats,
+                        void* v_codes, void* v_scales, float* v_stats, void* stream) {
+  int rc = check_common(total_tokens, num_seqs, cu_seqlens, plan);
+  if (!rc) rc = check_heads(hq, hkv, head_dim);
+  if (rc) return rc;
+  if (!q_bf16 || !k_bf16 || !v_bf16 || !q_codes || !q_scales || !k_codes || !k_scales || !v_codes || !v_scales)
+    return FLAMIA_ERR_INVALID_ARG;
+  auto bad8 = [](const float* p) { return p && (reinterpret_cast<uintptr_t>(p) & 7u); };
+  if (!aligned16(q_bf16) || !aligned16(k_bf16) || !aligned16(v_bf16) || !aligned16(q_codes) || !aligned16(k_codes) ||
+      !aligned16(v_codes) || bad8(k_stats) || bad8(v_stats))
+    return FLAMIA_ERR_MISALIGNED;
+  if (total_tokens == 0) return FLAMIA_OK;
+  return cuda_status(launch_quantize_qkv(q_bf16, k_bf16, v_bf16, (int)total_tokens, hq, hkv, head_dim, cu_seqlens,
+                                         num_seqs, plan, per_token, q_codes, q_scales, k_codes, k_scales, k_stats,
+                                         v_codes, v_scales, v_stats, (cudaStream_t)stream));
 }
 
 int flamia_quantize_hadamard(const void* x_bf16, int64_t total_tokens, int heads, int head_dim,

@@ -43,13 +43,26 @@ struct QShape {
   static constexpr int kMinBlocks = WITH_D || ROT ? 4 : 3;
 };
 
+// One launch quantizes up to three tensors of the same documents (Q, K and V of a
+// training call): job i owns the work units [jobs[i-1].end, jobs[i].end).
+struct QJob {
+  const __nv_bfloat16* x;     // bf16 [T, H, D]
+  uint8_t* codes;             // E4M3 [T, H, D]
+  uint8_t* scales;            // UE8M0 [T, H]
+  float2* stats;              // [T, H] row statistics, or null
+  int H;
+  int64_t end;                // one past the job's last work unit (cumulative over the jobs)
+};
+struct QJobs {
+  QJob j[3];
+};
+
 template <int D, bool PER_TOKEN, bool STATS, bool WITH_D, bool ROT = false>
 __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_D, ROT>::kMinBlocks)
-    quantize_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, const int32_t* __restrict__ cu, int N,
-                    const int* __restrict__ plan, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                    float2* __restrict__ stats, const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec,
-                    __half* __restrict__ dq_acc, const float2* __restrict__ k_stats,
-                    const float2* __restrict__ v_stats, int hkv, float* __restrict__ maxima, int64_t nwork) {
+    quantize_kernel(const QJobs jobs, int T, const int32_t* __restrict__ cu, int N, const int* __restrict__ plan,
+                    const __nv_bfloat16* __restrict__ o, float* __restrict__ dvec, __half* __restrict__ dq_acc,
+                    const float2* __restrict__ k_stats, const float2* __restrict__ v_stats, int hkv,
+                    float* __restrict__ maxima, int64_t nwork) {
   // Each lane owns 32 elements of a row as four 16-byte vectors, vector j at column
   // j * 8 kLpr + 8 (lane % kLpr): a load instruction reads kRpi rows x 16 kLpr
   // contiguous bytes, and per-row reductions take log2(kLpr) shuffle levels.
@@ -70,14 +83,17 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
   // Work unit gw = (32-row block, head); the warps walk the units with a grid stride.
   // Rows [r0, r0 + nrows); tail rows (no document) get zeros.
   struct QUnit {
-    int h, r0, nrows, doc, dq_row0;
+    int h, r0, nrows, doc, dq_row0, job;
     bool tail, skip;
     int64_t dq_tile0;     // backward prep: accumulator tile of the block's document tile
   };
   auto unit_setup = [&](int64_t gw) {
     QUnit U;
-    U.h = (int)(gw % H);
-    const int64_t unit = gw / H;
+    U.job = gw < jobs.j[0].end ? 0 : (gw < jobs.j[1].end ? 1 : 2);
+    const int64_t local = gw - (U.job ? jobs.j[U.job - 1].end : 0);
+    const int Hj = jobs.j[U.job].H;
+    U.h = (int)(local % Hj);
+    const int64_t unit = local / Hj;
     U.tail = false;
     U.skip = gw >= nwork;
     U.dq_tile0 = 0;
@@ -116,7 +132,8 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
       for (int j = 0; j < 4; ++j) {
         const int r = it * kRpi + sub;
         const bool lv = !U.skip && live_u(U, r);
-        const __nv_bfloat16* src = x + ((int64_t)(lv ? U.r0 + r : 0) * H + U.h) * D + col_of(j);
+        const QJob& J = jobs.j[U.job];
+        const __nv_bfloat16* src = J.x + ((int64_t)(lv ? U.r0 + r : 0) * J.H + U.h) * D + col_of(j);
         const uint32_t dst = smem_u32(&pf_buf[kHold ? (threadIdx.x >> 5) : 0][kHold ? it * 4 + j : 0][lane]);
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(lv ? 16 : 0) : "memory");
       }
@@ -143,6 +160,13 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
     if (!nextU.skip) prefetch(nextU);          // this lane's slots were just read
   }
   if (U.skip) continue;
+  const QJob& J = jobs.j[U.job];
+  const __nv_bfloat16* __restrict__ x = J.x;
+  uint8_t* __restrict__ codes = J.codes;
+  uint8_t* __restrict__ scales = J.scales;
+  float2* __restrict__ stats = J.stats;
+  const int H = J.H;
+  const bool with_stats = STATS && stats != nullptr;     // uniform over the warp
   const int h = U.h, r0 = U.r0, nrows = U.nrows, doc = U.doc, dq_row0 = U.dq_row0;
   const bool tail = U.tail;
   const int64_t dq_tile0 = U.dq_tile0;
@@ -276,7 +300,7 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
       }
       // statistics of the reconstructed row x^ = 2^e c and D = dO^ . O, from the codes:
       // sums over the decoded codes, scaled by 2^e (2^2e) once at the end (exact)
-      if (STATS || WITH_D) {
+      if (with_stats || WITH_D) {
         const uint4 oraw = WITH_D ? load8(o, r, j) : make_uint4(0, 0, 0, 0);
         const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oraw);
 #pragma unroll
@@ -299,7 +323,7 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
       }
     }
     float ss = 0.f, mx = 0.f, dd = 0.f;
-    if (STATS || WITH_D) {
+    if (with_stats || WITH_D) {
       ss = ss2.x + ss2.y;
       dd = dd2.x + dd2.y;
       uint32_t cmax = max(max(cmax4 & 0xFFu, (cmax4 >> 8) & 0xFFu), max((cmax4 >> 16) & 0xFFu, cmax4 >> 24));
@@ -315,7 +339,7 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
     }
     if (inrange && seg == 0) {
       const int64_t row = r0 + r;
-      if (STATS) stats[row * H + h] = make_float2(sqrtf(ss) * back, mx);
+      if (with_stats) stats[row * H + h] = make_float2(sqrtf(ss) * back, mx);
       if (WITH_D && !tail) mdo = fmaxf(mdo, sqrtf(ss) * back);
       if (WITH_D) dvec[(int64_t)h * T + row] = dd * back;
       if (PER_TOKEN) scales[row * H + h] = (uint8_t)(e + 127);
@@ -359,11 +383,14 @@ struct PrepExtra {          // backward prep only
 };
 
 template <int D, bool PT, bool ST, bool WD, bool ROT = false>
-cudaError_t launch_q(const void* x, int T, int H, const int32_t* cu, int N, const void* plan, void* codes,
-                     void* scales, float* stats, const void* o, float* dvec, void* dq_acc, const PrepExtra& px,
-                     cudaStream_t s) {
+cudaError_t launch_q_jobs(QJobs jobs, int njobs, int T, const int32_t* cu, int N, const void* plan, const void* o,
+                          float* dvec, void* dq_acc, const PrepExtra& px, cudaStream_t s) {
   const int64_t units = PT ? (T + 31) / 32 : (int64_t)T / 32 + N + 1;
-  const int64_t warps = units * H;
+  int64_t warps = 0;
+  for (int i = 0; i < 3; ++i) {
+    if (i < njobs) warps += units * jobs.j[i].H;
+    jobs.j[i].end = warps;
+  }
   constexpr int kWarps = QShape<WD, ROT>::kWarps;
   int64_t blocks = (warps + kWarps - 1) / kWarps;
   // the register-held variant walks several units per warp (its next block prefetched);
@@ -377,12 +404,30 @@ cudaError_t launch_q(const void* x, int T, int H, const int32_t* cu, int N, cons
   }
   if (blocks > 0x7FFFFFFF || blocks < 1) return cudaErrorInvalidValue;
   quantize_kernel<D, PT, ST, WD, ROT><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(x), T, H, cu, N, static_cast<const int*>(plan),
-      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), reinterpret_cast<float2*>(stats),
-      static_cast<const __nv_bfloat16*>(o), dvec, static_cast<__half*>(dq_acc),
-      reinterpret_cast<const float2*>(px.k_stats), reinterpret_cast<const float2*>(px.v_stats), px.hkv, px.maxima,
-      warps);
+      jobs, T, cu, N, static_cast<const int*>(plan), static_cast<const __nv_bfloat16*>(o), dvec,
+      static_cast<__half*>(dq_acc), reinterpret_cast<const float2*>(px.k_stats),
+      reinterpret_cast<const float2*>(px.v_stats), px.hkv, px.maxima, warps);
   return cudaGetLastError();
+}
+
+QJob make_job(const void* x, int H, void* codes, void* scales, float* stats) {
+  QJob j;
+  j.x = static_cast<const __nv_bfloat16*>(x);
+  j.codes = static_cast<uint8_t*>(codes);
+  j.scales = static_cast<uint8_t*>(scales);
+  j.stats = reinterpret_cast<float2*>(stats);
+  j.H = H;
+  j.end = 0;
+  return j;
+}
+
+template <int D, bool PT, bool ST, bool WD, bool ROT = false>
+cudaError_t launch_q(const void* x, int T, int H, const int32_t* cu, int N, const void* plan, void* codes,
+                     void* scales, float* stats, const void* o, float* dvec, void* dq_acc, const PrepExtra& px,
+                     cudaStream_t s) {
+  QJobs jobs;
+  jobs.j[0] = jobs.j[1] = jobs.j[2] = make_job(x, H, codes, scales, stats);
+  return launch_q_jobs<D, PT, ST, WD, ROT>(jobs, 1, T, cu, N, plan, o, dvec, dq_acc, px, s);
 }
 
 template <int D>
@@ -461,6 +506,23 @@ cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, voi
 // o / dvec non-null selects the backward-prep variant (stats required); with the
 // token-block rule it also zeroes dq_acc (if non-null) and folds the dQ boost
 // inputs into maxima (if non-null; k_stats / v_stats of the hkv K/V heads).
+// Q, K and V of one call in one launch (token-block or per-token rule; K and V
+// with row stats).
+cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, int T, int hq, int hkv, int D,
+                                const int32_t* cu, int N, const void* plan, int per_token, void* qc, void* qs,
+                                void* kc, void* ks, float* kst, void* vc, void* vs, float* vst, cudaStream_t s) {
+  QJobs jobs;
+  jobs.j[0] = make_job(q, hq, qc, qs, nullptr);
+  jobs.j[1] = make_job(k, hkv, kc, ks, kst);
+  jobs.j[2] = make_job(v, hkv, vc, vs, vst);
+  const PrepExtra px{nullptr, nullptr, 1, nullptr};
+  if (D == 128 && per_token) return launch_q_jobs<128, true, true, false>(jobs, 3, T, cu, N, plan, nullptr, nullptr, nullptr, px, s);
+  if (D == 128) return launch_q_jobs<128, false, true, false>(jobs, 3, T, cu, N, plan, nullptr, nullptr, nullptr, px, s);
+  if (D == 64 && per_token) return launch_q_jobs<64, true, true, false>(jobs, 3, T, cu, N, plan, nullptr, nullptr, nullptr, px, s);
+  if (D == 64) return launch_q_jobs<64, false, true, false>(jobs, 3, T, cu, N, plan, nullptr, nullptr, nullptr, px, s);
+  return cudaErrorInvalidValue;
+}
+
 // Hadamard-rotated token-block quantization of Q or K (stats optional).
 cudaError_t launch_quantize_rot(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
                                 void* codes, void* scales, float* stats, cudaStream_t s) {

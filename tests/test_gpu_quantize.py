@@ -140,3 +140,34 @@ def test_nvfp4_quantizer_bit_exact(F, dist, d):
     oc, osc = O.quantize_nvfp4(bf16_values(bits))
     assert np.array_equal(scales.cpu().numpy(), osc)
     assert np.array_equal(_unpack_e2m1(codes.cpu().numpy()), oc)
+
+
+@pytest.mark.parametrize("per_token", [False, True])
+def test_fused_qkv_launch_equals_separate_calls(F, per_token):
+    """flamia_quantize_qkv (Q, K and V in one launch) writes exactly what the three
+    flamia_quantize_tokenblock calls write, including K / V row stats, on a GQA
+    layout with tail tokens outside every document."""
+    import torch
+    lengths, hq, hkv, d = [300, 77, 129, 1], 4, 2, 128
+    T = sum(lengths) + 9
+    inp = W.make_inputs(W.custom([T], hq, hkv, d, dist="student_t3", seed=51))
+    q, k, v = (to_device_bf16(inp[n]) for n in ("q", "k", "v"))
+    cu, plan, _ = _plan(F, lengths, T)
+    u8, f32 = torch.uint8, torch.float32
+    mk = lambda H, *shape: torch.full((T, H) + shape, 0x5A, dtype=u8, device="cuda")
+    sep = dict(qc=mk(hq, d), qs=mk(hq), kc=mk(hkv, d), ks=mk(hkv), vc=mk(hkv, d), vs=mk(hkv),
+               kst=torch.full((T, hkv, 2), -1.0, dtype=f32, device="cuda"),
+               vst=torch.full((T, hkv, 2), -1.0, dtype=f32, device="cuda"))
+    fus = {n: t.clone() for n, t in sep.items()}
+    N = len(lengths)
+    F.flamia_quantize_tokenblock(q, cu, N, plan, sep["qc"], sep["qs"], None, per_token)
+    F.flamia_quantize_tokenblock(k, cu, N, plan, sep["kc"], sep["ks"], sep["kst"], per_token)
+    F.flamia_quantize_tokenblock(v, cu, N, plan, sep["vc"], sep["vs"], sep["vst"], per_token)
+    F.flamia_quantize_qkv(q, k, v, cu, N, plan, fus["qc"], fus["qs"], fus["kc"], fus["ks"], fus["kst"], fus["vc"],
+                          fus["vs"], fus["vst"], per_token)
+    torch.cuda.synchronize()
+    for n in sep:
+        assert torch.equal(sep[n], fus[n]), n
+    cuh = np.concatenate([[0], np.cumsum(lengths)])
+    oc, osb = O.quantize_tokenblock(bf16_values(inp["k"]), cuh, 1 if per_token else 32)
+    assert np.array_equal(fus["kc"].cpu().numpy(), oc) and np.array_equal(fus["ks"].cpu().numpy(), osb)
