@@ -558,7 +558,7 @@ def run_ours(args, rank, world, local_rank):
         "quantizer_roofline": ({"bound": "hbm", "achieved": qb / (q_ms * 1e-3) / 1e9, "peak": pk["hbm"],
                                 "unit": "GB/s", "frac": qb / (q_ms * 1e-3) / 1e9 / pk["hbm"],
                                 "bytes_per_step": qb, "ms": q_ms,
-                                "traffic": qrec["dram_bytes_per_launch"] * 3 if qrec else None,
+                                "traffic": qrec["dram_bytes_per_launch"] if qrec else None,
                                 "measured": "inside the CUDA graph (event-record nodes), median of replays"}
                                if ph else None),
         "e2e": {"value": world * run.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",

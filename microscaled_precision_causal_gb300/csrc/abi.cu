@@ -320,13 +320,12 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   const bool strict = is_strict(opt);
   cudaError_t e = cudaSuccess;
   if (!strict) e = cudaMemsetAsync(maxima, 0, (size_t)num_seqs * hq * 3 * 4, s);
-  // the fp16 dQ accumulator starts at zero: at head_dim 128 (head-dim-major chunks)
-  // by a memset, at 64 (query-major chunks) row by row in the dO quantizer
-  const bool acc_memset = !strict && head_dim == 128;
-  if (e == cudaSuccess && acc_memset) e = cudaMemsetAsync(dq_acc, 0, dq_acc_bytes(T, num_seqs, hq, head_dim), s);
+  // the fp16 dQ accumulator starts at zero: the dO quantizer clears, for each 32-token
+  // block, its query rows (head_dim 64, query-major chunks) or its query columns of every
+  // head-dim row (head_dim 128, head-dim-major chunks); the strict route has no accumulator
   if (e == cudaSuccess)
     e = launch_quantize(dout_bf16, T, hq, head_dim, cu_seqlens, num_seqs, plan, strict ? 1 : 0, do_codes, do_scales,
-                        do_stats, out_bf16, dvec, (strict || acc_memset) ? nullptr : dq_acc, s, k->stats, v->stats,
+                        do_stats, out_bf16, dvec, strict ? nullptr : dq_acc, s, k->stats, v->stats,
                         hkv, strict ? nullptr : maxima);
   record(ev, 1, s);
   record(ev, 2, s);

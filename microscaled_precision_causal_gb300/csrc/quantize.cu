@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
         const int64_t row = r0 + r;
         const int col = col_of(j);
         *reinterpret_cast<uint2*>(codes + (row * H + h) * D + col) = make_uint2(packed[0], packed[1]);
-        if (WITH_D && !PER_TOKEN && !tail && dq_acc)      // zero the row's slice of its accumulator chunk
+        if (WITH_D && D == 64 && !PER_TOKEN && !tail && dq_acc)      // zero the row's slice of its accumulator chunk
           *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(dq_acc + dq_chunk_elems(dq_tile0, h, col / 32, H, D)) +
                                     dq_chunk_byte(dq_row0 + r, (col % 32) * 2)) = make_uint4(0, 0, 0, 0);
       }
@@ -346,6 +346,18 @@ __global__ void __launch_bounds__(QShape<WITH_D, ROT>::kWarps * 32, QShape<WITH_
     }
   }
   if (!PER_TOKEN && lane < nrows) scales[(int64_t)(r0 + lane) * H + h] = (uint8_t)(tail ? 127 : e_block + 127);
+  if (WITH_D && D == 128 && !PER_TOKEN && !tail && dq_acc) {
+    // head-dim-major accumulator chunk of the block's tile and head: the block's 32 query
+    // columns are the same 64 bytes (four 16-byte units, permuted by d mod 8) of each of the
+    // 128 head-dim rows; the warp zeroes them with 16 stores of 16 bytes per lane
+    uint8_t* chunk = reinterpret_cast<uint8_t*>(dq_acc + dqt_chunk_elems(dq_tile0, h, H));
+    const int hf = dq_row0 >> 6, u0 = (dq_row0 & 63) >> 3;
+#pragma unroll
+    for (int k2 = 0; k2 < 16; ++k2) {
+      const int idx = k2 * 32 + lane;
+      *reinterpret_cast<uint4*>(chunk + dqt_chunk_byte(hf, idx >> 2, u0 + (idx & 3))) = make_uint4(0, 0, 0, 0);
+    }
+  }
   if (WITH_D && !PER_TOKEN && maxima && !tail) {
     // dQ boost inputs of (document, query head): max ||dO^_i||, max ||V^_j||, max |K^_jd|
     // over the block's rows, folded into the document maxima (non-negative floats
