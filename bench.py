@@ -218,6 +218,7 @@ def run_reference(args, rank, world):
 # (parity cases in the tests; here for their throughput): (workload, route).
 SECONDARY = (
     ("causal_b1_h2_s256_d64", "default"),
+    ("skewed_8192_224x256_h16_d128", "default"),
     ("gqa_b4_s8192_hq32_hkv8_d128", "default"),
     ("mixed_nvfp4_gqa_b4_s8192", "mixed"),
     ("strict_packed_4x8192_h16_t3", "strict"),

@@ -78,6 +78,11 @@ def _workloads():
     w["strict_packed_4x8192_h16_t3"] = Workload(
         "strict_packed_4x8192_h16_t3", (8192,) * 4, 16, 16, 128, dist="student_t3",
         description="4 documents of 8192, H=16, d=128, Student-t(3) inputs, strict options")
+    # the skewed packed row of the pages' training-call table: one long document and many
+    # short ones (the layout where the cost-ordered work list matters most)
+    w["skewed_8192_224x256_h16_d128"] = Workload(
+        "skewed_8192_224x256_h16_d128", (8192,) + (256,) * 224, 16, 16, 128,
+        description="packed causal MHA, one 8192-token document and 224 of 256 tokens, H=16, d=128")
     # the noncausal calls the pages time beside the causal ones (packed rows, and the
     # batched 2 x 8192 case)
     w["noncausal_packed_16k_h16_d128"] = Workload(

@@ -83,8 +83,8 @@ typedef struct flamia_options {
      With them, the dQ partials are summed in increasing key-tile order by one
      CTA per query tile (no atomics): results are bitwise reproducible and a
      later token never changes an earlier row's O, LSE or dQ.
-     Strict calls support documents of up to 16384 tokens (longer ones set
-     FLAMIA_DEV_CAPACITY and leave the outputs unspecified).
+     Documents of any length are supported (the forward reads the per-key
+     scale bytes of key tiles past its shared-memory table from global memory).
      deterministic: accepted only with the strict set (which implies it).
      mixed_nvfp4: the mixed NVFP4/FP8 route (head_dim 128 only; not with the
      strict options): scores and their backward recomputation from NVFP4 Q and

@@ -106,8 +106,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkv = ntq > 1 ? t0 + 2 : t0 + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool tab_ok = STRICT ? nkv * 32 <= L::kMaxTabTiles : nkv <= L::kMaxTabTiles;
-  const bool run = !STRICT || tab_ok;
+  // per-key scale bytes (strict) or per-tile scale words of the item's key tiles staged in
+  // shared memory: the strict table holds the first kStrictTabTiles tiles and the softmax
+  // reads later tiles' bytes from global memory
+  constexpr int kStrictTabTiles = L::kMaxTabTiles / 32;
+  const bool tab_ok = STRICT ? true : nkv <= L::kMaxTabTiles;
   constexpr int kEarly = kStages;                 // K/V tiles whose loads start in the prologue
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_full[w], 1);
     }
     fence_mbar_init();
-    if (run) {
+    {
       // the producer's first loads start before the scale table and the CTA barrier
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (STRICT && tab_ok) {
       // strict: per-token scale bytes of every key of the item, 128 K then 128 V per tile
       uint8_t* tb = reinterpret_cast<uint8_t*>(scale_tab);
-      for (int i = first; i < nkv * kTile; i += stride) {
+      for (int i = first; i < min(nkv, kStrictTabTiles) * kTile; i += stride) {
         const int uu = i >> 7, j = i & 127;
         const int kl = uu * kTile + j;
         const int64_t ktok = (int64_t)doc_start + kl;
@@ -175,8 +178,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
-  if (STRICT && !tab_ok && threadIdx.x == 0)
-    atomicOr(status, FLAMIA_DEV_CAPACITY);         // document too long for the strict per-key table
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -187,9 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
   constexpr uint32_t kAtom = 8 * D;
 
-  if (!run) {
-    // strict call on a document longer than the per-key table: nothing is computed
-  } else if (warp == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       for (int u = kEarly; u < nkv; ++u) {      // Q and the first kEarly K/V tiles: prologue
@@ -316,8 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* kf = nullptr;     // strict: per-key s_K, V exponent, 2^-eV of this tile
         if constexpr (STRICT) {
           float* buf = keyf + (u & 1) * (3 * 128);
-          const uint8_t* tb = reinterpret_cast<const uint8_t*>(scale_tab) + u * 256;
-          const int kb = tb[r], vb = tb[128 + r];
+          int kb = 127, vb = 127;
+          if (u < kStrictTabTiles) {
+            const uint8_t* tb = reinterpret_cast<const uint8_t*>(scale_tab) + u * 256;
+            kb = tb[r];
+            vb = tb[128 + r];
+          } else if (u * kTile + r < doc_len) {      // past the table: this key's bytes from global memory
+            const int64_t ktok = (int64_t)doc_start + u * kTile + r;
+            kb = __ldg(p.k_scales + ktok * p.hkv + hk);
+            vb = __ldg(p.v_scales + ktok * p.hkv + hk);
+          }
           buf[r] = ue8m0_to_f32((uint32_t)kb);
           buf[128 + r] = (float)(vb - 127);
           buf[256 + r] = ue8m0_to_f32((uint32_t)(254 - vb));

@@ -107,7 +107,7 @@ def test_documents_are_isolated_on_gpu():
     assert norm_max_err(b["dq"][s], a["dq"][s]) < 1e-2
 
 
-@pytest.mark.parametrize("wname", ["packed_16k_h16_d128", "gqa_b4_s8192_hq32_hkv8_d128"])
+@pytest.mark.parametrize("wname", ["packed_16k_h16_d128", "gqa_b4_s8192_hq32_hkv8_d128", "skewed_8192_224x256_h16_d128"])
 def test_full_size_sampled_parity(wname):
     """The full workload on the GPU in the benchmark's launch configuration; the
     oracle recomputes one document x one kv-head group on sampled tiles."""

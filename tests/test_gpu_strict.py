@@ -138,3 +138,24 @@ def test_strict_full_size_sampled_parity():
         hsel = heads if nme == "q" else [hk]
         assert np.array_equal(g[nme + "_codes"][s0:s1][:, hsel], o[nme + "_codes"]), nme
         assert np.array_equal(g[nme + "_scales"][s0:s1][:, hsel], o[nme + "_scales"]), nme
+
+
+def test_strict_forward_document_longer_than_the_scale_table():
+    """A strict call on a document of more than 128 key tiles (the forward's shared-memory
+    table of per-key scale bytes): the last query tiles read the later tiles' bytes from
+    global memory.  O and LSE of the first and last query tiles against the oracle."""
+    import oracle as O
+    L = 128 * 128 + 700
+    lengths = [200, L]
+    w = W.Workload("long_strict_document", tuple(lengths), 1, 1, 64, dist="student_t3", seed=13)
+    inp = W.make_inputs(w, tensors=("q", "k", "v"))
+    g = run_gpu(inp, lengths, 1, 1, 64, with_bwd=False, strict=True)
+    assert g["status"] == 0
+    s0 = lengths[0]
+    sub = {n: inp[n][s0:s0 + L] for n in ("q", "k", "v")}
+    nt = -(-L // 128)
+    o = run_oracle(sub, [L], 1, 1, 64, with_bwd=False, opts=O.Options(strict=True), q_tiles={0: [0, nt - 2, nt - 1]})
+    rows = np.r_[0:128, (nt - 2) * 128:L]
+    e = norm_max_err(g["o"][s0:s0 + L][rows], o["o"][rows])
+    assert e <= 1e-2, f"o: {e:.3e}"
+    assert np.max(np.abs(g["lse"][:, s0:s0 + L][:, rows] - o["lse"][:, rows])) < 1e-3
