@@ -137,6 +137,17 @@ typedef struct flamia_options {
      not rotated.  Default 0; the strict options and the mixed route do not
      take it (FLAMIA_ERR_UNSUPPORTED). */
   int rotate;
+  /* Work acquisition of flamia_fwd (FLAMIA review section 6, Algorithm 2):
+     0 (default) = static: the cost-sorted (work item, query head) units are
+     dealt to one persistent CTA per SM in boustrophedon order (step 06);
+     1 = dynamic: the grid holds a CTA per possible unit, and a running CTA,
+     right after issuing the last K/V load of a unit, cancels the launch of a
+     CTA that has not started (cluster launch control) and takes the next unit
+     of the cost-sorted list in its stead (steps 07 and 09).  Results are
+     identical either way.  Used by causal MXFP8 calls (not strict, not mixed,
+     no window); other calls take the static order.  0 or 1, else
+     FLAMIA_ERR_UNSUPPORTED. */
+  int dynamic_schedule;
 } flamia_options;
 
 /* Operands of the mixed NVFP4/FP8 route (FLAMIA review section 2, "The mixed

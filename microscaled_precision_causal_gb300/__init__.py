@@ -45,7 +45,8 @@ class Options(ctypes.Structure):
                                                                  ("debug_p_ds", ctypes.c_void_p),
                                                                  ("window_left", ctypes.c_int),
                                                                  ("window_right", ctypes.c_int),
-                                                                 ("rotate", ctypes.c_int)]
+                                                                 ("rotate", ctypes.c_int),
+                                                                 ("dynamic_schedule", ctypes.c_int)]
 
 
 class QTensor(ctypes.Structure):
@@ -232,11 +233,13 @@ class FlamiaAttention:
     torch, reused across calls: nothing is allocated per call).  causal=False
     gives attention over the whole document; window = (left, right) limits the
     visible keys to i - left <= j <= i + right (-1: no limit; causal calls use
-    right = 0)."""
+    right = 0).  dynamic_schedule=True makes the causal MXFP8 forward acquire
+    its work through cluster launch control instead of the static order (same
+    results)."""
 
     def __init__(self, total_tokens: int, num_seqs: int, hq: int, hkv: int, head_dim: int, device="cuda",
                  strict: bool = False, mixed: bool = False, causal: bool = True, window=(-1, -1),
-                 rotate: bool = False):
+                 rotate: bool = False, dynamic_schedule: bool = False):
         import torch
         self.T, self.N, self.hq, self.hkv, self.d = total_tokens, num_seqs, hq, hkv, head_dim
         self.causal = 1 if causal else 0
@@ -264,6 +267,7 @@ class FlamiaAttention:
         self.opts.window_left, self.opts.window_right = self.window
         self.rotate = bool(rotate)      # Q and K rotated by the Hadamard map before quantization
         self.opts.rotate = int(self.rotate)
+        self.opts.dynamic_schedule = int(bool(dynamic_schedule))
         self.strict = bool(strict)
         if self.strict:   # per-token operand scales, per-query-row dS exponents, causal dQ boost, deterministic dQ
             for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq", "deterministic"):

@@ -16,7 +16,7 @@ cudaError_t launch_quantize(const void* x, int T, int H, int D, const int32_t* c
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict,
-                       Window win);
+                       Window win, bool dynamic);
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t elems, void* codes, void* scales, cudaStream_t s);
 cudaError_t launch_quantize_rot(const void* x, int T, int H, int D, const int32_t* cu, int N, const void* plan,
                                 void* codes, void* scales, float* stats, cudaStream_t s);
@@ -66,6 +66,7 @@ int check_opts(const flamia_options* o) {
   const int s = o->strict_per_token + o->strict_row_ds + o->strict_causal_dq;
   if (s != 0 && s != 3) return FLAMIA_ERR_UNSUPPORTED;
   if (o->deterministic && s == 0) return FLAMIA_ERR_UNSUPPORTED;
+  if (o->dynamic_schedule != 0 && o->dynamic_schedule != 1) return FLAMIA_ERR_UNSUPPORTED;
   if (o->mixed_nvfp4) {
     if (s != 0) return FLAMIA_ERR_UNSUPPORTED;        // the strict options and the mixed route are separate
     const flamia_mixed_operands* m = o->mixed;
@@ -268,7 +269,8 @@ int flamia_fwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
   }
   return cuda_status(launch_fwd(head_dim, q->codes, q->scales, k->codes, k->scales, v->codes, v->scales, cu_seqlens,
                                 num_seqs, (int)total_tokens, hq, hkv, scale, plan, out_bf16, lse, (cudaStream_t)stream,
-                                opt ? opt->timing_events : nullptr, is_strict(opt), win));
+                                opt ? opt->timing_events : nullptr, is_strict(opt), win,
+                                opt && opt->dynamic_schedule));
 }
 
 size_t flamia_bwd_workspace_bytes(int64_t total_tokens, int num_seqs, int hq, int hkv, int head_dim) {

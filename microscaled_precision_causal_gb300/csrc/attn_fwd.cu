@@ -559,6 +559,8 @@ constexpr int kPersistRegCtl = 120;
 constexpr int kPersistRegSoftmax = 192;
 static_assert(kPersistRegCtl * 128 + kPersistRegSoftmax * 256 <= kPersistLaunchRegs * kThreads, "register split");
 
+constexpr int kClcSlots = 4;     // answers of dynamic work requests in flight or unread
+
 template <int D>
 struct PersistSmem {
   static constexpr int kTileBytes = kTile * D;
@@ -569,7 +571,8 @@ struct PersistSmem {
   static constexpr int kMaxTabTiles = 1024;                       // per key tile: K word, V word
   static constexpr int kTab = kP + 2 * kTile * kTile;             // [2 warpgroups][kMaxTabTiles]
   static constexpr int kBar = kTab + 2 * kMaxTabTiles * 8;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kClc = kBar + 256;                         // cancel answer (16 B), unit ring
+  static constexpr int kBytes = kClc + 16 + 4 * kClcSlots;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -606,12 +609,92 @@ __device__ __forceinline__ FwdUnit fwd_unit(const PlanView& pv, int i, int hq, i
   return U;
 }
 
-// Unit of round r for CTA c of G (boustrophedon).
-__device__ __forceinline__ int snake_unit(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
+
+// The CTA's sequence of units.  Static: the boustrophedon rounds over G = gridDim.x
+// persistent CTAs.  Dynamic (DYN, Algorithm 2 steps 07 and 09): the grid has a CTA
+// per possible unit, in the work list's cost order; a running CTA first takes the
+// unit of its own index, and the producer, right after issuing the last K/V load of
+// a unit, asks the hardware for the next CTA that has not started yet and takes over
+// its unit (cluster launch control).  The answer lands in a ring slot that every
+// role decodes; the MMA warp and the eight softmax warps hand the slot back.  A CTA
+// stops at the first request that cancels nothing, or cancels a CTA past the last
+// unit (those CTAs have no work; the ones never cancelled start and leave at once).
+// The CTA's sequence of units.  Static: the boustrophedon rounds over G = gridDim.x
+// persistent CTAs.  Dynamic (DYN, Algorithm 2 steps 07 and 09): the grid has a CTA
+// per possible unit.  A CTA that starts draws a ticket from the plan's counter; right
+// after issuing the last K/V load of a unit the producer asks the hardware to cancel
+// the launch of a CTA that has not started yet (cluster launch control) and, if one
+// was cancelled, draws the next ticket in its stead.  Ticket n is unit n of the
+// cost-sorted list: the hardware hands out cancelled CTAs only roughly in index
+// order (measured: up to about a wave out of place), so the tickets keep the units
+// in cost order.  Every CTA below the unit count either starts or is cancelled, and
+// each contributes a ticket, so the tickets cover every unit; each is run by the CTA
+// that drew it, and one past the last unit ends a CTA.
+// The producer puts each next unit into a ring slot; the MMA warp and the eight
+// softmax warps read it and hand the slot back.
+// A consumer warp's wait for the unit in slot (k - 1) % kClcSlots (out of line:
+// inlined into the softmax loop it raises register pressure across the whole loop).
+// Returns the unit, -1 when there is none, or -2 when the wait expired.
+__device__ __noinline__ int wait_next_unit(uint64_t* full, uint64_t* empty, const int* unit_slot, int k, bool arrive,
+                                           int* status) {
+  const int sl = (k - 1) % kClcSlots;
+  if (!__all_sync(0xffffffffu, mbar_wait(&full[sl], ((k - 1) / kClcSlots) & 1, status))) return -2;
+  const int x = unit_slot[sl];
+  __syncwarp();
+  if (arrive) mbar_arrive(&empty[sl]);
+  return x;
+}
+
+template <bool DYN>
+struct UnitSeq {
+  int c, G, n_units;
+  int first;           // dynamic: the ticket drawn at the start
+  int* unit_slot;      // [kClcSlots]
+  uint64_t* full;      // [kClcSlots] unit published
+  uint64_t* empty;     // [kClcSlots] unit read by the MMA warp and the softmax warps
+  // unit number k of this CTA (k = 0, 1, ...), or -1 when there is none (ok turns
+  // false when a wait expired).  A consumer is a whole converged warp (MMA warp: the
+  // elected lane arrives; softmax warp: lane 0) and hands the slot back; the producer
+  // (one thread) takes units 1, 2, ... from next().
+  __device__ __forceinline__ int unit(int k, bool arrive, bool& ok, int* status) const {
+    if constexpr (!DYN) {
+      const int r = k;
+      if ((int64_t)r * G >= n_units) return -1;
+      const int i = r * G + ((r & 1) ? G - 1 - c : c);
+      return i < n_units ? i : -1;
+    } else {
+      if (k == 0) return first < n_units ? first : -1;
+      const int x = wait_next_unit(full, empty, unit_slot, k, arrive, status);
+      ok = x != -2;
+      return x < 0 ? -1 : x;
+    }
+  }
+  // producer, after the last K/V load of unit k: unit k + 1, or -1
+  __device__ __forceinline__ int next(int k, uint8_t* resp, uint64_t* clc_bar, int* ticket, bool& ok,
+                                      int* status) const {
+    const int sl = k % kClcSlots;
+    if (k >= kClcSlots && !mbar_wait(&empty[sl], ((k / kClcSlots) - 1) & 1, status)) {
+      ok = false;
+      return -1;
+    }
+    fence_proxy_async_smem();        // the last answer was read before the next one lands
+    mbar_arrive_expect_tx(clc_bar, 16);
+    clc_try_cancel(resp, clc_bar);
+    if (!mbar_wait(clc_bar, k & 1, status)) {
+      ok = false;
+      return -1;
+    }
+    int x = clc_cancelled_x(resp) >= 0 ? atomicAdd(ticket, 1) : -1;
+    if (x >= n_units) x = -1;
+    unit_slot[sl] = x;
+    mbar_arrive(&full[sl]);
+    return x;
+  }
+};
 
 // WIN: a call with a window other than causal (noncausal, sliding); the causal
-// builds carry none of its code.
-template <int D, bool WIN = false>
+// builds carry none of its code.  DYN: dynamic work acquisition (UnitSeq).
+template <int D, bool WIN = false, bool DYN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -627,15 +710,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;                // [2]
   uint64_t* o_full = p_full + 2;                // [2]
   uint64_t* drain = o_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* clc_full = drain + 1;               // [kClcSlots]
+  uint64_t* clc_empty = clc_full + kClcSlots;   // [kClcSlots]
+  uint64_t* clc_bar = clc_empty + kClcSlots;    // the cancel answer landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_bar + 1);
+  int* first_slot = reinterpret_cast<int*>(tmem_slot + 1);
+  int* unit_slot = reinterpret_cast<int*>(smem + L::kClc + 16);   // [kClcSlots], after the answer
   int* status = const_cast<int*>(p.plan) + kPlanStatus;
+  int* ticket = const_cast<int*>(p.plan) + kPlanFwdTicket;
 
   const PlanView pv = plan_view(p.plan, p.T, p.N);
   const int n_units = p.plan[kPlanFwdItems] * p.hq;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int rounds = (n_units + G - 1) / G;
+  // dynamic: a CTA past the last unit leaves before any set-up without a ticket (a CTA
+  // below it contributes one ticket, drawn here or by the CTA that cancelled it, so
+  // the tickets still cover every unit)
+  if (DYN && (int)blockIdx.x >= n_units) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    if (DYN) *first_slot = atomicAdd(ticket, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
@@ -648,6 +740,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kClcSlots; ++i) {
+      mbar_init(&clc_full[i], 1);
+      mbar_init(&clc_empty[i], 9);
+    }
+    mbar_init(clc_bar, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -661,6 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  const UnitSeq<DYN> seq{(int)blockIdx.x, (int)gridDim.x, n_units, DYN ? *first_slot : 0, unit_slot, clc_full,
+                         clc_empty};
   constexpr uint32_t kSCol[2] = {0, 256};
   constexpr uint32_t kOCol[2] = {128, 384};
   constexpr uint32_t kRowBytes = D;
@@ -675,9 +774,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int qn = 0;        // units loaded so far (Q buffer qn & 1)
       int kvc = 0;       // K/V tiles loaded so far (ring stage kvc % kStages)
       bool ok = true;
-      for (int r = 0; r < rounds && ok; ++r) {
-        const int i = snake_unit(r, c, G);
-        if (i >= n_units) continue;
+      int nxt = -1;
+      for (int r = 0; ok; ++r) {
+        const int i = (DYN && r > 0) ? nxt : seq.unit(r, false, ok, status);
+        if (i < 0) break;
         const FwdUnit U = fwd_unit<WIN>(pv, i, p.hq, p.hkv, p.win);
         const int qb = qn & 1;
         if (qn >= 2 && !mbar_wait(&q_empty[qb], ((qn >> 1) - 1) & 1, status)) break;
@@ -697,6 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + L::kK + st * L::kTileBytes, &tm_k, &kv_full[st], 0, U.hk, U.doc_start + ku * kTile);
           tma_load_3d(smem + L::kV + st * L::kTileBytes, &tm_v, &kv_full[st], 0, U.hk, U.doc_start + ku * kTile);
         }
+        if (DYN && ok) nxt = seq.next(r, smem + L::kClc, clc_bar, ticket, ok, status);
       }
     }
   } else if (warp == 1) {
@@ -727,9 +828,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int qn = 0, kvc = 0;
     int pcnt0 = 0, pcnt1 = 0;   // P^ tiles handed in by each warpgroup so far
     bool ok = true;
-    for (int r = 0; r < rounds && ok; ++r) {
-      const int i = snake_unit(r, c, G);
-      if (i >= n_units) continue;
+    int i = seq.unit(0, leader, ok, status);
+    for (int r = 0; i >= 0 && ok; i = seq.unit(++r, leader, ok, status)) {
       const FwdUnit U = fwd_unit<WIN>(pv, i, p.hq, p.hkv, p.win);
       const int qb = qn & 1;
       ok = warp_wait(&q_full[qb], (qn >> 1) & 1, status) &&
@@ -799,9 +899,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
     int scnt = 0, ocnt = 0;               // S tiles and units of this warpgroup so far
     bool ok = true;
-    for (int rr = 0; rr < rounds && ok; ++rr) {
-      const int i = snake_unit(rr, c, G);
-      if (i >= n_units) continue;
+    for (int rr = 0; ok; ++rr) {
+      const int i = seq.unit(rr, lane == 0, ok, status);
+      if (i < 0) break;
       const FwdUnit U = fwd_unit<WIN>(pv, i, p.hq, p.hkv, p.win);
       if (w >= U.ntq) continue;
       const int t = U.t0 + w;
@@ -1012,6 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Rows outside every document: O = 0, LSE = +inf.
 template <int D>
 __global__ void fwd_tail_kernel(const int* plan, int T, int hq, __nv_bfloat16* out, float* lse) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) const_cast<int*>(plan)[kPlanFwdTicket] = 0;   // for the next forward
   const int valid = plan[kPlanValid];
   const int64_t n = (int64_t)(T - valid) * hq;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -1027,7 +1128,8 @@ __global__ void fwd_tail_kernel(const int* plan, int T, int hq, __nv_bfloat16* o
 template <int D, bool STRICT>
 cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                          const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
-                         const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, Window win) {
+                         const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, Window win,
+                         bool dynamic) {
   CUtensorMap tq, tk, tv;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
@@ -1058,7 +1160,8 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
     if (ev) record_timing_event(ev[0], stream);
     attn_fwd_kernel<D, STRICT><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   } else {
-    // persistent: one CTA per SM (fewer when there are fewer units than SMs)
+    // persistent, static order: one CTA per SM (fewer when there are fewer units than
+    // SMs); dynamic order (causal calls only): a CTA per possible unit
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1066,14 +1169,23 @@ cudaError_t launch_fwd_d(const void* qc, const void* qs, const void* kc, const v
     constexpr int smem = PersistSmem<D>::kAlloc;
     int regs = 0;
     const bool causal = win.left < 0 && win.right == 0;
-    e = causal ? prepare_kernel<attn_fwd_persist_kernel<D, false>>(smem, &regs)
-               : prepare_kernel<attn_fwd_persist_kernel<D, true>>(smem, &regs);
+    const bool dyn = causal && dynamic;
+    if (dyn) {
+      e = prepare_kernel<attn_fwd_persist_kernel<D, false, true>>(smem, &regs);
+    } else {
+      e = causal ? prepare_kernel<attn_fwd_persist_kernel<D, false>>(smem, &regs)
+                 : prepare_kernel<attn_fwd_persist_kernel<D, true>>(smem, &regs);
+    }
     if (e != cudaSuccess) return e;
     if (regs != kPersistLaunchRegs) return cudaErrorInvalidConfiguration;
     const unsigned pgrid = (unsigned)(grid < sms ? grid : sms);
     if (ev) record_timing_event(ev[0], stream);
-    if (causal) attn_fwd_persist_kernel<D, false><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
-    else attn_fwd_persist_kernel<D, true><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    if (dyn) {
+      attn_fwd_persist_kernel<D, false, true><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    } else {
+      if (causal) attn_fwd_persist_kernel<D, false><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
+      else attn_fwd_persist_kernel<D, true><<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    }
   }
   e = cudaGetLastError();
   if (ev) record_timing_event(ev[1], stream);
@@ -1100,8 +1212,8 @@ cudaError_t launch_fwd_tail(int D, const void* plan, int T, int hq, void* out, f
 cudaError_t launch_fwd(int D, const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                        const void* vs, const int32_t* cu, int N, int T, int hq, int hkv, float scale,
                        const void* plan, void* out, float* lse, cudaStream_t stream, void* const* ev, bool strict,
-                       Window win) {
-#define FLAMIA_FWD_ARGS qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev, win
+                       Window win, bool dynamic) {
+#define FLAMIA_FWD_ARGS qc, qs, kc, ks, vc, vs, cu, N, T, hq, hkv, scale, plan, out, lse, stream, ev, win, dynamic
   if (strict && (win.left >= 0 || win.right != 0)) return cudaErrorInvalidValue;   // the strict kernel is causal
   if (D == 128 && strict) return launch_fwd_d<128, true>(FLAMIA_FWD_ARGS);
   if (D == 128) return launch_fwd_d<128, false>(FLAMIA_FWD_ARGS);

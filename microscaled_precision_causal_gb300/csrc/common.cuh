@@ -28,6 +28,7 @@ enum PlanWord : int {
   kPlanCapacity = 8,
   kPlanWindowLeft = 9,      // the window the costs were computed for
   kPlanWindowRight = 10,
+  kPlanFwdTicket = 11,      // the forward's dynamic acquisition counter (0 between launches)
   kPlanHeaderWords = 16,
 };
 

@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     plan_words[kPlanCapacity] = cap;
     plan_words[kPlanWindowLeft] = win.left;
     plan_words[kPlanWindowRight] = win.right;
+    plan_words[kPlanFwdTicket] = 0;
   }
   if (bad || over) return;
   const unsigned long long kPad = ~0ull;

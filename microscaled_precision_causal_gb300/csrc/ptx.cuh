@@ -157,6 +157,41 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Ask the hardware to cancel the launch of a CTA of this grid that has not started
+// yet, so that the caller does its work instead.  The 16-byte answer is written to
+// `resp` (16-byte aligned shared memory) and completes 16 transaction bytes on `bar`.
+// After an answer that says "not cancelled" no further request may be made.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                   smem_u32(resp)),
+               "r"(smem_u32(bar))
+               : "memory");
+}
+// Decode an answer: the x index of the cancelled CTA, or -1 when none was cancelled
+// (every CTA of the grid has started).
+__device__ __forceinline__ int clc_cancelled_x(const void* resp) {
+  uint64_t lo, hi;
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(smem_u32(resp)) : "memory");
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "mov.b128 r, {%1, %2};\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "l"(lo), "l"(hi));
+  if (!ok) return -1;
+  uint32_t x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t"
+      "mov.b128 r, {%1, %2};\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x)
+      : "l"(lo), "l"(hi));
+  return (int)x;
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

@@ -116,3 +116,19 @@ def test_backward_diagnostic_output_limits(flamia):
     for f in ("strict_per_token", "strict_row_ds", "strict_causal_dq"):
         setattr(o, f, 1)
     assert bwd(o, 100) == -2
+
+
+def test_dynamic_schedule_option_values(flamia):
+    """The forward's work acquisition is 0 (static, the default) or 1 (cluster
+    launch control); anything else is refused before any CUDA call."""
+    L, F = flamia.lib(), flamia
+    q = F.QTensor(16, 16, None)
+
+    def fwd(o):
+        return L.flamia_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), 256, 1, 100, 4, 2, 128, 1, 0.0,
+                            ctypes.byref(o), 256, 258, 256, None)   # misaligned output: reached only if opts pass
+    o = F.default_options()
+    assert o.dynamic_schedule == 0
+    for val, want in ((0, -3), (1, -3), (2, -2), (-1, -2)):
+        o.dynamic_schedule = val
+        assert fwd(o) == want, val
