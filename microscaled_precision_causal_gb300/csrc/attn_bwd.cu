@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   uint64_t* dq_empty = s_full + 4;
   uint64_t* acc_full = s_full + 5;
   uint64_t* sf_ready = s_full + 6;            // mixed: score scale words of step 0 written
-  uint64_t* pt_full = s_full + 7;             // P^ tile and the dV scale words written
+  uint64_t* pt_full = s_full + 7;             // P^ tile and the dV scale words written (every compute thread;
+                                              // strict: warpgroup 0 after a barrier of all of them)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 8);
   int* status = const_cast<int*>(p.plan) + kPlanStatus;
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     mbar_init(dq_empty, 128 * kRO);
     mbar_init(acc_full, 1);
     mbar_init(sf_ready, 128 * kRO);
-    mbar_init(pt_full, 128);
+    mbar_init(pt_full, STRICT ? 128 : kCompute);
     fence_mbar_init();
     // the producer's first loads (K, V and the first kQStages steps' Q, dO) start
     // before the TMEM allocation and the CTA barrier
@@ -232,7 +233,10 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   // so S of the next step can be issued right after dV.
   constexpr bool kDQT = D == 128 && !STRICT;
   constexpr uint32_t kDQ = D == 128 ? kP : 320;
-  constexpr uint32_t kSFV = kS + 104;       // dV: A 4 words, B 4 words
+  // dV: A 4 words, B 4 words; default and mixed routes: in S columns only warpgroup 0
+  // reads (it writes them right after its own S load, so no barrier of all the compute
+  // warpgroups is needed before dV)
+  constexpr uint32_t kSFV = STRICT ? kS + 104 : kS;
   constexpr uint32_t kSFK = kP + 104;       // dK: A 4, B 4
   constexpr uint32_t kSFQ = D == 128 ? kP + 112 : 448;   // dQ: A 4, B 4 (d = 128: B lo 4, B hi 4)
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
@@ -509,15 +513,16 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       const float* rb = rowbuf + b * (L::kRowBuf / 4);
       const uint8_t* cs = reinterpret_cast<const uint8_t*>(rb + 256);
       // default and mixed routes: per warp, since no warpgroup needs another's data before
-      // the barrier that closes P^ (the block exponents of the last step were all read
-      // before that barrier); the strict options keep the warpgroups in step here, which
-      // measured faster for their per-key folds
+      // the barrier that closes dS^ (the block exponents of the last step were all read
+      // before every compute thread handed in that step, which the dP^T this step waits
+      // for follows); the strict options keep the warpgroups in step here, which measured
+      // faster for their per-key folds
       if constexpr (STRICT)
         ok = named_bar_and(1, kCompute, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       else
         ok = __all_sync(0xffffffffu, mbar_wait(&row_full[b], (k >> 1) & 1, status) && mbar_wait(s_full, k & 1, status));
       if (!ok) {
-        // a warp whose wait ran out still meets the barrier that closes P^ (with a false
+        // a warp whose wait ran out still meets the barrier that closes dS^ (with a false
         // vote), so that the other compute warps learn of it there and none is left waiting
         if constexpr (!STRICT) named_bar_and(1, kCompute, false);
         break;
@@ -531,6 +536,13 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         uint32_t vs[32];
         tmem_ld32(lane_base + kS + 32 * c, vs);
         tmem_ld_wait();
+        if (!STRICT && wg == 0 && cc == 0) {
+          // scale words of dV += P^^T dO into columns this warpgroup has just read: A = P^
+          // (1.0), B = dO per query chunk
+          const uint32_t bw = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
+          tmem_st4(lane_base + kSFV + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          tmem_st4(lane_base + kSFV + 4, bw, bw, bw, bw);
+        }
         const float fS = MIXED ? p.scale_log2 : p.scale_log2 * sk_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[c]));
         const float2 fS2 = make_float2(fS, fS);
         const float4* nl4 = reinterpret_cast<const float4*>(rb + 32 * c);   // -LSE * log2(e)
@@ -607,23 +619,30 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
       fence_proxy_async_smem();                // P^ (and, strict, its row exponents) published below
-      ok = named_bar_and(1, kCompute, mbar_wait(dp_full, k & 1, status));
-      if (!ok) break;
-      tc_fence_after();
-      if (wg == 0) {
-        // scale words of dV += P^^T dO (S^T has been read by every warpgroup): A = P^
-        // (1.0; strict: its per-key-row exponents), B = dO per query chunk (strict: 1.0)
-        if (STRICT) {
+      if constexpr (STRICT) {
+        ok = named_bar_and(1, kCompute, mbar_wait(dp_full, k & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        if (wg == 0) {
+          // scale words of dV += P^^T dO (S^T has been read by every warpgroup): A = P^'s
+          // per-key-row exponents, B = 1.0 (dO's per-token scales are folded into P^)
           tmem_st1(lane_base + kSFV + quarter, *reinterpret_cast<const uint32_t*>(Esm + 64 + j * 4));
           tmem_st4(lane_base + kSFV + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        } else {
-          const uint32_t bw = (uint32_t)cs[4] | (uint32_t)cs[5] << 8 | (uint32_t)cs[6] << 16 | (uint32_t)cs[7] << 24;
-          tmem_st4(lane_base + kSFV + 0, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          tmem_st4(lane_base + kSFV + 4, bw, bw, bw, bw);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(pt_full);
         }
-        tmem_st_wait();
+      } else {
+        // every compute thread hands in its part of P^ (warpgroup 0 also the scale words)
+        if (wg == 0) tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pt_full);
+        ok = __all_sync(0xffffffffu, mbar_wait(dp_full, k & 1, status));
+        if (!ok) {
+          named_bar_and(1, kCompute, false);   // meets the barrier that closes dS^ (false vote)
+          break;
+        }
+        tc_fence_after();
       }
 #pragma unroll
       for (int cc = 0; cc < kCPW; ++cc) {
@@ -661,10 +680,9 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           amax = fmax3(amax, fabsf(d1.x), fabsf(d1.y));
         }
         if constexpr (DBG) dbg_store(1, k, c, pr[cc], 1.0f);
-        if (!STRICT) {      // 32 x 32 block: the warp's 32 key rows
-#pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
-        }
+        // 32 x 32 block: the warp's 32 key rows (non-negative floats order like their bit
+        // patterns, so one warp-wide integer maximum)
+        if (!STRICT) amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
         const int e = roundup_exp(amax);
         const float sc = exp2i(-e);
         const float2 sc2 = make_float2(sc, sc);
@@ -685,7 +703,14 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         else if (lane == 0) Esm[quarter * 4 + c] = (uint8_t)(e + 127);
       }
       fence_proxy_async_smem();              // this thread's dS^ codes, for the MMAs
-      named_bar_sync(1, kCompute);           // all block exponents written; S^T and dP^T fully read
+      // all block exponents written; S^T and dP^T fully read (default and mixed routes: a
+      // vote, since a warp whose wait ran out meets this barrier with false)
+      if constexpr (STRICT) {
+        named_bar_sync(1, kCompute);
+      } else {
+        ok = named_bar_and(1, kCompute, true);
+        if (!ok) break;
+      }
       if (STRICT) {
         // A-operand scales are per key row: row j's word sits in lane j, column
         // (base + j / 32), i.e. this warp's quarter; B operands (dO, Q) are folded.
