@@ -1000,17 +1000,7 @@ __global__ void boost_from_max_kernel(const float* maxima, const int* plan, int 
                                       float* boost) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N * hq || (plan[kPlanStatus] & FLAMIA_DEV_BAD_CU_SEQLENS)) return;
-  const double M = 2.0 * (double)maxima[3 * i] * (double)maxima[3 * i + 1] * (double)maxima[3 * i + 2];
-  double cb = 1.0;
-  if (M > 0.0 && M < 1e300) {
-    const double target = ldexp(1.0, headroom);
-    int e = (int)floor(log2(target / M));
-    while (ldexp(M, e) > target) --e;
-    while (ldexp(M, e + 1) <= target) ++e;
-    e = e < -100 ? -100 : (e > 100 ? 100 : e);
-    cb = ldexp(1.0, e);
-  }
-  boost[i] = (float)cb;
+  boost[i] = dq_boost_from_maxima(maxima[3 * i], maxima[3 * i + 1], maxima[3 * i + 2], headroom);
 }
 
 // dQ = bf16(scale * acc / c), read from the accumulator chunks one (document
@@ -1138,24 +1128,46 @@ __global__ void __launch_bounds__(256) dqt_finalize_kernel(const __half* acc, co
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
   const int q = threadIdx.x & 127, half = threadIdx.x >> 7;
-  int buf = 0;
-  if ((int64_t)blockIdx.x < units) issue(blockIdx.x, 0);
-  for (int64_t un = blockIdx.x; un < units; un += gridDim.x, buf ^= 1) {
-    const bool more = un + gridDim.x < units;
-    if (more) issue(un + gridDim.x, buf ^ 1);   // that buffer was released by the barrier closing the last pass
-    if (more) asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-    const int tile = (int)(un / hq), h = (int)(un % hq);
+  // a unit's rows and scale; looked up for the next unit while its chunk is in flight
+  struct Meta {
+    int64_t row0;         // first token of the tile
+    int rows, h;
+    float mul;
+  };
+  auto meta = [&](int64_t un) {
+    Meta m;
+    const int tile = (int)(un / hq);
+    m.h = (int)(un % hq);
     const int doc = upper_doc(pv.tile_prefix, N, tile);
     const int t = tile - pv.tile_prefix[doc];
     const int s0 = cu[doc];
-    const int rows = min(kTile, cu[doc + 1] - s0 - t * kTile);
+    m.row0 = (int64_t)s0 + t * kTile;
+    m.rows = min(kTile, cu[doc + 1] - s0 - t * kTile);
+    m.mul = scale / boost[(int64_t)doc * hq + m.h];
+    return m;
+  };
+  int buf = 0;
+  Meta cur{};
+  if ((int64_t)blockIdx.x < units) {
+    issue(blockIdx.x, 0);
+    cur = meta(blockIdx.x);
+  }
+  for (int64_t un = blockIdx.x; un < units; un += gridDim.x, buf ^= 1) {
+    const bool more = un + gridDim.x < units;
+    Meta nxt{};
+    if (more) {
+      issue(un + gridDim.x, buf ^ 1);   // that buffer was released by the barrier closing the last pass
+      nxt = meta(un + gridDim.x);
+    }
+    if (more) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int rows = cur.rows, h = cur.h;
     if (q < rows) {
-      const float mul = scale / boost[(int64_t)doc * hq + h];
+      const float mul = cur.mul;
       const uint8_t* base = fsm + buf * 32768 + (q >> 6) * 16384 + (q & 7) * 2;
       const int unit = (q & 63) >> 3;
-      __nv_bfloat16* orow = dq + (((int64_t)s0 + t * kTile + q) * hq + h) * D + half * 64;
+      __nv_bfloat16* orow = dq + ((cur.row0 + q) * hq + h) * D + half * 64;
       auto val = [&](int d) {
         return __half2float(*reinterpret_cast<const __half*>(base + d * 128 + ((unit ^ (d & 7)) << 4)));
       };
@@ -1197,6 +1209,7 @@ __global__ void __launch_bounds__(256) dqt_finalize_kernel(const __half* acc, co
       }
     }
     __syncthreads();
+    cur = nxt;
   }
   constexpr int kVpr = D / 8;
   const int64_t tq = (int64_t)(T - valid) * hq * kVpr, tk = (int64_t)(T - valid) * hkv * kVpr;

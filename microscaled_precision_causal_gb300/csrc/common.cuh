@@ -148,6 +148,22 @@ __device__ __forceinline__ int upper_doc(const int* prefix, int N, int idx) {
   return lo;
 }
 
+// ---------------------------------------------------------------- dQ boost
+// dQ boost of one (document, query head) from its maxima (review section 4, "Forward
+// locality and backward locality differ"; reading C-10): c = 2^floor(log2(2^headroom /
+// M)), M = 2 max ||dO^_i|| max ||V^_j|| max |K^_jd|; 1 when M is 0 (or not finite).
+// With M = m 2^x, m in [0.5, 1) (frexp), the largest e with M 2^e <= 2^headroom is
+// headroom - x, plus one when m is exactly 1/2; e is clamped to [-100, 100].
+__device__ inline float dq_boost_from_maxima(float max_do, float max_v, float max_k, int headroom) {
+  const double M = 2.0 * (double)max_do * (double)max_v * (double)max_k;
+  if (!(M > 0.0 && M < 1e300)) return 1.0f;
+  int x;
+  const double m = frexp(M, &x);
+  int e = headroom - x + (m == 0.5 ? 1 : 0);
+  e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  return __int_as_float((e + 127) << 23);
+}
+
 // ---------------------------------------------------------------- exponent rule
 // Smallest integer e with amax <= 448 * 2^e, for a finite non-negative fp32
 // amax; 0 for amax == 0; clamped to [-127, 127].  Integer arithmetic on the

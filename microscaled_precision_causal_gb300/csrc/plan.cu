@@ -100,6 +100,8 @@ __device__ void bitonic_sort(unsigned long long* keys, int n) {  // n is a power
 }
 
 constexpr int kSmemKeys = 4096;   // sorts of up to this many keys run in shared memory
+constexpr int kMirror = 1024;     // up to this many documents, cu and the prefix arrays are read from
+                                  // shared-memory copies (each item's document is a binary search)
 
 __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restrict__ cu, int N, int T, Window win,
                                                         int* __restrict__ plan_words) {
@@ -107,6 +109,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
   __shared__ int warp_sums[32];
   __shared__ int s_bad;
   __shared__ int s_carry[3];
+  __shared__ int s_cu[kMirror + 1], s_tp[kMirror + 1], s_ip[kMirror + 1];
+  const bool mirror = N <= kMirror;
   PlanView pv = plan_view(plan_words, T, N);
   int* blk_prefix = const_cast<int*>(pv.blk_prefix);
   int* tile_prefix = const_cast<int*>(pv.tile_prefix);
@@ -126,14 +130,19 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
   for (int n = threadIdx.x; n < N; n += kThreads) {
     const int a = cu[n], b = cu[n + 1];
     if (b < a || (n == 0 && a != 0) || (n == N - 1 && b > T)) atomicOr(&s_bad, 1);
+    if (mirror) {
+      s_cu[n] = a;
+      if (n == N - 1) s_cu[N] = b;
+    }
   }
   __syncthreads();
   const int bad = s_bad;
+  const int32_t* cuv = mirror ? s_cu : cu;   // cu, from shared memory when it fits
   // 2. prefix counts (chunks of kThreads documents)
   for (int base = 0; base < N; base += kThreads) {
     const int n = base + threadIdx.x;
     int L = 0;
-    if (!bad && n < N) L = cu[n + 1] - cu[n];
+    if (!bad && n < N) L = cuv[n + 1] - cuv[n];
     const int nb = (L + kBlock - 1) / kBlock, nt = (L + kTile - 1) / kTile,
               ni = (L + kTile * kItemTiles - 1) / (kTile * kItemTiles);
     int tot;
@@ -153,6 +162,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
       blk_prefix[n] = cb + pb;
       tile_prefix[n] = ct + pt;
       item_prefix[n] = ci + pi;
+      if (mirror) {
+        s_tp[n] = ct + pt;
+        s_ip[n] = ci + pi;
+      }
     }
     __syncthreads();
   }
@@ -161,14 +174,20 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     blk_prefix[N] = nblk;
     tile_prefix[N] = ntile;
     item_prefix[N] = nitem;
+    if (mirror) {
+      s_tp[N] = ntile;
+      s_ip[N] = nitem;
+    }
   }
   __syncthreads();
+  const int* tpv = mirror ? s_tp : tile_prefix;   // the prefix arrays, from shared memory when they fit
+  const int* ipv = mirror ? s_ip : item_prefix;
   const bool over = ntile > cap || nitem > cap;
   if (threadIdx.x == 0) {
     plan_words[kPlanStatus] = (bad ? FLAMIA_DEV_BAD_CU_SEQLENS : 0) | (over ? FLAMIA_DEV_CAPACITY : 0);
     plan_words[kPlanNumSeqs] = N;
     plan_words[kPlanTotal] = T;
-    plan_words[kPlanValid] = bad ? 0 : (N > 0 ? cu[N] : 0);
+    plan_words[kPlanValid] = bad ? 0 : (N > 0 ? cuv[N] : 0);
     plan_words[kPlanBlocks] = bad ? 0 : nblk;
     plan_words[kPlanTiles] = (bad || over) ? 0 : ntile;
     plan_words[kPlanFwdItems] = (bad || over) ? 0 : nitem;
@@ -189,9 +208,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     for (int i = threadIdx.x; i < n2; i += kThreads) {
       unsigned long long key = kPad;
       if (i < nitem) {
-        const int doc = upper_doc(item_prefix, N, i);
-        const int nt = tile_prefix[doc + 1] - tile_prefix[doc];
-        const int t0 = (i - item_prefix[doc]) * kItemTiles;
+        const int doc = upper_doc(ipv, N, i);
+        const int nt = tpv[doc + 1] - tpv[doc];
+        const int t0 = (i - ipv[doc]) * kItemTiles;
         const int cnt = min(kItemTiles, nt - t0);
         int cost = 0;
         for (int t = t0; t < t0 + cnt; ++t) cost += win_khi(t, nt, win) - win_klo(t, win) + 1;
@@ -203,12 +222,12 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     bitonic_sort(keys, n2);
     for (int r = threadIdx.x; r < nitem; r += kThreads) {
       const int i = (int)(keys[r] & 0xFFFFFFFFull);
-      const int doc = upper_doc(item_prefix, N, i);
-      const int nt = tile_prefix[doc + 1] - tile_prefix[doc];
-      const int t0 = (i - item_prefix[doc]) * kItemTiles;
+      const int doc = upper_doc(ipv, N, i);
+      const int nt = tpv[doc + 1] - tpv[doc];
+      const int t0 = (i - ipv[doc]) * kItemTiles;
       const int cnt = min(kItemTiles, nt - t0);
       fwd[r] = make_int4(doc, t0, cnt, (int)(kCostMax - (unsigned)(keys[r] >> 32)));
-      fwd_span[r] = make_int2(cu[doc], cu[doc + 1] - cu[doc]);
+      fwd_span[r] = make_int2(cuv[doc], cuv[doc + 1] - cuv[doc]);
     }
     __syncthreads();
   }
@@ -219,9 +238,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     for (int i = threadIdx.x; i < n2; i += kThreads) {
       unsigned long long key = kPad;
       if (i < ntile) {
-        const int doc = upper_doc(tile_prefix, N, i);
-        const int nt = tile_prefix[doc + 1] - tile_prefix[doc];
-        const int u = i - tile_prefix[doc];
+        const int doc = upper_doc(tpv, N, i);
+        const int nt = tpv[doc + 1] - tpv[doc];
+        const int u = i - tpv[doc];
         const int cost = win_thi(u, nt, win) - win_tlo(u, win) + 1;
         key = ((unsigned long long)(kCostMax - (unsigned)cost) << 32) | (unsigned)i;
       }
@@ -231,9 +250,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     bitonic_sort(keys, n2);
     for (int r = threadIdx.x; r < ntile; r += kThreads) {
       const int i = (int)(keys[r] & 0xFFFFFFFFull);
-      const int doc = upper_doc(tile_prefix, N, i);
-      bwd[r] = make_int4(doc, i - tile_prefix[doc], (int)(kCostMax - (unsigned)(keys[r] >> 32)), 0);
-      bwd_span[r] = make_int2(cu[doc], cu[doc + 1] - cu[doc]);
+      const int doc = upper_doc(tpv, N, i);
+      bwd[r] = make_int4(doc, i - tpv[doc], (int)(kCostMax - (unsigned)(keys[r] >> 32)), 0);
+      bwd_span[r] = make_int2(cuv[doc], cuv[doc + 1] - cuv[doc]);
     }
   }
 }
