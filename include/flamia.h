@@ -13,7 +13,8 @@
  *    a cached driver entry point (and, for flamia_bwd_static_scratch, its
  *    static device scratch array and that array's per-device address).  Every call is asynchronous on `stream`
  *    (a cudaStream_t passed as void*; NULL = legacy default stream) and never
- *    synchronises the host, so calls can be captured in a CUDA graph.
+ *    synchronises the host (the plan, quantize, forward and backward calls
+ *    of a training call are replayed as a CUDA graph by the benchmark).
  *  - Packed variable-length batches: `cu_seqlens` (device, int32, num_seqs+1
  *    entries, cu[0] = 0, non-decreasing, cu[num_seqs] <= total_tokens).
  *    Document n holds tokens [cu[n], cu[n+1]).  Tokens at or after
@@ -340,8 +341,7 @@ int flamia_bwd(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qt
  * the process exits.  Problems whose flamia_bwd_workspace_bytes() exceeds it
  * are rejected with FLAMIA_ERR_WORKSPACE before anything is launched.  The
  * first call on each device resolves the array's address (cudaGetSymbolAddress,
- * with that device current) and caches it: make that first call before any
- * stream capture.  The cached address is only valid for the device's current
+ * with that device current) and caches it.  The cached address is only valid for the device's current
  * context: after cudaDeviceReset on that device do not call this function
  * again in the same process.  The call allocates nothing.  All calls share the array:
  * calls whose GPU work overlaps race and give wrong results; the fp16 dQ

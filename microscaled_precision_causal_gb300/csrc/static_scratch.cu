@@ -11,8 +11,7 @@
 // exits.
 //
 // Set-up: the first call on each device (with that device current) resolves
-// the array's device address with cudaGetSymbolAddress and caches it; make
-// that first call before any stream capture.  The cached address belongs to
+// the array's device address with cudaGetSymbolAddress and caches it.  The cached address belongs to
 // the device's current context: after cudaDeviceReset (or anything else that
 // destroys and re-creates the primary context) the array may move, so a
 // process that resets a device must not call this entry point on it again.  The call itself allocates
