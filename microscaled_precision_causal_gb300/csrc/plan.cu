@@ -55,24 +55,29 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 // through shared memory.  Ascending.
 __device__ void bitonic_sort_regs(unsigned long long* keys, int n) {
   const int i = threadIdx.x;
-  unsigned long long a = i < n ? keys[i] : ~0ull;
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      unsigned long long b;
-      if (j >= 32) {
-        __syncthreads();                       // every read of the previous round done
-        if (i < n) keys[i] = a;
-        __syncthreads();
-        b = i < n ? keys[i ^ j] : a;
-      } else {
-        b = __shfl_xor_sync(0xffffffffu, a, j);
+  // only the warps that hold keys sort (their rounds meet on named barrier 1, counted in
+  // whole warps); the others wait at the block barrier at the end
+  const int nlive = (n + 31) & ~31;
+  if (i < nlive) {
+    unsigned long long a = i < n ? keys[i] : ~0ull;
+    for (int k = 2; k <= n; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        unsigned long long b;
+        if (j >= 32) {
+          asm volatile("bar.sync 1, %0;" ::"r"(nlive) : "memory");   // every read of the previous round done
+          keys[i] = a;
+          asm volatile("bar.sync 1, %0;" ::"r"(nlive) : "memory");
+          b = keys[i ^ j];
+        } else {
+          b = __shfl_xor_sync(0xffffffffu, a, j);
+        }
+        const bool up = (i & k) == 0, lower = (i & j) == 0;
+        a = (lower == up) ? (a < b ? a : b) : (a < b ? b : a);
       }
-      const bool up = (i & k) == 0, lower = (i & j) == 0;
-      a = (lower == up) ? (a < b ? a : b) : (a < b ? b : a);
     }
+    asm volatile("bar.sync 1, %0;" ::"r"(nlive) : "memory");
+    if (i < n) keys[i] = a;
   }
-  __syncthreads();
-  if (i < n) keys[i] = a;
   __syncthreads();
 }
 
