@@ -899,6 +899,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
     int scnt = 0, ocnt = 0;               // S tiles and units of this warpgroup so far
     bool ok = true;
+    // static order: the Q scale byte of this thread's row and its two first K/V table
+    // entries (units of up to 64 key tiles) of the warpgroup's next unit, loaded before
+    // this unit's epilogue so that their latency overlaps it
+    uint32_t pre_kv = 0, pre_q = 0;
+    int pre_unit = -1;
     for (int rr = 0; ok; ++rr) {
       const int i = seq.unit(rr, lane == 0, ok, status);
       if (i < 0) break;
@@ -908,7 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qrow_local = t * kTile + r;
       const bool row_valid = qrow_local < U.doc_len;
       const int64_t tok = (int64_t)U.doc_start + qrow_local;
-      const float fq = p.scale_log2 * scale_of(p.q_scales, tok, p.hq, U.h, row_valid);
+      const bool pre = !DYN && pre_unit == i;
+      const float fq = p.scale_log2 * (pre ? (row_valid ? ue8m0_to_f32(pre_q) : 1.0f)
+                                           : scale_of(p.q_scales, tok, p.hq, U.h, row_valid));
       const int nk = U.nk(w), klo = U.klo(w);
       // K and V block-scale bytes of every key tile of the unit (one per 32-key group,
       // 127 past the document end), staged in this warpgroup's own table (tiles past
@@ -925,11 +932,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         kb = kv ? __ldg(p.k_scales + ktok * p.hkv + U.hk) : 127u;
         vb = kv ? __ldg(p.v_scales + ktok * p.hkv + U.hk) : 127u;
       };
-      for (int e = r; e < ntab * 4; e += 128) {
-        uint32_t kb, vb;
-        scale_bytes(klo + (e >> 2), e & 3, kb, vb);
-        tb[(e >> 2) * 8 + (e & 3)] = (uint8_t)kb;
-        tb[(e >> 2) * 8 + 4 + (e & 3)] = (uint8_t)vb;
+      if (pre && ntab * 4 <= 256) {
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int e = r + 128 * q2;
+          if (e < ntab * 4) {
+            tb[(e >> 2) * 8 + (e & 3)] = (uint8_t)(pre_kv >> (16 * q2));
+            tb[(e >> 2) * 8 + 4 + (e & 3)] = (uint8_t)(pre_kv >> (16 * q2 + 8));
+          }
+        }
+      } else {
+        for (int e = r; e < ntab * 4; e += 128) {
+          uint32_t kb, vb;
+          scale_bytes(klo + (e >> 2), e & 3, kb, vb);
+          tb[(e >> 2) * 8 + (e & 3)] = (uint8_t)kb;
+          tb[(e >> 2) * 8 + 4 + (e & 3)] = (uint8_t)vb;
+        }
       }
       named_bar_sync(2 + w, 128);
       float m = -INFINITY, lsum = 0.f;
@@ -1063,6 +1081,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[w]);
+      }
+      if constexpr (!DYN) {
+        // the next unit of this warpgroup in the static order (if it takes part in it)
+        pre_unit = -1;
+        bool tmp_ok = true;
+        const int i2 = seq.unit(rr + 1, false, tmp_ok, status);
+        if (i2 >= 0) {
+          const FwdUnit U2 = fwd_unit<WIN>(pv, i2, p.hq, p.hkv, p.win);
+          if (w < U2.ntq) {
+            pre_unit = i2;
+            const int q2l = (U2.t0 + w) * kTile + r;
+            const bool v2 = q2l < U2.doc_len;
+            pre_q = v2 ? __ldg(p.q_scales + ((int64_t)U2.doc_start + q2l) * p.hq + U2.h) : 127u;
+            pre_kv = 0;
+            const int ntab2 = min(U2.nk(w), L::kMaxTabTiles), klo2 = U2.klo(w);
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const int e = r + 128 * q2;
+              if (e < ntab2 * 4) {
+                const int kl = (klo2 + (e >> 2)) * kTile + (e & 3) * 32;
+                const bool kv = kl < U2.doc_len;
+                const int64_t ktok = (int64_t)U2.doc_start + kl;
+                const uint32_t kb = kv ? __ldg(p.k_scales + ktok * p.hkv + U2.hk) : 127u;
+                const uint32_t vb = kv ? __ldg(p.v_scales + ktok * p.hkv + U2.hk) : 127u;
+                pre_kv |= (kb | vb << 8) << (16 * q2);
+              }
+            }
+          }
+        }
       }
       // warpgroup-wide, so that the four warps leave together on a timeout
       ok = named_bar_and(2 + w, 128, ok && mbar_wait(&o_full[w], ocnt & 1, status));
