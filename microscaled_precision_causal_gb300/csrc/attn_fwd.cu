@@ -992,10 +992,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mx = -INFINITY;
         if (!diag) {
           float cm[4];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t v[32];
-            tmem_ld32_max(s_addr + 32 * g, v, cm[g]);
+          {                                     // the four loads in flight together (values unused)
+            uint32_t v0[32], v1[32], v2[32], v3[32];
+            tmem_ld32_max(s_addr, v0, cm[0]);
+            tmem_ld32_max(s_addr + 32, v1, cm[1]);
+            tmem_ld32_max(s_addr + 64, v2, cm[2]);
+            tmem_ld32_max(s_addr + 96, v3, cm[3]);
             tmem_ld_wait();
           }
 #pragma unroll
