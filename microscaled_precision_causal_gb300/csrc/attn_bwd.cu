@@ -1289,17 +1289,24 @@ __global__ void bwd_tail_kernel(const int* plan, int T, int hq, int hkv, __nv_bf
 
 // Deterministic dQ (strict options): one CTA per (forward work item, query head)
 // processes the item's query tiles one after another; for each, the visible key
-// tiles in increasing order.  Thread = query row.  Per key tile: S = Q K^T and
+// tiles in increasing order.  Two compute warpgroups share each (query tile, key
+// tile) pair: warpgroup g takes key columns [64 g, 64 g + 64) of S and dP and the
+// head-dim columns [D/2 g, D/2 (g + 1)) of the dQ accumulator.  Thread = query row
+// of its warpgroup.  Per key tile: S = Q K^T and
 // dP = dO V^T (unscaled E4M3 MMAs), P = 2^(x - LSE log2 e), dS = P o (dP - D),
 // the K fold dS'' = dS s_K(j) quantized with one round-up exponent per (query
 // row, 32-key block) (the strict per-row dS exponent), dQ partial = dS'' K^ codes
 // (MXF8 MMA), then acc = fp16(acc + fp16(c_i * partial)) in registers in the
 // fixed key-tile order; finally dQ = bf16(scale * acc / c_i).
-// Roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
-// allocator, warp 3 per-key factors (s_K, s_V) into SMEM, warps 4-7 compute.
-// TMEM: S [0,128), dP [128,256) (its last 8 columns carry the dQ MMA's scale
-// words once dP was read), dQ partial [256, 256 + D).
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
+// allocator, warp 3 per-key factors (s_K, s_V) into SMEM, warps 4-11 compute.
+// TMEM: S [0,128), dP [128,256), dQ partial [256, 256 + D).  The dQ MMA's four
+// instructions (one per 32-key block) take their A scale words from separate
+// columns, written by the warpgroup that owns the block into the dP columns it has
+// itself read (warpgroup 0: dP columns 0-7 and the B words in 8-11; warpgroup 1:
+// 64-71).
 constexpr int kDqStages = 2;
+constexpr int kDqThreads = 384;
 
 struct DqParams {
   const uint8_t* q_scales;
@@ -1332,7 +1339,7 @@ struct DqSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const DqParams p) {
@@ -1380,12 +1387,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kd_full[i], 32);
-      mbar_init(&kd_empty[i], 128);
+      mbar_init(&kd_empty[i], 256);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, 256);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -1397,7 +1404,9 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   constexpr uint32_t kS = 0, kP = 128, kDQ = 256;
-  constexpr uint32_t kSF = kP + 120;
+  // scale words of the dQ MMA: A of key block s (byte s, replicated), B (1.0)
+  auto a_sf = [](int s) -> uint32_t { return kP + 64 * (s >> 1) + 4 * (s & 1); };
+  constexpr uint32_t kSFB = kP + 8;
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
   constexpr uint32_t kAtom = 8 * D;
   float* kdbuf = reinterpret_cast<float*>(smem + L::kKD);
@@ -1453,7 +1462,7 @@ __global__ void __launch_bounds__(256, 1)
           // dQ partial = dS'' K (A: queries x keys, K-major; B: K keys x d, MN-major)
           mma_mxf8(tbase + kDQ, smem_desc(sds + 32 * s, 16, 1024, kSwizzle128B),
                    smem_desc(ka + s * 32 * D, kAtom, kAtom, kLayout), idesc_mxf8(128, D, 0, 1, s, s),
-                   tbase + kSF, tbase + kSF + 4, s > 0);
+                   tbase + a_sf(s), tbase + kSFB, s > 0);
         }
         mma_commit(dq_full);
         mma_commit(&kv_empty[st]);
@@ -1484,12 +1493,14 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive(&kd_full[b]);
     }
   } else if (warp >= 4) {
+    const int g = (warp - 4) >> 2;                   // warpgroup: key columns [64 g, 64 g + 64), dQ half g
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;               // query row within the tile (TMEM lane)
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     uint8_t* sDS = smem + L::kDS;
+    constexpr int kHalf = D / 2;                      // head-dim columns of this warpgroup's dQ half
     bool ok = true;
-    __half2 acc[D / 2];
+    __half2 acc[kHalf / 2];
     float nl = 0.f, nd = 0.f, fq = 0.f, sdo = 0.f, cb = 1.f;
     bool qv = false;
     int64_t qtok = 0;
@@ -1507,60 +1518,64 @@ __global__ void __launch_bounds__(256, 1)
         sdo = qv ? ue8m0_to_f32(p.do_scales[qtok * p.hq + h]) : 0.f;
         cb = qv ? p.cvec[(int64_t)h * p.T + qtok] : 1.f;
 #pragma unroll
-        for (int c = 0; c < D / 2; ++c) acc[c] = __floats2half2_rn(0.f, 0.f);
+        for (int c = 0; c < kHalf / 2; ++c) acc[c] = __floats2half2_rn(0.f, 0.f);
       }
       const bool diag = (u == t);
       const int b = k & 1;
       const float* kd = kdbuf + b * 256;
-      ok = named_bar_and(1, 128, mbar_wait(s_full, k & 1, status) && mbar_wait(&kd_full[b], (k >> 1) & 1, status));
+      ok = named_bar_and(1, 256, mbar_wait(s_full, k & 1, status) && mbar_wait(&kd_full[b], (k >> 1) & 1, status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sfa = 0;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t vs[32], vp[32];
-        tmem_ld32(lane_base + kS + 32 * c, vs);
-        tmem_ld32(lane_base + kP + 32 * c, vp);
-        tmem_ld_wait();
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * g + cc;                     // 32-key block
         float ds[32];
         float amax = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * c + jj;
-          const float sk = kd[j];
-          const float x = __uint_as_float(vs[jj]) * (fq * sk) + nl;
-          const bool vis = !diag || j <= i;
-          const float pr = vis ? fast_exp2(x) : 0.f;
-          const float dp = __uint_as_float(vp[jj]) * (sdo * kd[128 + j]) + nd;
-          const float v = pr * dp * sk;                // K fold
-          ds[jj] = v;
-          amax = fmaxf(amax, fabsf(v));
+        for (int hf = 0; hf < 2; ++hf) {              // S and dP in 16-column halves
+          uint32_t vs[16], vp[16];
+          tmem_ld16(lane_base + kS + 32 * c + 16 * hf, vs);
+          tmem_ld16(lane_base + kP + 32 * c + 16 * hf, vp);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jh = 0; jh < 16; ++jh) {
+            const int jj = 16 * hf + jh;
+            const int j = 32 * c + jj;
+            const float sk = kd[j];
+            const float x = __uint_as_float(vs[jh]) * (fq * sk) + nl;
+            const bool vis = !diag || j <= i;
+            const float pr = vis ? fast_exp2(x) : 0.f;
+            const float dp = __uint_as_float(vp[jh]) * (sdo * kd[128 + j]) + nd;
+            const float v = pr * dp * sk;              // K fold
+            ds[jj] = v;
+            amax = fmaxf(amax, fabsf(v));
+          }
         }
         const int e = roundup_exp(amax);
         const float sc = exp2i(-e);
-        sfa |= (uint32_t)(e + 127) << (8 * c);
         uint32_t pk[8];
 #pragma unroll
         for (int jj = 0; jj < 32; jj += 4)
           pk[jj >> 2] = (uint32_t)e4m3x2(ds[jj] * sc, ds[jj + 1] * sc) | ((uint32_t)e4m3x2(ds[jj + 2] * sc, ds[jj + 3] * sc) << 16);
         *reinterpret_cast<uint4*>(sDS + swz_offset(i, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(sDS + swz_offset(i, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        // A scale of row i for key block c: lane i, column (a_sf(c) + i / 32), the
+        // exponent in every byte (the instruction reads byte c)
+        tmem_st1(lane_base + a_sf(c) + quarter, (uint32_t)(e + 127) * 0x01010101u);
       }
-      // A scale of row i: lane i, column (base + i / 32); B (K codes) carries no scale
-      tmem_st1(lane_base + kSF + quarter, sfa);
-      tmem_st4(lane_base + kSF + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      if (g == 0) tmem_st4(lane_base + kSFB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);   // B: K codes, 1.0
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&kd_empty[b]);
       mbar_arrive(p_full);
-      ok = named_bar_and(1, 128, mbar_wait(dq_full, k & 1, status));
+      ok = named_bar_and(1, 256, mbar_wait(dq_full, k & 1, status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_base + kDQ + 32 * c, v);
+        tmem_ld32(lane_base + kDQ + kHalf * g + 32 * c, v);
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -1572,9 +1587,9 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive(dq_empty);
       if (u == t && qv) {          // last key tile of this query tile: dQ = bf16(scale * acc / c_i)
         const float mul = p.scale / cb;
-        __nv_bfloat16* orow = p.dq + (qtok * p.hq + h) * D;
+        __nv_bfloat16* orow = p.dq + (qtok * p.hq + h) * D + kHalf * g;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
+        for (int c = 0; c < kHalf / 8; ++c) {
           uint32_t o[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -1692,7 +1707,7 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
     if (e != cudaSuccess) return e;
     const int64_t dgrid = ((int64_t)T / (kTile * kItemTiles) + N + 1) * hq;
     if (dgrid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    attn_dq_kernel<D><<<(unsigned)dgrid, 256, dsmem, stream>>>(tq, tk, tv, tdo, dp);
+    attn_dq_kernel<D><<<(unsigned)dgrid, kDqThreads, dsmem, stream>>>(tq, tk, tv, tdo, dp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_tail_kernel<D><<<152, 256, 0, stream>>>(p.plan, T, hq, hkv, static_cast<__nv_bfloat16*>(dq), p.dk, p.dv);
