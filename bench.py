@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--mode", default="default", choices=["default", "strict", "mixed"],
                     help="strict options or the mixed NVFP4/FP8 route (head_dim 128)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -407,18 +407,23 @@ class WorkloadRun:
         t1 = time.time()
         ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
         assert self.att.device_status() == 0, "device status error during the timed steps"
-        per_round = [float(c.mean()) for c in np.array_split(ms, max(1, rounds))]
+        per_round = [float(c.mean()) for c in np.array_split(ms, max(1, min(rounds, len(ms))))]
         return dict(mean=float(ms.mean()), median_of_rounds=float(np.median(per_round)), rounds=per_round,
                     t_wall=(t0, t1))
 
-    def e2e(self, steps):
-        """The training call through the public API with host buffers: pinned inputs in and
-        results out inside the timed region.  The copies run on a second stream: dO comes
-        in while the forward runs and O goes out while the backward runs (Q, K, V and
-        cu_seqlens before the forward, dQ, dK, dV after the backward)."""
+    def _out_host(self):
+        att = self.att
+        return {n: self.torch.empty_like(t, device="cpu").pin_memory() for n, t in
+                (("o", att.out), ("dq", att.dq), ("dk", att.dk), ("dv", att.dv))}
+
+    def e2e_serial(self, steps):
+        """The training call through the public API with host buffers, one step at a time:
+        pinned inputs in and results out inside each step's events.  The copies run on a
+        second stream: dO comes in while the forward runs and O goes out while the
+        backward runs (Q, K, V and cu_seqlens before the forward, dQ, dK, dV after the
+        backward).  Returns the median ms per step and the bytes each way."""
         torch, att, x, host, stream = self.torch, self.att, self.x, self.host, self.stream
-        out_host = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in
-                    (("o", att.out), ("dq", att.dq), ("dk", att.dk), ("dv", att.dv))}
+        out_host = self._out_host()
         h2d = sum(t.numel() * t.element_size() for t in host.values()) + self.cu_host.numel() * 4
         d2h = sum(t.numel() * t.element_size() for t in out_host.values())
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -456,7 +461,113 @@ class WorkloadRun:
             e1.synchronize()
             if i > 0:
                 res.append(e0.elapsed_time(e1))
+        assert att.device_status() == 0, "device status error during the end-to-end steps"
         return float(np.median(res)), h2d, d2h
+
+    def e2e_pipelined(self, steps, rounds=3):
+        """The same steps as a training loop runs them: the inputs of step i + 1 (Q, K, V,
+        dO, cu_seqlens; two device buffer sets) are copied in on one stream while step i
+        computes and its results (O after the forward, dQ, dK, dV after the backward) are
+        copied out on another, so the two link directions overlap.  Every step's copies
+        are inside the timed region: ms per step = (the whole run of `steps` steps,
+        pipeline fill and drain included) / steps, median of `rounds` runs.  The inputs
+        (268 MB at the headline size) are larger than L2, so there is no flush."""
+        torch, att, host, stream = self.torch, self.att, self.host, self.stream
+        xs = [(self.x, self.cu), ({n: torch.empty_like(t) for n, t in self.x.items()}, torch.empty_like(self.cu))]
+        out_host = self._out_host()
+        cin, cout = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_used = [torch.cuda.Event() for _ in range(2)]
+        ev_fwd, ev_bwd, ev_o, ev_out = (torch.cuda.Event() for _ in range(4))
+
+        def copy_in(i):
+            b = i % 2
+            x, cu = xs[b]
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(ev_used[b])        # step i - 2 is done with this buffer set
+                cu.copy_(self.cu_host, non_blocking=True)
+                for n in ("q", "k", "v", "do"):
+                    x[n].copy_(host[n], non_blocking=True)
+                ev_in[b].record(cin)
+
+        res = []
+        for _ in range(rounds):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            cin.wait_event(e0)
+            cout.wait_event(e0)
+            copy_in(0)
+            for i in range(steps):
+                x, cu = xs[i % 2]
+                if i + 1 < steps:
+                    copy_in(i + 1)
+                stream.wait_event(ev_in[i % 2])
+                if i > 0:
+                    stream.wait_event(ev_o)            # O of step i - 1 has been read
+                att.plan_build(cu)
+                att.quantize(x["q"], x["k"], x["v"], cu)
+                att.forward(cu)
+                ev_fwd.record(stream)
+                if i > 0:
+                    stream.wait_event(ev_out)          # dQ, dK, dV of step i - 1 have been read
+                att.backward(x["do"], cu)
+                ev_used[i % 2].record(stream)
+                ev_bwd.record(stream)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_fwd)
+                    out_host["o"].copy_(att.out, non_blocking=True)
+                    ev_o.record(cout)
+                    cout.wait_event(ev_bwd)
+                    for n in ("dq", "dk", "dv"):
+                        out_host[n].copy_(getattr(att, n), non_blocking=True)
+                    ev_out.record(cout)
+            stream.wait_event(ev_out)
+            e1.record(stream)
+            e1.synchronize()
+            res.append(e0.elapsed_time(e1) / steps)
+        assert att.device_status() == 0, "device status error during the end-to-end steps"
+        del xs[1]
+        torch.cuda.empty_cache()
+        return float(np.median(res)), res
+
+    def link_bandwidth(self, h2d_bytes, d2h_bytes):
+        """Pinned host <-> device copy rates of this machine for the step's byte counts: each
+        direction alone and both at once (one stream each), best of 3, CUDA events."""
+        torch, dev = self.torch, self.dev
+        hi = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+        di = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+        ho = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+        do_ = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+        s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def best(which):
+            t = float("inf")
+            for _ in range(4):
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                cur = torch.cuda.current_stream(dev)
+                e0.record(cur)
+                for st, dst, src, on in ((s1, di, hi, "in"), (s2, ho, do_, "out")):
+                    if on in which:
+                        st.wait_event(e0)
+                        with torch.cuda.stream(st):
+                            dst.copy_(src, non_blocking=True)
+                        ev = torch.cuda.Event()
+                        ev.record(st)
+                        cur.wait_event(ev)
+                e1.record(cur)
+                e1.synchronize()
+                t = min(t, e0.elapsed_time(e1))
+            return t
+
+        t_in, t_out, t_both = best(("in",)), best(("out",)), best(("in", "out"))
+        del hi, di, ho, do_
+        torch.cuda.empty_cache()
+        return {"h2d_gbs": h2d_bytes / (t_in * 1e-3) / 1e9, "d2h_gbs": d2h_bytes / (t_out * 1e-3) / 1e9,
+                "both_directions_gbs": (h2d_bytes + d2h_bytes) / (t_both * 1e-3) / 1e9,
+                "both_directions_ms": t_both}
 
     def kernel_roofline(self, ph, fp8_peak):
         d, hq = self.w.d, self.w.hq
@@ -524,12 +635,14 @@ def run_ours(args, rank, world, local_rank):
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
-    e2e_ms, h2d, d2h = run.e2e(args.e2e_steps)
+    e2e_serial_ms, h2d, d2h = run.e2e_serial(5)
+    e2e_ms, e2e_rounds = run.e2e_pipelined(args.e2e_steps)
+    link = run.link_bandwidth(h2d, d2h)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
+        t = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        e2e_ms, e2e_serial_ms = (float(v) for v in t.tolist())
     lines = sampler.stop() if not args.no_clocks else None
     clocks = ClockSampler.summarize(lines, *tm["t_wall"]) if lines else None
     if rank != 0:
@@ -564,8 +677,17 @@ def run_ours(args, rank, world, local_rank):
                                if ph else None),
         "e2e": {"value": world * run.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "copies": "pinned host buffers; a second stream brings dO in during the forward and takes O out "
-                          "during the backward"},
+                "rounds_ms": e2e_rounds,
+                "copies": ("pinned host buffers, %d steps as a training loop runs them: step i + 1's inputs come in "
+                           "on one stream while step i computes and its results go out on another (two device "
+                           "input sets); ms_per_step = whole run / steps, fill and drain included, median of 3 "
+                           "runs; inputs > L2, no flush" % args.e2e_steps),
+                "serial": {"value": world * run.flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms,
+                           "copies": "one step at a time: Q, K, V in, then the call (dO in during the forward, "
+                                     "O out during the backward), then dQ, dK, dV out"},
+                "link": dict(link, floor_ms_per_step=link["both_directions_ms"],
+                             note="pinned copies of the step's bytes, each direction alone and both at once; "
+                                  "the pipelined loop cannot beat both_directions_ms per step")},
         "gpu_launches": LAUNCHES_PER_STEP[args.mode] * args.steps,
         "clocks": clocks,
     }
