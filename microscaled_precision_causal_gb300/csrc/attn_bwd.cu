@@ -237,6 +237,11 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
   // reads (it writes them right after its own S load, so no barrier of all the compute
   // warpgroups is needed before dV)
   constexpr uint32_t kSFV = STRICT ? kS + 104 : kS;
+  // P^ as dV's A operand: default and mixed routes in TMEM, 8 columns per 32-query chunk c at
+  // kPtCol + 32 c, inside the S^T columns that chunk's warpgroup has itself just read (the
+  // next step's S^T, issued after dV, overwrites them); the strict route stages it in SMEM
+  constexpr bool kPtT = !STRICT;
+  constexpr uint32_t kPtCol = kS + 16;
   constexpr uint32_t kSFK = kP + 104;       // dK: A 4, B 4
   constexpr uint32_t kSFQ = D == 128 ? kP + 112 : 448;   // dQ: A 4, B 4 (d = 128: B lo 4, B hi 4)
   constexpr uint32_t kLayout = D == 128 ? kSwizzle128B : kSwizzle64B;
@@ -350,8 +355,14 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
 #pragma unroll
           for (int s = 0; s < 4; ++s)
             // dV += P^^T dO (A: keys x queries K-major; B: dO queries x d, MN-major)
-            if (leader) mma_mxf8(tbase + kDV, pt_kmaj(32 * s), do_mn(st * L::kTileBytes + s * 32 * D), idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFV,
-                     tbase + kSFV + 4, (k > 0 || s > 0));
+            if (leader) {
+              if constexpr (kPtT)
+                mma_mxf8_ta(tbase + kDV, tbase + kPtCol + 32 * s, do_mn(st * L::kTileBytes + s * 32 * D),
+                            idesc_mxf8(128, D, 0, 1, s, s), tbase + kSFV, tbase + kSFV + 4, (k > 0 || s > 0));
+              else
+                mma_mxf8(tbase + kDV, pt_kmaj(32 * s), do_mn(st * L::kTileBytes + s * 32 * D), idesc_mxf8(128, D, 0, 1, s, s),
+                         tbase + kSFV, tbase + kSFV + 4, (k > 0 || s > 0));
+            }
         }
         if (!MIXED && more) {
           ok = warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
@@ -615,10 +626,14 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
             pk[i >> 2] = (uint32_t)e4m3x2(pf[i] * sc, pf[i + 1] * sc) | ((uint32_t)e4m3x2(pf[i + 2] * sc, pf[i + 3] * sc) << 16);
           Esm[64 + j * 4 + c] = (uint8_t)(ev + 127);
         }
-        *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        if constexpr (kPtT) {
+          tmem_st8(lane_base + kPtCol + 32 * c, pk);    // key row j of chunk c: 32 codes, query order
+        } else {
+          *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(sPt + swz_offset(j, 32 * c + 16, 128)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
       }
-      fence_proxy_async_smem();                // P^ (and, strict, its row exponents) published below
+      if constexpr (!kPtT) fence_proxy_async_smem();   // P^ and its row exponents, published below
       if constexpr (STRICT) {
         ok = named_bar_and(1, kCompute, mbar_wait(dp_full, k & 1, status));
         if (!ok) break;
@@ -634,7 +649,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         }
       } else {
         // every compute thread hands in its part of P^ (warpgroup 0 also the scale words)
-        if (wg == 0) tmem_st_wait();
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pt_full);
         ok = __all_sync(0xffffffffu, mbar_wait(dp_full, k & 1, status));
