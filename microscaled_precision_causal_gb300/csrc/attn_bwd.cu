@@ -665,6 +665,13 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         uint32_t vp[32];
         tmem_ld32(lane_base + kP + 32 * c, vp);
         tmem_ld_wait();
+        if (kDQT && wg == kWG - 1) {
+          // the scale words that do not depend on this step's dS^ exponents, into dP columns
+          // this warpgroup has just read: dK's B (Q per query chunk), dQ^T's A (K's blocks)
+          const uint32_t bq = *reinterpret_cast<const uint32_t*>(cs);
+          tmem_st4(lane_base + kSFK + 4, bq, bq, bq, bq);
+          tmem_st4(lane_base + kSFQ, ksf, ksf, ksf, ksf);
+        }
         const float fP = (1.0f / 256.0f) * sv_row * (STRICT ? 1.0f : ue8m0_to_f32(cs[4 + c]));
         const float2 fP2 = make_float2(fP, fP);
         const float4* nd4 = reinterpret_cast<const float4*>(rb + 128 + 32 * c);   // -D
@@ -739,7 +746,22 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
         mbar_arrive(p_full);
         continue;                            // dQ comes from the deterministic dQ kernel
       }
-      {
+      if constexpr (kDQT) {
+        // the exponent-dependent words of dK and dQ^T, one group per warpgroup: E holds
+        // one byte per (key block, query chunk), word b = key block b's four chunks
+        const uint4 e4 = *reinterpret_cast<const uint4*>(Esm);
+        if (wg == 1) {                        // dK: A row = key in block b, byte = query chunk
+          tmem_st4(lane_base + kSFK, e4.x, e4.y, e4.z, e4.w);
+        } else if (wg != 3) {
+          // dQ^T: B row = query, one word per query chunk c holding its four key blocks'
+          // bytes (the 4 x 4 byte transpose of E); warpgroup 2 the low half, 0 the high
+          const uint32_t lo = __byte_perm(e4.x, e4.y, wg == 2 ? 0x5140 : 0x7362);
+          const uint32_t hi = __byte_perm(e4.z, e4.w, wg == 2 ? 0x5140 : 0x7362);
+          const uint32_t c0 = __byte_perm(lo, hi, 0x5410), c1 = __byte_perm(lo, hi, 0x7632);
+          tmem_st4(lane_base + kSFQ + (wg == 2 ? 4 : 8), c0, c1, c0, c1);
+        }
+        tmem_st_wait();
+      } else {
         // block-scale words of the dK and dQ MMAs (dV's were written after P^), one
         // operand pair per warpgroup
         const uint8_t* E = Esm;               // E[key block][query chunk]
