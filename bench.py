@@ -219,6 +219,7 @@ def run_reference(args, rank, world):
 SECONDARY = (
     ("causal_b1_h2_s256_d64", "default"),
     ("skewed_8192_224x256_h16_d128", "default"),
+    ("packed_16x4096_h16_d128", "default"),
     ("gqa_b4_s8192_hq32_hkv8_d128", "default"),
     ("mixed_nvfp4_gqa_b4_s8192", "mixed"),
     ("strict_packed_4x8192_h16_t3", "strict"),
@@ -226,6 +227,12 @@ SECONDARY = (
     ("noncausal_packed_16k_h16_d128", "default"),
     ("noncausal_b2_s8192_h16_d128", "default"),
 )
+# whole training calls (forward and backward with quantization) that the pages time on B300
+# for the same shapes (FLAMIA technical review section 8, Table 1): context for those lines
+PAGES_CALL_MS = {
+    "skewed_8192_224x256_h16_d128": (1.67, "B300, MXFP8, FLAMIA technical review section 8, Table 1"),
+    "packed_16x4096_h16_d128": (3.17, "B300, MXFP8, FLAMIA technical review section 8, Table 1"),
+}
 EX2_PER_CLK_PER_SM = 32      # MUFU ex2 issue rate of B300-class SMs ([EN] section 7; probe in the design notes)
 
 
@@ -713,6 +720,10 @@ def run_ours(args, rank, world, local_rank):
                    "rounds_ms": t2["rounds"], "frac_of_fp8_peak": v2 / fp8_peak, "phases_ms": p2,
                    "roofline": r.kernel_roofline(p2, fp8_peak) if p2 else None,
                    "exp_ceiling_call_tflops": exp_ceiling(ws.d, sms, sm_mhz)["call_tflops"]}
+            if mode == "default" and wname in PAGES_CALL_MS:
+                ms_p, src = PAGES_CALL_MS[wname]
+                ent["pages_call_ms"] = {"value": ms_p, "source": src,
+                                        "ratio": ms_p / t2["median_of_rounds"]}
             r.release()
             if not args.no_cpu_baseline:
                 s = oracle_sample(ws, args.cpu_seconds / 3, mode=mode)

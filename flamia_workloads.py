@@ -83,6 +83,10 @@ def _workloads():
     w["skewed_8192_224x256_h16_d128"] = Workload(
         "skewed_8192_224x256_h16_d128", (8192,) + (256,) * 224, 16, 16, 128,
         description="packed causal MHA, one 8192-token document and 224 of 256 tokens, H=16, d=128")
+    # the uniform packed row of the same table: sixteen documents of 4096 tokens
+    w["packed_16x4096_h16_d128"] = Workload(
+        "packed_16x4096_h16_d128", (4096,) * 16, 16, 16, 128,
+        description="packed causal MHA, 16 documents of 4096 tokens, H=16, d=128")
     # the noncausal calls the pages time beside the causal ones (packed rows, and the
     # batched 2 x 8192 case)
     w["noncausal_packed_16k_h16_d128"] = Workload(

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_q4, const __grid_constant__ CUtensorMap tm_k4,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const BwdParams p) {
   static_assert(!(STRICT && MIXED), "the strict options and the mixed route are separate");
   static_assert(!MIXED || D == 128, "the mixed route is built for head_dim 128");
@@ -808,15 +809,18 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     if (ok) {
       tc_fence_after();
       // dV and dK tiles: each thread stages its row's slice as bf16 in the (now idle) Q
-      // and dO buffers, 16-byte units of row j permuted by XOR with (j mod 8), then the
-      // compute warps copy whole rows of the document's keys out with coalesced stores
+      // and dO buffers, as 64-column boxes of 128 rows x 128 bytes (16-byte unit c of
+      // row j at position c XOR (j mod 8), the 128-byte swizzle); a full tile leaves by
+      // TMA stores of those boxes, the last, partial tile of a document by coalesced
+      // row stores of its rows (a box would write into the next document)
       constexpr int kRowB = D * 2, kUnits = kRowB / 16;
       static_assert(kQStages * L::kTileBytes == kTile * kRowB, "a stage pair holds one bf16 tile");
+      auto stg_off = [](int r, int unit) { return (unit >> 3) * (kTile * 128) + r * 128 + (((unit & 7) ^ (r & 7)) << 4); };
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = (which == 0 ? kDV : kDK) + wg * kCols;
         float mul = which == 0 ? (1.0f / 256.0f) : p.scale;
-        uint8_t* stg = smem + (which == 0 ? L::kQ : L::kDO) + j * kRowB;
+        uint8_t* stg = smem + (which == 0 ? L::kQ : L::kDO);
         uint32_t v[32];
         if (ROT && which == 1) {
           // rotated operands: this warpgroup's 32 columns of dK_rot H / 2^k.  H = H_kWG x
@@ -856,20 +860,32 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int unit = (wg * kCols * 2) / 16 + q;
-          *reinterpret_cast<uint4*>(stg + ((unit ^ (j & 7)) << 4)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          *reinterpret_cast<uint4*>(stg + stg_off(j, unit)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
+      fence_proxy_async_smem();              // the staged tiles, for the TMA stores
       named_bar_sync(1, kCompute);
       const int rows = min(kTile, doc_len - u * kTile);
       const int64_t row0 = (int64_t)doc_start + u * kTile;
-      for (int idx = threadIdx.x - 128; idx < 2 * rows * kUnits; idx += kCompute) {
-        const int which = idx >= rows * kUnits;
-        const int rem = idx - which * rows * kUnits;
-        const int r = rem / kUnits, unit = rem % kUnits;
-        const uint4 val = *reinterpret_cast<const uint4*>(smem + (which == 0 ? L::kQ : L::kDO) + r * kRowB +
-                                                          ((unit ^ (r & 7)) << 4));
-        __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + ((row0 + r) * p.hkv + hk) * D + unit * 8;
-        *reinterpret_cast<uint4*>(dst) = val;
+      if (rows == kTile) {
+        if (threadIdx.x == 128) {
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb) {
+            tma_store_3d(&tm_dv, smem + L::kQ + hb * (kTile * 128), 64 * hb, hk, (int)row0);
+            tma_store_3d(&tm_dk, smem + L::kDO + hb * (kTile * 128), 64 * hb, hk, (int)row0);
+          }
+          bulk_commit();
+          bulk_wait_read<0>();               // the buffers stay valid until the stores have read them
+        }
+      } else {
+        for (int idx = threadIdx.x - 128; idx < 2 * rows * kUnits; idx += kCompute) {
+          const int which = idx >= rows * kUnits;
+          const int rem = idx - which * rows * kUnits;
+          const int r = rem / kUnits, unit = rem % kUnits;
+          const uint4 val = *reinterpret_cast<const uint4*>(smem + (which == 0 ? L::kQ : L::kDO) + stg_off(r, unit));
+          __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + ((row0 + r) * p.hkv + hk) * D + unit * 8;
+          *reinterpret_cast<uint4*>(dst) = val;
+        }
       }
     }
   } else {
@@ -1654,7 +1670,10 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
                          const void* plan, void* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
                          void* const* ev, const void* q4c, const void* q4s, const void* k4c, const void* k4s,
                          float* dbg, Window win) {
-  CUtensorMap tq, tk, tv, tdo, tq4, tk4;
+  CUtensorMap tq, tk, tv, tdo, tq4, tk4, tdk, tdv;
+  if (!make_tmap_bf16_3d(&tdk, dk, D, hkv, T, D * 2, (uint64_t)hkv * D * 2, 64, kTile) ||
+      !make_tmap_bf16_3d(&tdv, dv, D, hkv, T, D * 2, (uint64_t)hkv * D * 2, 64, kTile))
+    return cudaErrorInvalidValue;
   if (!make_tmap_u8_3d(&tq, qc, D, hq, T, D, (uint64_t)hq * D, D, kTile) ||
       !make_tmap_u8_3d(&tk, kc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
       !make_tmap_u8_3d(&tv, vc, D, hkv, T, D, (uint64_t)hkv * D, D, kTile) ||
@@ -1703,7 +1722,7 @@ cudaError_t launch_bwd_d(const void* qc, const void* qs, const void* kc, const v
   if (regs != BwdShape<D, STRICT>::kLaunchRegs) return cudaErrorInvalidConfiguration;
   if (ev) record_timing_event(ev[0], stream);
   attn_bwd_kernel<D, STRICT, MIXED, DBG, WIN, ROT>
-      <<<(unsigned)grid, BwdShape<D, STRICT>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, p);
+      <<<(unsigned)grid, BwdShape<D, STRICT>::kThreads, smem, stream>>>(tq, tk, tv, tdo, tq4, tk4, tdk, tdv, p);
   e = cudaGetLastError();
   if (ev) record_timing_event(ev[1], stream);
   if (e != cudaSuccess) return e;

@@ -119,6 +119,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// 3-D tiled store of a shared-memory box to global memory (coordinates x innermost,
+// y, z; none negative), tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // Bulk (non-tensor) reduce-add of `bytes` bytes of fp16 from shared memory into
 // global memory (IEEE fp16 additions, subnormals kept), tracked by the issuing
 // thread's bulk groups.  Both addresses 16-byte aligned, bytes a multiple of 16.

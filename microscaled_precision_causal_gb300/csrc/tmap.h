@@ -72,4 +72,20 @@ inline bool make_tmap_u8_3d(CUtensorMap* m, const void* base, uint64_t dim0, uin
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor [dim2][dim1][dim0] (dim0 contiguous) with byte strides stride1 and stride2;
+// box (box0, 1, box2), the swizzle of a box0 * 2-byte row.
+inline bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                              uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box2) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3] = {dim0, dim1, dim2};
+  cuuint64_t gstr[2] = {stride1, stride2};
+  cuuint32_t box[3] = {box0, 1, box2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstr, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for_row_bytes(box0 * 2), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace flamia
