@@ -1358,7 +1358,8 @@ __global__ void bwd_tail_kernel(const int* plan, int T, int hq, int hkv, __nv_bf
 // columns, written by the warpgroup that owns the block into the dP columns it has
 // itself read (warpgroup 0: dP columns 0-7 and the B words in 8-11; warpgroup 1:
 // 64-71).
-constexpr int kDqStages = 2;
+constexpr int kDqStages = 4;     // K/V ring: each pair loads a new key tile
+constexpr int kDqKd = 4;         // per-key factor buffers
 constexpr int kDqThreads = 384;
 
 struct DqParams {
@@ -1384,8 +1385,8 @@ struct DqSmem {
   static constexpr int kK = kDO + kTileBytes;                  // [kDqStages]
   static constexpr int kV = kK + kDqStages * kTileBytes;       // [kDqStages]
   static constexpr int kDS = kV + kDqStages * kTileBytes;      // dS'' codes, [query][key]
-  static constexpr int kKD = kDS + kTile * kTile;              // per-key factors [2 buffers][2][128] floats
-  static constexpr int kBar = kKD + 2 * 2 * 128 * 4;
+  static constexpr int kKD = kDS + kTile * kTile;              // per-key factors [kDqKd buffers][2][128] floats
+  static constexpr int kBar = kKD + kDqKd * 2 * 128 * 4;
   static constexpr int kBytes = kBar + 256;
   // at least 116 KB so that one CTA (holding all 512 TMEM columns) fits per SM
   static constexpr int kAlloc = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
@@ -1404,9 +1405,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint64_t* qd_empty = bars + 1;
   uint64_t* kv_full = bars + 2;                 // [kDqStages]
   uint64_t* kv_empty = bars + 2 + kDqStages;    // [kDqStages]
-  uint64_t* kd_full = bars + 2 + 2 * kDqStages; // [2]
-  uint64_t* kd_empty = kd_full + 2;             // [2]
-  uint64_t* s_full = kd_empty + 2;
+  uint64_t* kd_full = bars + 2 + 2 * kDqStages; // [kDqKd]
+  uint64_t* kd_empty = kd_full + kDqKd;         // [kDqKd]
+  uint64_t* s_full = kd_empty + kDqKd;
   uint64_t* p_full = s_full + 1;
   uint64_t* dq_full = s_full + 2;
   uint64_t* dq_empty = s_full + 3;
@@ -1438,7 +1439,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kDqKd; ++i) {
       mbar_init(&kd_full[i], 32);
       mbar_init(&kd_empty[i], 256);
     }
@@ -1527,21 +1528,28 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
     }
   } else if (warp == 3) {
-    // per-key factors s_K(j), s_V(j) of each key tile
+    // per-key factors s_K(j), s_V(j) of each key tile; a pair's global loads are all
+    // issued into registers before the wait for the buffer and the shared-memory stores,
+    // so that their latencies overlap instead of queueing behind stores the compiler
+    // cannot reorder them past
     for (int k = 0; k < npairs; ++k) {
       int w, u;
       pair_of(k, w, u);
-      const int b = k & 1;
-      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&kd_empty[b], ((k >> 1) - 1) & 1, status))) break;
+      const int b = k % kDqKd;
+      uint32_t ks[4], vs[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kl = u * kTile + q * 32 + lane;
+        const int64_t ktok = (int64_t)doc_start + kl;
+        ks[q] = kl < doc_len ? __ldg(p.k_scales + ktok * p.hkv + hk) : 127u;   // 127: 2^0 past the end
+        vs[q] = kl < doc_len ? __ldg(p.v_scales + ktok * p.hkv + hk) : 127u;
+      }
+      if (k >= kDqKd && !__all_sync(0xffffffffu, mbar_wait(&kd_empty[b], ((k / kDqKd) - 1) & 1, status))) break;
       float* kd = kdbuf + b * 256;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int j = q * 32 + lane;
-        const int kl = u * kTile + j;
-        const bool kv = kl < doc_len;
-        const int64_t ktok = (int64_t)doc_start + kl;
-        kd[j] = kv ? ue8m0_to_f32(p.k_scales[ktok * p.hkv + hk]) : 1.0f;
-        kd[128 + j] = kv ? ue8m0_to_f32(p.v_scales[ktok * p.hkv + hk]) : 1.0f;
+        kd[q * 32 + lane] = ue8m0_to_f32(ks[q]);
+        kd[128 + q * 32 + lane] = ue8m0_to_f32(vs[q]);
       }
       mbar_arrive(&kd_full[b]);
     }
@@ -1574,9 +1582,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         for (int c = 0; c < kHalf / 2; ++c) acc[c] = __floats2half2_rn(0.f, 0.f);
       }
       const bool diag = (u == t);
-      const int b = k & 1;
+      const int b = k % kDqKd;
       const float* kd = kdbuf + b * 256;
-      ok = named_bar_and(1, 256, mbar_wait(s_full, k & 1, status) && mbar_wait(&kd_full[b], (k >> 1) & 1, status));
+      ok = named_bar_and(1, 256, mbar_wait(s_full, k & 1, status) && mbar_wait(&kd_full[b], (k / kDqKd) & 1, status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
