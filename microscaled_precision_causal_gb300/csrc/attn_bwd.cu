@@ -21,25 +21,29 @@
 //
 // One CTA per (document-local 128-key tile, kv head); it visits every query
 // head of the kv head's group and every query tile at or after the key tile.
-// Roles (768 threads at d = 128, 512 at d = 64):
+// Roles (896 threads at d = 128, 768 with the strict options, 512 at d = 64):
 //   warp 0      TMA producer (K, V once; Q and dO codes per step)
-//   warp 1      MMA issuer (one thread)
+//   warp 1      MMA issuer (a converged warp; one elected lane issues)
 //   warp 2      TMEM allocator
 //   warp 3      per-query row data of the next steps (LSE, D, chunk scales) into SMEM
 //   warps 4..   compute warpgroups (four at d = 128, two at d = 64): each owns
 //               32 of the 128 query columns of a step and 32 of the head-dim
 //               columns of the dK / dV accumulators
-//   last WG     dQ readout: TMEM -> fp16 staging -> bulk reduce into the accumulator
+//   last WGs    dQ readout (two at d = 128): TMEM -> fp16 staging -> bulk reduce
+//               into the accumulator
 // Thread = key row while building P^ and dS^ codes.  TMEM: S^T [0,128), dP^T
-// [128,256), dV [256, 256+D), dK [384, 384+D).  At d = 128 the dQ^T halves take
-// dP^T's first 64 columns once dS^ is built; at d = 64 the dQ partial has
-// [320, 384).  Block-scale words: dV's in S^T's columns [104, 112) (written once
-// S^T has been read), dK's and dQ's in dP^T's columns [104, 124) (written once
-// dP^T has been read; at d = 64 dQ's in [448, 456)).  Per step the MMA thread
-// issues dV(k) as soon as P^ is in SMEM, then S^T(k+1) (the exponentials of the
-// next step overlap the dS^ work of this one), then dK(k), dQ(k) and dP^T(k+1)
-// once the dQ columns have been read.  The mixed route's S~ MMA (NVFP4) takes its
-// scale words from dP^T's first 16 columns and so is issued late, after dQ.
+// [128,256), dV [256, 256+D), dK [384, 384+D).  P^ (dV's A operand) goes to TMEM
+// into S^T columns its warpgroup has read (default and mixed routes) or to SMEM
+// (strict).  At d = 128 the dQ^T halves take dP^T's first 64 columns once dS^ is
+// built; at d = 64 the dQ partial has [320, 384).  Block-scale words: dV's in
+// S^T's columns [0, 8) ([104, 112) strict), written once S^T has been read; dK's
+// and dQ's in dP^T's columns [104, 124) (at d = 64 dQ's in [448, 456)), written
+// once dP^T has been read.  Per step the MMA warp issues dV(k) as soon as P^ is
+// written, then S^T(k+1) (the exponentials of the next step overlap the dS^ work
+// of this one), then dK(k), dQ(k) and dP^T(k+1) once the dQ columns have been
+// read.  The mixed route's S~ MMA (NVFP4) takes its scale words from dP^T's first
+// 16 columns and so is issued late, after dQ.  dK and dV are staged as bf16 and
+// leave by TMA stores (a document's partial last tile by row stores).
 #include <type_traits>
 
 #include "common.cuh"
@@ -104,7 +108,7 @@ struct BwdSmem {
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;                  // [kQStages]
   static constexpr int kDO = kQ + kQStages * kTileBytes;      // [kQStages]
-  static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query]
+  static constexpr int kPt = kDO + kQStages * kTileBytes;     // P^ codes, [key][query] (strict route)
   static constexpr int kDS = kPt + kTile * kTile;             // dS^ codes, [key][query]
   static constexpr int kRow = kDS + kTile * kTile;            // per-query data, 2 buffers
   // per-query row data: -lse2[128], -D[128], chunk scale bytes[8] (4 words reserved),
