@@ -1596,15 +1596,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int c = 2 * g + cc;                     // 32-key block
         float ds[32];
         float amax = 0.f;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {              // S and dP in 16-column halves
-          uint32_t vs[16], vp[16];
-          tmem_ld16(lane_base + kS + 32 * c + 16 * hf, vs);
-          tmem_ld16(lane_base + kP + 32 * c + 16 * hf, vp);
+        {
+          uint32_t vs[32], vp[32];
+          tmem_ld32(lane_base + kS + 32 * c, vs);
+          tmem_ld32(lane_base + kP + 32 * c, vp);
           tmem_ld_wait();
 #pragma unroll
-          for (int jh = 0; jh < 16; ++jh) {
-            const int jj = 16 * hf + jh;
+          for (int jh = 0; jh < 32; ++jh) {
+            const int jj = jh;
             const int j = 32 * c + jj;
             const float sk = kd[j];
             const float x = __uint_as_float(vs[jh]) * (fq * sk) + nl;
@@ -1638,14 +1637,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kHalf / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + kDQ + kHalf * g + 32 * c, v);
+      {
+        uint32_t v[kHalf];                             // the partial's columns, one TMEM round trip
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c)
+          tmem_ld32(lane_base + kDQ + kHalf * g + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
         tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < kHalf / 2; ++q) {
           const __half2 hpart = __floats2half2_rn(__uint_as_float(v[2 * q]) * cb, __uint_as_float(v[2 * q + 1]) * cb);
-          acc[16 * c + q] = __hadd2(acc[16 * c + q], hpart);
+          acc[q] = __hadd2(acc[q], hpart);
         }
       }
       tc_fence_before();
