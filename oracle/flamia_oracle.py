@@ -19,7 +19,7 @@ Fast and Causally Safe Training on Blackwell", arXiv 2611.03344):
 Everything is float64 numpy except where the method fixes a narrower format
 (E4M3 / E2M1 / UE8M0 codes, bf16 outputs, fp16 dQ partials); those are
 emulated exactly.  Where the pages are silent or garbled, the reading taken
-is named in the docstring (C-1 ... C-14, listed with reasons in the design
+is named in the docstring (C-1 ... C-19, listed with reasons in the design
 notes).
 
 Parity status: the codecs, exponent rules, cost model, work list, the
