@@ -71,6 +71,8 @@ def _sampled_reference(q, k, v, do, window, rows, cols):
 CONFIGS = [
     ("causal_b1_h2_s256_d64", "default"),
     ("packed_16k_h16_d128", "default"),
+    ("packed_16x4096_h16_d128", "default"),
+    ("skewed_8192_224x256_h16_d128", "default"),
     ("gqa_b4_s8192_hq32_hkv8_d128", "default"),
     ("mixed_nvfp4_gqa_b4_s8192", "mixed"),
     ("strict_packed_4x8192_h16_t3", "strict"),
