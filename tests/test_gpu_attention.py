@@ -1,8 +1,11 @@
 """GPU parity of the causal MXFP8 forward and backward against the oracle.
 
-Tolerance (from the target statement of this build): O, dQ, dK and dV within
-1e-2 of the oracle in max-abs error normalised by the oracle tensor's max-abs;
-codes and scale bytes bit-exact; LSE within 1e-3 absolute (natural log).
+Tolerance: O, dQ, dK and dV within 1e-2 of the oracle in max-abs error
+normalised by the oracle tensor's max-abs (the two sides round the same E4M3
+operands but accumulate in different orders, and ex2.approx differs from the
+oracle's fp64 exponential by a few fp32 ulps, which can move an E4M3 rounding by
+one code); codes and scale bytes bit-exact; LSE within 1e-3 absolute (natural
+log).
 """
 import numpy as np
 import pytest
