@@ -1,4 +1,5 @@
-"""The target statement's gates on the GPU, on the pages' workloads.
+"""The method's correctness gates on the GPU, on the pages' workloads: the
+centred softmax gradient's row-sum bound and strict prefix isolation.
 
 - The single causal batched call (B=1, H=2, seq 256, head_dim 64, N(0,1), seed 0):
   the training call against the oracle, and the centred softmax gradient
