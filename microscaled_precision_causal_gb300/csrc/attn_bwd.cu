@@ -41,8 +41,9 @@
 // once dP^T has been read.  Per step the MMA warp issues dV(k) as soon as P^ is
 // written, then S^T(k+1) (the exponentials of the next step overlap the dS^ work
 // of this one), then dK(k), dQ(k) and dP^T(k+1) once the dQ columns have been
-// read.  The mixed route's S~ MMA (NVFP4) takes its scale words from dP^T's first
-// 16 columns and so is issued late, after dQ.  dK and dV are staged as bf16 and
+// read.  The mixed route's S~ MMA (NVFP4) takes its scale words from dP^T's
+// columns [64, 80), written by the readout warpgroups once dP^T has been read.  dK
+// and dV are staged as bf16 and
 // leave by TMA stores (a document's partial last tile by row stores).
 #include <type_traits>
 
@@ -302,13 +303,13 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       auto issue_s = [&](int st) {
         if constexpr (MIXED) {
           // S^T = K~ Q~^T from the NVFP4 copies (64 E2M1 elements per instruction); the
-          // scale words sit in dP columns 0-7 (K~) and 32-39 (Q~), free once the dQ^T
-          // high half was read
+          // scale words sit in dP columns 64-71 (K~) and 72-79 (Q~): the dQ^T halves do not
+          // use them, and they are free once the compute warps have read dP^T
 #pragma unroll
           for (int s = 0; s < 2; ++s)
             if (leader) mma_nvf4(tbase + kS, sdesc_at(b16(), L::kK4 + 32 * s, 16, 8 * 64, kSwizzle64B),
                      sdesc_at(b16(), L::kQ4 + st * L::kScoreBytes + 32 * s, 16, 8 * 64, kSwizzle64B),
-                     idesc_nvf4(128, 128), tbase + kP + 4 * s, tbase + kP + 32 + 4 * s, s > 0);
+                     idesc_nvf4(128, 128), tbase + kP + 64 + 4 * s, tbase + kP + 72 + 4 * s, s > 0);
         } else {
 #pragma unroll
           for (int s = 0; s < D / 32; ++s)
@@ -369,8 +370,11 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
                          tbase + kSFV, tbase + kSFV + 4, (k > 0 || s > 0));
             }
         }
-        if (!MIXED && more) {
-          ok = warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
+        if (more) {
+          // mixed route: the next step's score scale words are written by the readout
+          // warpgroups once this step's dP^T has been read (the compute warps' hand-in)
+          ok = (!MIXED || warp_wait(sf_ready, (k + 1) & 1, status)) &&
+               warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
           if (!ok) break;
           tc_fence_after();
           issue_s(st1);
@@ -423,13 +427,6 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
             ok = warp_wait(dq_empty, 1, status);
             if (!ok) break;
             tc_fence_after();
-          }
-          if (MIXED) {                         // score scale words of step k + 1 were written with the release
-            ok = warp_wait(&qd_full[st1], ((k + 1) / kQStages) & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(st1);
-            if (leader) mma_commit(s_full);
           }
           if (kDQT && !MIXED) issue_dp_half(st1, 0);
           else issue_dp(st1);
@@ -908,9 +905,10 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
     // mixed route: scale words of the score MMA, written into dP columns before every
     // score MMA, replicated over the four lane quarters (lane 32q + l, column c holds
     // row 32c + l); per row and instruction one word of four E4M3 scales.  Readout
-    // warpgroup 0 holds the K~ rows' words (A, fixed, columns 0-7), warpgroup 1 the
-    // Q~ rows' words of the next step's query tile (B, columns 32-39): each writes
-    // only into the dQ^T columns it has itself just read.
+    // warpgroup 0 holds the K~ rows' words (A, fixed, columns 64-71), warpgroup 1 the
+    // Q~ rows' words of the next step's query tile (B, columns 72-79).  They are
+    // written once the compute warps have handed in the step (its dP^T read), so the
+    // next score MMA goes out before this step's dQ^T.
     uint2 sfw[4] = {};
     auto load_sf_rows = [&](const uint8_t* base, int64_t tok0, int H, int hh_) {
 #pragma unroll
@@ -923,8 +921,8 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       load_sf_rows(p.q4_scales, (int64_t)doc_start + (tlo + kk % qtiles) * kTile, p.hq, hk * g + kk / qtiles);
     };
     auto store_score_sf = [&]() {
-      tmem_st4(lane_base + kP + 32 * ro, sfw[0].x, sfw[1].x, sfw[2].x, sfw[3].x);
-      tmem_st4(lane_base + kP + 32 * ro + 4, sfw[0].y, sfw[1].y, sfw[2].y, sfw[3].y);
+      tmem_st4(lane_base + kP + 64 + 8 * ro, sfw[0].x, sfw[1].x, sfw[2].x, sfw[3].x);
+      tmem_st4(lane_base + kP + 64 + 8 * ro + 4, sfw[0].y, sfw[1].y, sfw[2].y, sfw[3].y);
     };
     if (MIXED) {
       if (ro == 0) load_sf_rows(p.k4_scales, (int64_t)doc_start + u * kTile, p.hkv, hk);
@@ -943,6 +941,16 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
       const int h = hk * g + hh;
       const float cb = p.boost[(int64_t)doc * p.hq + h];
       const int qvalid = doc_len - t * kTile;          // query rows of the tile inside the document
+      if (MIXED && k + 1 < nsteps) {
+        // the next step's score scale words, once this step's dP^T has been read
+        ok = named_bar_and(6, 128 * kRO, mbar_wait(p_full, k & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        store_score_sf();                      // warpgroup 1: the Q~ rows of step k + 1
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(sf_ready);
+      }
       if constexpr (kDQT) {
         // dQ^T: thread = head-dim row d = i; per 64-query half this warpgroup reads its
         // 32 query columns and packs them into four 16-byte units of the staged chunk
@@ -957,10 +965,6 @@ __global__ void __launch_bounds__(BwdShape<D, STRICT>::kThreads, 1)
           uint32_t v[32];
           tmem_ld32(lane_base + kDQ + 32 * ro, v);
           tmem_ld_wait();
-          if (MIXED && hf == 1 && k + 1 < nsteps) {
-            store_score_sf();                // warpgroup 1: the Q~ rows of step k + 1
-            tmem_st_wait();
-          }
           tc_fence_before();
           mbar_arrive(dq_empty);             // the columns are in registers
           const int nq = qvalid - hf * 64 - 32 * ro;   // valid queries among the 32
