@@ -266,6 +266,18 @@ def quantizer_bytes(w, mode):
     return total
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the process group (the slowest rank's
+    time is the job's time); the values unchanged without a group of more than one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def measure_fp8_peak(dev):
     """Dense E4M3 GEMM throughput of this GPU: torch._scaled_mm at 8192^3 (per-tensor
     scales, bf16 out), best of 10 after warm-up, CUDA events.  None if unavailable."""
@@ -636,20 +648,11 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.3)
     ph = run.phases(min(args.steps, 30))
     tm = run.timed(args.steps, args.rounds, world)
-    ms_step = tm["median_of_rounds"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    (ms_step,) = max_over_ranks([tm["median_of_rounds"]], dev)
     e2e_serial_ms, h2d, d2h = run.e2e_serial(5)
     e2e_ms, e2e_rounds = run.e2e_pipelined(args.e2e_steps)
     link = run.link_bandwidth(h2d, d2h)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms, e2e_serial_ms = (float(v) for v in t.tolist())
+    e2e_ms, e2e_serial_ms = max_over_ranks([e2e_ms, e2e_serial_ms], dev)
     lines = sampler.stop() if not args.no_clocks else None
     clocks = ClockSampler.summarize(lines, *tm["t_wall"]) if lines else None
     if rank != 0:
